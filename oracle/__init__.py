@@ -1,0 +1,168 @@
+"""CPU oracle for paged decode attention (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product library never links or calls it,
+and it shares no code with the CUDA path: it is a plain C implementation in
+double precision (``pkv_oracle.c``) of the definitions on the pages, compiled
+with gcc and reached through ctypes.
+
+Every function here takes the exact stored bit patterns the GPU reads
+(float32 / bf16 bits / fp8-e5m2 codes) and widens them with the oracle's own
+decoders.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pkv_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libpkv_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, BF16, FP8_E5M2 = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (IEEE arithmetic, no FMA contraction, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if not force and os.path.exists(_LIB_PATH) and \
+            os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+           "-fno-fast-math", "-fopenmp", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            vp, ip, i32p, i64p, dp = (ctypes.c_void_p, ctypes.c_int,
+                                      ctypes.POINTER(ctypes.c_int32),
+                                      ctypes.POINTER(ctypes.c_int64),
+                                      ctypes.POINTER(ctypes.c_double))
+            lib.pkvo_decode_values.argtypes = [vp, ip, ctypes.c_size_t, dp]
+            lib.pkvo_decode_values.restype = None
+            lib.pkvo_encode_values.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_size_t,
+                                               ip, ctypes.c_float, vp]
+            lib.pkvo_encode_values.restype = ip
+            common = [vp, ip, vp, vp, ip, ctypes.c_double, ctypes.c_double, i32p, i32p,
+                      ip, ip, ip, ip, ip, ip, ip, ctypes.c_double]
+            lib.pkvo_paged_decode.argtypes = common + [ip, dp, ip]
+            lib.pkvo_paged_decode.restype = ip
+            lib.pkvo_paged_decode_seqs.argtypes = common + [i32p, ip, dp, ip]
+            lib.pkvo_paged_decode_seqs.restype = ip
+            lib.pkvo_reshape_and_cache.argtypes = [vp, vp, ip, i64p, ip, ip, ip, ip, ip, vp, vp,
+                                                   ip, ctypes.c_float, ctypes.c_float]
+            lib.pkvo_reshape_and_cache.restype = ip
+            lib.pkvo_max_threads.argtypes = []
+            lib.pkvo_max_threads.restype = ip
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray, ctype=None):
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    if ctype is None:
+        return ctypes.c_void_p(a.ctypes.data)
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def max_threads() -> int:
+    return int(_load().pkvo_max_threads())
+
+
+def decode_values(bits: np.ndarray, dtype: int) -> np.ndarray:
+    """Widen stored elements to float64 with the oracle's own decoders."""
+    bits = np.ascontiguousarray(bits)
+    out = np.empty(bits.size, dtype=np.float64)
+    _load().pkvo_decode_values(_ptr(bits), dtype, bits.size, _ptr(out, ctypes.c_double))
+    return out.reshape(bits.shape)
+
+
+def encode_values(x: np.ndarray, dtype: int, scale: float = 1.0) -> np.ndarray:
+    """Encode float32 values to a stored dtype with the oracle's own encoders."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    storage = {F32: np.float32, BF16: np.uint16, FP8_E5M2: np.uint8}[dtype]
+    out = np.empty(x.shape, dtype=storage)
+    rc = _load().pkvo_encode_values(_ptr(x, ctypes.c_float), x.size, dtype, scale, _ptr(out))
+    if rc:
+        raise ValueError(f"encode_values failed ({rc})")
+    return out
+
+
+def _attn_args(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_lens, scale,
+               k_scale, v_scale):
+    S, Hq, D = q.shape
+    N, Hkv, D2, B = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    q = np.ascontiguousarray(q)
+    k_cache = np.ascontiguousarray(k_cache)
+    v_cache = np.ascontiguousarray(v_cache)
+    keep = (q, k_cache, v_cache, bt, sl)
+    args = [_ptr(q), q_dtype, _ptr(k_cache), _ptr(v_cache), kv_dtype, float(k_scale),
+            float(v_scale), _ptr(bt, ctypes.c_int32), _ptr(sl, ctypes.c_int32), S, Hq, Hkv, D, B,
+            N, bt.shape[1], float(scale)]
+    return args, keep, (S, Hq, D)
+
+
+def paged_decode(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_lens, scale,
+                 k_scale=1.0, v_scale=1.0, partition_tokens=0, num_threads=0) -> np.ndarray:
+    """Paged decode attention of the whole batch in float64: out [S, Hq, D].
+
+    ``partition_tokens > 0`` evaluates the split-sequence form with the
+    log-sum-exp merge instead of one softmax per sequence.
+    """
+    args, keep, shape = _attn_args(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
+                                   seq_lens, scale, k_scale, v_scale)
+    out = np.zeros(shape, dtype=np.float64)
+    rc = _load().pkvo_paged_decode(*args, int(partition_tokens), _ptr(out, ctypes.c_double),
+                                   int(num_threads))
+    del keep
+    if rc:
+        raise ValueError(f"oracle paged_decode failed ({rc})")
+    return out
+
+
+def paged_decode_seqs(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_lens, scale,
+                      seqs, k_scale=1.0, v_scale=1.0, num_threads=0) -> np.ndarray:
+    """Like ``paged_decode`` but only for the listed sequences: returns [len(seqs), Hq, D]."""
+    args, keep, shape = _attn_args(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
+                                   seq_lens, scale, k_scale, v_scale)
+    seqs = np.ascontiguousarray(seqs, dtype=np.int32)
+    out = np.zeros(shape, dtype=np.float64)
+    rc = _load().pkvo_paged_decode_seqs(*args, _ptr(seqs, ctypes.c_int32), seqs.size,
+                                        _ptr(out, ctypes.c_double), int(num_threads))
+    del keep
+    if rc:
+        raise ValueError(f"oracle paged_decode_seqs failed ({rc})")
+    return out[seqs]
+
+
+def reshape_and_cache(k, v, in_dtype, slot_mapping, k_cache, v_cache, kv_dtype,
+                      k_scale=1.0, v_scale=1.0) -> int:
+    """Scatter new K/V rows into host cache copies in place; returns the status code."""
+    T, Hkv, D = k.shape
+    N, Hkv2, D2, B = k_cache.shape
+    assert Hkv2 == Hkv and D2 == D and v.shape == k.shape
+    assert k_cache.flags["C_CONTIGUOUS"] and v_cache.flags["C_CONTIGUOUS"]
+    k = np.ascontiguousarray(k)
+    v = np.ascontiguousarray(v)
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    return int(_load().pkvo_reshape_and_cache(_ptr(k), _ptr(v), in_dtype,
+                                              _ptr(sm, ctypes.c_int64), T, Hkv, D, B, N,
+                                              _ptr(k_cache), _ptr(v_cache), kv_dtype,
+                                              float(k_scale), float(v_scale)))
