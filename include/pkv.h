@@ -1,0 +1,183 @@
+/*
+ * pkv.h - C ABI of the GB300 (sm_103a) paged KV-cache decode library.
+ *
+ * Two operations, both from the pages' statement of the problem:
+ *
+ *  - pkv_paged_attn_decode: PagedAttention decode ("vLLM e PagedAttention:
+ *    serving high-throughput", simplified PagedAttention CUDA-kernel
+ *    pseudocode).  For every sequence s and query head h the kernel walks the
+ *    sequence's logical blocks, looks up each block's physical id in
+ *    block_tables[s], reads that block's K and V tile, and folds the scores
+ *    into an online (running max / running sum) softmax; the result is
+ *    softmax(scale * q K^T) V over the first seq_lens[s] logical rows, i.e.
+ *    the dense single-query attention of the "Inference optimization" lesson
+ *    (Step 2, scaled_dot_product_attention) on the gathered rows.
+ *
+ *  - pkv_reshape_and_cache: the KV-cache update ("Inference optimization"
+ *    lesson, section "Caches de KV": only the new token's K and V are computed
+ *    and appended; section "PagedAttention": fixed-size pages anywhere in GPU
+ *    memory, mapped by a per-request table).  Each new token's K/V row is
+ *    written into its slot of the paged pool.
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless a
+ *    comment says "host".  The library allocates no memory and keeps no
+ *    device state between calls; scratch space is the caller's `workspace`.
+ *  - All tensors are dense, row-major, with the shapes given below, and every
+ *    device pointer must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Calls only enqueue work on it; none synchronises, except
+ *    pkv_read_status which copies a status word to the host.
+ *  - Argument errors are returned before anything is enqueued.  Problems only
+ *    the device can see (a block id or slot outside the pool, a seq_len
+ *    longer than its table, a wait that timed out) are never trapped: the
+ *    kernels skip the offending access, record a pkv_status in the status
+ *    word, and carry on; pkv_read_status returns it.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size or count      */
+    PKV_ERR_UNSUPPORTED = 2,   /* valid but not implemented (dtype, head_dim, ...) */
+    PKV_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed             */
+    PKV_ERR_OUT_OF_RANGE = 4,  /* device side: block id / slot / seq_len invalid   */
+    PKV_ERR_TIMEOUT = 5,       /* device side: a bounded wait gave up              */
+    PKV_ERR_WORKSPACE = 6      /* workspace missing or smaller than required       */
+} pkv_status;
+
+typedef enum {
+    PKV_F32 = 0,       /* IEEE binary32                                   */
+    PKV_BF16 = 1,      /* bfloat16                                        */
+    PKV_FP8_E5M2 = 2   /* OCP fp8 E5M2 (KV cache only), value = code * scale */
+} pkv_dtype;
+
+/* Flags of pkv_paged_attn_decode. */
+#define PKV_FLAG_IMPL_AUTO 0x0      /* tensor-core path when it applies, else CUDA cores */
+#define PKV_FLAG_IMPL_SIMT 0x1      /* force the CUDA-core (FFMA) kernel                 */
+#define PKV_FLAG_IMPL_MMA  0x2      /* force the tensor-core (mma.sync) kernel           */
+#define PKV_FLAG_IMPL_MASK 0x3
+/* Test hook for the failure path: the first page copy of the first work item
+ * is never issued, so its bounded wait runs out and the call records
+ * PKV_ERR_TIMEOUT (after about one second) instead of hanging.  Output rows
+ * are then undefined. */
+#define PKV_FLAG_TEST_DROP_FIRST_COPY 0x100
+
+/*
+ * Workspace bytes pkv_paged_attn_decode needs for these sizes (always >= 256:
+ * the first 256 bytes hold the status word and a work counter).
+ *   partition_tokens: 0 = automatic choice, -1 = never split (one pass over
+ *   each sequence), > 0 = split every sequence into partitions of this many
+ *   tokens (a multiple of block_size) merged by a log-sum-exp kernel.
+ * Returns 0 for invalid sizes.  Host only; touches no device.
+ */
+size_t pkv_paged_attn_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int max_seq_len,
+                                     int partition_tokens);
+
+/*
+ * The partition size pkv_paged_attn_decode will use for these sizes
+ * (0 = no split), or -1 for invalid sizes.  Host only.
+ */
+int pkv_paged_attn_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int max_seq_len,
+                                    int partition_tokens);
+
+/*
+ * Paged decode attention.
+ *
+ *   q            [num_seqs, num_q_heads, head_dim], q_dtype in {F32, BF16}
+ *   k_cache,
+ *   v_cache      [num_blocks, num_kv_heads, head_dim, block_size], kv_dtype in
+ *                {F32, BF16, FP8_E5M2}: tokens of a page are contiguous for
+ *                each (head, dim), as in the pages' K_cache layout.
+ *   k_scale,
+ *   v_scale      dequant scales of FP8_E5M2 caches (value = code * scale);
+ *                ignored for F32/BF16.
+ *   block_tables int32 [num_seqs, max_blocks_per_seq]; entry j of row s is the
+ *                physical block holding logical tokens [16j, 16j+16) of
+ *                sequence s.  Entries past ceil(seq_lens[s]/block_size) are
+ *                never read.  Rows may share blocks (shared prefixes).
+ *   seq_lens     int32 [num_seqs]; 0 gives a zero output row.
+ *   num_q_heads  a multiple of num_kv_heads; query head h uses KV head
+ *                h / (num_q_heads / num_kv_heads).  At most 16 query heads
+ *                per KV head.
+ *   head_dim     64 or 128.   block_size: 16.
+ *   max_seq_len  an upper bound of every seq_lens[s] (<= max_blocks_per_seq *
+ *                block_size), used to size the launch and the workspace (no
+ *                device-to-host copy of seq_lens).  A seq_lens[s] outside
+ *                [0, max_seq_len] is clamped and reported as
+ *                PKV_ERR_OUT_OF_RANGE in the status word.
+ *   scale        multiplies q.k (e.g. 1/sqrt(head_dim)).
+ *   out          [num_seqs, num_q_heads, head_dim], out_dtype in {F32, BF16}.
+ *   workspace    >= pkv_paged_attn_workspace_size(...) bytes of device memory,
+ *                256-byte aligned.  Its content on entry does not matter; it
+ *                is overwritten.  Concurrent calls need separate workspaces.
+ *   partition_tokens  as for pkv_paged_attn_workspace_size.
+ *   flags        PKV_FLAG_IMPL_* and test hooks.
+ *
+ * The status word in the workspace is cleared at the start of the call.
+ * Returns PKV_OK when the work was enqueued.
+ */
+pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype,
+                                 const void *k_cache, const void *v_cache, pkv_dtype kv_dtype,
+                                 float k_scale, float v_scale,
+                                 const int32_t *block_tables, const int32_t *seq_lens,
+                                 int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int num_blocks, int max_blocks_per_seq,
+                                 int max_seq_len, float scale,
+                                 void *out, pkv_dtype out_dtype,
+                                 void *workspace, size_t workspace_bytes,
+                                 int partition_tokens, int flags, void *stream);
+
+/*
+ * Paged cache write: for every token i < num_tokens with
+ * slot = slot_mapping[i] >= 0, writes
+ *   k_cache[slot / block_size, h, d, slot % block_size] = cvt(k[i, h, d])
+ * (and the same for v) for all h < num_kv_heads, d < head_dim.
+ *
+ *   k, v          [num_tokens, num_kv_heads, head_dim], in_dtype in {F32, BF16}
+ *   slot_mapping  int64 [num_tokens]; negative = padding token, skipped.
+ *                 Non-negative slots must be distinct (duplicates race).
+ *   k_cache,
+ *   v_cache       [num_blocks, num_kv_heads, head_dim, block_size] of kv_dtype.
+ *   cvt           F32 -> F32 and BF16 -> BF16 copy the bits; F32 -> BF16 rounds
+ *                 to nearest even; BF16 -> F32 widens exactly; -> FP8_E5M2
+ *                 stores round-to-nearest-even(x / scale) computed in float32
+ *                 and saturated to +-57344.  NaN inputs give a NaN code of
+ *                 unspecified payload.
+ *   status        optional device int32 (NULL = none): set to
+ *                 PKV_ERR_OUT_OF_RANGE if a slot lies past the pool (that
+ *                 token is skipped).  It is never cleared by this call.
+ */
+pkv_status pkv_reshape_and_cache(const void *k, const void *v, pkv_dtype in_dtype,
+                                 const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                                 int head_dim, int block_size, int num_blocks,
+                                 void *k_cache, void *v_cache, pkv_dtype kv_dtype,
+                                 float k_scale, float v_scale, int32_t *status, void *stream);
+
+/*
+ * Waits for `stream`, then copies the status word of a decode workspace to
+ * *host_status (a pkv_status value); clear != 0 also resets it to PKV_OK.
+ */
+pkv_status pkv_read_status(void *workspace, int clear, int32_t *host_status, void *stream);
+
+/* A static string naming a status code. */
+const char *pkv_status_string(pkv_status status);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,223 @@
+"""GB300 (sm_103a) paged KV-cache decode attention.
+
+Thin Python binding over the C ABI of ``_build/libpkv.so`` (include/pkv.h):
+argument marshalling only.  Every step of the computation runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback, and the calls
+raise if the library is missing.  PyTorch provides device memory, the
+current stream and the workspace allocation.
+
+    paged_attn_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out)
+    reshape_and_cache(k, v, slot_mapping, k_cache, v_cache)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = ["paged_attn_decode", "reshape_and_cache", "workspace_size", "partition_tokens",
+           "read_status", "PkvError", "lib", "F32", "BF16", "FP8_E5M2"]
+
+F32, BF16, FP8_E5M2 = 0, 1, 2
+IMPL = {"auto": 0x0, "simt": 0x1, "mma": 0x2}
+FLAG_TEST_DROP_FIRST_COPY = 0x100
+STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
+          4: "PKV_ERR_OUT_OF_RANGE", 5: "PKV_ERR_TIMEOUT", 6: "PKV_ERR_WORKSPACE"}
+
+_lock = threading.Lock()
+_lib = None
+_workspaces: dict = {}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        msg = _lib.pkv_status_string(code).decode() if _lib is not None else STATUS.get(code, "?")
+        super().__init__(f"{what}: {msg}")
+
+
+def lib(build_if_missing: bool = True) -> ctypes.CDLL:
+    """The loaded C library (compiled on first use if ``build_if_missing``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if build_if_missing:
+                path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"paged KV-cache CUDA library not built: {path}")
+            L = ctypes.CDLL(path)
+            vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+            L.pkv_paged_attn_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.pkv_paged_attn_workspace_size.restype = sz
+            L.pkv_paged_attn_partition_tokens.argtypes = [i, i, i, i, i, i, i]
+            L.pkv_paged_attn_partition_tokens.restype = i
+            L.pkv_paged_attn_decode.argtypes = [vp, i, vp, vp, i, f, f, vp, vp, i, i, i, i, i, i,
+                                                i, i, f, vp, i, vp, sz, i, i, vp]
+            L.pkv_paged_attn_decode.restype = i
+            L.pkv_reshape_and_cache.argtypes = [vp, vp, i, vp, i, i, i, i, i, vp, vp, i, f, f, vp,
+                                                vp]
+            L.pkv_reshape_and_cache.restype = i
+            L.pkv_read_status.argtypes = [vp, i, ctypes.POINTER(ctypes.c_int32), vp]
+            L.pkv_read_status.restype = i
+            L.pkv_status_string.argtypes = [i]
+            L.pkv_status_string.restype = ctypes.c_char_p
+            L.pkv_version.argtypes = []
+            L.pkv_version.restype = i
+            _lib = L
+    return _lib
+
+
+def _dtype_code(t: torch.Tensor, what: str) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float8_e5m2:
+        return FP8_E5M2
+    raise TypeError(f"{what}: unsupported dtype {t.dtype}")
+
+
+def _check(t: torch.Tensor, what: str, ndim: int, device: torch.device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{what} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{what} must be a CUDA tensor (the library has no CPU path)")
+    if t.device != device:
+        raise ValueError(f"{what} is on {t.device}, expected {device}")
+    if t.dim() != ndim:
+        raise ValueError(f"{what} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{what} must be contiguous")
+
+
+def _stream(device: torch.device, stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                   max_seq_len: int, partition_tokens: int = 0, block_size: int = 16) -> int:
+    n = lib().pkv_paged_attn_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                            block_size, max_seq_len, partition_tokens)
+    if n == 0:
+        raise ValueError("invalid sizes for the decode workspace")
+    return int(n)
+
+
+def partition_tokens(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                     max_seq_len: int, partition_tokens: int = 0, block_size: int = 16) -> int:
+    """Tokens per split partition the decode call will use (0 = one pass)."""
+    return int(lib().pkv_paged_attn_partition_tokens(num_seqs, num_q_heads, num_kv_heads,
+                                                     head_dim, block_size, max_seq_len,
+                                                     partition_tokens))
+
+
+def get_workspace(nbytes: int, device: torch.device) -> torch.Tensor:
+    """A cached device workspace of at least ``nbytes`` (grown on demand)."""
+    key = (device.type, device.index)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                      out: torch.Tensor, *, k_scale: float = 1.0, v_scale: float = 1.0,
+                      max_seq_len: Optional[int] = None, partition_tokens: int = 0,
+                      impl: str = "auto", workspace: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None, flags: int = 0) -> torch.Tensor:
+    """PagedAttention decode: out[s, h] = softmax(scale q[s,h] K_s^T) V_s.
+
+    q [S, Hq, D] (f32/bf16); k_cache, v_cache [N, Hkv, D, 16] (f32/bf16/
+    float8_e5m2); block_tables int32 [S, max_blocks]; seq_lens int32 [S];
+    out [S, Hq, D] (f32/bf16).  ``max_seq_len`` bounds seq_lens (default:
+    max_blocks * 16, no device sync).  Returns ``out``.
+    """
+    dev = q.device
+    _check(q, "q", 3, dev)
+    _check(k_cache, "k_cache", 4, dev)
+    _check(v_cache, "v_cache", 4, dev)
+    _check(block_tables, "block_tables", 2, dev)
+    _check(seq_lens, "seq_lens", 1, dev)
+    _check(out, "out", 3, dev)
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must have the same shape and dtype")
+    S, Hq, D = q.shape
+    N, Hkv, D2, B = k_cache.shape
+    if D2 != D or out.shape != q.shape or block_tables.shape[0] != S or seq_lens.shape[0] != S:
+        raise ValueError("inconsistent shapes")
+    max_blocks = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_blocks * B
+    L = lib()
+    need = L.pkv_paged_attn_workspace_size(S, Hq, Hkv, D, B, max_seq_len, partition_tokens)
+    if need == 0:
+        raise ValueError("invalid sizes or partition_tokens")
+    if workspace is None:
+        workspace = get_workspace(need, dev)
+    flags |= IMPL[impl]
+    rc = L.pkv_paged_attn_decode(
+        q.data_ptr(), _dtype_code(q, "q"), k_cache.data_ptr(), v_cache.data_ptr(),
+        _dtype_code(k_cache, "k_cache"), float(k_scale), float(v_scale), block_tables.data_ptr(),
+        seq_lens.data_ptr(), S, Hq, Hkv, D, B, N, max_blocks, int(max_seq_len), float(scale),
+        out.data_ptr(), _dtype_code(out, "out"), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), int(partition_tokens), int(flags),
+        _stream(dev, stream))
+    if rc != 0:
+        raise PkvError(rc, "pkv_paged_attn_decode")
+    return out
+
+
+def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                      k_cache: torch.Tensor, v_cache: torch.Tensor, *, k_scale: float = 1.0,
+                      v_scale: float = 1.0, status: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Writes k, v [T, Hkv, D] into their slots (block*16+offset; <0 = skip)."""
+    dev = k.device
+    _check(k, "k", 3, dev)
+    _check(v, "v", 3, dev)
+    _check(slot_mapping, "slot_mapping", 1, dev)
+    _check(k_cache, "k_cache", 4, dev)
+    _check(v_cache, "v_cache", 4, dev)
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    T, Hkv, D = k.shape
+    N, Hkv2, D2, B = k_cache.shape
+    if v.shape != k.shape or Hkv2 != Hkv or D2 != D or v_cache.shape != k_cache.shape:
+        raise ValueError("inconsistent shapes")
+    if slot_mapping.shape[0] != T:
+        raise ValueError("slot_mapping must have one entry per token")
+    st_ptr = None
+    if status is not None:
+        _check(status, "status", 1, dev)
+        st_ptr = status.data_ptr()
+    rc = lib().pkv_reshape_and_cache(
+        k.data_ptr(), v.data_ptr(), _dtype_code(k, "k"), slot_mapping.data_ptr(), T, Hkv, D, B,
+        N, k_cache.data_ptr(), v_cache.data_ptr(), _dtype_code(k_cache, "k_cache"),
+        float(k_scale), float(v_scale), st_ptr, _stream(dev, stream))
+    if rc != 0:
+        raise PkvError(rc, "pkv_reshape_and_cache")
+
+
+def read_status(workspace: Optional[torch.Tensor] = None, clear: bool = True,
+                device: Optional[torch.device] = None) -> int:
+    """Status word of a decode workspace (default: the cached one of ``device``)."""
+    if workspace is None:
+        dev = device or torch.device("cuda", torch.cuda.current_device())
+        workspace = _workspaces[(dev.type, dev.index)]
+    out = ctypes.c_int32(0)
+    rc = lib().pkv_read_status(workspace.data_ptr(), int(clear), ctypes.byref(out),
+                               _stream(workspace.device, None))
+    if rc != 0:
+        raise PkvError(rc, "pkv_read_status")
+    return int(out.value)

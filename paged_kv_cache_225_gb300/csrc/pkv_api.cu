@@ -1,0 +1,284 @@
+// C ABI of the paged KV-cache decode library (declared in include/pkv.h):
+// argument validation, split planning, workspace layout and dispatch.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+int device_sm_count()
+{
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
+        return 1;
+    if (dev >= 64) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        return n > 0 ? n : 1;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            n <= 0)
+            n = 1;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// Resident decode CTAs the split heuristic plans for (2 per SM of a GB300).
+// A fixed number keeps the plan, and so the workspace size, independent of
+// the device that happens to be current.
+constexpr long kPlanSlots = 2L * 152;
+
+// Partition size for these sizes: > 0 split, 0 one pass, -1 invalid.
+static int resolve_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_seq_len, int requested)
+{
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size != kBlockSize || max_seq_len < 0 || num_q_heads % num_kv_heads != 0)
+        return -1;
+    if (requested == -1)
+        return 0;
+    if (requested > 0)
+        return (requested % kBlockSize == 0) ? requested : -1;
+    if (requested != 0)
+        return -1;
+    const long units = static_cast<long>(num_seqs) * num_kv_heads;
+    if (max_seq_len <= 1024 && units >= kPlanSlots)
+        return 0;
+    int P = 512;
+    while (P > 64 && units * ((max_seq_len + P - 1) / P) < 4 * kPlanSlots)
+        P /= 2;
+    return max_seq_len <= P ? 0 : P;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Plan {
+    int partition;  // 0 = no split
+    int max_parts;
+    size_t part_o_off, part_ml_off, bytes;
+};
+
+static bool make_plan(int S, int Hq, int Hkv, int D, int B, int max_len, int requested, Plan *pl)
+{
+    const int P = resolve_partition(S, Hq, Hkv, D, B, max_len, requested);
+    if (P < 0)
+        return false;
+    pl->partition = P;
+    pl->max_parts = 1;
+    pl->part_o_off = pl->part_ml_off = 0;
+    pl->bytes = kWorkspaceHeader;
+    if (P > 0) {
+        pl->max_parts = max_len > P ? (max_len + P - 1) / P : 1;
+        const size_t rows = static_cast<size_t>(S) * Hq * pl->max_parts;
+        pl->part_o_off = kWorkspaceHeader;
+        pl->part_ml_off = pl->part_o_off + align256(rows * D * sizeof(float));
+        pl->bytes = pl->part_ml_off + align256(rows * 2 * sizeof(float));
+    }
+    return true;
+}
+
+static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+size_t pkv_paged_attn_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int max_seq_len,
+                                     int partition_tokens)
+{
+    Plan pl;
+    if (!make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                   partition_tokens, &pl))
+        return 0;
+    return pl.bytes;
+}
+
+int pkv_paged_attn_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int max_seq_len,
+                                    int partition_tokens)
+{
+    return resolve_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                             max_seq_len, partition_tokens);
+}
+
+pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype, const void *k_cache,
+                                 const void *v_cache, pkv_dtype kv_dtype, float k_scale,
+                                 float v_scale, const int32_t *block_tables,
+                                 const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                 int max_blocks_per_seq, int max_seq_len, float scale, void *out,
+                                 pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                                 int partition_tokens, int flags, void *stream)
+{
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+        max_blocks_per_seq <= 0 || max_seq_len < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (static_cast<long>(max_seq_len) > static_cast<long>(max_blocks_per_seq) * kBlockSize)
+        return PKV_ERR_INVALID_ARG;
+    if (q_dtype != PKV_F32 && q_dtype != PKV_BF16)
+        return PKV_ERR_UNSUPPORTED;
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E5M2)
+        return PKV_ERR_UNSUPPORTED;
+    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
+        return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128)
+        return PKV_ERR_UNSUPPORTED;
+    if (block_size != kBlockSize)
+        return PKV_ERR_UNSUPPORTED;
+    const int group = num_q_heads / num_kv_heads;
+    if (group > 16)
+        return PKV_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+        return PKV_ERR_INVALID_ARG;
+    if ((flags & ~(PKV_FLAG_IMPL_MASK | PKV_FLAG_TEST_DROP_FIRST_COPY)) != 0 ||
+        (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_MASK)
+        return PKV_ERR_INVALID_ARG;
+    Plan pl;
+    if (!make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
+                   partition_tokens, &pl))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.bytes)
+        return PKV_ERR_WORKSPACE;
+    if (num_seqs == 0)
+        return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+
+    const int impl = flags & PKV_FLAG_IMPL_MASK;
+    const bool mma_ok = mma_supports(kv_dtype, q_dtype, head_dim, group);
+    if (impl == PKV_FLAG_IMPL_MMA && !mma_ok)
+        return PKV_ERR_UNSUPPORTED;
+    const bool use_mma = (impl == PKV_FLAG_IMPL_MMA) || (impl == PKV_FLAG_IMPL_AUTO && mma_ok);
+
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.status = reinterpret_cast<int *>(ws);
+    p.counter = reinterpret_cast<unsigned *>(ws + 4);
+    p.part_o = pl.partition > 0 ? reinterpret_cast<float *>(ws + pl.part_o_off) : nullptr;
+    p.part_ml = pl.partition > 0 ? reinterpret_cast<float *>(ws + pl.part_ml_off) : nullptr;
+    p.q_dtype = q_dtype;
+    p.out_dtype = out_dtype;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.max_len = max_seq_len;
+    p.group = group;
+    const float k_mul = (kv_dtype == PKV_FP8_E5M2) ? k_scale : 1.0f;
+    p.score_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * k_mul);
+    p.out_scale = (kv_dtype == PKV_FP8_E5M2) ? v_scale : 1.0f;
+    p.partition = pl.partition > 0 ? pl.partition : max_blocks_per_seq * kBlockSize;
+    p.max_parts = pl.max_parts;
+    p.split = pl.partition > 0 ? 1 : 0;
+    p.drop_first_copy = (flags & PKV_FLAG_TEST_DROP_FIRST_COPY) ? 1 : 0;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    pkv_status rc = use_mma ? launch_decode_mma(p, kv_dtype, st) : launch_decode_simt(p, kv_dtype, st);
+    if (rc != PKV_OK)
+        return rc;
+    if (p.split && p.max_parts > 1)
+        rc = launch_merge(p, st);
+    return rc;
+}
+
+pkv_status pkv_reshape_and_cache(const void *k, const void *v, pkv_dtype in_dtype,
+                                 const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                                 int head_dim, int block_size, int num_blocks, void *k_cache,
+                                 void *v_cache, pkv_dtype kv_dtype, float k_scale, float v_scale,
+                                 int32_t *status, void *stream)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (block_size != kBlockSize)
+        return PKV_ERR_UNSUPPORTED;
+    if (in_dtype != PKV_F32 && in_dtype != PKV_BF16)
+        return PKV_ERR_UNSUPPORTED;
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E5M2)
+        return PKV_ERR_UNSUPPORTED;
+    if (kv_dtype == PKV_F32 && in_dtype == PKV_BF16) {
+        // widening is exact and supported
+    }
+    if (kv_dtype == PKV_FP8_E5M2 &&
+        (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale == 0.f || v_scale == 0.f))
+        return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0)
+        return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(slot_mapping, 8) || !aligned(k_cache, 16) ||
+        !aligned(v_cache, 16) || (status && !aligned(status, 4)))
+        return PKV_ERR_INVALID_ARG;
+    return launch_reshape_and_cache(k, v, in_dtype, slot_mapping, num_tokens, num_kv_heads,
+                                    head_dim, num_blocks, k_cache, v_cache, kv_dtype, k_scale,
+                                    v_scale, status, static_cast<cudaStream_t>(stream));
+}
+
+pkv_status pkv_read_status(void *workspace, int clear, int32_t *host_status, void *stream)
+{
+    if (!workspace || !host_status)
+        return PKV_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (clear && cudaMemsetAsync(workspace, 0, sizeof v, st) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    *host_status = v;
+    return PKV_OK;
+}
+
+const char *pkv_status_string(pkv_status status)
+{
+    switch (status) {
+    case PKV_OK:
+        return "PKV_OK";
+    case PKV_ERR_INVALID_ARG:
+        return "PKV_ERR_INVALID_ARG: invalid argument";
+    case PKV_ERR_UNSUPPORTED:
+        return "PKV_ERR_UNSUPPORTED: unsupported dtype or shape";
+    case PKV_ERR_CUDA:
+        return "PKV_ERR_CUDA: CUDA runtime error";
+    case PKV_ERR_OUT_OF_RANGE:
+        return "PKV_ERR_OUT_OF_RANGE: block id, slot or seq_len outside the pool or table";
+    case PKV_ERR_TIMEOUT:
+        return "PKV_ERR_TIMEOUT: a bounded device wait gave up";
+    case PKV_ERR_WORKSPACE:
+        return "PKV_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    default:
+        return "PKV_ERR_?: unknown status";
+    }
+}
+
+int pkv_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,879 @@
+// Paged decode attention kernels for sm_103a.
+//
+// What is computed follows the PagedAttention kernel pseudocode of
+// "vLLM e PagedAttention: serving high-throughput": for each sequence and
+// query head, walk the logical blocks, look up the physical block in the
+// block table, score the block's keys, fold them into a running max / running
+// sum softmax, accumulate the value rows, and divide by the sum at the end.
+//
+// How it is laid out on the GPU (not taken from the pages):
+//  * A work item is (sequence, KV head, partition of `partition` tokens).  One
+//    CTA of four warps owns an item; the G = Hq/Hkv query heads of the KV head
+//    share every K/V page it reads, so each page crosses HBM once per KV head.
+//  * The warps split the item's pages round-robin.  Each warp streams its
+//    pages through a private ring of R shared-memory stages, filled by 1-D
+//    bulk (TMA) copies of the contiguous [head_dim x 16] K and V tiles and
+//    completed on an mbarrier; waits are bounded and report a timeout
+//    instead of hanging.
+//  * Each warp keeps its own softmax state; at the end of an item the four
+//    states are merged through shared memory with log-sum-exp weights.  A
+//    sequence that fits one partition is written straight to `out`;
+//    otherwise normalised partials go to the workspace and a second kernel
+//    merges them.
+//  * In split mode the grid is persistent: CTAs pull items from an atomic
+//    counter and map the item index to (sequence, partition) with a warp
+//    prefix scan over the per-sequence partition counts.
+//  * Per page, scores and the value accumulation run either on CUDA cores
+//    (SimtPolicy) or on tensor cores with mma.sync (MmaBf16Policy,
+//    MmaFp8Policy): S^T = K^T Q^T puts the page's 16 tokens on the MMA's M
+//    dimension and the (up to 8) grouped heads on N; P^T is transposed in
+//    registers with movmatrix and O^T = V P^T puts head_dim on M.
+#pragma once
+
+#include <climits>
+#include <cmath>
+
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per bounded wait
+
+template <int KV> struct KvBytes;
+template <> struct KvBytes<PKV_F32> { static constexpr int v = 4; };
+template <> struct KvBytes<PKV_BF16> { static constexpr int v = 2; };
+template <> struct KvBytes<PKV_FP8_E5M2> { static constexpr int v = 1; };
+
+// Per-warp ring geometry: about 24 KB of page stages per warp (2..8 stages).
+template <int KV, int D> struct Ring {
+    static constexpr int kTileBytes = D * kBlockSize * KvBytes<KV>::v;  // one K or V page tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kRaw = (24 * 1024) / kStageBytes;
+    static constexpr int R = kRaw < 2 ? 2 : (kRaw > 8 ? 8 : kRaw);
+    static constexpr int kRingBytes = R * kStageBytes;
+};
+
+__device__ __forceinline__ float load_q(const DecodeParams &p, size_t idx)
+{
+    if (p.q_dtype == PKV_F32)
+        return static_cast<const float *>(p.q)[idx];
+    const unsigned short b = static_cast<const unsigned short *>(p.q)[idx];
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// ============================================================== CUDA cores
+
+// Scores: lane (t, half) owns token t of the page and half of head_dim; the
+// two halves are summed with one shuffle.  Values: lane owns head_dim rows
+// lane + 32j and walks the page's valid tokens.  GT = heads padded to 2^k.
+template <int KV, int D, int GT>
+struct SimtPolicy {
+    using RingT = Ring<KV, D>;
+    static constexpr int R = RingT::R;
+    static constexpr int kTileBytes = RingT::kTileBytes;
+    static constexpr int kStageBytes = RingT::kStageBytes;
+    static constexpr int kRingBytes = RingT::kRingBytes;
+    static constexpr int kDim = D;
+    static constexpr int GP = GT;
+    static constexpr int kHalf = D / 2;
+    static constexpr int kQHalfStride = kHalf * GT + 4;  // pad: the halves hit other banks
+    static constexpr int kExtraBytes = (2 * kQHalfStride + kWarps * kBlockSize * GT) * 4;
+    static constexpr int DJ = D / 32;
+
+    struct State {
+        float m[GT];
+        float l[GT];
+        float o[DJ][GT];
+    };
+
+    __device__ static float kv_at(const unsigned char *tile, int idx)
+    {
+        if constexpr (KV == PKV_F32)
+            return reinterpret_cast<const float *>(tile)[idx];
+        else if constexpr (KV == PKV_BF16)
+            return __uint_as_float(
+                static_cast<uint32_t>(reinterpret_cast<const unsigned short *>(tile)[idx]) << 16);
+        else
+            return e5m2_to_float(tile[idx]);
+    }
+
+    // One page row V[d][0..15] widened to floats.
+    __device__ static void kv_row(const unsigned char *tile, int d, float (&v)[kBlockSize])
+    {
+        if constexpr (KV == PKV_F32) {
+            const float4 *r = reinterpret_cast<const float4 *>(tile + d * kBlockSize * 4);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                float4 x = r[i];
+                v[4 * i] = x.x;
+                v[4 * i + 1] = x.y;
+                v[4 * i + 2] = x.z;
+                v[4 * i + 3] = x.w;
+            }
+        } else if constexpr (KV == PKV_BF16) {
+            const uint4 *r = reinterpret_cast<const uint4 *>(tile + d * kBlockSize * 2);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                uint4 x = r[i];
+                const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    v[8 * i + 2 * k] = bf16_lo(w[k]);
+                    v[8 * i + 2 * k + 1] = bf16_hi(w[k]);
+                }
+            }
+        } else {
+            const uint4 x = *reinterpret_cast<const uint4 *>(tile + d * kBlockSize);
+            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    v[4 * k + b] = e5m2_to_float(w[k] >> (8 * b));
+        }
+    }
+
+    __device__ static void begin(State &st, const DecodeParams &p, int s, int hkv, int lane,
+                                 unsigned char *extra)
+    {
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+            st.m[g] = -INFINITY;
+            st.l[g] = 0.f;
+#pragma unroll
+            for (int j = 0; j < DJ; ++j)
+                st.o[j][g] = 0.f;
+        }
+        float *sq = reinterpret_cast<float *>(extra);
+        const int G = p.group;
+        for (int idx = threadIdx.x; idx < D * GT; idx += kThreads) {
+            const int d = idx / GT, g = idx - d * GT;
+            float v = 0.f;
+            if (g < G)
+                v = load_q(p, (static_cast<size_t>(s) * p.num_q_heads + hkv * G + g) * D + d);
+            const int half = d / kHalf;
+            sq[half * kQHalfStride + (d - half * kHalf) * GT + g] = v;
+        }
+        (void)lane;
+    }
+
+    __device__ static void page(State &st, const unsigned char *sK, const unsigned char *sV,
+                                int valid, int lane, int warp, unsigned char *extra, float c)
+    {
+        const float *sq = reinterpret_cast<const float *>(extra);
+        float *sp = reinterpret_cast<float *>(extra) + 2 * kQHalfStride + warp * kBlockSize * GT;
+        const int t = lane & 15, half = lane >> 4;
+        const float *qh = sq + half * kQHalfStride;
+        float acc[GT];
+#pragma unroll
+        for (int g = 0; g < GT; ++g)
+            acc[g] = 0.f;
+#pragma unroll 8
+        for (int i = 0; i < kHalf; ++i) {
+            const float k = kv_at(sK, (half * kHalf + i) * kBlockSize + t);
+#pragma unroll
+            for (int g = 0; g < GT; ++g)
+                acc[g] = fmaf(qh[i * GT + g], k, acc[g]);
+        }
+        float alpha[GT];
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+            acc[g] += __shfl_xor_sync(kFullMask, acc[g], 16);
+            const float sc = (t < valid) ? acc[g] * c : -INFINITY;
+            float mx = sc;
+#pragma unroll
+            for (int off = 1; off < 16; off <<= 1)
+                mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, off));
+            const float mnew = fmaxf(st.m[g], mx);
+            alpha[g] = (st.m[g] == -INFINITY) ? 0.f : exp2f(st.m[g] - mnew);
+            const float pr = (t < valid) ? exp2f(sc - mnew) : 0.f;
+            st.l[g] = st.l[g] * alpha[g] + (half == 0 ? pr : 0.f);
+            st.m[g] = mnew;
+            if (half == 0)
+                sp[t * GT + g] = pr;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < DJ; ++j) {
+            float v[kBlockSize];
+            kv_row(sV, lane + 32 * j, v);
+#pragma unroll
+            for (int g = 0; g < GT; ++g)
+                st.o[j][g] *= alpha[g];
+#pragma unroll
+            for (int tt = 0; tt < kBlockSize; ++tt) {
+                if (tt < valid) {
+#pragma unroll
+                    for (int g = 0; g < GT; ++g)
+                        st.o[j][g] = fmaf(sp[tt * GT + g], v[tt], st.o[j][g]);
+                }
+            }
+        }
+        __syncwarp();
+    }
+
+    __device__ static void finish(State &st, float *so, float *sm, float *sl, int lane)
+    {
+#pragma unroll
+        for (int g = 0; g < GT; ++g) {
+            float l = st.l[g];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1)
+                l += __shfl_xor_sync(kFullMask, l, off);
+            if (lane == 0) {
+                sm[g] = st.m[g];
+                sl[g] = l;
+            }
+#pragma unroll
+            for (int j = 0; j < DJ; ++j)
+                so[g * D + lane + 32 * j] = st.o[j][g];
+        }
+    }
+};
+
+// ============================================================ tensor cores
+
+// Shared by the bf16 and fp8 tensor-core policies: online-softmax update of
+// one N tile from S^T accumulators.  tokA/tokB are the page tokens of the
+// accumulator rows r and r+8 this lane holds; heads 8n+2c, 8n+2c+1.
+struct MmaSoftmax {
+    __device__ static void update(const float (&sacc)[4], int tokA, int tokB, int valid, float c,
+                                  float (&m)[2], float (&l)[2], float (&p)[4], float (&alpha)[2])
+    {
+        const float s0 = tokA < valid ? sacc[0] * c : -INFINITY;
+        const float s1 = tokA < valid ? sacc[1] * c : -INFINITY;
+        const float s2 = tokB < valid ? sacc[2] * c : -INFINITY;
+        const float s3 = tokB < valid ? sacc[3] * c : -INFINITY;
+        float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+        }
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        alpha[0] = (m[0] == -INFINITY) ? 0.f : exp2f(m[0] - mn0);
+        alpha[1] = (m[1] == -INFINITY) ? 0.f : exp2f(m[1] - mn1);
+        p[0] = tokA < valid ? exp2f(s0 - mn0) : 0.f;
+        p[1] = tokA < valid ? exp2f(s1 - mn1) : 0.f;
+        p[2] = tokB < valid ? exp2f(s2 - mn0) : 0.f;
+        p[3] = tokB < valid ? exp2f(s3 - mn1) : 0.f;
+        l[0] = l[0] * alpha[0] + p[0] + p[2];
+        l[1] = l[1] * alpha[1] + p[1] + p[3];
+        m[0] = mn0;
+        m[1] = mn1;
+    }
+};
+
+template <int D, int NT>
+struct MmaStateBase {
+    static constexpr int KS = D / 16;  // 16-wide k steps of q.K
+    static constexpr int MT = D / 16;  // 16-row tiles of head_dim in O^T
+    struct State {
+        float o[MT][NT][4];
+        float m[NT][2];
+        float l[NT][2];
+        uint32_t qf[KS][NT][2];
+    };
+
+    __device__ static void reset(State &st)
+    {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    st.o[mt][n][e] = 0.f;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            st.m[n][0] = st.m[n][1] = -INFINITY;
+            st.l[n][0] = st.l[n][1] = 0.f;
+        }
+    }
+
+    // Query fragments (B operand of S^T = K^T Q^T): lane (r, c) holds
+    // q[head 8n+r][16ks + 2c, +1] and [16ks + 8 + 2c, +1]; heads >= G are 0.
+    template <bool F16>
+    __device__ static void load_q_frags(State &st, const DecodeParams &p, int s, int hkv, int lane)
+    {
+        const int r = lane >> 2, c = lane & 3;
+        const int G = p.group;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int g = 8 * n + r;
+            const bool ok = g < G;
+            const size_t row = (static_cast<size_t>(s) * p.num_q_heads + hkv * G + (ok ? g : 0)) * D;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int d = 16 * ks + 8 * hh + 2 * c;
+                    uint32_t w = 0;
+                    if (ok) {
+                        if (!F16) {
+                            w = *reinterpret_cast<const uint32_t *>(
+                                static_cast<const unsigned short *>(p.q) + row + d);
+                        } else {
+                            const float a = load_q(p, row + d), b = load_q(p, row + d + 1);
+                            w = pack_f16(a, b);
+                        }
+                    }
+                    st.qf[ks][n][hh] = w;
+                }
+            }
+        }
+    }
+
+    // O^T accumulator element (mt, n, e) is O[head 8n + 2c + (e&1)][16mt + r + 8(e>>1)].
+    __device__ static void finish(State &st, float *so, float *sm, float *sl, int lane)
+    {
+        const int r = lane >> 2, c = lane & 3;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float l = st.l[n][e];
+                l += __shfl_xor_sync(kFullMask, l, 4);
+                l += __shfl_xor_sync(kFullMask, l, 8);
+                l += __shfl_xor_sync(kFullMask, l, 16);
+                if (r == 0) {
+                    sm[8 * n + 2 * c + e] = st.m[n][e];
+                    sl[8 * n + 2 * c + e] = l;
+                }
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    so[(8 * n + 2 * c + (e & 1)) * D + 16 * mt + r + 8 * (e >> 1)] = st.o[mt][n][e];
+        }
+    }
+
+    __device__ static void rescale(State &st, int n, const float (&alpha)[2])
+    {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            st.o[mt][n][0] *= alpha[0];
+            st.o[mt][n][1] *= alpha[1];
+            st.o[mt][n][2] *= alpha[0];
+            st.o[mt][n][3] *= alpha[1];
+        }
+    }
+};
+
+// bf16 KV: the page tile is [D][16] bf16 (32-byte rows).  K^T fragments come
+// from ldmatrix.trans, V fragments from ldmatrix.  P is split into a bf16 high
+// part and a bf16 residual so that P V keeps ~16 mantissa bits.
+template <int D, int NT>
+struct MmaBf16Policy : MmaStateBase<D, NT> {
+    using Base = MmaStateBase<D, NT>;
+    using State = typename Base::State;
+    using RingT = Ring<PKV_BF16, D>;
+    static constexpr int R = RingT::R;
+    static constexpr int kTileBytes = RingT::kTileBytes;
+    static constexpr int kStageBytes = RingT::kStageBytes;
+    static constexpr int kRingBytes = RingT::kRingBytes;
+    static constexpr int kDim = D;
+    static constexpr int GP = 8 * NT;
+    static constexpr int kExtraBytes = 0;
+    static constexpr int KS = Base::KS, MT = Base::MT;
+
+    __device__ static void begin(State &st, const DecodeParams &p, int s, int hkv, int lane,
+                                 unsigned char *)
+    {
+        Base::reset(st);
+        Base::template load_q_frags<false>(st, p, s, hkv, lane);
+    }
+
+    __device__ static void page(State &st, const unsigned char *sK, const unsigned char *sV,
+                                int valid, int lane, int, unsigned char *, float c)
+    {
+        const int r = lane >> 2, cc = lane & 3;
+        const int mi = lane >> 3, ri = lane & 7;
+        // ldmatrix row addresses.  K (.trans): matrix mi covers head_dim rows
+        // 8(mi>>1).. and token half mi&1.  V: rows 8(mi&1).., token half mi>>1.
+        const uint32_t ka = smem_u32(sK) + (ri + 8 * (mi >> 1)) * 32 + (mi & 1) * 16;
+        const uint32_t va = smem_u32(sV) + (ri + 8 * (mi & 1)) * 32 + (mi >> 1) * 16;
+
+        float sacc[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+            sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            uint32_t a[4];
+            ldsm_x4_t(a, ka + ks * 16 * 32);
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                mma_bf16(sacc[n], a, st.qf[ks][n][0], st.qf[ks][n][1]);
+        }
+
+        uint32_t bh0[NT], bh1[NT], bl0[NT], bl1[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            float pr[4], alpha[2];
+            MmaSoftmax::update(sacc[n], r, r + 8, valid, c, st.m[n], st.l[n], pr, alpha);
+            Base::rescale(st, n, alpha);
+            const uint32_t hx = pack_bf16(pr[0], pr[1]);
+            const uint32_t hy = pack_bf16(pr[2], pr[3]);
+            const uint32_t lx = pack_bf16(pr[0] - bf16_lo(hx), pr[1] - bf16_hi(hx));
+            const uint32_t ly = pack_bf16(pr[2] - bf16_lo(hy), pr[3] - bf16_hi(hy));
+            bh0[n] = movmatrix_t(hx);
+            bh1[n] = movmatrix_t(hy);
+            bl0[n] = movmatrix_t(lx);
+            bl1[n] = movmatrix_t(ly);
+        }
+
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if (valid < kBlockSize) {
+            mlo = (2 * cc < valid ? 0x0000ffffu : 0u) | (2 * cc + 1 < valid ? 0xffff0000u : 0u);
+            mhi = (8 + 2 * cc < valid ? 0x0000ffffu : 0u) |
+                  (9 + 2 * cc < valid ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            uint32_t a[4];
+            ldsm_x4(a, va + mt * 16 * 32);
+            a[0] &= mlo;
+            a[1] &= mlo;
+            a[2] &= mhi;
+            a[3] &= mhi;
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                mma_bf16(st.o[mt][n], a, bh0[n], bh1[n]);
+                mma_bf16(st.o[mt][n], a, bl0[n], bl1[n]);
+            }
+        }
+    }
+
+    __device__ static void finish(State &st, float *so, float *sm, float *sl, int lane)
+    {
+        Base::finish(st, so, sm, sl, lane);
+    }
+};
+
+// fp8-e5m2 KV: the page tile is [D][16] bytes (16-byte rows), read by
+// ldmatrix as 16-bit pairs; byte_perm widens each code to an f16 (the code
+// is the f16's high byte, exactly).  Token order inside a fragment is
+// permuted consistently on both operands (see the byte selectors).
+template <int D, int NT>
+struct MmaFp8Policy : MmaStateBase<D, NT> {
+    using Base = MmaStateBase<D, NT>;
+    using State = typename Base::State;
+    using RingT = Ring<PKV_FP8_E5M2, D>;
+    static constexpr int R = RingT::R;
+    static constexpr int kTileBytes = RingT::kTileBytes;
+    static constexpr int kStageBytes = RingT::kStageBytes;
+    static constexpr int kRingBytes = RingT::kRingBytes;
+    static constexpr int kDim = D;
+    static constexpr int GP = 8 * NT;
+    static constexpr int kExtraBytes = 0;
+    static constexpr int KS = Base::KS, MT = Base::MT;
+    static constexpr uint32_t kSelEven = 0x2404u;  // bytes 0, 2 -> high bytes of two f16
+    static constexpr uint32_t kSelOdd = 0x3414u;   // bytes 1, 3 -> high bytes of two f16
+
+    __device__ static void begin(State &st, const DecodeParams &p, int s, int hkv, int lane,
+                                 unsigned char *)
+    {
+        Base::reset(st);
+        Base::template load_q_frags<true>(st, p, s, hkv, lane);
+    }
+
+    __device__ static void page(State &st, const unsigned char *sK, const unsigned char *sV,
+                                int valid, int lane, int, unsigned char *, float c)
+    {
+        const int r = lane >> 2, cc = lane & 3;
+        const int mi = lane >> 3, ri = lane & 7;
+        // Both tiles: matrix mi of one ldmatrix.x4 is head_dim rows 8mi..8mi+7.
+        const uint32_t ka = smem_u32(sK) + (8 * mi + ri) * 16;
+        const uint32_t va = smem_u32(sV) + (8 * mi + ri) * 16;
+
+        // S^T: A row r <-> token 2r, row r+8 <-> token 2r+1.
+        float sacc[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+            sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+#pragma unroll
+        for (int kp = 0; kp < KS / 2; ++kp) {
+            uint32_t w[4];
+            ldsm_x4_t(w, ka + kp * 32 * 16);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t a[4] = {e5m2x2_to_f16x2(w[2 * h], kSelEven),
+                                       e5m2x2_to_f16x2(w[2 * h], kSelOdd),
+                                       e5m2x2_to_f16x2(w[2 * h + 1], kSelEven),
+                                       e5m2x2_to_f16x2(w[2 * h + 1], kSelOdd)};
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+                    mma_f16(sacc[n], a, st.qf[2 * kp + h][n][0], st.qf[2 * kp + h][n][1]);
+            }
+        }
+
+        // P^T: k slots (2c, 2c+1) <-> tokens (4c, 4c+2), (2c+8, 2c+9) <-> (4c+1, 4c+3).
+        uint32_t b0[NT], b1[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            float pr[4], alpha[2];
+            MmaSoftmax::update(sacc[n], 2 * r, 2 * r + 1, valid, c, st.m[n], st.l[n], pr, alpha);
+            Base::rescale(st, n, alpha);
+            b0[n] = movmatrix_t(pack_f16(pr[0], pr[1]));
+            b1[n] = movmatrix_t(pack_f16(pr[2], pr[3]));
+        }
+
+        uint32_t me = 0xffffffffu, mo = 0xffffffffu;
+        if (valid < kBlockSize) {
+            me = (4 * cc < valid ? 0x0000ffffu : 0u) | (4 * cc + 2 < valid ? 0xffff0000u : 0u);
+            mo = (4 * cc + 1 < valid ? 0x0000ffffu : 0u) |
+                 (4 * cc + 3 < valid ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int mp = 0; mp < MT / 2; ++mp) {
+            uint32_t w[4];
+            ldsm_x4(w, va + mp * 32 * 16);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t a[4] = {e5m2x2_to_f16x2(w[2 * h], kSelEven) & me,
+                                       e5m2x2_to_f16x2(w[2 * h + 1], kSelEven) & me,
+                                       e5m2x2_to_f16x2(w[2 * h], kSelOdd) & mo,
+                                       e5m2x2_to_f16x2(w[2 * h + 1], kSelOdd) & mo};
+#pragma unroll
+                for (int n = 0; n < NT; ++n)
+                    mma_f16(st.o[2 * mp + h][n], a, b0[n], b1[n]);
+            }
+        }
+    }
+
+    __device__ static void finish(State &st, float *so, float *sm, float *sl, int lane)
+    {
+        Base::finish(st, so, sm, sl, lane);
+    }
+};
+
+// ==================================================================== kernel
+
+// A length outside [0, max_len] is reported and clamped, so no item reads
+// past the table or writes past the workspace's partial rows.
+__device__ __forceinline__ int clamp_len(const DecodeParams &p, int L)
+{
+    const int maxL = p.max_len;
+    if (L < 0 || L > maxL) {
+        set_status(p.status, PKV_ERR_OUT_OF_RANGE);
+        L = L < 0 ? 0 : maxL;
+    }
+    return L;
+}
+
+__device__ __forceinline__ int parts_of(int L, int P) { return L > P ? (L + P - 1) / P : 1; }
+
+// Writes the merged result of one item: the four warps' (m, l, O) sit at the
+// start of each warp's ring.
+template <int D, int GP>
+__device__ void merge_item(const DecodeParams &p, const unsigned char *smem, int ring_bytes, int s,
+                           int hkv, int part, int nparts)
+{
+    constexpr int Q4 = D / 4;
+    const int G = p.group;
+    for (int idx = threadIdx.x; idx < G * Q4; idx += kThreads) {
+        const int g = idx / Q4, q4 = idx - g * Q4;
+        float mw[kWarps], mx = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float *sm = reinterpret_cast<const float *>(smem + w * ring_bytes) + GP * D;
+            mw[w] = sm[g];
+            mx = fmaxf(mx, mw[w]);
+        }
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float *so = reinterpret_cast<const float *>(smem + w * ring_bytes);
+            const float f = (mw[w] == -INFINITY) ? 0.f : exp2f(mw[w] - mx);
+            const float4 o = reinterpret_cast<const float4 *>(so + g * D)[q4];
+            acc.x += f * o.x;
+            acc.y += f * o.y;
+            acc.z += f * o.z;
+            acc.w += f * o.w;
+            lsum += f * so[GP * D + GP + g];
+        }
+        const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+        const int h = hkv * G + g;
+        if (nparts == 1) {
+            const float sc = inv * p.out_scale;
+            const size_t off = (static_cast<size_t>(s) * p.num_q_heads + h) * D + 4 * q4;
+            if (p.out_dtype == PKV_F32) {
+                *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) =
+                    make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
+            } else {
+                uint2 w;
+                w.x = pack_bf16(acc.x * sc, acc.y * sc);
+                w.y = pack_bf16(acc.z * sc, acc.w * sc);
+                *reinterpret_cast<uint2 *>(static_cast<unsigned short *>(p.out) + off) = w;
+            }
+        } else {
+            const size_t row = (static_cast<size_t>(s) * p.num_q_heads + h) * p.max_parts + part;
+            reinterpret_cast<float4 *>(p.part_o + row * D)[q4] =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            if (q4 == 0) {
+                p.part_ml[2 * row] = mx;
+                p.part_ml[2 * row + 1] = lsum;
+            }
+        }
+    }
+}
+
+template <class Pol>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams p)
+{
+    constexpr int D = Pol::kDim;
+    static_assert((Pol::GP * D + 2 * Pol::GP) * 4 <= Pol::kRingBytes,
+                  "merge scratch must fit in one warp's ring");
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_item[8];
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    unsigned char *ring = smem + warp * Pol::kRingBytes;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kWarps * Pol::kRingBytes) + warp * Pol::R;
+    unsigned char *extra = smem + kWarps * Pol::kRingBytes + kWarps * Pol::R * sizeof(uint64_t);
+
+    if (lane == 0)
+        for (int st = 0; st < Pol::R; ++st)
+            mbar_init(&bars[st], 1);
+    if (threadIdx.x == 0)
+        s_abort = 0;
+    fence_mbar_init();
+    __syncthreads();
+
+    const int Hkv = p.num_kv_heads;
+    const int S = p.num_seqs;
+    const int P = p.partition;
+    const size_t tile_stride = static_cast<size_t>(Pol::kTileBytes);
+    const size_t block_stride = static_cast<size_t>(Hkv) * tile_stride;
+    const float c = p.score_scale;
+
+    uint32_t pages_done = 0;  // pages this warp has consumed (ring position / phase)
+    int cur_s = 0, cur_base = 0;  // warp 0: scan cursor over sequences (split mode)
+    bool first = true;
+
+    for (;;) {
+        // ---------------------------------------------- next work item
+        if (warp == 0) {
+            int s = 0, part = 0, hkv = 0, L = 0, nparts = 1, item = 0, done = 0;
+            if (p.split) {
+                unsigned v = 0;
+                if (lane == 0)
+                    v = atomicAdd(p.counter, 1u);
+                item = static_cast<int>(__shfl_sync(kFullMask, v, 0));
+                const int u = item / Hkv;
+                hkv = item - u * Hkv;
+                for (;;) {
+                    const int sl = cur_s + lane;
+                    int n = 0, Ls = 0;
+                    if (sl < S) {
+                        Ls = clamp_len(p, __ldg(p.seq_lens + sl));
+                        n = parts_of(Ls, P);
+                    }
+                    int incl = n;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const int t = __shfl_up_sync(kFullMask, incl, off);
+                        if (lane >= off)
+                            incl += t;
+                    }
+                    const int tot = __shfl_sync(kFullMask, incl, 31);
+                    if (u < cur_base + tot) {
+                        const unsigned bal = __ballot_sync(kFullMask, cur_base + incl > u);
+                        const int ln = __ffs(bal) - 1;
+                        const int excl = __shfl_sync(kFullMask, incl - n, ln);
+                        s = cur_s + ln;
+                        part = u - cur_base - excl;
+                        L = __shfl_sync(kFullMask, Ls, ln);
+                        nparts = __shfl_sync(kFullMask, n, ln);
+                        break;
+                    }
+                    if (cur_s + 32 >= S) {
+                        done = 1;
+                        break;
+                    }
+                    cur_base += tot;
+                    cur_s += 32;
+                }
+            } else {
+                item = first ? static_cast<int>(blockIdx.x) : INT_MAX;
+                if (item >= S * Hkv) {
+                    done = 1;
+                } else {
+                    s = item / Hkv;
+                    hkv = item - s * Hkv;
+                    L = clamp_len(p, __ldg(p.seq_lens + s));
+                }
+            }
+            if (lane == 0) {
+                s_item[0] = s;
+                s_item[1] = part;
+                s_item[2] = hkv;
+                s_item[3] = L;
+                s_item[4] = nparts;
+                s_item[5] = item;
+                s_item[6] = done;
+            }
+        }
+        first = false;
+        __syncthreads();
+        if (s_item[6])
+            break;
+        const int s = s_item[0], part = s_item[1], hkv = s_item[2], L = s_item[3];
+        const int nparts = s_item[4], item = s_item[5];
+
+        // ---------------------------------------------- this warp's pages
+        const int t0 = part * P;
+        const int t1 = min(L, t0 + P);
+        const int pg0 = t0 / kBlockSize;
+        const int npages = t1 > t0 ? (t1 - t0 + kBlockSize - 1) / kBlockSize : 0;
+        const int nw = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;
+        const int32_t *bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks + pg0 + warp;
+        const size_t head_off = static_cast<size_t>(hkv) * tile_stride;
+
+        int id_reg = -1, id_chunk = -1;
+        uint32_t okmask = 0;
+        // Warp-collective: physical id of this warp's page i (32 ids per load).
+        auto page_id = [&](int i) -> int {
+            const int ch = i >> 5;
+            if (ch != id_chunk) {
+                const int j = (ch << 5) + lane;
+                id_reg = j < nw ? __ldg(bt + kWarps * j) : -1;
+                id_chunk = ch;
+            }
+            return __shfl_sync(kFullMask, id_reg, i & 31);
+        };
+        auto issue = [&](int i) {
+            const int phys = page_id(i);
+            const int stg = (pages_done + i) % Pol::R;
+            const bool ok = phys >= 0 && phys < p.num_blocks;
+            okmask = ok ? (okmask | (1u << stg)) : (okmask & ~(1u << stg));
+            if (lane == 0) {
+                uint64_t *bar = &bars[stg];
+                if (!ok) {
+                    set_status(p.status, PKV_ERR_OUT_OF_RANGE);
+                    mbar_arrive(bar);
+                } else {
+                    mbar_arrive_expect_tx(bar, 2 * Pol::kTileBytes);
+                    const bool drop = p.drop_first_copy && item == 0 && warp == 0 && i == 0;
+                    if (!drop) {
+                        const size_t off = static_cast<size_t>(phys) * block_stride + head_off;
+                        unsigned char *dst = ring + stg * Pol::kStageBytes;
+                        bulk_g2s(dst, static_cast<const unsigned char *>(p.k_cache) + off,
+                                 Pol::kTileBytes, bar);
+                        bulk_g2s(dst + Pol::kTileBytes,
+                                 static_cast<const unsigned char *>(p.v_cache) + off,
+                                 Pol::kTileBytes, bar);
+                    }
+                }
+            }
+        };
+
+        int issued = 0;
+        const int pre = nw < Pol::R ? nw : Pol::R;
+        for (; issued < pre; ++issued)
+            issue(issued);
+
+        typename Pol::State st;
+        Pol::begin(st, p, s, hkv, lane, extra);
+        __syncthreads();  // policy shared data (SIMT query) is ready
+
+        for (int i = 0; i < nw; ++i) {
+            const uint32_t n = pages_done + i;
+            const int stg = n % Pol::R;
+            const uint32_t parity = (n / Pol::R) & 1u;
+            const bool ok = mbar_wait_bounded(&bars[stg], parity, kWaitLimitNs);
+            if (!__all_sync(kFullMask, ok)) {
+                if (lane == 0) {
+                    set_status(p.status, PKV_ERR_TIMEOUT);
+                    atomicExch(&s_abort, 1);
+                }
+                // Let every other copy already in flight land before leaving.
+                for (int j = i + 1; j < issued; ++j) {
+                    const uint32_t n2 = pages_done + j;
+                    mbar_wait_bounded(&bars[n2 % Pol::R], (n2 / Pol::R) & 1u, kWaitLimitNs);
+                }
+                break;
+            }
+            if ((okmask >> stg) & 1u) {
+                const int tok0 = (pg0 + warp + kWarps * i) * kBlockSize;
+                const int valid = min(kBlockSize, t1 - tok0);
+                const unsigned char *sk = ring + stg * Pol::kStageBytes;
+                Pol::page(st, sk, sk + Pol::kTileBytes, valid, lane, warp, extra, c);
+            }
+            fence_proxy_async();
+            __syncwarp();
+            if (issued < nw) {
+                issue(issued);
+                ++issued;
+            }
+        }
+        pages_done += nw;
+
+        // ---------------------------------------------- merge the warps
+        {
+            float *so = reinterpret_cast<float *>(ring);
+            float *sm = so + Pol::GP * D;
+            float *sl = sm + Pol::GP;
+            Pol::finish(st, so, sm, sl, lane);
+        }
+        __syncthreads();
+        merge_item<D, Pol::GP>(p, smem, Pol::kRingBytes, s, hkv, part, nparts);
+        // The rings were used as generic scratch: order that before the next
+        // item's bulk copies into them.
+        fence_proxy_async();
+        __syncthreads();
+        if (*static_cast<volatile int *>(&s_abort))
+            break;
+    }
+}
+
+template <class Pol>
+constexpr int decode_smem_bytes()
+{
+    return kWarps * Pol::kRingBytes + kWarps * Pol::R * 8 + Pol::kExtraBytes;
+}
+
+// Launches decode_kernel<Pol>: one CTA per item without split, else a
+// persistent grid sized from the occupancy of this instantiation.
+template <class Pol>
+pkv_status launch_policy(const DecodeParams &p, cudaStream_t stream)
+{
+    constexpr int smem = decode_smem_bytes<Pol>();
+    static int occ = -1;  // resident CTAs per SM (per process; one device type)
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(decode_kernel<Pol>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        attr_set = true;
+    }
+    long grid;
+    if (p.split) {
+        if (occ < 0) {
+            int o = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<Pol>, kThreads,
+                                                              smem) != cudaSuccess)
+                return PKV_ERR_CUDA;
+            occ = o > 0 ? o : 1;
+        }
+        const long items = static_cast<long>(p.num_seqs) * p.num_kv_heads * p.max_parts;
+        const long slots = static_cast<long>(occ) * device_sm_count();
+        grid = items < slots ? items : slots;
+    } else {
+        grid = static_cast<long>(p.num_seqs) * p.num_kv_heads;
+    }
+    if (grid <= 0)
+        return PKV_OK;
+    decode_kernel<Pol><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace pkv

@@ -1,0 +1,33 @@
+// Tensor-core (mma.sync) decode kernels: bf16 and fp8-e5m2 KV with a bf16
+// query, head_dim 64/128, up to 16 query heads per KV head (one or two
+// 8-wide N tiles).
+#include "pkv_decode.cuh"
+
+namespace pkv {
+
+bool mma_supports(int kv_dtype, int q_dtype, int head_dim, int group)
+{
+    return (kv_dtype == PKV_BF16 || kv_dtype == PKV_FP8_E5M2) && q_dtype == PKV_BF16 &&
+           (head_dim == 64 || head_dim == 128) && group >= 1 && group <= 16;
+}
+
+template <int D>
+static pkv_status dispatch(const DecodeParams &p, int kv_dtype, cudaStream_t stream)
+{
+    const bool two = p.group > 8;
+    if (kv_dtype == PKV_BF16)
+        return two ? launch_policy<MmaBf16Policy<D, 2>>(p, stream)
+                   : launch_policy<MmaBf16Policy<D, 1>>(p, stream);
+    return two ? launch_policy<MmaFp8Policy<D, 2>>(p, stream)
+               : launch_policy<MmaFp8Policy<D, 1>>(p, stream);
+}
+
+pkv_status launch_decode_mma(const DecodeParams &p, int kv_dtype, cudaStream_t stream)
+{
+    if (!mma_supports(kv_dtype, p.q_dtype, p.head_dim, p.group))
+        return PKV_ERR_UNSUPPORTED;
+    return p.head_dim == 64 ? dispatch<64>(p, kv_dtype, stream)
+                            : dispatch<128>(p, kv_dtype, stream);
+}
+
+}  // namespace pkv

@@ -1,0 +1,56 @@
+// Internal interface between the C ABI (pkv_api.cu) and the kernel units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/pkv.h"
+
+namespace pkv {
+
+// Everything a decode launch needs; passed by value as the kernel parameter.
+struct DecodeParams {
+    const void *q;
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    void *out;
+    float *part_o;        // [S][Hq][max_parts][D] normalised partial outputs
+    float *part_ml;       // [S][Hq][max_parts][2] (max of log2-scaled scores, sum)
+    int *status;          // workspace word 0
+    unsigned *counter;    // workspace word 1: next work item (split mode)
+    int q_dtype, out_dtype;
+    int num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks;
+    int max_len;          // caller's bound on seq_lens (<= max_blocks * 16)
+    int group;            // query heads per KV head
+    float score_scale;    // scale * log2(e) (* k_scale for fp8)
+    float out_scale;      // v_scale for fp8, else 1
+    int partition;        // tokens per work item (multiple of 16)
+    int max_parts;        // partitions per sequence the workspace holds
+    int split;            // 1: persistent grid, work counter, partials + merge
+    int drop_first_copy;  // test hook: never issue the first copy of item 0
+};
+
+constexpr int kBlockSize = 16;
+constexpr size_t kWorkspaceHeader = 256;
+
+// Kernel-unit entry points.  Each launches on `stream` and returns a status
+// (PKV_OK, PKV_ERR_UNSUPPORTED for a shape with no kernel, PKV_ERR_CUDA).
+// `grid_items` is the number of CTAs to launch (0 = let the unit decide).
+pkv_status launch_decode_simt(const DecodeParams &p, int kv_dtype, cudaStream_t stream);
+pkv_status launch_decode_mma(const DecodeParams &p, int kv_dtype, cudaStream_t stream);
+pkv_status launch_merge(const DecodeParams &p, cudaStream_t stream);
+bool mma_supports(int kv_dtype, int q_dtype, int head_dim, int group);
+
+pkv_status launch_reshape_and_cache(const void *k, const void *v, int in_dtype,
+                                    const int64_t *slot_mapping, int num_tokens,
+                                    int num_kv_heads, int head_dim, int num_blocks,
+                                    void *k_cache, void *v_cache, int kv_dtype, float k_scale,
+                                    float v_scale, int32_t *status, cudaStream_t stream);
+
+int device_sm_count();
+
+}  // namespace pkv

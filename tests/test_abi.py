@@ -1,0 +1,145 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/pkv.h declares, plans workspaces, and rejects bad arguments
+before it touches CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_225_gb300 as pkv
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+OK, INVALID, UNSUPPORTED, CUDA, OOR, TIMEOUT, WORKSPACE = range(7)
+F32, BF16, FP8 = pkv.F32, pkv.BF16, pkv.FP8_E5M2
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        txt = open(h).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        txt = re.sub(r"//[^\n]*", "", txt)
+        names += re.findall(r"\b(pkv_\w+)\s*\(", txt)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("pkv_paged_attn_decode", "pkv_reshape_and_cache",
+                     "pkv_paged_attn_workspace_size", "pkv_read_status", "pkv_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol():
+    L = pkv.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in include/*.h but not exported"
+
+
+def test_status_strings_and_version():
+    L = pkv.lib()
+    for code in range(7):
+        assert L.pkv_status_string(code).decode().startswith(pkv.STATUS[code])
+    assert L.pkv_version() >= 100
+
+
+def test_partition_plan():
+    P = pkv.partition_tokens
+    assert P(4, 4, 4, 64, 65, -1) == 0
+    assert P(4, 4, 4, 64, 65, 48) == 48
+    assert P(4, 4, 4, 64, 65, 40) == -1           # not a multiple of the block size
+    assert P(128, 64, 8, 128, 514, 0) == 0          # 1024 units, short context: one pass
+    assert P(128, 64, 8, 128, 14626, 0) == 512      # 70B-shaped layer
+    assert P(8, 64, 8, 128, 32769, 0) == 512        # long context: split
+    assert P(1, 8, 8, 128, 512, 0) == 64            # few units: small partitions
+
+
+def test_workspace_size():
+    W = pkv.workspace_size
+    assert W(4, 4, 4, 64, 65, -1) == 256
+    S, Hq, D, P, L = 8, 64, 128, 512, 32769
+    parts = -(-L // P)
+    rows = S * Hq * parts
+
+    def a(x):
+        return (x + 255) // 256 * 256
+    assert W(S, Hq, 8, D, L, P) == 256 + a(rows * D * 4) + a(rows * 8)
+    with pytest.raises(ValueError):
+        W(4, 6, 4, 64, 65, 0)                       # heads do not divide
+
+
+def _decode(**kw):
+    args = dict(q=0x1000, q_dtype=BF16, k=0x2000, v=0x3000, kv_dtype=BF16, ks=1.0, vs=1.0,
+                bt=0x4000, sl=0x5000, S=2, Hq=8, Hkv=2, D=128, B=16, N=10, maxb=4, maxl=64,
+                scale=0.1, out=0x6000, out_dtype=F32, ws=0x7000, wsb=1 << 20, part=0, flags=0)
+    args.update(kw)
+    return pkv.lib().pkv_paged_attn_decode(
+        args["q"], args["q_dtype"], args["k"], args["v"], args["kv_dtype"], args["ks"], args["vs"],
+        args["bt"], args["sl"], args["S"], args["Hq"], args["Hkv"], args["D"], args["B"], args["N"],
+        args["maxb"], args["maxl"], args["scale"], args["out"], args["out_dtype"], args["ws"],
+        args["wsb"], args["part"], args["flags"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hq=6, Hkv=4), INVALID),
+    (dict(D=96), UNSUPPORTED),
+    (dict(B=32), UNSUPPORTED),
+    (dict(Hq=34, Hkv=2), UNSUPPORTED),            # 17 query heads per KV head
+    (dict(q_dtype=FP8), UNSUPPORTED),
+    (dict(out_dtype=FP8), UNSUPPORTED),
+    (dict(kv_dtype=7), UNSUPPORTED),
+    (dict(maxl=65), INVALID),                     # longer than the table allows
+    (dict(ws=0), WORKSPACE),
+    (dict(ws=0x7010), WORKSPACE),                 # not 256-byte aligned
+    (dict(wsb=100), WORKSPACE),
+    (dict(q=0), INVALID),
+    (dict(k=0x2008), INVALID),                    # misaligned cache
+    (dict(bt=0x4002), INVALID),
+    (dict(part=40), INVALID),
+    (dict(flags=0x3), INVALID),
+    (dict(flags=0x40), INVALID),
+    (dict(flags=0x2, kv_dtype=F32), UNSUPPORTED),  # tensor cores need bf16/fp8 KV
+    (dict(flags=0x2, q_dtype=F32), UNSUPPORTED),
+    (dict(scale=float("nan")), INVALID),
+    (dict(S=0), OK),                              # nothing to do, nothing enqueued
+])
+def test_decode_argument_errors(kw, code):
+    assert _decode(**kw) == code
+
+
+def _cache(**kw):
+    args = dict(k=0x1000, v=0x2000, in_dtype=BF16, slots=0x3000, T=4, Hkv=2, D=128, B=16, N=8,
+                kc=0x4000, vc=0x5000, kv_dtype=BF16, ks=1.0, vs=1.0, status=None)
+    args.update(kw)
+    return pkv.lib().pkv_reshape_and_cache(
+        args["k"], args["v"], args["in_dtype"], args["slots"], args["T"], args["Hkv"], args["D"],
+        args["B"], args["N"], args["kc"], args["vc"], args["kv_dtype"], args["ks"], args["vs"],
+        args["status"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(in_dtype=FP8), UNSUPPORTED),
+    (dict(kv_dtype=9), UNSUPPORTED),
+    (dict(B=8), UNSUPPORTED),
+    (dict(k=0), INVALID),
+    (dict(slots=0x3004), INVALID),
+    (dict(kc=0x4004), INVALID),
+    (dict(kv_dtype=FP8, ks=0.0), INVALID),
+    (dict(T=-1), INVALID),
+    (dict(T=0), OK),
+])
+def test_reshape_argument_errors(kw, code):
+    assert _cache(**kw) == code
+
+
+def test_binding_rejects_cpu_tensors_without_fallback():
+    import torch
+    q = torch.zeros(1, 1, 64)
+    kc = torch.zeros(1, 1, 64, 16)
+    with pytest.raises((ValueError, RuntimeError, TypeError)):
+        pkv.paged_attn_decode(q, kc, kc, torch.zeros(1, 1, dtype=torch.int32),
+                              torch.ones(1, dtype=torch.int32), 0.125, torch.empty_like(q))

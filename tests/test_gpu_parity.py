@@ -1,0 +1,251 @@
+"""GPU parity: the CUDA path against the fp64 oracle, element by element.
+
+All five benchmark layers at full size (decode step = cache write of one new
+token per sequence, then attention over the grown sequences), both kernel
+families, forced split sizes, edge lengths, head groupings, dtypes, garbage
+in unowned slots, and the device-side error reports.
+"""
+import dataclasses
+import functools
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_225_gb300 as pkv
+from paged_kv_cache_225_gb300 import workloads as W
+
+from gpu_util import TOL, bits, device_workload, gpu_step, max_abs, oracle_step, to_torch
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+@functools.lru_cache(maxsize=2)
+def _config(name):
+    w = W.make_workload(name)
+    ref, kc, vc = oracle_step(w)
+    return w, ref, kc, vc
+
+
+@pytest.mark.parametrize("name", W.CONFIG_ORDER)
+def test_config_parity_auto(name):
+    w, ref, kc, vc = _config(name)
+    d = device_workload(w, DEV)
+    out, status, _ = gpu_step(w, d)
+    assert status == 0
+    # The cache write is bit-exact over the whole pools.
+    assert np.array_equal(bits(d["k_cache"]), kc.view(np.uint8).reshape(-1))
+    assert np.array_equal(bits(d["v_cache"]), vc.view(np.uint8).reshape(-1))
+    err = max_abs(out, ref)
+    assert err <= TOL[w.cfg.kv_dtype], f"{name}: max-abs {err}"
+
+
+@pytest.mark.parametrize("name", W.CONFIG_ORDER)
+def test_config_parity_simt(name):
+    w, ref, kc, vc = _config(name)
+    d = device_workload(w, DEV)
+    out, status, _ = gpu_step(w, d, impl="simt")
+    assert status == 0
+    err = max_abs(out, ref)
+    assert err <= TOL[w.cfg.kv_dtype], f"{name}: max-abs {err}"
+
+
+@pytest.mark.parametrize("name", ["llama3_8b", "long_split", "fp8_chat"])
+@pytest.mark.parametrize("part", [-1, 16, 48, 256, 4096])
+def test_config_parity_forced_split(name, part):
+    w, ref, kc, vc = _config(name)
+    d = device_workload(w, DEV)
+    out, status, _ = gpu_step(w, d, partition_tokens=part)
+    assert status == 0
+    assert max_abs(out, ref) <= TOL[w.cfg.kv_dtype]
+
+
+def _custom(base="llama3_8b", seed=100, lens=None, **kw):
+    cfg = dataclasses.replace(W.CONFIGS[base], name="custom", **kw)
+    return W.make_workload(cfg, seed=seed, seq_lens=lens)
+
+
+EDGE_LENS = [0, 1, 15, 16, 17, 31, 33, 100, 511, 512, 513, 1000]
+
+
+@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2, W.F32])
+@pytest.mark.parametrize("impl", ["auto", "simt"])
+@pytest.mark.parametrize("part", [0, -1, 32, 48])
+def test_edge_lengths_with_nan_garbage(kv_dtype, impl, part):
+    q_dtype = W.F32 if kv_dtype == W.F32 else W.BF16
+    w = _custom(num_seqs=len(EDGE_LENS), num_q_heads=16, num_kv_heads=2, q_dtype=q_dtype,
+                kv_dtype=kv_dtype, garbage="nan", lens=np.array(EDGE_LENS))
+    ref, _, _ = oracle_step(w)
+    d = device_workload(w, DEV)
+    out, status, _ = gpu_step(w, d, impl=impl, partition_tokens=part)
+    assert status == 0
+    assert np.isfinite(out).all()
+    assert max_abs(out, ref) <= TOL[kv_dtype]
+
+
+@pytest.mark.parametrize("group", [1, 2, 3, 4, 5, 8, 12, 16])
+@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2])
+@pytest.mark.parametrize("head_dim", [64, 128])
+@pytest.mark.parametrize("impl", ["mma", "simt"])
+def test_head_groups_and_dims(group, kv_dtype, head_dim, impl):
+    w = _custom(num_seqs=5, num_q_heads=2 * group, num_kv_heads=2, head_dim=head_dim,
+                kv_dtype=kv_dtype, len_lo=1, len_hi=700, seed=group)
+    ref, _, _ = oracle_step(w)
+    d = device_workload(w, DEV)
+    for part in (0, 64):
+        out, status, _ = gpu_step(w, d, impl=impl, partition_tokens=part, append=False)
+        assert status == 0
+        ref_noappend = oracle.paged_decode(w.q, w.cfg.q_dtype, w.k_cache, w.v_cache, kv_dtype,
+                                           w.block_tables, w.seq_lens, w.scale)
+        assert max_abs(out, ref_noappend) <= TOL[kv_dtype]
+
+
+def test_fp32_kv_groups():
+    for group in (1, 4, 16):
+        w = _custom(num_seqs=4, num_q_heads=2 * group, num_kv_heads=2, head_dim=64,
+                    q_dtype=W.F32, kv_dtype=W.F32, len_lo=1, len_hi=300, seed=7 + group)
+        ref, _, _ = oracle_step(w)
+        d = device_workload(w, DEV)
+        out, status, _ = gpu_step(w, d)
+        assert status == 0
+        assert max_abs(out, ref) <= 1e-5
+
+
+def test_bf16_kv_with_fp32_query_uses_cuda_cores():
+    w = _custom(num_seqs=6, q_dtype=W.F32, kv_dtype=W.BF16, len_lo=1, len_hi=900)
+    ref, _, _ = oracle_step(w)
+    d = device_workload(w, DEV)
+    out, status, _ = gpu_step(w, d)
+    assert status == 0 and max_abs(out, ref) <= 4e-3
+    with pytest.raises(pkv.PkvError):
+        gpu_step(w, d, impl="mma", append=False)
+
+
+@pytest.mark.parametrize("scale", [0.5, 2.0, 0.3])
+def test_fp8_scales(scale):
+    w = _custom(base="fp8_chat", num_seqs=16, kv_scale=scale, len_lo=256, len_hi=512)
+    ref, kc, vc = oracle_step(w)
+    d = device_workload(w, DEV)
+    out, status, _ = gpu_step(w, d)
+    assert status == 0
+    assert np.array_equal(bits(d["k_cache"]), kc.view(np.uint8).reshape(-1))
+    assert max_abs(out, ref) <= 3e-2 * max(1.0, scale)
+
+
+def test_bf16_output_within_one_ulp():
+    w, ref, kc, vc = _config("llama3_8b")
+    d = device_workload(w, DEV)
+    out, status, _ = gpu_step(w, d, out_dtype=torch.bfloat16)
+    assert status == 0
+    ref_b = torch.from_numpy(ref.astype(np.float32)).to(torch.bfloat16).float().numpy()
+    ulp = np.abs(ref_b) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(out - ref_b) <= ulp + TOL[W.BF16])
+
+
+def test_long_sequence_32768_single_pass_and_split():
+    w = _custom(num_seqs=2, num_q_heads=16, num_kv_heads=2, len_dist="const", len_lo=32768,
+                len_hi=32768, heavy_key_frac=0.01, seed=5)
+    ref, _, _ = oracle_step(w)
+    d = device_workload(w, DEV)
+    a, st_a, _ = gpu_step(w, d, partition_tokens=-1)
+    b, st_b, _ = gpu_step(w, d, partition_tokens=512, append=False)
+    assert st_a == 0 and st_b == 0
+    assert max_abs(a, ref) <= 4e-3 and max_abs(b, ref) <= 4e-3
+
+
+def test_results_are_deterministic():
+    w, ref, _, _ = _config("llama3_8b")
+    d = device_workload(w, DEV)
+    a, _, _ = gpu_step(w, d)
+    b, _, _ = gpu_step(w, d, append=False)
+    assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------ cache write
+
+@pytest.mark.parametrize("in_dtype,kv_dtype,scale", [
+    (W.F32, W.F32, 1.0), (W.F32, W.BF16, 1.0), (W.BF16, W.BF16, 1.0), (W.BF16, W.F32, 1.0),
+    (W.BF16, W.FP8_E5M2, 1.0), (W.F32, W.FP8_E5M2, 0.25), (W.BF16, W.FP8_E5M2, 3.0)])
+def test_reshape_and_cache_bit_exact(in_dtype, kv_dtype, scale):
+    rng = np.random.default_rng(31)
+    N, Hkv, D, B, T = 40, 4, 128, 16, 97
+    k_cache = W.round_to_storage(rng.standard_normal((N, Hkv, D, B)).astype(np.float32), kv_dtype)
+    v_cache = W.round_to_storage(rng.standard_normal((N, Hkv, D, B)).astype(np.float32), kv_dtype)
+    big = rng.standard_normal((T, Hkv, D)).astype(np.float32) * \
+        np.float32(2.0) ** rng.integers(-20, 17, (T, Hkv, D)).astype(np.float32)
+    kin = W.round_to_storage(big, in_dtype)
+    vin = W.round_to_storage(rng.standard_normal((T, Hkv, D)).astype(np.float32), in_dtype)
+    slots = rng.choice(N * B, size=T, replace=False).astype(np.int64)
+    slots[::7] = -1
+    kc, vc = k_cache.copy(), v_cache.copy()
+    assert oracle.reshape_and_cache(kin, vin, in_dtype, slots, kc, vc, kv_dtype, scale, scale) == 0
+    dk, dv = to_torch(k_cache, kv_dtype).to(DEV), to_torch(v_cache, kv_dtype).to(DEV)
+    pkv.reshape_and_cache(to_torch(kin, in_dtype).to(DEV), to_torch(vin, in_dtype).to(DEV),
+                          torch.from_numpy(slots).to(DEV), dk, dv, k_scale=scale, v_scale=scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(dk), kc.view(np.uint8).reshape(-1))
+    assert np.array_equal(bits(dv), vc.view(np.uint8).reshape(-1))
+
+
+def test_reshape_and_cache_out_of_pool_slot_is_reported_and_skipped():
+    N, Hkv, D = 4, 2, 64
+    kc = torch.zeros(N, Hkv, D, 16, device=DEV)
+    vc = torch.zeros_like(kc)
+    k = torch.ones(2, Hkv, D, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    slots = torch.tensor([N * 16 + 3, 5], dtype=torch.int64, device=DEV)
+    pkv.reshape_and_cache(k, k, slots, kc, vc, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 4
+    assert float(kc.sum()) == Hkv * D        # only slot 5 was written
+
+
+# ------------------------------------------------------- device-side errors
+
+def test_out_of_range_block_id_is_reported_not_trapped():
+    w = _custom(num_seqs=4, len_lo=40, len_hi=80, seed=9)
+    d = device_workload(w, DEV)
+    bt = d["block_tables"].clone()
+    bt[1, 0] = w.num_blocks + 1000
+    out = torch.empty(d["q"].shape, dtype=torch.float32, device=DEV)
+    pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], bt, d["seq_lens"], w.scale, out,
+                          max_seq_len=int(w.seq_lens.max()))
+    torch.cuda.synchronize()
+    assert pkv.read_status(device=DEV) == 4
+    ref = oracle.paged_decode(w.q, w.cfg.q_dtype, w.k_cache, w.v_cache, w.cfg.kv_dtype,
+                              w.block_tables, w.seq_lens, w.scale)
+    o = out.cpu().numpy()
+    for s in (0, 2, 3):
+        assert max_abs(o[s], ref[s]) <= 4e-3
+
+
+def test_seq_len_past_table_is_reported():
+    w = _custom(num_seqs=3, len_lo=20, len_hi=40, seed=10)
+    d = device_workload(w, DEV)
+    lens = d["seq_lens"].clone()
+    lens[0] = w.max_blocks_per_seq * 16 + 5
+    out = torch.empty(d["q"].shape, dtype=torch.float32, device=DEV)
+    pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], lens, w.scale,
+                          out)
+    torch.cuda.synchronize()
+    assert pkv.read_status(device=DEV) == 4
+
+
+@pytest.mark.parametrize("part", [0, 64])
+def test_bounded_wait_reports_timeout_and_context_survives(part):
+    w = _custom(num_seqs=3, len_lo=100, len_hi=200, seed=12)
+    d = device_workload(w, DEV)
+    out = torch.empty(d["q"].shape, dtype=torch.float32, device=DEV)
+    pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["seq_lens"],
+                          w.scale, out, max_seq_len=int(w.seq_lens.max()), partition_tokens=part,
+                          flags=pkv.FLAG_TEST_DROP_FIRST_COPY)
+    torch.cuda.synchronize()
+    assert pkv.read_status(device=DEV) == 5
+    # The context is still usable: a normal call afterwards is correct.
+    out2, status, _ = gpu_step(w, d, append=False)
+    ref = oracle.paged_decode(w.q, w.cfg.q_dtype, w.k_cache, w.v_cache, w.cfg.kv_dtype,
+                              w.block_tables, w.seq_lens, w.scale)
+    assert status == 0 and max_abs(out2, ref) <= 4e-3
