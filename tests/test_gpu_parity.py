@@ -160,7 +160,7 @@ def test_results_are_deterministic():
     w, ref, _, _ = _config("llama3_8b")
     d = device_workload(w, DEV)
     a, _, _ = gpu_step(w, d)
-    b, _, _ = gpu_step(w, d, append=False)
+    b, _, _ = gpu_step(w, d)      # rewrites the same slots, attends the same L+1 tokens
     assert np.array_equal(a, b)
 
 
