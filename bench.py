@@ -113,6 +113,24 @@ def workload_text(name: str) -> str:
     return CONFIG_TEXT[name]
 
 
+def max_over_ranks(x: float) -> float:
+    """Max of a host float over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    dev = torch.device("cuda", torch.cuda.current_device()) \
+        if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, elapsed_s: float) -> float:
+    """Units all ranks processed per second of the slowest rank (weak scaling)."""
+    return units_per_rank * world / elapsed_s
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -241,10 +259,7 @@ def run_ours(args):
     clocks = sampler.stop()
     elapsed_ms = t0.elapsed_time(t1)
     decode_ms = [a.elapsed_time(b) for a, b in evs]
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms)
     status = pkv.read_status(ws)
     if status != 0:
         raise RuntimeError(f"device status {pkv.STATUS.get(status, status)} in the timed run")
@@ -279,7 +294,7 @@ def run_ours(args):
                "ms_per_step": e_ms, "steps": Ke}
 
     ms_step = elapsed_ms / K
-    kv_gbs = ab["kv"] * world / (ms_step * 1e-3) / 1e9
+    kv_gbs = whole_job_rate(ab["kv"], world, ms_step * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
     dec_ms = statistics.mean(decode_ms)
     achieved = ab["total"] / (dec_ms * 1e-3) / 1e9
@@ -302,7 +317,7 @@ def run_ours(args):
                          "(129 MB)" if ab["kv"] > 256e6 else
                          "no flush: KV per step smaller than 2x L2 (reported, not corrected)",
                    "step": "reshape_and_cache of 1 token/seq + paged decode over L+1"},
-        "tokens_per_s": S * world / (ms_step * 1e-3),
+        "tokens_per_s": whole_job_rate(S, world, ms_step * 1e-3),
         "pct_hbm_peak": 100.0 * ab["total"] / (ms_step * 1e-3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
