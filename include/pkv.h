@@ -139,6 +139,41 @@ pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype,
                                  int partition_tokens, int flags, void *stream);
 
 /*
+ * Decode without a caller workspace (the pages have no counterpart; this is
+ * an interface for callers that cannot allocate device memory, e.g. a plugin
+ * inside a runtime that owns all device memory, or a loop where cudaMalloc's
+ * implicit synchronisation is not allowed).
+ *
+ * Same arguments and result as pkv_paged_attn_decode, minus the workspace.
+ * The scratch is a fixed array of PKV_NOALLOC_SCRATCH_BYTES inside this
+ * library; every GPU that loads the library keeps it allocated until the
+ * process exits.  The call allocates nothing and never calls cudaMalloc or
+ * cudaFree.
+ *  - Sizes whose pkv_paged_attn_workspace_size(...) exceeds
+ *    PKV_NOALLOC_SCRATCH_BYTES are rejected with PKV_ERR_WORKSPACE before
+ *    anything is enqueued (pass a larger partition_tokens, or -1, to need less).
+ *  - The first call on a device looks up the array's device address with
+ *    cudaGetSymbolAddress while that device is current; make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps the previous call's contents
+ *    (each call clears the parts that must start at zero).  Calls that can
+ *    overlap on the GPU (different streams, no ordering between them) race on
+ *    it: serialise them.
+ *  - The device status word sits in that shared array and is not readable by
+ *    the caller; use pkv_paged_attn_decode with a workspace to see it.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+pkv_status pkv_paged_attn_decode_noalloc(const void *q, pkv_dtype q_dtype,
+                                         const void *k_cache, const void *v_cache,
+                                         pkv_dtype kv_dtype, float k_scale, float v_scale,
+                                         const int32_t *block_tables, const int32_t *seq_lens,
+                                         int num_seqs, int num_q_heads, int num_kv_heads,
+                                         int head_dim, int block_size, int num_blocks,
+                                         int max_blocks_per_seq, int max_seq_len, float scale,
+                                         void *out, pkv_dtype out_dtype, int partition_tokens,
+                                         int flags, void *stream);
+
+/*
  * Paged cache write: for every token i < num_tokens with
  * slot = slot_mapping[i] >= 0, writes
  *   k_cache[slot / block_size, h, d, slot % block_size] = cvt(k[i, h, d])
