@@ -65,6 +65,10 @@ typedef enum {
 #define PKV_FLAG_IMPL_SIMT 0x1      /* force the CUDA-core (FFMA) kernel                 */
 #define PKV_FLAG_IMPL_MMA  0x2      /* force the tensor-core (mma.sync) kernel           */
 #define PKV_FLAG_IMPL_MASK 0x3
+/* Split sequences are merged by the decode kernel itself (the CTA finishing a
+ * sequence's last partition merges it).  This flag merges them in a second
+ * log-sum-exp kernel instead; the results are identical. */
+#define PKV_FLAG_SEPARATE_MERGE 0x4
 /* Test hook for the failure path: the first page copy of the first work item
  * is never issued, so its bounded wait runs out and the call records
  * PKV_ERR_TIMEOUT (after about one second) instead of hanging.  Output rows
@@ -76,7 +80,7 @@ typedef enum {
  * the first 256 bytes hold the status word and a work counter).
  *   partition_tokens: 0 = automatic choice, -1 = never split (one pass over
  *   each sequence), > 0 = split every sequence into partitions of this many
- *   tokens (a multiple of block_size) merged by a log-sum-exp kernel.
+ *   tokens (a multiple of block_size) merged with log-sum-exp weights.
  * Returns 0 for invalid sizes.  Host only; touches no device.
  */
 size_t pkv_paged_attn_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,

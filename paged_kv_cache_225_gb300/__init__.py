@@ -25,6 +25,7 @@ __all__ = ["paged_attn_decode", "reshape_and_cache", "workspace_size", "partitio
 
 F32, BF16, FP8_E5M2 = 0, 1, 2
 IMPL = {"auto": 0x0, "simt": 0x1, "mma": 0x2}
+FLAG_SEPARATE_MERGE = 0x4
 FLAG_TEST_DROP_FIRST_COPY = 0x100
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
           4: "PKV_ERR_OUT_OF_RANGE", 5: "PKV_ERR_TIMEOUT", 6: "PKV_ERR_WORKSPACE"}

@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 UNITS = ["pkv_api.cu", "pkv_cache.cu", "pkv_merge.cu", "pkv_decode_simt.cu", "pkv_decode_mma.cu",
          "pkv_noalloc.cu"]
-HEADERS = ["pkv_common.cuh", "pkv_decode.cuh", "pkv_internal.h"]
+HEADERS = ["pkv_common.cuh", "pkv_decode.cuh", "pkv_merge.cuh", "pkv_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 
@@ -40,9 +40,14 @@ def _stale() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of libpkv.so."""
-    if not force and not _stale():
+def build(force: bool = False, verbose: bool = False, defines=(), out: str = None) -> str:
+    """Compile (if stale) and return the path of libpkv.so.
+
+    ``defines`` (e.g. ``["PKV_RING_BYTES_PER_WARP=16384"]``) and ``out`` build
+    a variant library elsewhere (always rebuilt).
+    """
+    target = out or LIB
+    if out is None and not defines and not force and not _stale():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
@@ -50,7 +55,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_unit(unit: str):
         obj = os.path.join(BUILD, unit.replace(".cu", f".{tag}.o"))
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(SRC, unit), "-o", obj]
+        cmd = [nvcc, *ARCH, *FLAGS, *[f"-D{d}" for d in defines], "-c",
+               os.path.join(SRC, unit), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return unit, obj, r
 
@@ -63,7 +69,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
             raise RuntimeError(f"nvcc failed on {unit}:\n{r.stderr[-4000:]}")
     with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
         f.write("\n".join(log))
-    tmp = LIB + f".{tag}.tmp"
+    os.makedirs(os.path.dirname(os.path.abspath(target)), exist_ok=True)
+    tmp = target + f".{tag}.tmp"
     objs = [obj for _, obj, _ in results]
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"],
                        capture_output=True, text=True)
@@ -71,10 +78,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
         os.remove(o)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, target)
     if verbose:
-        print(f"built {LIB}", file=sys.stderr)
-    return LIB
+        print(f"built {target}", file=sys.stderr)
+    return target
 
 
 if __name__ == "__main__":

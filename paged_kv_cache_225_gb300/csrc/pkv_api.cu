@@ -61,10 +61,12 @@ static int resolve_partition(int num_seqs, int num_q_heads, int num_kv_heads, in
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Workspace: [256-byte header: status, work counter][arrive counters
+// S*Hkv u32][partial outputs S*Hq*max_parts*D f32][partial (m, l) pairs].
 struct Plan {
     int partition;  // 0 = no split
     int max_parts;
-    size_t part_o_off, part_ml_off, bytes;
+    size_t arrive_off, part_o_off, part_ml_off, bytes;
 };
 
 static bool make_plan(int S, int Hq, int Hkv, int D, int B, int max_len, int requested, Plan *pl)
@@ -74,12 +76,13 @@ static bool make_plan(int S, int Hq, int Hkv, int D, int B, int max_len, int req
         return false;
     pl->partition = P;
     pl->max_parts = 1;
-    pl->part_o_off = pl->part_ml_off = 0;
+    pl->arrive_off = pl->part_o_off = pl->part_ml_off = 0;
     pl->bytes = kWorkspaceHeader;
     if (P > 0) {
         pl->max_parts = max_len > P ? (max_len + P - 1) / P : 1;
         const size_t rows = static_cast<size_t>(S) * Hq * pl->max_parts;
-        pl->part_o_off = kWorkspaceHeader;
+        pl->arrive_off = kWorkspaceHeader;
+        pl->part_o_off = pl->arrive_off + align256(static_cast<size_t>(S) * Hkv * sizeof(unsigned));
         pl->part_ml_off = pl->part_o_off + align256(rows * D * sizeof(float));
         pl->bytes = pl->part_ml_off + align256(rows * 2 * sizeof(float));
     }
@@ -144,7 +147,8 @@ pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype, const void *k
         return PKV_ERR_UNSUPPORTED;
     if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
         return PKV_ERR_INVALID_ARG;
-    if ((flags & ~(PKV_FLAG_IMPL_MASK | PKV_FLAG_TEST_DROP_FIRST_COPY)) != 0 ||
+    if ((flags & ~(PKV_FLAG_IMPL_MASK | PKV_FLAG_SEPARATE_MERGE | PKV_FLAG_TEST_DROP_FIRST_COPY)) !=
+            0 ||
         (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_MASK)
         return PKV_ERR_INVALID_ARG;
     Plan pl;
@@ -178,6 +182,7 @@ pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype, const void *k
     p.out = out;
     p.status = reinterpret_cast<int *>(ws);
     p.counter = reinterpret_cast<unsigned *>(ws + 4);
+    p.arrive = pl.partition > 0 ? reinterpret_cast<unsigned *>(ws + pl.arrive_off) : nullptr;
     p.part_o = pl.partition > 0 ? reinterpret_cast<float *>(ws + pl.part_o_off) : nullptr;
     p.part_ml = pl.partition > 0 ? reinterpret_cast<float *>(ws + pl.part_ml_off) : nullptr;
     p.q_dtype = q_dtype;
@@ -196,15 +201,18 @@ pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype, const void *k
     p.partition = pl.partition > 0 ? pl.partition : max_blocks_per_seq * kBlockSize;
     p.max_parts = pl.max_parts;
     p.split = pl.partition > 0 ? 1 : 0;
+    p.fused_merge = (flags & PKV_FLAG_SEPARATE_MERGE) ? 0 : 1;
     p.drop_first_copy = (flags & PKV_FLAG_TEST_DROP_FIRST_COPY) ? 1 : 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess)
+    // Status word, work counter and (split) arrival counters start at zero.
+    const size_t zero_bytes = p.split ? pl.part_o_off : 16;
+    if (cudaMemsetAsync(ws, 0, zero_bytes, st) != cudaSuccess)
         return PKV_ERR_CUDA;
     pkv_status rc = use_mma ? launch_decode_mma(p, kv_dtype, st) : launch_decode_simt(p, kv_dtype, st);
     if (rc != PKV_OK)
         return rc;
-    if (p.split && p.max_parts > 1)
+    if (p.split && p.max_parts > 1 && !p.fused_merge)
         rc = launch_merge(p, st);
     return rc;
 }

@@ -35,11 +35,16 @@
 
 #include "pkv_common.cuh"
 #include "pkv_internal.h"
+#include "pkv_merge.cuh"
+
+// Shared-memory budget of one warp's page ring (bytes); the stage count
+// follows from it (2..8 stages).
+#ifndef PKV_RING_BYTES_PER_WARP
+#define PKV_RING_BYTES_PER_WARP (24 * 1024)
+#endif
 
 namespace pkv {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per bounded wait
 
 template <int KV> struct KvBytes;
@@ -47,11 +52,11 @@ template <> struct KvBytes<PKV_F32> { static constexpr int v = 4; };
 template <> struct KvBytes<PKV_BF16> { static constexpr int v = 2; };
 template <> struct KvBytes<PKV_FP8_E5M2> { static constexpr int v = 1; };
 
-// Per-warp ring geometry: about 24 KB of page stages per warp (2..8 stages).
+// Per-warp ring geometry: PKV_RING_BYTES_PER_WARP of page stages per warp.
 template <int KV, int D> struct Ring {
     static constexpr int kTileBytes = D * kBlockSize * KvBytes<KV>::v;  // one K or V page tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kRaw = (24 * 1024) / kStageBytes;
+    static constexpr int kRaw = (PKV_RING_BYTES_PER_WARP) / kStageBytes;
     static constexpr int R = kRaw < 2 ? 2 : (kRaw > 8 ? 8 : kRaw);
     static constexpr int kRingBytes = R * kStageBytes;
 };
@@ -554,22 +559,72 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
 
 // ==================================================================== kernel
 
-// A length outside [0, max_len] is reported and clamped, so no item reads
-// past the table or writes past the workspace's partial rows.
-__device__ __forceinline__ int clamp_len(const DecodeParams &p, int L)
+// Counts of the two item phases of a sequence of L tokens under partition
+// P: full partitions first, then the one shorter remainder (or the single
+// item of an empty sequence).  Issuing every full partition before any
+// remainder leaves short items for the end of the grid.
+__device__ __forceinline__ int full_parts(int L, int P) { return L / P; }
+__device__ __forceinline__ int tail_parts(int L, int P) { return (L % P != 0 || L == 0) ? 1 : 0; }
+
+// Warp-collective scan over sequences: finds the sequence holding unit u of a
+// stream in which sequence s contributes count(L_s) units.  `cur_s` /
+// `cur_base` remember where the previous search ended (u only grows).
+// Returns false when u lies past the last sequence.
+template <bool kTail>
+__device__ bool find_unit(const DecodeParams &p, int u, int &cur_s, int &cur_base, int lane,
+                          int &s_out, int &k_out, int &L_out)
 {
-    const int maxL = p.max_len;
-    if (L < 0 || L > maxL) {
-        set_status(p.status, PKV_ERR_OUT_OF_RANGE);
-        L = L < 0 ? 0 : maxL;
+    const int S = p.num_seqs, P = p.partition;
+    for (;;) {
+        const int sl = cur_s + lane;
+        int n = 0, Ls = 0;
+        if (sl < S) {
+            Ls = clamp_len(p, __ldg(p.seq_lens + sl));
+            n = kTail ? tail_parts(Ls, P) : full_parts(Ls, P);
+        }
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(kFullMask, incl, off);
+            if (lane >= off)
+                incl += t;
+        }
+        const int tot = __shfl_sync(kFullMask, incl, 31);
+        if (u < cur_base + tot) {
+            const unsigned bal = __ballot_sync(kFullMask, cur_base + incl > u);
+            const int ln = __ffs(bal) - 1;
+            const int excl = __shfl_sync(kFullMask, incl - n, ln);
+            s_out = cur_s + ln;
+            k_out = u - cur_base - excl;
+            L_out = __shfl_sync(kFullMask, Ls, ln);
+            return true;
+        }
+        if (cur_s + 32 >= S)
+            return false;
+        cur_base += tot;
+        cur_s += 32;
     }
-    return L;
 }
 
-__device__ __forceinline__ int parts_of(int L, int P) { return L > P ? (L + P - 1) / P : 1; }
+// Total full partitions over all sequences (warp-collective).
+__device__ __forceinline__ int count_full_parts(const DecodeParams &p, int lane)
+{
+    int tot = 0;
+    for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
+        int n = 0;
+        if (s0 + lane < p.num_seqs)
+            n = full_parts(clamp_len(p, __ldg(p.seq_lens + s0 + lane)), p.partition);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            n += __shfl_xor_sync(kFullMask, n, off);
+        tot += n;
+    }
+    return tot;
+}
 
-// Writes the merged result of one item: the four warps' (m, l, O) sit at the
-// start of each warp's ring.
+// Combines the four warps' (m, l, O) states of one item (at the start of each
+// warp's ring) and writes the output rows (one partition) or the item's
+// normalised partial (split sequences).
 template <int D, int GP>
 __device__ void merge_item(const DecodeParams &p, const unsigned char *smem, int ring_bytes, int s,
                            int hkv, int part, int nparts)
@@ -602,16 +657,7 @@ __device__ void merge_item(const DecodeParams &p, const unsigned char *smem, int
         const int h = hkv * G + g;
         if (nparts == 1) {
             const float sc = inv * p.out_scale;
-            const size_t off = (static_cast<size_t>(s) * p.num_q_heads + h) * D + 4 * q4;
-            if (p.out_dtype == PKV_F32) {
-                *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) =
-                    make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc);
-            } else {
-                uint2 w;
-                w.x = pack_bf16(acc.x * sc, acc.y * sc);
-                w.y = pack_bf16(acc.z * sc, acc.w * sc);
-                *reinterpret_cast<uint2 *>(static_cast<unsigned short *>(p.out) + off) = w;
-            }
+            store_out4(p, D, s, h, q4, make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
         } else {
             const size_t row = (static_cast<size_t>(s) * p.num_q_heads + h) * p.max_parts + part;
             reinterpret_cast<float4 *>(p.part_o + row * D)[q4] =
@@ -633,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_item[8];
     __shared__ int s_abort;
+    __shared__ int s_last;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -656,7 +703,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
     const float c = p.score_scale;
 
     uint32_t pages_done = 0;  // pages this warp has consumed (ring position / phase)
-    int cur_s = 0, cur_base = 0;  // warp 0: scan cursor over sequences (split mode)
+    // Warp 0 only: scan cursors of the two item phases and the phase-1 size.
+    int full_s = 0, full_base = 0, tail_s = 0, tail_base = 0, n_full = 0;
+    if (p.split && warp == 0)
+        n_full = count_full_parts(p, lane);
     bool first = true;
 
     for (;;) {
@@ -670,38 +720,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
                 item = static_cast<int>(__shfl_sync(kFullMask, v, 0));
                 const int u = item / Hkv;
                 hkv = item - u * Hkv;
-                for (;;) {
-                    const int sl = cur_s + lane;
-                    int n = 0, Ls = 0;
-                    if (sl < S) {
-                        Ls = clamp_len(p, __ldg(p.seq_lens + sl));
-                        n = parts_of(Ls, P);
-                    }
-                    int incl = n;
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const int t = __shfl_up_sync(kFullMask, incl, off);
-                        if (lane >= off)
-                            incl += t;
-                    }
-                    const int tot = __shfl_sync(kFullMask, incl, 31);
-                    if (u < cur_base + tot) {
-                        const unsigned bal = __ballot_sync(kFullMask, cur_base + incl > u);
-                        const int ln = __ffs(bal) - 1;
-                        const int excl = __shfl_sync(kFullMask, incl - n, ln);
-                        s = cur_s + ln;
-                        part = u - cur_base - excl;
-                        L = __shfl_sync(kFullMask, Ls, ln);
-                        nparts = __shfl_sync(kFullMask, n, ln);
-                        break;
-                    }
-                    if (cur_s + 32 >= S) {
-                        done = 1;
-                        break;
-                    }
-                    cur_base += tot;
-                    cur_s += 32;
+                int k = 0;
+                bool found;
+                if (u < n_full) {
+                    found = find_unit<false>(p, u, full_s, full_base, lane, s, k, L);
+                    part = k;
+                } else {
+                    found = find_unit<true>(p, u - n_full, tail_s, tail_base, lane, s, k, L);
+                    part = full_parts(L, P);
                 }
+                done = found ? 0 : 1;
+                nparts = parts_of(L, P);
             } else {
                 item = first ? static_cast<int>(blockIdx.x) : INT_MAX;
                 if (item >= S * Hkv) {
@@ -826,6 +855,22 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
         }
         __syncthreads();
         merge_item<D, Pol::GP>(p, smem, Pol::kRingBytes, s, hkv, part, nparts);
+        if (nparts > 1 && p.fused_merge) {
+            // Publish this partial; the CTA that completes the sequence's last
+            // partial merges all of them (threadfence-reduction pattern).
+            __threadfence();
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                const unsigned old =
+                    atomicAdd(p.arrive + static_cast<size_t>(s) * Hkv + hkv, 1u);
+                s_last = (old == static_cast<unsigned>(nparts - 1)) ? 1 : 0;
+            }
+            __syncthreads();
+            if (s_last) {
+                __threadfence();
+                merge_partials<D>(p, s, hkv, nparts);
+            }
+        }
         // The rings were used as generic scratch: order that before the next
         // item's bulk copies into them.
         fence_proxy_async();

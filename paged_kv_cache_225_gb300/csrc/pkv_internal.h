@@ -22,6 +22,7 @@ struct DecodeParams {
     float *part_ml;       // [S][Hq][max_parts][2] (max of log2-scaled scores, sum)
     int *status;          // workspace word 0
     unsigned *counter;    // workspace word 1: next work item (split mode)
+    unsigned *arrive;     // [S][Hkv] partials written so far (in-kernel merge)
     int q_dtype, out_dtype;
     int num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks;
     int max_len;          // caller's bound on seq_lens (<= max_blocks * 16)
@@ -31,6 +32,7 @@ struct DecodeParams {
     int partition;        // tokens per work item (multiple of 16)
     int max_parts;        // partitions per sequence the workspace holds
     int split;            // 1: persistent grid, work counter, partials + merge
+    int fused_merge;      // 1: the CTA finishing a sequence's last partial merges it
     int drop_first_copy;  // test hook: never issue the first copy of item 0
 };
 

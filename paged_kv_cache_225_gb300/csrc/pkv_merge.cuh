@@ -1,0 +1,84 @@
+// Device helpers shared by the decode kernel and the stand-alone merge kernel:
+// sequence-length clamping, partition counts, output stores, and the
+// log-sum-exp merge of split-sequence partials.
+#pragma once
+
+#include <cmath>
+
+#include "pkv_common.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = 32 * kWarps;
+
+// A length outside [0, max_len] is reported and clamped, so no item reads
+// past the table or writes past the workspace's partial rows.
+__device__ __forceinline__ int clamp_len(const DecodeParams &p, int L)
+{
+    const int maxL = p.max_len;
+    if (L < 0 || L > maxL) {
+        set_status(p.status, PKV_ERR_OUT_OF_RANGE);
+        L = L < 0 ? 0 : maxL;
+    }
+    return L;
+}
+
+// Partitions of a sequence of L tokens (an empty sequence still has one item,
+// which writes its zero row).
+__device__ __forceinline__ int parts_of(int L, int P) { return L > P ? (L + P - 1) / P : 1; }
+
+// out[s, h, 4*q4 .. 4*q4+3] = v (f32 or bf16 output).
+__device__ __forceinline__ void store_out4(const DecodeParams &p, int D, int s, int h, int q4,
+                                           float4 v)
+{
+    const size_t off = (static_cast<size_t>(s) * p.num_q_heads + h) * D + 4 * q4;
+    if (p.out_dtype == PKV_F32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) = v;
+    } else {
+        uint2 w;
+        w.x = pack_bf16(v.x, v.y);
+        w.y = pack_bf16(v.z, v.w);
+        *reinterpret_cast<uint2 *>(static_cast<unsigned short *>(p.out) + off) = w;
+    }
+}
+
+// Merges the nparts partials of (sequence s, KV head hkv) for its G query
+// heads and writes the output rows.  Partition i carries its normalised
+// output o_i, the max m_i of its log2-scaled scores and l_i = sum 2^(z - m_i);
+// by the associativity of the online-softmax recurrence the full result is
+//     M = max_i m_i,  w_i = l_i 2^(m_i - M),  out = sum_i w_i o_i / sum_i w_i.
+// Partitions are summed in index order, so the result does not depend on
+// which CTA wrote which partial.  Called by all threads of a CTA.
+template <int D>
+__device__ void merge_partials(const DecodeParams &p, int s, int hkv, int nparts)
+{
+    constexpr int Q4 = D / 4;
+    const int G = p.group;
+    for (int idx = threadIdx.x; idx < G * Q4; idx += blockDim.x) {
+        const int g = idx / Q4, q4 = idx - g * Q4;
+        const int h = hkv * G + g;
+        const size_t row0 = (static_cast<size_t>(s) * p.num_q_heads + h) * p.max_parts;
+        const float *ml = p.part_ml + 2 * row0;
+        float mx = -INFINITY;
+        for (int i = 0; i < nparts; ++i)
+            mx = fmaxf(mx, __ldcg(ml + 2 * i));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wsum = 0.f;
+        for (int i = 0; i < nparts; ++i) {
+            const float m = __ldcg(ml + 2 * i), l = __ldcg(ml + 2 * i + 1);
+            const float w = (m == -INFINITY) ? 0.f : l * exp2f(m - mx);
+            wsum += w;
+            const float4 o = __ldcg(reinterpret_cast<const float4 *>(p.part_o + (row0 + i) * D) + q4);
+            acc.x += w * o.x;
+            acc.y += w * o.y;
+            acc.z += w * o.z;
+            acc.w += w * o.w;
+        }
+        const float sc = (wsum > 0.f ? 1.f / wsum : 0.f) * p.out_scale;
+        store_out4(p, D, s, h, q4, make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
+    }
+}
+
+}  // namespace pkv

@@ -46,7 +46,7 @@ def device_workload(w: W.Workload, dev: torch.device) -> dict:
 
 
 def gpu_step(w: W.Workload, d: dict, *, impl="auto", partition_tokens=0, out_dtype=torch.float32,
-             append=True, kv_scale=None):
+             append=True, kv_scale=None, flags=0):
     """One decode step on the GPU: write the new tokens, attend over L+1 tokens."""
     cfg = w.cfg
     ks = vs = cfg.kv_scale if kv_scale is None else kv_scale
@@ -59,7 +59,7 @@ def gpu_step(w: W.Workload, d: dict, *, impl="auto", partition_tokens=0, out_dty
     out = torch.empty(d["q"].shape, dtype=out_dtype, device=d["q"].device)
     pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], lens_dev,
                           w.scale, out, k_scale=ks, v_scale=vs, max_seq_len=int(lens.max()),
-                          partition_tokens=partition_tokens, impl=impl)
+                          partition_tokens=partition_tokens, impl=impl, flags=flags)
     torch.cuda.synchronize()
     status = pkv.read_status(device=d["q"].device)
     return out.float().cpu().numpy().astype(np.float64), status, lens

@@ -67,7 +67,8 @@ def test_workspace_size():
 
     def a(x):
         return (x + 255) // 256 * 256
-    assert W(S, Hq, 8, D, L, P) == 256 + a(rows * D * 4) + a(rows * 8)
+    # header | arrival counters [S*Hkv] | partial outputs | partial (m, l)
+    assert W(S, Hq, 8, D, L, P) == 256 + a(S * 8 * 4) + a(rows * D * 4) + a(rows * 8)
     with pytest.raises(ValueError):
         W(4, 6, 4, 64, 65, 0)                       # heads do not divide
 
@@ -102,6 +103,7 @@ def _decode(**kw):
     (dict(part=40), INVALID),
     (dict(flags=0x3), INVALID),
     (dict(flags=0x40), INVALID),
+    (dict(flags=0x8), INVALID),
     (dict(flags=0x2, kv_dtype=F32), UNSUPPORTED),  # tensor cores need bf16/fp8 KV
     (dict(flags=0x2, q_dtype=F32), UNSUPPORTED),
     (dict(scale=float("nan")), INVALID),

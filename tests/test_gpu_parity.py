@@ -55,12 +55,22 @@ def test_config_parity_simt(name):
 
 @pytest.mark.parametrize("name", ["llama3_8b", "long_split", "fp8_chat"])
 @pytest.mark.parametrize("part", [-1, 16, 48, 256, 4096])
-def test_config_parity_forced_split(name, part):
+@pytest.mark.parametrize("merge", ["in_kernel", "merge_kernel"])
+def test_config_parity_forced_split(name, part, merge):
     w, ref, kc, vc = _config(name)
     d = device_workload(w, DEV)
-    out, status, _ = gpu_step(w, d, partition_tokens=part)
+    flags = pkv.FLAG_SEPARATE_MERGE if merge == "merge_kernel" else 0
+    out, status, _ = gpu_step(w, d, partition_tokens=part, flags=flags)
     assert status == 0
     assert max_abs(out, ref) <= TOL[w.cfg.kv_dtype]
+
+
+def test_in_kernel_and_separate_merge_agree_bitwise():
+    w, ref, _, _ = _config("llama3_8b")
+    d = device_workload(w, DEV)
+    a, _, _ = gpu_step(w, d, partition_tokens=256)
+    b, _, _ = gpu_step(w, d, partition_tokens=256, flags=pkv.FLAG_SEPARATE_MERGE)
+    assert np.array_equal(a, b)
 
 
 def _custom(base="llama3_8b", seed=100, lens=None, **kw):
