@@ -32,10 +32,10 @@ int device_sm_count()
     return cache[dev];
 }
 
-// Resident decode CTAs the split heuristic plans for (2 per SM of a GB300).
+// Resident decode CTAs the split heuristic plans for (3 per SM of a GB300).
 // A fixed number keeps the plan, and so the workspace size, independent of
 // the device that happens to be current.
-constexpr long kPlanSlots = 2L * 152;
+constexpr long kPlanSlots = 3L * 152;
 
 // Partition size for these sizes: > 0 split, 0 one pass, -1 invalid.
 static int resolve_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -53,7 +53,7 @@ static int resolve_partition(int num_seqs, int num_q_heads, int num_kv_heads, in
     const long units = static_cast<long>(num_seqs) * num_kv_heads;
     if (max_seq_len <= 1024 && units >= kPlanSlots)
         return 0;
-    int P = 512;
+    int P = 1024;
     while (P > 64 && units * ((max_seq_len + P - 1) / P) < 4 * kPlanSlots)
         P /= 2;
     return max_seq_len <= P ? 0 : P;

@@ -38,9 +38,11 @@
 #include "pkv_merge.cuh"
 
 // Shared-memory budget of one warp's page ring (bytes); the stage count
-// follows from it (2..8 stages).
+// follows from it (2..8 stages).  16 KB (two 8 KB bf16 stages) leaves room
+// for three CTAs per SM, which hides each CTA's item-boundary bubbles better
+// than deeper rings with fewer CTAs (measured on GB300).
 #ifndef PKV_RING_BYTES_PER_WARP
-#define PKV_RING_BYTES_PER_WARP (24 * 1024)
+#define PKV_RING_BYTES_PER_WARP (16 * 1024)
 #endif
 
 namespace pkv {

@@ -53,8 +53,8 @@ def test_partition_plan():
     assert P(4, 4, 4, 64, 65, 48) == 48
     assert P(4, 4, 4, 64, 65, 40) == -1           # not a multiple of the block size
     assert P(128, 64, 8, 128, 514, 0) == 0          # 1024 units, short context: one pass
-    assert P(128, 64, 8, 128, 14626, 0) == 512      # 70B-shaped layer
-    assert P(8, 64, 8, 128, 32769, 0) == 512        # long context: split
+    assert P(128, 64, 8, 128, 14626, 0) == 1024     # 70B-shaped layer
+    assert P(8, 64, 8, 128, 32769, 0) == 1024       # long context: split
     assert P(1, 8, 8, 128, 512, 0) == 64            # few units: small partitions
 
 
