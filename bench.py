@@ -312,7 +312,11 @@ def run_ours(args):
         "config": {"workload": workload_text(args.config), "name": args.config,
                    "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
                    "block_size": cfg.block_size, "tokens_per_step": ab["tokens"],
-                   "kv_bytes_per_step": ab["kv"], "partition_tokens": part,
+                   "kv_bytes_per_step": ab["kv"],
+                   "schedule": ("stream-K (equal page ranges per CTA)"
+                                if part == pkv.SCHEDULE_STREAMK else
+                                f"{part}-token partitions" if part > 0 else
+                                "one CTA per (sequence, KV head)"),
                    "kernel": kernel_impl,
                    "l2": f"no flush: KV read per step ({ab['kv'] / 1e9:.2f} GB) exceeds L2 "
                          "(129 MB)" if ab["kv"] > 256e6 else

@@ -78,9 +78,16 @@ typedef enum {
 /*
  * Workspace bytes pkv_paged_attn_decode needs for these sizes (always >= 256:
  * the first 256 bytes hold the status word and a work counter).
- *   partition_tokens: 0 = automatic choice, -1 = never split (one pass over
- *   each sequence), > 0 = split every sequence into partitions of this many
- *   tokens (a multiple of block_size) merged with log-sum-exp weights.
+ *   partition_tokens:
+ *     0  = automatic: the stream-K schedule.  The flattened (sequence, KV
+ *          head, page) space is cut into one equal contiguous range per CTA;
+ *          sequences cut by range boundaries are merged with log-sum-exp
+ *          weights by the CTA that finishes their last piece.  The workspace
+ *          does not depend on the sequence lengths.
+ *    -1  = never split: one CTA per (sequence, KV head), one pass.
+ *    > 0 = split every sequence into partitions of this many tokens (a
+ *          multiple of block_size), scheduled dynamically, merged with
+ *          log-sum-exp weights.
  * Returns 0 for invalid sizes.  Host only; touches no device.
  */
 size_t pkv_paged_attn_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
@@ -88,9 +95,11 @@ size_t pkv_paged_attn_workspace_size(int num_seqs, int num_q_heads, int num_kv_h
                                      int partition_tokens);
 
 /*
- * The partition size pkv_paged_attn_decode will use for these sizes
- * (0 = no split), or -1 for invalid sizes.  Host only.
+ * The schedule pkv_paged_attn_decode will use for these sizes: > 0 tokens per
+ * fixed partition, 0 one pass per (sequence, KV head), PKV_SCHEDULE_STREAMK
+ * for the stream-K schedule, -1 for invalid sizes.  Host only.
  */
+#define PKV_SCHEDULE_STREAMK (-2)
 int pkv_paged_attn_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads,
                                     int head_dim, int block_size, int max_seq_len,
                                     int partition_tokens);

@@ -111,9 +111,13 @@ def workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim:
     return int(n)
 
 
+SCHEDULE_STREAMK = -2
+
+
 def partition_tokens(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
                      max_seq_len: int, partition_tokens: int = 0, block_size: int = 16) -> int:
-    """Tokens per split partition the decode call will use (0 = one pass)."""
+    """Schedule of the decode call: tokens per fixed partition (> 0), 0 for one
+    pass per (sequence, KV head), SCHEDULE_STREAMK for equal page ranges per CTA."""
     return int(lib().pkv_paged_attn_partition_tokens(num_seqs, num_q_heads, num_kv_heads,
                                                      head_dim, block_size, max_seq_len,
                                                      partition_tokens))

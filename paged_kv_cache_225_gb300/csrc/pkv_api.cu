@@ -32,12 +32,11 @@ int device_sm_count()
     return cache[dev];
 }
 
-// Resident decode CTAs the split heuristic plans for (3 per SM of a GB300).
-// A fixed number keeps the plan, and so the workspace size, independent of
-// the device that happens to be current.
-constexpr long kPlanSlots = 3L * 152;
+constexpr int kStreamK = -2;  // plan code of the stream-K schedule
 
-// Partition size for these sizes: > 0 split, 0 one pass, -1 invalid.
+// Schedule for these sizes: > 0 fixed partitions of that many tokens, 0 one
+// pass per (sequence, KV head), kStreamK equal page ranges per CTA (the
+// automatic choice), -1 invalid.
 static int resolve_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                              int block_size, int max_seq_len, int requested)
 {
@@ -50,13 +49,7 @@ static int resolve_partition(int num_seqs, int num_q_heads, int num_kv_heads, in
         return (requested % kBlockSize == 0) ? requested : -1;
     if (requested != 0)
         return -1;
-    const long units = static_cast<long>(num_seqs) * num_kv_heads;
-    if (max_seq_len <= 1024 && units >= kPlanSlots)
-        return 0;
-    int P = 1024;
-    while (P > 64 && units * ((max_seq_len + P - 1) / P) < 4 * kPlanSlots)
-        P /= 2;
-    return max_seq_len <= P ? 0 : P;
+    return kStreamK;
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -72,13 +65,20 @@ struct Plan {
 static bool make_plan(int S, int Hq, int Hkv, int D, int B, int max_len, int requested, Plan *pl)
 {
     const int P = resolve_partition(S, Hq, Hkv, D, B, max_len, requested);
-    if (P < 0)
+    if (P == -1)
         return false;
     pl->partition = P;
     pl->max_parts = 1;
     pl->arrive_off = pl->part_o_off = pl->part_ml_off = 0;
     pl->bytes = kWorkspaceHeader;
-    if (P > 0) {
+    if (P == kStreamK) {
+        // Two partial slots per CTA, G rows each.
+        const size_t rows = static_cast<size_t>(2) * kStreamKMaxCtas * (Hq / Hkv);
+        pl->arrive_off = kWorkspaceHeader;
+        pl->part_o_off = pl->arrive_off + align256(static_cast<size_t>(S) * Hkv * sizeof(unsigned));
+        pl->part_ml_off = pl->part_o_off + align256(rows * D * sizeof(float));
+        pl->bytes = pl->part_ml_off + align256(rows * 2 * sizeof(float));
+    } else if (P > 0) {
         pl->max_parts = max_len > P ? (max_len + P - 1) / P : 1;
         const size_t rows = static_cast<size_t>(S) * Hq * pl->max_parts;
         pl->arrive_off = kWorkspaceHeader;
@@ -182,9 +182,10 @@ pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype, const void *k
     p.out = out;
     p.status = reinterpret_cast<int *>(ws);
     p.counter = reinterpret_cast<unsigned *>(ws + 4);
-    p.arrive = pl.partition > 0 ? reinterpret_cast<unsigned *>(ws + pl.arrive_off) : nullptr;
-    p.part_o = pl.partition > 0 ? reinterpret_cast<float *>(ws + pl.part_o_off) : nullptr;
-    p.part_ml = pl.partition > 0 ? reinterpret_cast<float *>(ws + pl.part_ml_off) : nullptr;
+    const bool partials = pl.partition != 0;
+    p.arrive = partials ? reinterpret_cast<unsigned *>(ws + pl.arrive_off) : nullptr;
+    p.part_o = partials ? reinterpret_cast<float *>(ws + pl.part_o_off) : nullptr;
+    p.part_ml = partials ? reinterpret_cast<float *>(ws + pl.part_ml_off) : nullptr;
     p.q_dtype = q_dtype;
     p.out_dtype = out_dtype;
     p.num_seqs = num_seqs;
@@ -201,12 +202,14 @@ pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype, const void *k
     p.partition = pl.partition > 0 ? pl.partition : max_blocks_per_seq * kBlockSize;
     p.max_parts = pl.max_parts;
     p.split = pl.partition > 0 ? 1 : 0;
+    p.streamk = pl.partition == kStreamK ? 1 : 0;
+    p.streamk_max_ctas = kStreamKMaxCtas;
     p.fused_merge = (flags & PKV_FLAG_SEPARATE_MERGE) ? 0 : 1;
     p.drop_first_copy = (flags & PKV_FLAG_TEST_DROP_FIRST_COPY) ? 1 : 0;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // Status word, work counter and (split) arrival counters start at zero.
-    const size_t zero_bytes = p.split ? pl.part_o_off : 16;
+    // Status word, work counter and arrival counters start at zero.
+    const size_t zero_bytes = partials ? pl.part_o_off : 16;
     if (cudaMemsetAsync(ws, 0, zero_bytes, st) != cudaSuccess)
         return PKV_ERR_CUDA;
     pkv_status rc = use_mma ? launch_decode_mma(p, kv_dtype, st) : launch_decode_simt(p, kv_dtype, st);

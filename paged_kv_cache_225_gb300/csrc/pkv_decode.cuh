@@ -54,11 +54,41 @@ template <> struct KvBytes<PKV_F32> { static constexpr int v = 4; };
 template <> struct KvBytes<PKV_BF16> { static constexpr int v = 2; };
 template <> struct KvBytes<PKV_FP8_E5M2> { static constexpr int v = 1; };
 
-// Per-warp ring geometry: PKV_RING_BYTES_PER_WARP of page stages per warp.
-template <int KV, int D> struct Ring {
+// Per-CTA shared memory the stream-K kernel plans for (two CTAs per SM) and
+// the ring budget per warp it may use at most.
+#ifndef PKV_CTA_SMEM_TARGET
+#define PKV_CTA_SMEM_TARGET (113 * 1024)
+#endif
+#ifndef PKV_STREAMK_RING_BYTES_PER_WARP
+#define PKV_STREAMK_RING_BYTES_PER_WARP (24 * 1024)
+#endif
+
+// Merge scratch of one warp: O[GP][D], m[GP], l[GP] in fp32, padded to a
+// multiple of 4 floats so every warp's O rows stay 16-byte aligned for float4
+// reads.
+__host__ __device__ constexpr int scratch_floats(int GP, int D)
+{
+    return (GP * D + 2 * GP + 3) / 4 * 4;
+}
+__host__ __device__ constexpr int scratch_bytes(int GP, int D)
+{
+    return kWarps * scratch_floats(GP, D) * 4;
+}
+
+// Ring bytes per warp for a kernel whose other shared memory (policy data and
+// a separate merge scratch) takes `other` bytes of the per-CTA target.
+__host__ __device__ constexpr int ring_budget(int other)
+{
+    return (PKV_CTA_SMEM_TARGET - other - 256) / kWarps < PKV_STREAMK_RING_BYTES_PER_WARP
+               ? (PKV_CTA_SMEM_TARGET - other - 256) / kWarps
+               : PKV_STREAMK_RING_BYTES_PER_WARP;
+}
+
+// Per-warp ring geometry: `Budget` bytes of page stages per warp.
+template <int KV, int D, int Budget> struct Ring {
     static constexpr int kTileBytes = D * kBlockSize * KvBytes<KV>::v;  // one K or V page tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kRaw = (PKV_RING_BYTES_PER_WARP) / kStageBytes;
+    static constexpr int kRaw = Budget / kStageBytes;
     static constexpr int R = kRaw < 2 ? 2 : (kRaw > 8 ? 8 : kRaw);
     static constexpr int kRingBytes = R * kStageBytes;
 };
@@ -76,9 +106,9 @@ __device__ __forceinline__ float load_q(const DecodeParams &p, size_t idx)
 // Scores: lane (t, half) owns token t of the page and half of head_dim; the
 // two halves are summed with one shuffle.  Values: lane owns head_dim rows
 // lane + 32j and walks the page's valid tokens.  GT = heads padded to 2^k.
-template <int KV, int D, int GT>
+template <int KV, int D, int GT, int Budget = PKV_RING_BYTES_PER_WARP>
 struct SimtPolicy {
-    using RingT = Ring<KV, D>;
+    using RingT = Ring<KV, D, Budget>;
     static constexpr int R = RingT::R;
     static constexpr int kTileBytes = RingT::kTileBytes;
     static constexpr int kStageBytes = RingT::kStageBytes;
@@ -89,6 +119,8 @@ struct SimtPolicy {
     static constexpr int kQHalfStride = kHalf * GT + 4;  // pad: the halves hit other banks
     static constexpr int kExtraBytes = (2 * kQHalfStride + kWarps * kBlockSize * GT) * 4;
     static constexpr int DJ = D / 32;
+    // The same policy with a separate merge scratch and the ring that fits.
+    using StreamK = SimtPolicy<KV, D, GT, ring_budget(kExtraBytes + scratch_bytes(GT, D))>;
 
     struct State {
         float m[GT];
@@ -374,11 +406,13 @@ struct MmaStateBase {
 // bf16 KV: the page tile is [D][16] bf16 (32-byte rows).  K^T fragments come
 // from ldmatrix.trans, V fragments from ldmatrix.  P is split into a bf16 high
 // part and a bf16 residual so that P V keeps ~16 mantissa bits.
-template <int D, int NT>
+template <int D, int NT, int Budget = PKV_RING_BYTES_PER_WARP>
 struct MmaBf16Policy : MmaStateBase<D, NT> {
     using Base = MmaStateBase<D, NT>;
     using State = typename Base::State;
-    using RingT = Ring<PKV_BF16, D>;
+    using RingT = Ring<PKV_BF16, D, Budget>;
+    // The same policy with a separate merge scratch and the ring that fits.
+    using StreamK = MmaBf16Policy<D, NT, ring_budget(scratch_bytes(8 * NT, D))>;
     static constexpr int R = RingT::R;
     static constexpr int kTileBytes = RingT::kTileBytes;
     static constexpr int kStageBytes = RingT::kStageBytes;
@@ -466,11 +500,13 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
 // ldmatrix as 16-bit pairs; byte_perm widens each code to an f16 (the code
 // is the f16's high byte, exactly).  Token order inside a fragment is
 // permuted consistently on both operands (see the byte selectors).
-template <int D, int NT>
+template <int D, int NT, int Budget = PKV_RING_BYTES_PER_WARP>
 struct MmaFp8Policy : MmaStateBase<D, NT> {
     using Base = MmaStateBase<D, NT>;
     using State = typename Base::State;
-    using RingT = Ring<PKV_FP8_E5M2, D>;
+    using RingT = Ring<PKV_FP8_E5M2, D, Budget>;
+    // The same policy with a separate merge scratch and the ring that fits.
+    using StreamK = MmaFp8Policy<D, NT, ring_budget(scratch_bytes(8 * NT, D))>;
     static constexpr int R = RingT::R;
     static constexpr int kTileBytes = RingT::kTileBytes;
     static constexpr int kStageBytes = RingT::kStageBytes;

@@ -1,7 +1,7 @@
 // Tensor-core (mma.sync) decode kernels: bf16 and fp8-e5m2 KV with a bf16
 // query, head_dim 64/128, up to 16 query heads per KV head (one or two
 // 8-wide N tiles).
-#include "pkv_decode.cuh"
+#include "pkv_streamk.cuh"
 
 namespace pkv {
 
@@ -16,10 +16,10 @@ static pkv_status dispatch(const DecodeParams &p, int kv_dtype, cudaStream_t str
 {
     const bool two = p.group > 8;
     if (kv_dtype == PKV_BF16)
-        return two ? launch_policy<MmaBf16Policy<D, 2>>(p, stream)
-                   : launch_policy<MmaBf16Policy<D, 1>>(p, stream);
-    return two ? launch_policy<MmaFp8Policy<D, 2>>(p, stream)
-               : launch_policy<MmaFp8Policy<D, 1>>(p, stream);
+        return two ? launch_any<MmaBf16Policy<D, 2>>(p, stream)
+                   : launch_any<MmaBf16Policy<D, 1>>(p, stream);
+    return two ? launch_any<MmaFp8Policy<D, 2>>(p, stream)
+               : launch_any<MmaFp8Policy<D, 1>>(p, stream);
 }
 
 pkv_status launch_decode_mma(const DecodeParams &p, int kv_dtype, cudaStream_t stream)

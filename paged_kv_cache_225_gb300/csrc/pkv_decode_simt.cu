@@ -1,6 +1,6 @@
 // CUDA-core (FFMA) decode kernels: every KV dtype, head_dim 64/128, up to 16
 // query heads per KV head (padded to a power of two).
-#include "pkv_decode.cuh"
+#include "pkv_streamk.cuh"
 
 namespace pkv {
 
@@ -9,15 +9,15 @@ static pkv_status dispatch_group(const DecodeParams &p, cudaStream_t stream)
 {
     const int G = p.group;
     if (G <= 1)
-        return launch_policy<SimtPolicy<KV, D, 1>>(p, stream);
+        return launch_any<SimtPolicy<KV, D, 1>>(p, stream);
     if (G <= 2)
-        return launch_policy<SimtPolicy<KV, D, 2>>(p, stream);
+        return launch_any<SimtPolicy<KV, D, 2>>(p, stream);
     if (G <= 4)
-        return launch_policy<SimtPolicy<KV, D, 4>>(p, stream);
+        return launch_any<SimtPolicy<KV, D, 4>>(p, stream);
     if (G <= 8)
-        return launch_policy<SimtPolicy<KV, D, 8>>(p, stream);
+        return launch_any<SimtPolicy<KV, D, 8>>(p, stream);
     if (G <= 16)
-        return launch_policy<SimtPolicy<KV, D, 16>>(p, stream);
+        return launch_any<SimtPolicy<KV, D, 16>>(p, stream);
     return PKV_ERR_UNSUPPORTED;
 }
 

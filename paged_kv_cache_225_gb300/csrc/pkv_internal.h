@@ -31,13 +31,16 @@ struct DecodeParams {
     float out_scale;      // v_scale for fp8, else 1
     int partition;        // tokens per work item (multiple of 16)
     int max_parts;        // partitions per sequence the workspace holds
-    int split;            // 1: persistent grid, work counter, partials + merge
+    int split;            // 1: fixed partitions: persistent grid, work counter, partials
+    int streamk;          // 1: stream-K schedule (equal page ranges per CTA)
+    int streamk_max_ctas; // CTAs the stream-K partial slots are sized for
     int fused_merge;      // 1: the CTA finishing a sequence's last partial merges it
     int drop_first_copy;  // test hook: never issue the first copy of item 0
 };
 
 constexpr int kBlockSize = 16;
 constexpr size_t kWorkspaceHeader = 256;
+constexpr int kStreamKMaxCtas = 1024;  // partial slots of the stream-K schedule
 
 // Kernel-unit entry points.  Each launches on `stream` and returns a status
 // (PKV_OK, PKV_ERR_UNSUPPORTED for a shape with no kernel, PKV_ERR_CUDA).

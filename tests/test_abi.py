@@ -52,10 +52,10 @@ def test_partition_plan():
     assert P(4, 4, 4, 64, 65, -1) == 0
     assert P(4, 4, 4, 64, 65, 48) == 48
     assert P(4, 4, 4, 64, 65, 40) == -1           # not a multiple of the block size
-    assert P(128, 64, 8, 128, 514, 0) == 0          # 1024 units, short context: one pass
-    assert P(128, 64, 8, 128, 14626, 0) == 1024     # 70B-shaped layer
-    assert P(8, 64, 8, 128, 32769, 0) == 1024       # long context: split
-    assert P(1, 8, 8, 128, 512, 0) == 64            # few units: small partitions
+    # Automatic: the stream-K schedule, whatever the lengths.
+    for sizes in [(128, 64, 8, 128, 514), (128, 64, 8, 128, 14626), (8, 64, 8, 128, 32769),
+                  (1, 8, 8, 128, 512)]:
+        assert P(*sizes, 0) == pkv.SCHEDULE_STREAMK
 
 
 def test_workspace_size():
@@ -69,6 +69,12 @@ def test_workspace_size():
         return (x + 255) // 256 * 256
     # header | arrival counters [S*Hkv] | partial outputs | partial (m, l)
     assert W(S, Hq, 8, D, L, P) == 256 + a(S * 8 * 4) + a(rows * D * 4) + a(rows * 8)
+    # Stream-K: two partial slots of G rows for each of up to 1024 CTAs,
+    # independent of the lengths.
+    G = Hq // 8
+    rows = 2 * 1024 * G
+    sk = 256 + a(S * 8 * 4) + a(rows * D * 4) + a(rows * 8)
+    assert W(S, Hq, 8, D, L, 0) == sk == W(S, Hq, 8, D, 16, 0)
     with pytest.raises(ValueError):
         W(4, 6, 4, 64, 65, 0)                       # heads do not divide
 
@@ -76,7 +82,7 @@ def test_workspace_size():
 def _decode(**kw):
     args = dict(q=0x1000, q_dtype=BF16, k=0x2000, v=0x3000, kv_dtype=BF16, ks=1.0, vs=1.0,
                 bt=0x4000, sl=0x5000, S=2, Hq=8, Hkv=2, D=128, B=16, N=10, maxb=4, maxl=64,
-                scale=0.1, out=0x6000, out_dtype=F32, ws=0x7000, wsb=1 << 20, part=0, flags=0)
+                scale=0.1, out=0x6000, out_dtype=F32, ws=0x7000, wsb=1 << 26, part=0, flags=0)
     args.update(kw)
     return pkv.lib().pkv_paged_attn_decode(
         args["q"], args["q_dtype"], args["k"], args["v"], args["kv_dtype"], args["ks"], args["vs"],

@@ -166,6 +166,23 @@ def test_long_sequence_32768_single_pass_and_split():
     assert max_abs(a, ref) <= 4e-3 and max_abs(b, ref) <= 4e-3
 
 
+@pytest.mark.parametrize("lens", [[1], [0], [0, 0, 5], [3] * 300, [16] * 7 + [4000],
+                                  [1] * 50 + [20000], [700, 0, 1, 33, 9000, 2]])
+@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2])
+def test_streamk_ranges_cut_units_anywhere(lens, kv_dtype):
+    """Few pages (fewer than CTAs), empty sequences, many tiny units, and one
+    long unit cut across many CTAs next to short ones."""
+    w = _custom(num_seqs=len(lens), num_q_heads=8, num_kv_heads=2, kv_dtype=kv_dtype,
+                garbage="nan", lens=np.array(lens))
+    ref, _, _ = oracle_step(w)
+    d = device_workload(w, DEV)
+    for impl in ("auto", "simt"):
+        out, status, _ = gpu_step(w, d, impl=impl)
+        assert status == 0
+        assert np.isfinite(out).all()
+        assert max_abs(out, ref) <= TOL[kv_dtype]
+
+
 def test_results_are_deterministic():
     w, ref, _, _ = _config("llama3_8b")
     d = device_workload(w, DEV)

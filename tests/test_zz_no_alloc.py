@@ -41,28 +41,31 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls():
     S, Hq, D = w.q.shape
     N, Hkv, _, B = w.k_cache.shape
     max_len = int(w.seq_lens.max())
-    # These sizes split the sequences, so the decode really uses scratch memory.
-    assert pkv.partition_tokens(S, Hq, Hkv, D, max_len) > 0
-    assert 256 < pkv.workspace_size(S, Hq, Hkv, D, max_len) <= NOALLOC_SCRATCH_BYTES
-
-    ref = torch.empty((S, Hq, D), dtype=torch.float32, device=dev)
-    pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["seq_lens"],
-                          w.scale, ref, max_seq_len=max_len)
-    torch.cuda.synchronize()
-    assert pkv.read_status(device=dev) == 0
-    ref_np = ref.cpu().numpy()
-
     f = _noalloc()
     stream = torch.cuda.current_stream(dev).cuda_stream
-    for _ in range(2):
-        out = torch.full((S, Hq, D), float("nan"), dtype=torch.float32, device=dev)
-        rc = f(d["q"].data_ptr(), pkv.BF16, d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
-               pkv.BF16, 1.0, 1.0, d["block_tables"].data_ptr(), d["seq_lens"].data_ptr(), S, Hq,
-               Hkv, D, B, N, w.max_blocks_per_seq, max_len, w.scale, out.data_ptr(), pkv.F32, 0, 0,
-               stream)
-        assert rc == 0
+    # Both schedules that keep partial results in scratch memory: the
+    # automatic (stream-K) one and fixed 256-token partitions.
+    for part in (0, 256):
+        assert pkv.partition_tokens(S, Hq, Hkv, D, max_len, part) != 0
+        assert 256 < pkv.workspace_size(S, Hq, Hkv, D, max_len, part) <= NOALLOC_SCRATCH_BYTES
+
+        ref = torch.empty((S, Hq, D), dtype=torch.float32, device=dev)
+        pkv.paged_attn_decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                              d["seq_lens"], w.scale, ref, max_seq_len=max_len,
+                              partition_tokens=part)
         torch.cuda.synchronize()
-        assert max_abs(out.cpu().numpy(), ref_np) <= TOL[W.BF16]
+        assert pkv.read_status(device=dev) == 0
+        ref_np = ref.cpu().numpy()
+
+        for _ in range(2):
+            out = torch.full((S, Hq, D), float("nan"), dtype=torch.float32, device=dev)
+            rc = f(d["q"].data_ptr(), pkv.BF16, d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
+                   pkv.BF16, 1.0, 1.0, d["block_tables"].data_ptr(), d["seq_lens"].data_ptr(), S,
+                   Hq, Hkv, D, B, N, w.max_blocks_per_seq, max_len, w.scale, out.data_ptr(),
+                   pkv.F32, part, 0, stream)
+            assert rc == 0
+            torch.cuda.synchronize()
+            assert max_abs(out.cpu().numpy(), ref_np) <= TOL[W.BF16]
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
