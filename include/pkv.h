@@ -79,11 +79,14 @@ typedef enum {
  * Workspace bytes pkv_paged_attn_decode needs for these sizes (always >= 256:
  * the first 256 bytes hold the status word and a work counter).
  *   partition_tokens:
- *     0  = automatic: the stream-K schedule.  The flattened (sequence, KV
- *          head, page) space is cut into one equal contiguous range per CTA;
- *          sequences cut by range boundaries are merged with log-sum-exp
- *          weights by the CTA that finishes their last piece.  The workspace
- *          does not depend on the sequence lengths.
+ *     0  = automatic: with at least 608 (sequence, KV head) units, one pass
+ *          per unit when max_seq_len <= 2048, else 2048-token partitions;
+ *          with fewer units, the stream-K schedule (PKV_SCHEDULE_STREAMK):
+ *          the flattened (sequence, KV head, page) space is cut into one
+ *          equal contiguous range per CTA, and sequences cut by range
+ *          boundaries are merged with log-sum-exp weights by the CTA that
+ *          finishes their last piece (workspace independent of the lengths).
+ *    -2  = (PKV_SCHEDULE_STREAMK) the stream-K schedule, whatever the sizes.
  *    -1  = never split: one CTA per (sequence, KV head), one pass.
  *    > 0 = split every sequence into partitions of this many tokens (a
  *          multiple of block_size), scheduled dynamically, merged with

@@ -45,10 +45,23 @@ static int resolve_partition(int num_seqs, int num_q_heads, int num_kv_heads, in
         return -1;
     if (requested == -1)
         return 0;
+    if (requested == kStreamK)
+        return kStreamK;
     if (requested > 0)
         return (requested % kBlockSize == 0) ? requested : -1;
     if (requested != 0)
         return -1;
+    // Automatic choice.  Many (sequence, KV head) units keep every CTA busy
+    // with whole units: one pass each when contexts are short, else 2048-token
+    // items scheduled dynamically (few partials, no per-unit boundaries inside
+    // an item).  Few units -- long contexts on a small batch -- use stream-K,
+    // which splits them evenly across all CTAs.  The threshold is twice the
+    // CTAs resident on a GB300 (two per SM); a fixed number keeps the plan,
+    // and so the workspace size, independent of the current device.
+    const long units = static_cast<long>(num_seqs) * num_kv_heads;
+    const long many = 2L * 2 * 152;
+    if (units >= many)
+        return max_seq_len <= 2048 ? 0 : 2048;
     return kStreamK;
 }
 

@@ -45,6 +45,7 @@
 #define PKV_RING_BYTES_PER_WARP (16 * 1024)
 #endif
 
+
 namespace pkv {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // one second per bounded wait
@@ -127,6 +128,11 @@ struct SimtPolicy {
         float l[GT];
         float o[DJ][GT];
     };
+    static constexpr bool kStaged = false;  // reads K/V straight from the stage
+    static constexpr bool kSharedBegin = true;  // begin() writes the query to shared memory
+    struct Frags {};
+    __device__ static void load(Frags &, const unsigned char *, const unsigned char *, int) {}
+    __device__ static void compute(State &, Frags &, int, int, float) {}
 
     __device__ static float kv_at(const unsigned char *tile, int idx)
     {
@@ -279,13 +285,39 @@ struct SimtPolicy {
 // one N tile from S^T accumulators.  tokA/tokB are the page tokens of the
 // accumulator rows r and r+8 this lane holds; heads 8n+2c, 8n+2c+1.
 struct MmaSoftmax {
-    __device__ static void update(const float (&sacc)[4], int tokA, int tokB, int valid, float c,
+    // Scores may run up to 2^kLazy above the running max before the max is
+    // raised: p = 2^(s - m) then stays <= 2^8, harmless in fp32, and the
+    // cross-lane max reduction and the O rescale are skipped on most pages.
+    // (m, l, O) stay mutually consistent, so the result is the same softmax.
+    static constexpr float kLazy = 8.f;
+
+    __device__ static float ex2(float x)
+    {
+        float y;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+        return y;
+    }
+
+    // Returns true when the running max moved (the caller rescales O by alpha).
+    __device__ static bool update(const float (&sacc)[4], int tokA, int tokB, int valid, float c,
                                   float (&m)[2], float (&l)[2], float (&p)[4], float (&alpha)[2])
     {
         const float s0 = tokA < valid ? sacc[0] * c : -INFINITY;
         const float s1 = tokA < valid ? sacc[1] * c : -INFINITY;
         const float s2 = tokB < valid ? sacc[2] * c : -INFINITY;
         const float s3 = tokB < valid ? sacc[3] * c : -INFINITY;
+        const bool fast = s0 <= m[0] + kLazy && s2 <= m[0] + kLazy && s1 <= m[1] + kLazy &&
+                          s3 <= m[1] + kLazy;
+        if (__all_sync(kFullMask, fast)) {
+            // m finite here: masked positions (s = -inf) give p = 0.
+            p[0] = ex2(s0 - m[0]);
+            p[1] = ex2(s1 - m[1]);
+            p[2] = ex2(s2 - m[0]);
+            p[3] = ex2(s3 - m[1]);
+            l[0] += p[0] + p[2];
+            l[1] += p[1] + p[3];
+            return false;
+        }
         float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -293,16 +325,17 @@ struct MmaSoftmax {
             mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
         }
         const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-        alpha[0] = (m[0] == -INFINITY) ? 0.f : exp2f(m[0] - mn0);
-        alpha[1] = (m[1] == -INFINITY) ? 0.f : exp2f(m[1] - mn1);
-        p[0] = tokA < valid ? exp2f(s0 - mn0) : 0.f;
-        p[1] = tokA < valid ? exp2f(s1 - mn1) : 0.f;
-        p[2] = tokB < valid ? exp2f(s2 - mn0) : 0.f;
-        p[3] = tokB < valid ? exp2f(s3 - mn1) : 0.f;
+        alpha[0] = (m[0] == -INFINITY) ? 0.f : ex2(m[0] - mn0);
+        alpha[1] = (m[1] == -INFINITY) ? 0.f : ex2(m[1] - mn1);
+        p[0] = tokA < valid ? ex2(s0 - mn0) : 0.f;
+        p[1] = tokA < valid ? ex2(s1 - mn1) : 0.f;
+        p[2] = tokB < valid ? ex2(s2 - mn0) : 0.f;
+        p[3] = tokB < valid ? ex2(s3 - mn1) : 0.f;
         l[0] = l[0] * alpha[0] + p[0] + p[2];
         l[1] = l[1] * alpha[1] + p[1] + p[3];
         m[0] = mn0;
         m[1] = mn1;
+        return true;
     }
 };
 
@@ -406,13 +439,18 @@ struct MmaStateBase {
 // bf16 KV: the page tile is [D][16] bf16 (32-byte rows).  K^T fragments come
 // from ldmatrix.trans, V fragments from ldmatrix.  P is split into a bf16 high
 // part and a bf16 residual so that P V keeps ~16 mantissa bits.
-template <int D, int NT, int Budget = PKV_RING_BYTES_PER_WARP>
+//
+// Staged: the whole page is first copied into registers (64 per lane), so
+// the ring stage can be refilled before the math runs; the math then no
+// longer holds a stage, which keeps more copies in flight.
+template <int D, int NT, int Budget = PKV_RING_BYTES_PER_WARP, bool Staged = false>
 struct MmaBf16Policy : MmaStateBase<D, NT> {
     using Base = MmaStateBase<D, NT>;
     using State = typename Base::State;
     using RingT = Ring<PKV_BF16, D, Budget>;
     // The same policy with a separate merge scratch and the ring that fits.
-    using StreamK = MmaBf16Policy<D, NT, ring_budget(scratch_bytes(8 * NT, D))>;
+    // Stream-K stages pages in registers when G <= 8 (no spills there).
+    using StreamK = MmaBf16Policy<D, NT, ring_budget(scratch_bytes(8 * NT, D)), NT == 1>;
     static constexpr int R = RingT::R;
     static constexpr int kTileBytes = RingT::kTileBytes;
     static constexpr int kStageBytes = RingT::kStageBytes;
@@ -421,6 +459,13 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
     static constexpr int GP = 8 * NT;
     static constexpr int kExtraBytes = 0;
     static constexpr int KS = Base::KS, MT = Base::MT;
+    static constexpr bool kStaged = Staged;
+    static constexpr bool kSharedBegin = false;  // begin() only fills registers
+
+    struct Frags {
+        uint32_t k[KS][4];  // K^T A fragments, one per 16-wide k step
+        uint32_t v[MT][4];  // V A fragments, one per 16-row head_dim tile
+    };
 
     __device__ static void begin(State &st, const DecodeParams &p, int s, int hkv, int lane,
                                  unsigned char *)
@@ -429,35 +474,49 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
         Base::template load_q_frags<false>(st, p, s, hkv, lane);
     }
 
-    __device__ static void page(State &st, const unsigned char *sK, const unsigned char *sV,
-                                int valid, int lane, int, unsigned char *, float c)
+    __device__ static void load(Frags &f, const unsigned char *sK, const unsigned char *sV,
+                                int lane)
     {
-        const int r = lane >> 2, cc = lane & 3;
         const int mi = lane >> 3, ri = lane & 7;
         // ldmatrix row addresses.  K (.trans): matrix mi covers head_dim rows
         // 8(mi>>1).. and token half mi&1.  V: rows 8(mi&1).., token half mi>>1.
         const uint32_t ka = smem_u32(sK) + (ri + 8 * (mi >> 1)) * 32 + (mi & 1) * 16;
         const uint32_t va = smem_u32(sV) + (ri + 8 * (mi & 1)) * 32 + (mi >> 1) * 16;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
+            ldsm_x4_t(f.k[ks], ka + ks * 16 * 32);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+            ldsm_x4(f.v[mt], va + mt * 16 * 32);
+    }
 
-        float sacc[NT][4];
+    __device__ static void compute(State &st, Frags &f, int valid, int lane, float c)
+    {
+        const int r = lane >> 2, cc = lane & 3;
+        // S^T = K^T Q^T in two independent accumulation chains (even / odd k).
+        float sacc[NT][4], sodd[NT][4];
 #pragma unroll
         for (int n = 0; n < NT; ++n)
-            sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a[4];
-            ldsm_x4_t(a, ka + ks * 16 * 32);
+            for (int e = 0; e < 4; ++e)
+                sacc[n][e] = sodd[n][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
             for (int n = 0; n < NT; ++n)
-                mma_bf16(sacc[n], a, st.qf[ks][n][0], st.qf[ks][n][1]);
-        }
+                mma_bf16((ks & 1) ? sodd[n] : sacc[n], f.k[ks], st.qf[ks][n][0], st.qf[ks][n][1]);
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sacc[n][e] += sodd[n][e];
 
         uint32_t bh0[NT], bh1[NT], bl0[NT], bl1[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             float pr[4], alpha[2];
-            MmaSoftmax::update(sacc[n], r, r + 8, valid, c, st.m[n], st.l[n], pr, alpha);
-            Base::rescale(st, n, alpha);
+            if (MmaSoftmax::update(sacc[n], r, r + 8, valid, c, st.m[n], st.l[n], pr, alpha))
+                Base::rescale(st, n, alpha);
             const uint32_t hx = pack_bf16(pr[0], pr[1]);
             const uint32_t hy = pack_bf16(pr[2], pr[3]);
             const uint32_t lx = pack_bf16(pr[0] - bf16_lo(hx), pr[1] - bf16_hi(hx));
@@ -468,26 +527,39 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
             bl1[n] = movmatrix_t(ly);
         }
 
-        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-        if (valid < kBlockSize) {
-            mlo = (2 * cc < valid ? 0x0000ffffu : 0u) | (2 * cc + 1 < valid ? 0xffff0000u : 0u);
-            mhi = (8 + 2 * cc < valid ? 0x0000ffffu : 0u) |
-                  (9 + 2 * cc < valid ? 0xffff0000u : 0u);
-        }
+        if (valid < kBlockSize) {  // last page of a sequence: zero the unused tokens
+            const uint32_t mlo = (2 * cc < valid ? 0x0000ffffu : 0u) |
+                                 (2 * cc + 1 < valid ? 0xffff0000u : 0u);
+            const uint32_t mhi = (8 + 2 * cc < valid ? 0x0000ffffu : 0u) |
+                                 (9 + 2 * cc < valid ? 0xffff0000u : 0u);
 #pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-            uint32_t a[4];
-            ldsm_x4(a, va + mt * 16 * 32);
-            a[0] &= mlo;
-            a[1] &= mlo;
-            a[2] &= mhi;
-            a[3] &= mhi;
-#pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                mma_bf16(st.o[mt][n], a, bh0[n], bh1[n]);
-                mma_bf16(st.o[mt][n], a, bl0[n], bl1[n]);
+            for (int mt = 0; mt < MT; ++mt) {
+                f.v[mt][0] &= mlo;
+                f.v[mt][1] &= mlo;
+                f.v[mt][2] &= mhi;
+                f.v[mt][3] &= mhi;
             }
         }
+        // High parts of P first, residuals second: products into the same
+        // accumulator sit MT instructions apart.
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                mma_bf16(st.o[mt][n], f.v[mt], bh0[n], bh1[n]);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                mma_bf16(st.o[mt][n], f.v[mt], bl0[n], bl1[n]);
+    }
+
+    __device__ static void page(State &st, const unsigned char *sK, const unsigned char *sV,
+                                int valid, int lane, int, unsigned char *, float c)
+    {
+        Frags f;
+        load(f, sK, sV, lane);
+        compute(st, f, valid, lane, c);
     }
 
     __device__ static void finish(State &st, float *so, float *sm, float *sl, int lane)
@@ -499,14 +571,16 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
 // fp8-e5m2 KV: the page tile is [D][16] bytes (16-byte rows), read by
 // ldmatrix as 16-bit pairs; byte_perm widens each code to an f16 (the code
 // is the f16's high byte, exactly).  Token order inside a fragment is
-// permuted consistently on both operands (see the byte selectors).
-template <int D, int NT, int Budget = PKV_RING_BYTES_PER_WARP>
+// permuted consistently on both operands (see the byte selectors).  Staged
+// like the bf16 policy: 32 registers hold a page's raw codes.
+template <int D, int NT, int Budget = PKV_RING_BYTES_PER_WARP, bool Staged = false>
 struct MmaFp8Policy : MmaStateBase<D, NT> {
     using Base = MmaStateBase<D, NT>;
     using State = typename Base::State;
     using RingT = Ring<PKV_FP8_E5M2, D, Budget>;
     // The same policy with a separate merge scratch and the ring that fits.
-    using StreamK = MmaFp8Policy<D, NT, ring_budget(scratch_bytes(8 * NT, D))>;
+    // Stream-K stages pages in registers when G <= 8 (no spills there).
+    using StreamK = MmaFp8Policy<D, NT, ring_budget(scratch_bytes(8 * NT, D)), NT == 1>;
     static constexpr int R = RingT::R;
     static constexpr int kTileBytes = RingT::kTileBytes;
     static constexpr int kStageBytes = RingT::kStageBytes;
@@ -515,8 +589,15 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
     static constexpr int GP = 8 * NT;
     static constexpr int kExtraBytes = 0;
     static constexpr int KS = Base::KS, MT = Base::MT;
+    static constexpr bool kStaged = Staged;
+    static constexpr bool kSharedBegin = false;  // begin() only fills registers
     static constexpr uint32_t kSelEven = 0x2404u;  // bytes 0, 2 -> high bytes of two f16
     static constexpr uint32_t kSelOdd = 0x3414u;   // bytes 1, 3 -> high bytes of two f16
+
+    struct Frags {
+        uint32_t k[KS / 2][4];  // raw codes of 32 head_dim rows of K per entry
+        uint32_t v[MT / 2][4];  // raw codes of 32 head_dim rows of V per entry
+    };
 
     __device__ static void begin(State &st, const DecodeParams &p, int s, int hkv, int lane,
                                  unsigned char *)
@@ -525,24 +606,35 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
         Base::template load_q_frags<true>(st, p, s, hkv, lane);
     }
 
-    __device__ static void page(State &st, const unsigned char *sK, const unsigned char *sV,
-                                int valid, int lane, int, unsigned char *, float c)
+    __device__ static void load(Frags &f, const unsigned char *sK, const unsigned char *sV,
+                                int lane)
     {
-        const int r = lane >> 2, cc = lane & 3;
         const int mi = lane >> 3, ri = lane & 7;
         // Both tiles: matrix mi of one ldmatrix.x4 is head_dim rows 8mi..8mi+7.
         const uint32_t ka = smem_u32(sK) + (8 * mi + ri) * 16;
         const uint32_t va = smem_u32(sV) + (8 * mi + ri) * 16;
+#pragma unroll
+        for (int kp = 0; kp < KS / 2; ++kp)
+            ldsm_x4_t(f.k[kp], ka + kp * 32 * 16);
+#pragma unroll
+        for (int mp = 0; mp < MT / 2; ++mp)
+            ldsm_x4(f.v[mp], va + mp * 32 * 16);
+    }
 
-        // S^T: A row r <-> token 2r, row r+8 <-> token 2r+1.
-        float sacc[NT][4];
+    __device__ static void compute(State &st, Frags &f, int valid, int lane, float c)
+    {
+        const int r = lane >> 2, cc = lane & 3;
+        // S^T: A row r <-> token 2r, row r+8 <-> token 2r+1; two accumulation
+        // chains (the two k steps of each ldmatrix.x4).
+        float sacc[NT][4], sodd[NT][4];
 #pragma unroll
         for (int n = 0; n < NT; ++n)
-            sacc[n][0] = sacc[n][1] = sacc[n][2] = sacc[n][3] = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sacc[n][e] = sodd[n][e] = 0.f;
 #pragma unroll
         for (int kp = 0; kp < KS / 2; ++kp) {
-            uint32_t w[4];
-            ldsm_x4_t(w, ka + kp * 32 * 16);
+            const uint32_t *w = f.k[kp];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint32_t a[4] = {e5m2x2_to_f16x2(w[2 * h], kSelEven),
@@ -551,17 +643,24 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
                                        e5m2x2_to_f16x2(w[2 * h + 1], kSelOdd)};
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
-                    mma_f16(sacc[n], a, st.qf[2 * kp + h][n][0], st.qf[2 * kp + h][n][1]);
+                    mma_f16(h ? sodd[n] : sacc[n], a, st.qf[2 * kp + h][n][0],
+                            st.qf[2 * kp + h][n][1]);
             }
         }
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sacc[n][e] += sodd[n][e];
 
         // P^T: k slots (2c, 2c+1) <-> tokens (4c, 4c+2), (2c+8, 2c+9) <-> (4c+1, 4c+3).
         uint32_t b0[NT], b1[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             float pr[4], alpha[2];
-            MmaSoftmax::update(sacc[n], 2 * r, 2 * r + 1, valid, c, st.m[n], st.l[n], pr, alpha);
-            Base::rescale(st, n, alpha);
+            if (MmaSoftmax::update(sacc[n], 2 * r, 2 * r + 1, valid, c, st.m[n], st.l[n], pr,
+                                   alpha))
+                Base::rescale(st, n, alpha);
             b0[n] = movmatrix_t(pack_f16(pr[0], pr[1]));
             b1[n] = movmatrix_t(pack_f16(pr[2], pr[3]));
         }
@@ -574,8 +673,7 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
         }
 #pragma unroll
         for (int mp = 0; mp < MT / 2; ++mp) {
-            uint32_t w[4];
-            ldsm_x4(w, va + mp * 32 * 16);
+            const uint32_t *w = f.v[mp];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint32_t a[4] = {e5m2x2_to_f16x2(w[2 * h], kSelEven) & me,
@@ -587,6 +685,14 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
                     mma_f16(st.o[2 * mp + h][n], a, b0[n], b1[n]);
             }
         }
+    }
+
+    __device__ static void page(State &st, const unsigned char *sK, const unsigned char *sV,
+                                int valid, int lane, int, unsigned char *, float c)
+    {
+        Frags f;
+        load(f, sK, sV, lane);
+        compute(st, f, valid, lane, c);
     }
 
     __device__ static void finish(State &st, float *so, float *sm, float *sl, int lane)
@@ -869,18 +975,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
                 }
                 break;
             }
-            if ((okmask >> stg) & 1u) {
-                const int tok0 = (pg0 + warp + kWarps * i) * kBlockSize;
-                const int valid = min(kBlockSize, t1 - tok0);
-                const unsigned char *sk = ring + stg * Pol::kStageBytes;
-                Pol::page(st, sk, sk + Pol::kTileBytes, valid, lane, warp, extra, c);
+            const bool have = (okmask >> stg) & 1u;
+            const int tok0 = (pg0 + warp + kWarps * i) * kBlockSize;
+            const int valid = min(kBlockSize, t1 - tok0);
+            const unsigned char *sk = ring + stg * Pol::kStageBytes;
+            typename Pol::Frags fr;
+            if (have) {
+                if constexpr (Pol::kStaged)
+                    Pol::load(fr, sk, sk + Pol::kTileBytes, lane);
+                else
+                    Pol::page(st, sk, sk + Pol::kTileBytes, valid, lane, warp, extra, c);
             }
+            // The stage is free: reads are ordered before the next bulk copy.
             fence_proxy_async();
             __syncwarp();
             if (issued < nw) {
                 issue(issued);
                 ++issued;
             }
+            if constexpr (Pol::kStaged)
+                if (have)
+                    Pol::compute(st, fr, valid, lane, c);
         }
         pages_done += nw;
 
@@ -895,10 +1010,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
         merge_item<D, Pol::GP>(p, smem, Pol::kRingBytes, s, hkv, part, nparts);
         if (nparts > 1 && p.fused_merge) {
             // Publish this partial; the CTA that completes the sequence's last
-            // partial merges all of them (threadfence-reduction pattern).
-            __threadfence();
+            // partial merges all of them.  The barrier orders every thread's
+            // partial writes before thread 0's gpu-scope fence and arrival.
             __syncthreads();
             if (threadIdx.x == 0) {
+                __threadfence();
                 const unsigned old =
                     atomicAdd(p.arrive + static_cast<size_t>(s) * Hkv + hkv, 1u);
                 s_last = (old == static_cast<unsigned>(nparts - 1)) ? 1 : 0;

@@ -322,14 +322,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
     // ---------------------------------------------- segments (all warps)
     Unit su = start;
     bool aborted = false;
+    typename Pol::State st;
+    Pol::begin(st, p, su.s, su.hkv, lane, extra);
+    __syncthreads();  // policy shared data (SIMT query) is ready
     for (int k = 0;; ++k) {
         const long long lo = su.off > a ? su.off : a;
         const long long hi = (su.off + su.np < b) ? su.off + su.np : b;
         const bool complete = (lo == su.off) && (hi == su.off + su.np);
-
-        typename Pol::State st;
-        Pol::begin(st, p, su.s, su.hkv, lane, extra);
-        __syncthreads();  // policy shared data (SIMT query) is ready
+        const bool last = hi >= b;
 
         // This warp's pages of the segment: g in [lo, hi), g == a + warp (mod 4).
         long long g = lo + ((warp - ((lo - a) & 3)) & 3);
@@ -347,30 +347,47 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
                 aborted = true;
                 break;
             }
-            if ((okmask >> stg) & 1u) {
-                const int pg = static_cast<int>(g - su.off);
-                const int valid = min(kBlockSize, su.L - pg * kBlockSize);
-                const unsigned char *sk = ring + stg * Pol::kStageBytes;
-                Pol::page(st, sk, sk + Pol::kTileBytes, valid, lane, warp, extra, c);
+            const bool have = (okmask >> stg) & 1u;
+            const int valid = min(kBlockSize, su.L - static_cast<int>(g - su.off) * kBlockSize);
+            const unsigned char *sk = ring + stg * Pol::kStageBytes;
+            typename Pol::Frags fr;
+            if (have) {
+                if constexpr (Pol::kStaged)
+                    Pol::load(fr, sk, sk + Pol::kTileBytes, lane);
+                else
+                    Pol::page(st, sk, sk + Pol::kTileBytes, valid, lane, warp, extra, c);
             }
             ++pos_c;
+            // The stage is free: reads are ordered before the next bulk copy.
             fence_proxy_async();
             __syncwarp();
             refill();
+            if constexpr (Pol::kStaged)
+                if (have)
+                    Pol::compute(st, fr, valid, lane, c);
         }
 
         // ------------------------------------------ merge the segment
         float *mine = scratch + warp * kScratchFloats;
         Pol::finish(st, mine, mine + Pol::GP * D, mine + Pol::GP * D + Pol::GP, lane);
+        Unit nu = su;
+        if (!last)
+            unit_next(p, nu);
+        // Register-only policies start the next segment's query loads now, so
+        // their latency overlaps the merge below.
+        if constexpr (!Pol::kSharedBegin)
+            if (!last)
+                Pol::begin(st, p, nu.s, nu.hkv, lane, extra);
         __syncthreads();
         const int slot = (k == 0) ? 0 : 1;
         merge_segment<D, Pol::GP>(p, scratch, su.s, su.hkv, complete, cta, slot);
         if (!complete) {
             // Publish this partial; the CTA writing the unit's last partial
-            // merges them all (threadfence-reduction pattern).
-            __threadfence();
+            // merges them all.  The barrier orders every thread's partial
+            // writes before thread 0's gpu-scope fence and arrival.
             __syncthreads();
             if (threadIdx.x == 0) {
+                __threadfence();
                 const int n_ch =
                     owner_cta(su.off + su.np - 1, T, C) - owner_cta(su.off, T, C) + 1;
                 const unsigned old =
@@ -390,9 +407,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
                     mbar_wait_bounded(&bars[q % R], (q / R) & 1u, kWaitLimitNs);
             break;
         }
-        if (hi >= b)
+        if (last)
             break;
-        unit_next(p, su);
+        su = nu;
+        if constexpr (Pol::kSharedBegin) {
+            Pol::begin(st, p, su.s, su.hkv, lane, extra);
+            __syncthreads();  // policy shared data (SIMT query) is ready
+        }
     }
 }
 

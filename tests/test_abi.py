@@ -52,10 +52,14 @@ def test_partition_plan():
     assert P(4, 4, 4, 64, 65, -1) == 0
     assert P(4, 4, 4, 64, 65, 48) == 48
     assert P(4, 4, 4, 64, 65, 40) == -1           # not a multiple of the block size
-    # Automatic: the stream-K schedule, whatever the lengths.
-    for sizes in [(128, 64, 8, 128, 514), (128, 64, 8, 128, 14626), (8, 64, 8, 128, 32769),
-                  (1, 8, 8, 128, 512)]:
-        assert P(*sizes, 0) == pkv.SCHEDULE_STREAMK
+    # Automatic: many (sequence, KV head) units -> one pass (short contexts) or
+    # 2048-token items; few units -> stream-K.
+    assert P(128, 64, 8, 128, 514, 0) == 0              # fp8 chat mix: 1024 units
+    assert P(128, 64, 8, 128, 14626, 0) == 2048         # 70B-shaped layer: 1024 units
+    assert P(64, 32, 8, 128, 4097, 0) == pkv.SCHEDULE_STREAMK    # 8B-shaped: 512 units
+    assert P(8, 64, 8, 128, 32769, 0) == pkv.SCHEDULE_STREAMK    # long context: 64 units
+    assert P(1, 8, 8, 128, 512, 0) == pkv.SCHEDULE_STREAMK
+    assert P(128, 64, 8, 128, 14626, -2) == pkv.SCHEDULE_STREAMK   # asked for explicitly
 
 
 def test_workspace_size():

@@ -54,13 +54,23 @@ def test_config_parity_simt(name):
 
 
 @pytest.mark.parametrize("name", ["llama3_8b", "long_split", "fp8_chat"])
-@pytest.mark.parametrize("part", [-1, 16, 48, 256, 4096])
+@pytest.mark.parametrize("part", [-2, -1, 16, 48, 256, 4096])
 @pytest.mark.parametrize("merge", ["in_kernel", "merge_kernel"])
 def test_config_parity_forced_split(name, part, merge):
     w, ref, kc, vc = _config(name)
     d = device_workload(w, DEV)
     flags = pkv.FLAG_SEPARATE_MERGE if merge == "merge_kernel" else 0
     out, status, _ = gpu_step(w, d, partition_tokens=part, flags=flags)
+    assert status == 0
+    assert max_abs(out, ref) <= TOL[w.cfg.kv_dtype]
+
+
+@pytest.mark.parametrize("name", ["llama3_70b"])
+@pytest.mark.parametrize("part", [-2, -1, 512])
+def test_70b_layer_every_schedule(name, part):
+    w, ref, kc, vc = _config(name)
+    d = device_workload(w, DEV)
+    out, status, _ = gpu_step(w, d, partition_tokens=part)
     assert status == 0
     assert max_abs(out, ref) <= TOL[w.cfg.kv_dtype]
 
@@ -180,6 +190,35 @@ def test_streamk_ranges_cut_units_anywhere(lens, kv_dtype):
         out, status, _ = gpu_step(w, d, impl=impl)
         assert status == 0
         assert np.isfinite(out).all()
+        assert max_abs(out, ref) <= TOL[kv_dtype]
+
+
+@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2])
+@pytest.mark.parametrize("direction", [1.0, -1.0])
+def test_scores_ramping_across_the_running_max(kv_dtype, direction):
+    """Keys scaled so each query head's scores drift steadily along the sequence
+    (by ~0.05 per token in log2 units up to ~+-60): the running max is raised
+    many times by small steps, exercising the lazily-rescaled softmax."""
+    w = _custom(num_seqs=3, num_q_heads=16, num_kv_heads=2, kv_dtype=kv_dtype,
+                lens=np.array([2500, 1200, 777]), seed=21)
+    q = W.storage_to_float32(w.q, w.cfg.q_dtype)
+    k = W.storage_to_float32(w.k_cache, kv_dtype)
+    B = 16
+    for s_i, L in enumerate(w.seq_lens):
+        for hkv in range(2):
+            qm = q[s_i, hkv * 8:(hkv + 1) * 8].mean(axis=0)       # shared direction
+            qm = qm / np.linalg.norm(qm)
+            for t in range(int(L)):
+                blk = w.block_tables[s_i, t // B]
+                ramp = direction * (t / float(L) - 0.5) * 120.0  # log2 units of score
+                target = ramp / (w.scale * np.log2(np.e)) / max(np.linalg.norm(qm), 1e-6)
+                k[blk, hkv, :, t % B] = (qm * target / 16.0 + 0.1 * k[blk, hkv, :, t % B])
+    w.k_cache = W.round_to_storage(k.astype(np.float32), kv_dtype)
+    ref, _, _ = oracle_step(w, append=False)
+    d = device_workload(w, DEV)
+    for impl in ("auto", "simt"):
+        out, status, _ = gpu_step(w, d, impl=impl, append=False)
+        assert status == 0
         assert max_abs(out, ref) <= TOL[kv_dtype]
 
 
