@@ -64,12 +64,16 @@ def parse_args(argv=None):
     return ap.parse_args(argv)
 
 
+# Sources that do not define or launch the decode kernels.
+_NOT_DECODE = {"pkv_cache.cu", "pkv_noalloc.cu"}
+
+
 def source_hash() -> str:
-    """Hash of the kernel sources; ties a stored ncu traffic figure to them."""
+    """Hash of the decode-kernel sources; ties a stored ncu traffic figure to them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_225_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
+        if f.endswith((".cu", ".cuh", ".h")) and f not in _NOT_DECODE:
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

@@ -17,9 +17,9 @@
 
 #include "pkv_internal.h"
 
-namespace {
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
 
-__device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCRATCH_BYTES];
+namespace {
 
 constexpr int kMaxDevices = 256;
 std::mutex g_scratch_mu;
