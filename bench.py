@@ -9,6 +9,11 @@ heads, head_dim 128, 16-token blocks, bf16 KV, lognormal lengths with median
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--config NAME] [--kernel auto|simt|mma] [--partition P]
+                    [--unfused] [--eager]
+
+The timed steps replay the step captured once as a CUDA graph (``--eager``
+launches each step from Python instead); ``--unfused`` runs the cache write
+and the decode as two launches.
 
 ``--impl reference`` times the fp64 CPU oracle on this host's cores on a
 bounded sample of the same workload (the reference arm of this repository).
@@ -61,6 +66,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="cache write and decode as two launches instead of one")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every step from Python instead of replaying a CUDA graph")
     return ap.parse_args(argv)
 
 
@@ -203,6 +212,10 @@ def run_ours(args):
     lens = (w.seq_lens + 1).astype(np.int32)           # each step appends one token
     max_len = int(lens.max())
     ab = algorithmic_bytes(w, lens)
+    # The fused launch also reads the new K/V rows and writes them to the cache.
+    new_rows = cfg.num_seqs * cfg.num_kv_heads * cfg.head_dim * 2
+    append_bytes = 0 if args.unfused else \
+        new_rows * (W.ELEM_BYTES[cfg.q_dtype] + W.ELEM_BYTES[cfg.kv_dtype])
 
     def t(a, dt):
         a = np.ascontiguousarray(a)
@@ -214,9 +227,11 @@ def run_ours(args):
 
     host = {
         "q": t(w.q, cfg.q_dtype), "new_k": t(w.new_k, cfg.q_dtype),
-        "new_v": t(w.new_v, cfg.q_dtype), "slots": torch.from_numpy(w.slot_mapping),
+        "new_v": t(w.new_v, cfg.q_dtype),
         "tables": torch.from_numpy(w.block_tables), "lens": torch.from_numpy(lens),
     }
+    if args.unfused:
+        host["slots"] = torch.from_numpy(w.slot_mapping)
     kc = t(w.k_cache, cfg.kv_dtype).to(dev)
     vc = t(w.v_cache, cfg.kv_dtype).to(dev)
     d = {k: v.to(dev) for k, v in host.items()}
@@ -228,13 +243,22 @@ def run_ours(args):
     ks = vs = cfg.kv_scale
 
     def step(dd, ev=None):
-        pkv.reshape_and_cache(dd["new_k"], dd["new_v"], dd["slots"], kc, vc, k_scale=ks,
-                              v_scale=vs)
+        if args.unfused:
+            pkv.reshape_and_cache(dd["new_k"], dd["new_v"], dd["slots"], kc, vc, k_scale=ks,
+                                  v_scale=vs)
         if ev is not None:
             ev[0].record(stream)
-        pkv.paged_attn_decode(dd["q"], kc, vc, dd["tables"], dd["lens"], w.scale, out,
-                              k_scale=ks, v_scale=vs, max_seq_len=max_len,
-                              partition_tokens=args.partition, impl=args.kernel, workspace=ws)
+        if args.unfused:
+            pkv.paged_attn_decode(dd["q"], kc, vc, dd["tables"], dd["lens"], w.scale, out,
+                                  k_scale=ks, v_scale=vs, max_seq_len=max_len,
+                                  partition_tokens=args.partition, impl=args.kernel,
+                                  workspace=ws)
+        else:
+            pkv.paged_attn_decode_append(dd["q"], dd["new_k"], dd["new_v"], kc, vc,
+                                         dd["tables"], dd["lens"], w.scale, out, k_scale=ks,
+                                         v_scale=vs, max_seq_len=max_len,
+                                         partition_tokens=args.partition, impl=args.kernel,
+                                         workspace=ws)
         if ev is not None:
             ev[1].record(stream)
 
@@ -246,23 +270,58 @@ def run_ours(args):
         raise RuntimeError(f"device status {pkv.STATUS.get(status, status)} during warm-up")
 
     K = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if args.eager:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    else:
+        # The step (workspace memset + kernel launches) captured once as a
+        # CUDA graph and replayed K times: no CPU launch gaps on small layers.
+        graph_stream = torch.cuda.Stream(dev)
+        graph_stream.wait_stream(stream)
+        g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step, stream=graph_stream):
+            step(d)
+        g_call = None
+        if args.unfused:  # the decode call alone, for the roofline timing
+            g_call = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_call, stream=graph_stream):
+                pkv.paged_attn_decode(d["q"], kc, vc, d["tables"], d["lens"], w.scale, out,
+                                      k_scale=ks, v_scale=vs, max_seq_len=max_len,
+                                      partition_tokens=args.partition, impl=args.kernel,
+                                      workspace=ws)
+        stream.wait_stream(graph_stream)
+        for _ in range(3):
+            g_step.replay()
+        torch.cuda.synchronize()
     sampler = ClockSampler(local, enabled=not args.no_clocks)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     t0.record(stream)
     for i in range(K):
-        step(d, evs[i])
+        if args.eager:
+            step(d, evs[i])
+        else:
+            g_step.replay()
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
     elapsed_ms = t0.elapsed_time(t1)
-    decode_ms = [a.elapsed_time(b) for a, b in evs]
+    if args.eager:
+        decode_ms = [a.elapsed_time(b) for a, b in evs]
+    elif g_call is None:
+        decode_ms = [elapsed_ms / K]  # the step is the one decode launch
+    else:
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(K):
+            g_call.replay()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        decode_ms = [c0.elapsed_time(c1) / K]
     elapsed_ms = max_over_ranks(elapsed_ms)
     status = pkv.read_status(ws)
     if status != 0:
@@ -301,13 +360,14 @@ def run_ours(args):
     kv_gbs = whole_job_rate(ab["kv"], world, ms_step * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
     dec_ms = statistics.mean(decode_ms)
-    achieved = ab["total"] / (dec_ms * 1e-3) / 1e9
+    launch_bytes = ab["total"] + append_bytes
+    achieved = launch_bytes / (dec_ms * 1e-3) / 1e9
     kernel_impl = args.kernel
     if kernel_impl == "auto":
         kernel_impl = "mma" if (cfg.kv_dtype != W.F32 and cfg.q_dtype == W.BF16) else "simt"
     traffic = stored_traffic(args.config, kernel_impl)
-    # Cache write + decode; a second merge kernel only when asked for.
-    launches_per_step = 2
+    # One fused launch (or cache write + decode when --unfused).
+    launches_per_step = 2 if args.unfused else 1
     line = {
         "metric": METRIC, "value": kv_gbs, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -325,14 +385,21 @@ def run_ours(args):
                    "l2": f"no flush: KV read per step ({ab['kv'] / 1e9:.2f} GB) exceeds L2 "
                          "(129 MB)" if ab["kv"] > 256e6 else
                          "no flush: KV per step smaller than 2x L2 (reported, not corrected)",
-                   "step": "reshape_and_cache of 1 token/seq + paged decode over L+1"},
+                   "step": ("reshape_and_cache of 1 token/seq, then paged decode over L+1"
+                            if args.unfused else
+                            "one launch: cache write of 1 token/seq fused into paged decode "
+                            "over L+1"),
+                   "launch": "eager from Python" if args.eager else
+                             "step captured once as a CUDA graph, replayed per step"},
         "tokens_per_s": whole_job_rate(S, world, ms_step * 1e-3),
         "pct_hbm_peak": 100.0 * ab["total"] / (ms_step * 1e-3) / 1e9 / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": f"paged_attn_decode call ({kernel_impl}; mean of {K} launches, "
-                               "CUDA events on the launch stream)",
-                     "algorithmic_bytes_per_launch": ab["total"],
+                     "kernel": (f"paged_attn_decode{'' if args.unfused else '_append'} call "
+                                f"({kernel_impl}; mean of {K} launches, CUDA events on the "
+                                "launch stream" + (")" if args.eager else
+                                                   ", CUDA-graph replays)")),
+                     "algorithmic_bytes_per_launch": launch_bytes,
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "gpu_launches": K * launches_per_step,
         "clocks": clocks,

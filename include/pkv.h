@@ -155,6 +155,30 @@ pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype,
                                  int partition_tokens, int flags, void *stream);
 
 /*
+ * One decode step with the cache write fused in: for every sequence s with
+ * seq_lens[s] > 0, its new token is logical position seq_lens[s] - 1; its
+ * K/V rows new_k[s], new_v[s] ([num_seqs, num_kv_heads, head_dim] of
+ * new_dtype, F32 or BF16) are converted and written into that position's
+ * slot of k_cache / v_cache (block block_tables[s][(L-1)/16], offset
+ * (L-1)%16), and the attention over the seq_lens[s] tokens includes them.
+ * Bit-identical to pkv_reshape_and_cache of those slots followed by
+ * pkv_paged_attn_decode, in one launch ("Inference optimization" lesson,
+ * section "Caches de KV": compute K, V only for the new token, append, attend).
+ * The block holding position L-1 must not be shared with another sequence.
+ * Other arguments, errors and the workspace as for pkv_paged_attn_decode.
+ */
+pkv_status pkv_paged_attn_decode_append(const void *q, pkv_dtype q_dtype, const void *new_k,
+                                        const void *new_v, pkv_dtype new_dtype, void *k_cache,
+                                        void *v_cache, pkv_dtype kv_dtype, float k_scale,
+                                        float v_scale, const int32_t *block_tables,
+                                        const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int num_blocks, int max_blocks_per_seq, int max_seq_len,
+                                        float scale, void *out, pkv_dtype out_dtype,
+                                        void *workspace, size_t workspace_bytes,
+                                        int partition_tokens, int flags, void *stream);
+
+/*
  * Decode without a caller workspace (the pages have no counterpart; this is
  * an interface for callers that cannot allocate device memory, e.g. a plugin
  * inside a runtime that owns all device memory, or a loop where cudaMalloc's

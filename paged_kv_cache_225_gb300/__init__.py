@@ -20,7 +20,8 @@ import torch
 
 from . import build as _build
 
-__all__ = ["paged_attn_decode", "reshape_and_cache", "workspace_size", "partition_tokens",
+__all__ = ["paged_attn_decode", "paged_attn_decode_append", "reshape_and_cache",
+           "workspace_size", "partition_tokens",
            "read_status", "PkvError", "lib", "F32", "BF16", "FP8_E5M2"]
 
 F32, BF16, FP8_E5M2 = 0, 1, 2
@@ -61,6 +62,10 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.pkv_paged_attn_decode.argtypes = [vp, i, vp, vp, i, f, f, vp, vp, i, i, i, i, i, i,
                                                 i, i, f, vp, i, vp, sz, i, i, vp]
             L.pkv_paged_attn_decode.restype = i
+            L.pkv_paged_attn_decode_append.argtypes = [vp, i, vp, vp, i, vp, vp, i, f, f, vp, vp,
+                                                       i, i, i, i, i, i, i, i, f, vp, i, vp, sz, i,
+                                                       i, vp]
+            L.pkv_paged_attn_decode_append.restype = i
             L.pkv_reshape_and_cache.argtypes = [vp, vp, i, vp, i, i, i, i, i, vp, vp, i, f, f, vp,
                                                 vp]
             L.pkv_reshape_and_cache.restype = i
@@ -180,6 +185,60 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
         _stream(dev, stream))
     if rc != 0:
         raise PkvError(rc, "pkv_paged_attn_decode")
+    return out
+
+
+def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.Tensor,
+                             k_cache: torch.Tensor, v_cache: torch.Tensor,
+                             block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                             out: torch.Tensor, *, k_scale: float = 1.0, v_scale: float = 1.0,
+                             max_seq_len: Optional[int] = None, partition_tokens: int = 0,
+                             impl: str = "auto", workspace: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None,
+                             flags: int = 0) -> torch.Tensor:
+    """One decode step with the cache write fused in.
+
+    new_k, new_v [S, Hkv, D] (f32/bf16) are the K/V rows of each sequence's
+    new token, logical position seq_lens[s] - 1 (seq_lens include it); they
+    are written into the cache and attended in the same launch.  Other
+    arguments as for ``paged_attn_decode``.  Returns ``out``.
+    """
+    dev = q.device
+    for t, name, nd in ((q, "q", 3), (new_k, "new_k", 3), (new_v, "new_v", 3),
+                        (k_cache, "k_cache", 4), (v_cache, "v_cache", 4),
+                        (block_tables, "block_tables", 2), (seq_lens, "seq_lens", 1),
+                        (out, "out", 3)):
+        _check(t, name, nd, dev)
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must have the same shape and dtype")
+    S, Hq, D = q.shape
+    N, Hkv, D2, B = k_cache.shape
+    if (D2 != D or out.shape != q.shape or block_tables.shape[0] != S
+            or seq_lens.shape[0] != S or new_k.shape != (S, Hkv, D)
+            or new_v.shape != new_k.shape or new_v.dtype != new_k.dtype):
+        raise ValueError("inconsistent shapes")
+    max_blocks = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_blocks * B
+    L = lib()
+    need = L.pkv_paged_attn_workspace_size(S, Hq, Hkv, D, B, max_seq_len, partition_tokens)
+    if need == 0:
+        raise ValueError("invalid sizes or partition_tokens")
+    if workspace is None:
+        workspace = get_workspace(need, dev)
+    flags |= IMPL[impl]
+    rc = L.pkv_paged_attn_decode_append(
+        q.data_ptr(), _dtype_code(q, "q"), new_k.data_ptr(), new_v.data_ptr(),
+        _dtype_code(new_k, "new_k"), k_cache.data_ptr(), v_cache.data_ptr(),
+        _dtype_code(k_cache, "k_cache"), float(k_scale), float(v_scale), block_tables.data_ptr(),
+        seq_lens.data_ptr(), S, Hq, Hkv, D, B, N, max_blocks, int(max_seq_len), float(scale),
+        out.data_ptr(), _dtype_code(out, "out"), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), int(partition_tokens), int(flags),
+        _stream(dev, stream))
+    if rc != 0:
+        raise PkvError(rc, "pkv_paged_attn_decode_append")
     return out
 
 

@@ -129,14 +129,21 @@ int pkv_paged_attn_partition_tokens(int num_seqs, int num_q_heads, int num_kv_he
                              max_seq_len, partition_tokens);
 }
 
-pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype, const void *k_cache,
-                                 const void *v_cache, pkv_dtype kv_dtype, float k_scale,
-                                 float v_scale, const int32_t *block_tables,
-                                 const int32_t *seq_lens, int num_seqs, int num_q_heads,
-                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                 int max_blocks_per_seq, int max_seq_len, float scale, void *out,
-                                 pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
-                                 int partition_tokens, int flags, void *stream)
+}  // extern "C"
+
+namespace pkv {
+
+// Decode, optionally with the fused cache write of one new token per
+// sequence (new_k non-null).
+static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_cache,
+                              const void *v_cache, pkv_dtype kv_dtype, float k_scale,
+                              float v_scale, const int32_t *block_tables,
+                              const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                              int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                              int max_blocks_per_seq, int max_seq_len, float scale, void *out,
+                              pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                              int partition_tokens, int flags, void *stream, const void *new_k,
+                              const void *new_v, pkv_dtype new_dtype)
 {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
         max_blocks_per_seq <= 0 || max_seq_len < 0)
@@ -219,6 +226,12 @@ pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype, const void *k
     p.streamk_max_ctas = kStreamKMaxCtas;
     p.fused_merge = (flags & PKV_FLAG_SEPARATE_MERGE) ? 0 : 1;
     p.drop_first_copy = (flags & PKV_FLAG_TEST_DROP_FIRST_COPY) ? 1 : 0;
+    p.new_k = new_k;
+    p.new_v = new_v;
+    p.new_dtype = new_dtype;
+    p.kv_dtype = kv_dtype;
+    p.k_scale = k_scale;
+    p.v_scale = v_scale;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // Status word, work counter and arrival counters start at zero.
@@ -231,6 +244,50 @@ pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype, const void *k
     if (p.split && p.max_parts > 1 && !p.fused_merge)
         rc = launch_merge(p, st);
     return rc;
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype, const void *k_cache,
+                                 const void *v_cache, pkv_dtype kv_dtype, float k_scale,
+                                 float v_scale, const int32_t *block_tables,
+                                 const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                 int max_blocks_per_seq, int max_seq_len, float scale, void *out,
+                                 pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                                 int partition_tokens, int flags, void *stream)
+{
+    return decode_impl(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_tables,
+                       seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, max_blocks_per_seq, max_seq_len, scale, out, out_dtype,
+                       workspace, workspace_bytes, partition_tokens, flags, stream, nullptr,
+                       nullptr, PKV_F32);
+}
+
+pkv_status pkv_paged_attn_decode_append(const void *q, pkv_dtype q_dtype, const void *new_k,
+                                        const void *new_v, pkv_dtype new_dtype, void *k_cache,
+                                        void *v_cache, pkv_dtype kv_dtype, float k_scale,
+                                        float v_scale, const int32_t *block_tables,
+                                        const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int num_blocks, int max_blocks_per_seq, int max_seq_len,
+                                        float scale, void *out, pkv_dtype out_dtype,
+                                        void *workspace, size_t workspace_bytes,
+                                        int partition_tokens, int flags, void *stream)
+{
+    if (new_dtype != PKV_F32 && new_dtype != PKV_BF16)
+        return PKV_ERR_UNSUPPORTED;
+    if (kv_dtype == PKV_FP8_E5M2 && (k_scale == 0.f || v_scale == 0.f))
+        return PKV_ERR_INVALID_ARG;
+    if (num_seqs > 0 && (!new_k || !new_v || !aligned(new_k, 16) || !aligned(new_v, 16)))
+        return PKV_ERR_INVALID_ARG;
+    return decode_impl(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_tables,
+                       seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, max_blocks_per_seq, max_seq_len, scale, out, out_dtype,
+                       workspace, workspace_bytes, partition_tokens, flags, stream, new_k, new_v,
+                       new_dtype);
 }
 
 pkv_status pkv_reshape_and_cache(const void *k, const void *v, pkv_dtype in_dtype,

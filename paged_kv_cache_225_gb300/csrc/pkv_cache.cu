@@ -5,39 +5,9 @@
 // (section "PagedAttention") the append lands in a 16-token page anywhere in
 // the pool.  Token i goes to slot = slot_mapping[i] = block * 16 + offset of
 // every KV head; element (h, d) is stored at [block, h, d, offset].
-#include <cuda_fp8.h>
-
-#include "pkv_common.cuh"
-#include "pkv_internal.h"
+#include "pkv_convert.cuh"
 
 namespace pkv {
-
-__device__ __forceinline__ float load_in(const void *src, int dtype, size_t i)
-{
-    if (dtype == PKV_F32)
-        return static_cast<const float *>(src)[i];
-    return __uint_as_float(static_cast<uint32_t>(static_cast<const unsigned short *>(src)[i])
-                           << 16);
-}
-
-__device__ __forceinline__ void store_kv(void *cache, int dtype, size_t i, const void *src,
-                                         int in_dtype, size_t j, float scale)
-{
-    if (dtype == PKV_F32) {
-        static_cast<float *>(cache)[i] = load_in(src, in_dtype, j);
-    } else if (dtype == PKV_BF16) {
-        unsigned short b;
-        if (in_dtype == PKV_BF16)
-            b = static_cast<const unsigned short *>(src)[j];
-        else
-            b = __bfloat16_as_ushort(__float2bfloat16_rn(static_cast<const float *>(src)[j]));
-        static_cast<unsigned short *>(cache)[i] = b;
-    } else {
-        const float x = load_in(src, in_dtype, j) / scale;
-        static_cast<unsigned char *>(cache)[i] =
-            static_cast<unsigned char>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E5M2));
-    }
-}
 
 // One CTA per new token; threads stride over (head, dim).
 __global__ void __launch_bounds__(256)

@@ -34,6 +34,7 @@
 #include <cmath>
 
 #include "pkv_common.cuh"
+#include "pkv_convert.cuh"
 #include "pkv_internal.h"
 #include "pkv_merge.cuh"
 
@@ -703,6 +704,73 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
 
 // ==================================================================== kernel
 
+// Fused cache write: before the bulk copy of the page that holds a
+// sequence's new token (position L - 1) is issued, the warp that will issue it
+// writes the converted K/V row of KV head hkv into the cache slot (block
+// `phys`) and fences those generic writes against the copy engine's reads,
+// so the ordinary page copy brings the new token in with the rest.
+// Bytes of one warp's staging buffer for the new K and V rows (head_dim up
+// to 128 elements of up to 4 bytes each, K then V).
+constexpr int kNewRowBytes = 2 * 128 * 4;
+
+// Starts copying the new K and V rows of (s, hkv) into `buf` (shared memory)
+// without waiting; write_new_token_from(buf) consumes them.
+__device__ __forceinline__ void prefetch_new_rows(const DecodeParams &p, int s, int hkv, int D,
+                                                  unsigned char *buf, int lane)
+{
+    const int eb = p.new_dtype == PKV_F32 ? 4 : 2;
+    const int row_bytes = D * eb;  // multiple of 16
+    const size_t src0 = (static_cast<size_t>(s) * p.num_kv_heads + hkv) * row_bytes;
+    for (int c = lane; c < 2 * row_bytes / 16; c += 32) {
+        const bool is_v = c * 16 >= row_bytes;
+        const int off = c * 16 - (is_v ? row_bytes : 0);
+        const unsigned char *src =
+            static_cast<const unsigned char *>(is_v ? p.new_v : p.new_k) + src0 + off;
+        cp_async_16(buf + (is_v ? row_bytes : 0) + off, src);
+    }
+    cp_async_commit();
+}
+
+// write_new_token with the rows already staged in shared memory by
+// prefetch_new_rows.
+__device__ __forceinline__ void write_new_token_from(const DecodeParams &p, int hkv, int L,
+                                                     int phys, int D, const unsigned char *buf,
+                                                     int lane)
+{
+    cp_async_wait_all();
+    __syncwarp();
+    const int t = (L - 1) % kBlockSize;
+    const int row_bytes = D * (p.new_dtype == PKV_F32 ? 4 : 2);
+    const size_t dst0 = (static_cast<size_t>(phys) * p.num_kv_heads + hkv) * D;
+    void *kc = const_cast<void *>(p.k_cache);
+    void *vc = const_cast<void *>(p.v_cache);
+    for (int d = lane; d < D; d += 32) {
+        const size_t g = (dst0 + d) * kBlockSize + t;
+        store_kv(kc, p.kv_dtype, g, buf, p.new_dtype, d, p.k_scale);
+        store_kv(vc, p.kv_dtype, g, buf + row_bytes, p.new_dtype, d, p.v_scale);
+    }
+    fence_proxy_async_all();
+    __syncwarp();
+}
+
+__device__ __forceinline__ void write_new_token(const DecodeParams &p, int s, int hkv, int L,
+                                                int phys, int D, int lane)
+{
+    const int t = (L - 1) % kBlockSize;
+    const size_t src0 = (static_cast<size_t>(s) * p.num_kv_heads + hkv) * D;
+    const size_t dst0 = (static_cast<size_t>(phys) * p.num_kv_heads + hkv) * D;
+    void *kc = const_cast<void *>(p.k_cache);
+    void *vc = const_cast<void *>(p.v_cache);
+    for (int d = lane; d < D; d += 32) {
+        const size_t g = (dst0 + d) * kBlockSize + t;
+        store_kv(kc, p.kv_dtype, g, p.new_k, p.new_dtype, src0 + d, p.k_scale);
+        store_kv(vc, p.kv_dtype, g, p.new_v, p.new_dtype, src0 + d, p.v_scale);
+    }
+    fence_proxy_async_all();
+    __syncwarp();
+}
+
+
 // Counts of the two item phases of a sequence of L tokens under partition
 // P: full partitions first, then the one shorter remainder (or the single
 // item of an empty sequence).  Issuing every full partition before any
@@ -830,6 +898,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
     unsigned char *ring = smem + warp * Pol::kRingBytes;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kWarps * Pol::kRingBytes) + warp * Pol::R;
     unsigned char *extra = smem + kWarps * Pol::kRingBytes + kWarps * Pol::R * sizeof(uint64_t);
+    unsigned char *newrow = extra + Pol::kExtraBytes + warp * kNewRowBytes;
 
     if (lane == 0)
         for (int st = 0; st < Pol::R; ++st)
@@ -923,10 +992,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
             }
             return __shfl_sync(kFullMask, id_reg, i & 31);
         };
+        // Fused cache write: the warp that owns the sequence's last page
+        // stages the new rows now and writes them just before that page's
+        // copy is issued.
+        const int i_new = (p.new_k && t1 == L && L > 0 && npages > 0 &&
+                           (npages - 1) % kWarps == warp)
+                              ? (npages - 1) / kWarps
+                              : -1;
+        if (i_new >= 0)
+            prefetch_new_rows(p, s, hkv, D, newrow, lane);
         auto issue = [&](int i) {
             const int phys = page_id(i);
             const int stg = (pages_done + i) % Pol::R;
             const bool ok = phys >= 0 && phys < p.num_blocks;
+            if (i == i_new && ok)
+                write_new_token_from(p, hkv, L, phys, D, newrow, lane);
             okmask = ok ? (okmask | (1u << stg)) : (okmask & ~(1u << stg));
             if (lane == 0) {
                 uint64_t *bar = &bars[stg];
@@ -998,6 +1078,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
                     Pol::compute(st, fr, valid, lane, c);
         }
         pages_done += nw;
+        if (i_new >= 0)
+            cp_async_wait_all();  // staged rows landed even if their page was skipped
 
         // ---------------------------------------------- merge the warps
         {
@@ -1037,7 +1119,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
 template <class Pol>
 constexpr int decode_smem_bytes()
 {
-    return kWarps * Pol::kRingBytes + kWarps * Pol::R * 8 + Pol::kExtraBytes;
+    return kWarps * Pol::kRingBytes + kWarps * Pol::R * 8 + Pol::kExtraBytes +
+           kWarps * kNewRowBytes;
 }
 
 // Launches decode_kernel<Pol>: one CTA per item without split, else a

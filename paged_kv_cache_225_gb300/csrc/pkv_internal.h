@@ -36,6 +36,15 @@ struct DecodeParams {
     int streamk_max_ctas; // CTAs the stream-K partial slots are sized for
     int fused_merge;      // 1: the CTA finishing a sequence's last partial merges it
     int drop_first_copy;  // test hook: never issue the first copy of item 0
+    // Fused cache write (null new_k: none): the new token of sequence s is its
+    // position seq_lens[s] - 1; its K/V rows [S][Hkv][D] of new_dtype are
+    // converted to the cache dtype and written to the cache and into the
+    // page tile the kernel is about to attend.
+    const void *new_k;
+    const void *new_v;
+    int new_dtype;
+    int kv_dtype;
+    float k_scale, v_scale;
 };
 
 constexpr int kBlockSize = 16;

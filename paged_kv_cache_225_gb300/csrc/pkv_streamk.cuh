@@ -317,6 +317,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
         while (pos_i < n_mine && pos_i < pos_c + R)
             issue_next();
     };
+
+    // Fused cache write: every new token whose page this warp will copy is
+    // written now, before the first copy and while HBM is still idle (a
+    // write on the issue path would wait behind the saturated queue).
+    if (p.new_k) {
+        Unit wu = start;
+        while (wu.off < b) {
+            const long long g_last = wu.off + wu.np - 1;
+            if (wu.L > 0 && g_last >= a && g_last < b && ((g_last - a) & 3) == warp) {
+                const int phys = __ldg(p.block_tables +
+                                       static_cast<size_t>(wu.s) * p.max_blocks + wu.np - 1);
+                if (phys >= 0 && phys < p.num_blocks)
+                    write_new_token(p, wu.s, wu.hkv, wu.L, phys, D, lane);
+            }
+            unit_next(p, wu);
+        }
+    }
     refill();
 
     // ---------------------------------------------- segments (all warps)
@@ -348,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
                 break;
             }
             const bool have = (okmask >> stg) & 1u;
-            const int valid = min(kBlockSize, su.L - static_cast<int>(g - su.off) * kBlockSize);
+            const int pg = static_cast<int>(g - su.off);
+            const int valid = min(kBlockSize, su.L - pg * kBlockSize);
             const unsigned char *sk = ring + stg * Pol::kStageBytes;
             typename Pol::Frags fr;
             if (have) {

@@ -84,3 +84,21 @@ def oracle_step(w: W.Workload, append=True, kv_scale=None):
 def max_abs(a, b) -> float:
     d = np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64))
     return float(np.nanmax(d)) if not np.isnan(d).any() else float("inf")
+
+
+def gpu_step_fused(w: W.Workload, d: dict, *, impl="auto", partition_tokens=0,
+                   out_dtype=torch.float32, kv_scale=None, flags=0):
+    """The same decode step in one launch: cache write fused into the decode."""
+    cfg = w.cfg
+    ks = vs = cfg.kv_scale if kv_scale is None else kv_scale
+    lens = w.seq_lens + 1
+    lens_dev = torch.from_numpy(lens.astype(np.int32)).to(d["q"].device)
+    out = torch.empty(d["q"].shape, dtype=out_dtype, device=d["q"].device)
+    pkv.paged_attn_decode_append(d["q"], d["new_k"], d["new_v"], d["k_cache"], d["v_cache"],
+                                 d["block_tables"], lens_dev, w.scale, out, k_scale=ks,
+                                 v_scale=vs, max_seq_len=int(lens.max()),
+                                 partition_tokens=partition_tokens, impl=impl, flags=flags)
+    torch.cuda.synchronize()
+    status = pkv.read_status(device=d["q"].device)
+    return out.float().cpu().numpy().astype(np.float64), status, lens
+

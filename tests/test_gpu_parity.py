@@ -16,7 +16,8 @@ import oracle
 import paged_kv_cache_225_gb300 as pkv
 from paged_kv_cache_225_gb300 import workloads as W
 
-from gpu_util import TOL, bits, device_workload, gpu_step, max_abs, oracle_step, to_torch
+from gpu_util import (TOL, bits, device_workload, gpu_step, gpu_step_fused, max_abs, oracle_step,
+                      to_torch)
 
 pytestmark = pytest.mark.gpu
 
@@ -219,6 +220,38 @@ def test_scores_ramping_across_the_running_max(kv_dtype, direction):
     for impl in ("auto", "simt"):
         out, status, _ = gpu_step(w, d, impl=impl, append=False)
         assert status == 0
+        assert max_abs(out, ref) <= TOL[kv_dtype]
+
+
+# ------------------------------------------------ fused cache write + decode
+
+@pytest.mark.parametrize("name", W.CONFIG_ORDER)
+@pytest.mark.parametrize("part", [0, -2, -1, 256])
+def test_fused_step_matches_write_then_decode_bitwise(name, part):
+    w, ref, kc, vc = _config(name)
+    d1 = device_workload(w, DEV)
+    a, st_a, _ = gpu_step(w, d1, partition_tokens=part)
+    d2 = device_workload(w, DEV)
+    b, st_b, _ = gpu_step_fused(w, d2, partition_tokens=part)
+    assert st_a == 0 and st_b == 0
+    assert np.array_equal(a, b)
+    assert np.array_equal(bits(d2["k_cache"]), kc.view(np.uint8).reshape(-1))
+    assert np.array_equal(bits(d2["v_cache"]), vc.view(np.uint8).reshape(-1))
+    assert max_abs(b, ref) <= TOL[w.cfg.kv_dtype]
+
+
+@pytest.mark.parametrize("kv_dtype", [W.F32, W.BF16, W.FP8_E5M2])
+def test_fused_step_cuda_cores_and_edge_lengths(kv_dtype):
+    q_dtype = W.F32 if kv_dtype == W.F32 else W.BF16
+    lens = np.array(EDGE_LENS)
+    w = _custom(num_seqs=len(lens), num_q_heads=16, num_kv_heads=2, q_dtype=q_dtype,
+                kv_dtype=kv_dtype, garbage="nan", lens=lens)
+    ref, kc, vc = oracle_step(w)
+    for impl in ("auto", "simt"):
+        d = device_workload(w, DEV)
+        out, status, _ = gpu_step_fused(w, d, impl=impl)
+        assert status == 0 and np.isfinite(out).all()
+        assert np.array_equal(bits(d["k_cache"]), kc.view(np.uint8).reshape(-1))
         assert max_abs(out, ref) <= TOL[kv_dtype]
 
 
