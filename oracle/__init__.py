@@ -63,6 +63,8 @@ def _load():
             lib.pkvo_paged_decode.restype = ip
             lib.pkvo_paged_decode_seqs.argtypes = common + [i32p, ip, dp, ip]
             lib.pkvo_paged_decode_seqs.restype = ip
+            lib.pkvo_paged_prefill.argtypes = [vp, ip, i32p] + common[2:] + [ip, dp, ip]
+            lib.pkvo_paged_prefill.restype = ip
             lib.pkvo_reshape_and_cache.argtypes = [vp, vp, ip, i64p, ip, ip, ip, ip, ip, vp, vp,
                                                    ip, ctypes.c_float, ctypes.c_float]
             lib.pkvo_reshape_and_cache.restype = ip
@@ -150,6 +152,37 @@ def paged_decode_seqs(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_
     if rc:
         raise ValueError(f"oracle paged_decode_seqs failed ({rc})")
     return out[seqs]
+
+
+def paged_prefill(q, q_dtype, q_start, k_cache, v_cache, kv_dtype, block_tables, seq_lens,
+                  scale, k_scale=1.0, v_scale=1.0, partition_tokens=0,
+                  num_threads=0) -> np.ndarray:
+    """Paged attention of several causal query tokens per sequence: out [T, Hq, D].
+
+    ``q`` is [T, Hq, D]; the queries of sequence s are rows
+    ``q_start[s] .. q_start[s+1]-1``, the last positions of its
+    ``seq_lens[s]`` cached tokens.
+    """
+    T, Hq, D = q.shape
+    N, Hkv, D2, B = k_cache.shape
+    assert D2 == D and v_cache.shape == k_cache.shape
+    qs = np.ascontiguousarray(q_start, dtype=np.int32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    S = sl.size
+    assert qs.size == S + 1 and qs[0] == 0 and qs[-1] == T
+    q = np.ascontiguousarray(q)
+    k_cache = np.ascontiguousarray(k_cache)
+    v_cache = np.ascontiguousarray(v_cache)
+    out = np.zeros((T, Hq, D), dtype=np.float64)
+    rc = _load().pkvo_paged_prefill(
+        _ptr(q), q_dtype, _ptr(qs, ctypes.c_int32), _ptr(k_cache), _ptr(v_cache), kv_dtype,
+        float(k_scale), float(v_scale), _ptr(bt, ctypes.c_int32), _ptr(sl, ctypes.c_int32), S,
+        Hq, Hkv, D, B, N, bt.shape[1], float(scale), int(partition_tokens),
+        _ptr(out, ctypes.c_double), int(num_threads))
+    if rc:
+        raise ValueError(f"oracle paged_prefill failed ({rc})")
+    return out
 
 
 def reshape_and_cache(k, v, in_dtype, slot_mapping, k_cache, v_cache, kv_dtype,

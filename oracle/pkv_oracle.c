@@ -26,6 +26,11 @@
  *    rearrangement of this definition, so the oracle is the definition.
  *    seq_len == 0 gives a zero row.
  *
+ *  - Several query tokens per sequence (chunked prefill, speculative
+ *    verification): the n queries of a sequence of L tokens are its last n
+ *    positions; query i attends rows t <= L - n + i, the causal mask of the
+ *    "Inference optimization" lesson, Step 2.  Decode is n = 1.
+ *
  *  - Split-sequence attention with a log-sum-exp merge (used only to pin the
  *    merge algebra): the same softmax on each partition of partition_tokens
  *    rows, then M* = max_p m_p, w_p = l_p exp(m_p - M*),
@@ -273,24 +278,75 @@ static void softmax_attend(const double *qrow, const double *K, const double *V,
     *l_out = Z;
 }
 
-static void load_q_row(const pkvo_problem *P, int s, int h, double *qrow)
+static void load_q_row(const pkvo_problem *P, int row, int h, double *qrow)
 {
-    size_t base = ((size_t)s * P->num_q_heads + h) * P->head_dim;
+    size_t base = ((size_t)row * P->num_q_heads + h) * P->head_dim;
     for (int d = 0; d < P->head_dim; ++d)
         qrow[d] = elem_value(P->q, P->q_dtype, base + d);
 }
 
-/* Attention for every (s, h) whose KV head is hkv, written into out
- * [S, Hq, D].  partition_tokens > 0 computes each partition separately and
- * merges them with the log-sum-exp weights. */
-static int attend_group(const pkvo_problem *P, int s, int hkv, int partition_tokens,
-                        double *out)
+/* Attention of one query row over the gathered rows [0, t_end), written
+ * into dst[D].  partition_tokens > 0 computes each partition of
+ * partition_tokens rows separately and merges them with the log-sum-exp
+ * weights.  z, o and acc are caller scratch of t_end (>= 1), D and D
+ * doubles.  Returns 3 on allocation failure. */
+static int attend_row(const double *qrow, const double *K, const double *V, int D, int t_end,
+                      double scale, int partition_tokens, double *z, double *o, double *acc,
+                      double *dst)
+{
+    if (partition_tokens <= 0 || t_end <= partition_tokens) {
+        double m, l;
+        softmax_attend(qrow, K, V, D, 0, t_end, scale, z, o, &m, &l);
+        for (int d = 0; d < D; ++d)
+            dst[d] = o[d];
+        return 0;
+    }
+    /* Log-sum-exp merge of the partitions. */
+    int nparts = (t_end + partition_tokens - 1) / partition_tokens;
+    double Mstar = -INFINITY;
+    double *mp = malloc(nparts * sizeof(double));
+    double *lp = malloc(nparts * sizeof(double));
+    double *op = malloc((size_t)nparts * D * sizeof(double));
+    if (!mp || !lp || !op) {
+        free(mp); free(lp); free(op);
+        return 3;
+    }
+    for (int p = 0; p < nparts; ++p) {
+        int t0 = p * partition_tokens;
+        int t1 = (t0 + partition_tokens < t_end) ? t0 + partition_tokens : t_end;
+        softmax_attend(qrow, K, V, D, t0, t1, scale, z, op + (size_t)p * D, &mp[p], &lp[p]);
+        if (mp[p] > Mstar)
+            Mstar = mp[p];
+    }
+    double W = 0.0;
+    for (int d = 0; d < D; ++d)
+        acc[d] = 0.0;
+    for (int p = 0; p < nparts; ++p) {
+        double w = lp[p] * exp(mp[p] - Mstar);
+        W += w;
+        for (int d = 0; d < D; ++d)
+            acc[d] += w * op[(size_t)p * D + d];
+    }
+    for (int d = 0; d < D; ++d)
+        dst[d] = acc[d] / W;
+    free(mp); free(lp); free(op);
+    return 0;
+}
+
+/* Attention of the n_q query tokens q_row0 .. q_row0 + n_q - 1 (rows of q
+ * [T, Hq, D]) of sequence s for every query head of KV head hkv, written into
+ * out [T, Hq, D].  Query i sits at logical position L - n_q + i and sees the
+ * rows t <= that position.  Decode is n_q = 1, q_row0 = s. */
+static int attend_group_rows(const pkvo_problem *P, int s, int hkv, int q_row0, int n_q,
+                             int partition_tokens, double *out)
 {
     const int D = P->head_dim;
     const int G = P->num_q_heads / P->num_kv_heads;
     int L = P->seq_lens[s];
     int rc = 0;
     if (L < 0 || (size_t)L > (size_t)P->max_blocks_per_seq * P->block_size)
+        return 2;
+    if (n_q < 0 || n_q > (L > 0 ? L : 1))
         return 2;
     size_t rows = (L > 0) ? (size_t)L : 1;
     double *K = malloc(rows * D * sizeof(double));
@@ -307,52 +363,25 @@ static int attend_group(const pkvo_problem *P, int s, int hkv, int partition_tok
         rc = 1;
         goto done;
     }
-    for (int g = 0; g < G; ++g) {
-        int h = hkv * G + g;
-        double *dst = out + ((size_t)s * P->num_q_heads + h) * D;
-        load_q_row(P, s, h, qrow);
-        if (partition_tokens <= 0 || L <= partition_tokens) {
-            double m, l;
-            softmax_attend(qrow, K, V, D, 0, L, P->scale, z, o, &m, &l);
-            for (int d = 0; d < D; ++d)
-                dst[d] = o[d];
-            continue;
+    for (int i = 0; i < n_q; ++i) {
+        const int t_end = (L > 0) ? L - n_q + i + 1 : 0;
+        for (int g = 0; g < G; ++g) {
+            int h = hkv * G + g;
+            double *dst = out + ((size_t)(q_row0 + i) * P->num_q_heads + h) * D;
+            load_q_row(P, q_row0 + i, h, qrow);
+            rc |= attend_row(qrow, K, V, D, t_end, P->scale, partition_tokens, z, o, acc, dst);
         }
-        /* Log-sum-exp merge of the partitions. */
-        int nparts = (L + partition_tokens - 1) / partition_tokens;
-        double Mstar = -INFINITY;
-        double *mp = malloc(nparts * sizeof(double));
-        double *lp = malloc(nparts * sizeof(double));
-        double *op = malloc((size_t)nparts * D * sizeof(double));
-        if (!mp || !lp || !op) {
-            free(mp); free(lp); free(op);
-            rc = 3;
-            goto done;
-        }
-        for (int p = 0; p < nparts; ++p) {
-            int t0 = p * partition_tokens;
-            int t1 = (t0 + partition_tokens < L) ? t0 + partition_tokens : L;
-            softmax_attend(qrow, K, V, D, t0, t1, P->scale, z, op + (size_t)p * D,
-                           &mp[p], &lp[p]);
-            if (mp[p] > Mstar)
-                Mstar = mp[p];
-        }
-        double W = 0.0;
-        for (int d = 0; d < D; ++d)
-            acc[d] = 0.0;
-        for (int p = 0; p < nparts; ++p) {
-            double w = lp[p] * exp(mp[p] - Mstar);
-            W += w;
-            for (int d = 0; d < D; ++d)
-                acc[d] += w * op[(size_t)p * D + d];
-        }
-        for (int d = 0; d < D; ++d)
-            dst[d] = acc[d] / W;
-        free(mp); free(lp); free(op);
     }
 done:
     free(K); free(V); free(z); free(qrow); free(o); free(acc);
     return rc;
+}
+
+/* Decode: one query per sequence, row s of q. */
+static int attend_group(const pkvo_problem *P, int s, int hkv, int partition_tokens,
+                        double *out)
+{
+    return attend_group_rows(P, s, hkv, s, 1, partition_tokens, out);
 }
 
 static int run_attention(const pkvo_problem *P, int partition_tokens, double *out,
@@ -429,6 +458,50 @@ int pkvo_paged_decode_seqs(const void *q, int q_dtype, const void *k_cache,
             continue;
         }
         rc |= attend_group(&P, s, hkv, 0, out);
+    }
+    (void)num_threads;
+    return rc;
+}
+
+/*
+ * Paged attention with several query tokens per sequence (chunked prefill,
+ * speculative verification).  q is [T, Hq, D]; the queries of sequence s are
+ * rows q_start[s] .. q_start[s+1] - 1, the last n_s = q_start[s+1] - q_start[s]
+ * positions of its seq_lens[s] cached tokens (their K/V already written).
+ * Query i of the sequence sits at logical position L - n_s + i and attends
+ * the rows t <= that position: the causal mask of the "Inference
+ * optimization" lesson, Step 2 (scores of keys j >= i + L - n_s + 1 get
+ * -1e9, whose weight underflows to exactly zero; the oracle leaves them out).
+ * out is [T, Hq, D].  Returns 0, or 1 (block id out of range), 2 (a length
+ * or query count out of range), 3 (allocation), 4 (head counts).
+ */
+int pkvo_paged_prefill(const void *q, int q_dtype, const int32_t *q_start,
+                       const void *k_cache, const void *v_cache, int kv_dtype, double k_scale,
+                       double v_scale, const int32_t *block_tables, const int32_t *seq_lens,
+                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int num_blocks, int max_blocks_per_seq, double scale,
+                       int partition_tokens, double *out, int num_threads)
+{
+    pkvo_problem P = {q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                      block_tables, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                      head_dim, block_size, num_blocks, max_blocks_per_seq, scale};
+    if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
+        return 4;
+    for (int s = 0; s < num_seqs; ++s)
+        if (q_start[s + 1] < q_start[s] || q_start[s + 1] - q_start[s] > seq_lens[s])
+            return 2;
+    long units = (long)num_seqs * num_kv_heads;
+    int rc = 0;
+#ifdef _OPENMP
+    if (num_threads <= 0)
+        num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads) reduction(|:rc)
+#endif
+    for (long u = 0; u < units; ++u) {
+        int s = (int)(u / num_kv_heads);
+        int hkv = (int)(u % num_kv_heads);
+        rc |= attend_group_rows(&P, s, hkv, q_start[s], q_start[s + 1] - q_start[s],
+                                partition_tokens, out);
     }
     (void)num_threads;
     return rc;
