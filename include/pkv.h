@@ -179,6 +179,64 @@ pkv_status pkv_paged_attn_decode_append(const void *q, pkv_dtype q_dtype, const 
                                         int partition_tokens, int flags, void *stream);
 
 /*
+ * Paged attention of several query tokens per sequence: chunked prefill
+ * ("vLLM e PagedAttention: serving high-throughput", the
+ * --enable-chunked-prefill flag) and speculative verification of draft
+ * tokens ("Inference optimization" lesson, section on speculative decoding).
+ * The queries of sequence s are rows q_start[s] .. q_start[s+1]-1 of q; with
+ * n_s of them and L_s = seq_lens[s] cached tokens they are the sequence's last
+ * n_s positions (their K/V already written, e.g. by pkv_reshape_and_cache),
+ * and query i attends the rows t <= L_s - n_s + i: the causal mask of the
+ * lesson's Step 2 scaled_dot_product_attention (triu of offset
+ * seq_len_k - seq_len_q + 1).  For every row of q and query head h:
+ *   out[row, h, :] = sum_{t <= pos} softmax_t(scale * q[row, h, :] . k_t) v_t
+ * with k_t, v_t read through the block table as in pkv_paged_attn_decode and
+ * KV head h / (num_q_heads / num_kv_heads).  n_s = 1 for every s is decode.
+ *
+ *   q            [num_tokens, num_q_heads, head_dim] BF16 (device).
+ *   q_start      int32 [num_seqs + 1] (device), non-decreasing, q_start[0] = 0,
+ *                q_start[num_seqs] = num_tokens.
+ *   k_cache,
+ *   v_cache      [num_blocks, num_kv_heads, head_dim, 16] BF16 (device).
+ *   k_scale,
+ *   v_scale      reserved for quantised caches; ignored for BF16.
+ *   block_tables, seq_lens   as for pkv_paged_attn_decode.
+ *   max_q_len    host bound on every n_s; max_seq_len bound on every L_s.
+ *   out          [num_tokens, num_q_heads, head_dim], F32 or BF16 (device).
+ *   workspace    >= pkv_paged_attn_prefill_workspace_size(...) bytes of
+ *                device memory, 256-byte aligned; word 0 is the status word
+ *                read by pkv_read_status.
+ *   partition_tokens   0 automatic, -1 never split a context, > 0 (multiple
+ *                of 16) split every context into partitions of that many
+ *                tokens merged with log-sum-exp weights.
+ *   flags        PKV_FLAG_IMPL_AUTO or PKV_FLAG_IMPL_MMA, optionally
+ *                PKV_FLAG_TEST_DROP_FIRST_COPY.
+ * head_dim 64 or 128, up to 16 query heads per KV head.  Errors as for
+ * pkv_paged_attn_decode; on the device a sequence with n_s > L_s, n_s >
+ * max_q_len, or q_start outside [0, num_tokens] is reported as
+ * PKV_ERR_OUT_OF_RANGE and its rows are not written.
+ */
+size_t pkv_paged_attn_prefill_workspace_size(int num_seqs, int num_tokens, int num_q_heads,
+                                             int num_kv_heads, int head_dim, int block_size,
+                                             int max_q_len, int max_seq_len,
+                                             int partition_tokens);
+/* The partition the call will use: 0 = none, > 0 tokens per partition,
+ * -1 invalid arguments. */
+int pkv_paged_attn_prefill_partition_tokens(int num_seqs, int num_tokens, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size,
+                                            int max_q_len, int max_seq_len,
+                                            int partition_tokens);
+pkv_status pkv_paged_attn_prefill(const void *q, pkv_dtype q_dtype, const int32_t *q_start,
+                                  const void *k_cache, const void *v_cache, pkv_dtype kv_dtype,
+                                  float k_scale, float v_scale, const int32_t *block_tables,
+                                  const int32_t *seq_lens, int num_seqs, int num_tokens,
+                                  int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int num_blocks, int max_blocks_per_seq,
+                                  int max_q_len, int max_seq_len, float scale, void *out,
+                                  pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                                  int partition_tokens, int flags, void *stream);
+
+/*
  * Decode without a caller workspace (the pages have no counterpart; this is
  * an interface for callers that cannot allocate device memory, e.g. a plugin
  * inside a runtime that owns all device memory, or a loop where cudaMalloc's

@@ -7,6 +7,8 @@ raise if the library is missing.  PyTorch provides device memory, the
 current stream and the workspace allocation.
 
     paged_attn_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out)
+    paged_attn_decode_append(q, new_k, new_v, k_cache, v_cache, ..., out)
+    paged_attn_prefill(q, q_start, k_cache, v_cache, block_tables, seq_lens, scale, out)
     reshape_and_cache(k, v, slot_mapping, k_cache, v_cache)
 """
 from __future__ import annotations
@@ -20,8 +22,9 @@ import torch
 
 from . import build as _build
 
-__all__ = ["paged_attn_decode", "paged_attn_decode_append", "reshape_and_cache",
-           "workspace_size", "partition_tokens",
+__all__ = ["paged_attn_decode", "paged_attn_decode_append", "paged_attn_prefill",
+           "reshape_and_cache", "workspace_size", "partition_tokens",
+           "prefill_workspace_size", "prefill_partition_tokens",
            "read_status", "PkvError", "lib", "F32", "BF16", "FP8_E5M2"]
 
 F32, BF16, FP8_E5M2 = 0, 1, 2
@@ -66,6 +69,13 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
                                                        i, i, i, i, i, i, i, i, f, vp, i, vp, sz, i,
                                                        i, vp]
             L.pkv_paged_attn_decode_append.restype = i
+            L.pkv_paged_attn_prefill_workspace_size.argtypes = [i] * 9
+            L.pkv_paged_attn_prefill_workspace_size.restype = sz
+            L.pkv_paged_attn_prefill_partition_tokens.argtypes = [i] * 9
+            L.pkv_paged_attn_prefill_partition_tokens.restype = i
+            L.pkv_paged_attn_prefill.argtypes = [vp, i, vp, vp, vp, i, f, f, vp, vp, i, i, i, i,
+                                                 i, i, i, i, i, i, f, vp, i, vp, sz, i, i, vp]
+            L.pkv_paged_attn_prefill.restype = i
             L.pkv_reshape_and_cache.argtypes = [vp, vp, i, vp, i, i, i, i, i, vp, vp, i, f, f, vp,
                                                 vp]
             L.pkv_reshape_and_cache.restype = i
@@ -239,6 +249,82 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
         _stream(dev, stream))
     if rc != 0:
         raise PkvError(rc, "pkv_paged_attn_decode_append")
+    return out
+
+
+def prefill_workspace_size(num_seqs: int, num_tokens: int, num_q_heads: int, num_kv_heads: int,
+                           head_dim: int, max_q_len: int, max_seq_len: int,
+                           partition_tokens: int = 0, block_size: int = 16) -> int:
+    n = lib().pkv_paged_attn_prefill_workspace_size(num_seqs, num_tokens, num_q_heads,
+                                                    num_kv_heads, head_dim, block_size,
+                                                    max_q_len, max_seq_len, partition_tokens)
+    if n == 0:
+        raise ValueError("invalid sizes for the prefill workspace")
+    return int(n)
+
+
+def prefill_partition_tokens(num_seqs: int, num_tokens: int, num_q_heads: int,
+                             num_kv_heads: int, head_dim: int, max_q_len: int, max_seq_len: int,
+                             partition_tokens: int = 0, block_size: int = 16) -> int:
+    """Partition of the several-queries call: 0 none, > 0 tokens per partition."""
+    return int(lib().pkv_paged_attn_prefill_partition_tokens(
+        num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size, max_q_len,
+        max_seq_len, partition_tokens))
+
+
+def paged_attn_prefill(q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Tensor,
+                       v_cache: torch.Tensor, block_tables: torch.Tensor,
+                       seq_lens: torch.Tensor, scale: float, out: torch.Tensor, *,
+                       max_q_len: Optional[int] = None, max_seq_len: Optional[int] = None,
+                       partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
+                       stream: Optional[torch.cuda.Stream] = None,
+                       flags: int = 0) -> torch.Tensor:
+    """Causal paged attention of several query tokens per sequence.
+
+    q [T, Hq, D] bf16; q_start int32 [S+1] (queries of sequence s are rows
+    q_start[s]..q_start[s+1]-1, its last positions); k_cache, v_cache
+    [N, Hkv, D, 16] bf16 already holding the queries' K/V; block_tables int32
+    [S, max_blocks]; seq_lens int32 [S] (queries included); out [T, Hq, D]
+    f32/bf16.  ``max_q_len`` defaults to T, ``max_seq_len`` to max_blocks*16.
+    Returns ``out``.
+    """
+    dev = q.device
+    for t, name, nd in ((q, "q", 3), (q_start, "q_start", 1), (k_cache, "k_cache", 4),
+                        (v_cache, "v_cache", 4), (block_tables, "block_tables", 2),
+                        (seq_lens, "seq_lens", 1), (out, "out", 3)):
+        _check(t, name, nd, dev)
+    if (block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32
+            or q_start.dtype != torch.int32):
+        raise TypeError("q_start, block_tables and seq_lens must be int32")
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must have the same shape and dtype")
+    T, Hq, D = q.shape
+    N, Hkv, D2, B = k_cache.shape
+    S = seq_lens.shape[0]
+    if (D2 != D or out.shape != q.shape or block_tables.shape[0] != S
+            or q_start.shape[0] != S + 1):
+        raise ValueError("inconsistent shapes")
+    max_blocks = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_blocks * B
+    if max_q_len is None:
+        max_q_len = T
+    L = lib()
+    need = L.pkv_paged_attn_prefill_workspace_size(S, T, Hq, Hkv, D, B, int(max_q_len),
+                                                   int(max_seq_len), int(partition_tokens))
+    if need == 0:
+        raise ValueError("invalid sizes or partition_tokens")
+    if workspace is None:
+        workspace = get_workspace(need, dev)
+    rc = L.pkv_paged_attn_prefill(
+        q.data_ptr(), _dtype_code(q, "q"), q_start.data_ptr(), k_cache.data_ptr(),
+        v_cache.data_ptr(), _dtype_code(k_cache, "k_cache"), 1.0, 1.0, block_tables.data_ptr(),
+        seq_lens.data_ptr(), S, T, Hq, Hkv, D, B, N, max_blocks, int(max_q_len),
+        int(max_seq_len), float(scale), out.data_ptr(), _dtype_code(out, "out"),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        int(partition_tokens), int(flags), _stream(dev, stream))
+    if rc != 0:
+        raise PkvError(rc, "pkv_paged_attn_prefill")
     return out
 
 

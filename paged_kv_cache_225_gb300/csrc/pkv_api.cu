@@ -322,6 +322,178 @@ pkv_status pkv_reshape_and_cache(const void *k, const void *v, pkv_dtype in_dtyp
                                     v_scale, status, static_cast<cudaStream_t>(stream));
 }
 
+}  // extern "C"
+
+namespace pkv {
+
+// Split plan of the several-queries kernel.  Items are (sequence, KV head,
+// partition, 64-row block); the host knows only T, S and the length bounds,
+// so it estimates the unsplit item count from them.  Enough items keep every
+// CTA busy without a split (contexts over 2048 tokens still use 2048-token
+// partitions so long items do not dominate the tail); fewer are split so
+// that about four items per resident CTA exist.
+static int resolve_prefill_partition(int S, int T, int Hq, int Hkv, int B, int max_q_len,
+                                     int max_len, int requested)
+{
+    if (S < 0 || T < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || B != kBlockSize ||
+        max_len < 0 || max_q_len < 0)
+        return -1;
+    if (requested == -1)
+        return 0;
+    if (requested > 0)
+        return requested % kBlockSize == 0 ? requested : -1;
+    if (requested != 0)
+        return -1;
+    const long G = Hq / Hkv;
+    const long blocks = (static_cast<long>(T) * G + 63) / 64;
+    const long est = static_cast<long>(Hkv) * (blocks > S ? blocks : S);
+    const long many = 2L * 2 * 152;
+    if (est >= many)
+        return max_len <= 2048 ? 0 : 2048;
+    const long parts = (many + est - 1) / (est > 0 ? est : 1);
+    long P = (max_len + parts - 1) / parts;
+    P = (P + 255) / 256 * 256;
+    if (P < 256)
+        P = 256;
+    return max_len <= P ? 0 : static_cast<int>(P);
+}
+
+struct PrefillPlan {
+    int partition;  // 0 = no split
+    int max_parts;
+    size_t part_o_off, part_ml_off, bytes;
+};
+
+static bool make_prefill_plan(int S, int T, int Hq, int Hkv, int D, int B, int max_q_len,
+                              int max_len, int requested, PrefillPlan *pl)
+{
+    const int P = resolve_prefill_partition(S, T, Hq, Hkv, B, max_q_len, max_len, requested);
+    if (P < 0)
+        return false;
+    pl->partition = P;
+    pl->max_parts = (P > 0 && max_len > P) ? (max_len + P - 1) / P : 1;
+    pl->part_o_off = pl->part_ml_off = 0;
+    pl->bytes = kWorkspaceHeader;
+    if (pl->max_parts > 1) {
+        const size_t rows = static_cast<size_t>(T) * Hq * pl->max_parts;
+        pl->part_o_off = kWorkspaceHeader;
+        pl->part_ml_off = pl->part_o_off + align256(rows * D * sizeof(float));
+        pl->bytes = pl->part_ml_off + align256(rows * 2 * sizeof(float));
+    }
+    return true;
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+size_t pkv_paged_attn_prefill_workspace_size(int num_seqs, int num_tokens, int num_q_heads,
+                                             int num_kv_heads, int head_dim, int block_size,
+                                             int max_q_len, int max_seq_len,
+                                             int partition_tokens)
+{
+    PrefillPlan pl;
+    if (!make_prefill_plan(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_q_len, max_seq_len, partition_tokens, &pl))
+        return 0;
+    return pl.bytes;
+}
+
+int pkv_paged_attn_prefill_partition_tokens(int num_seqs, int num_tokens, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size,
+                                            int max_q_len, int max_seq_len,
+                                            int partition_tokens)
+{
+    (void)head_dim;
+    return resolve_prefill_partition(num_seqs, num_tokens, num_q_heads, num_kv_heads, block_size,
+                                     max_q_len, max_seq_len, partition_tokens);
+}
+
+pkv_status pkv_paged_attn_prefill(const void *q, pkv_dtype q_dtype, const int32_t *q_start,
+                                  const void *k_cache, const void *v_cache, pkv_dtype kv_dtype,
+                                  float k_scale, float v_scale, const int32_t *block_tables,
+                                  const int32_t *seq_lens, int num_seqs, int num_tokens,
+                                  int num_q_heads, int num_kv_heads, int head_dim,
+                                  int block_size, int num_blocks, int max_blocks_per_seq,
+                                  int max_q_len, int max_seq_len, float scale, void *out,
+                                  pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
+                                  int partition_tokens, int flags, void *stream)
+{
+    (void)k_scale;
+    (void)v_scale;
+    if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 || max_q_len < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0)
+        return PKV_ERR_INVALID_ARG;
+    if (static_cast<long>(max_seq_len) > static_cast<long>(max_blocks_per_seq) * kBlockSize)
+        return PKV_ERR_INVALID_ARG;
+    if (q_dtype != PKV_BF16 || kv_dtype != PKV_BF16)
+        return PKV_ERR_UNSUPPORTED;
+    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
+        return PKV_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128)
+        return PKV_ERR_UNSUPPORTED;
+    if (block_size != kBlockSize)
+        return PKV_ERR_UNSUPPORTED;
+    const int group = num_q_heads / num_kv_heads;
+    if (group > 16)
+        return PKV_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale))
+        return PKV_ERR_INVALID_ARG;
+    if ((flags & ~(PKV_FLAG_IMPL_MASK | PKV_FLAG_TEST_DROP_FIRST_COPY)) != 0 ||
+        (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_SIMT ||
+        (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_MASK)
+        return PKV_ERR_INVALID_ARG;
+    PrefillPlan pl;
+    if (!make_prefill_plan(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_q_len, max_seq_len, partition_tokens, &pl))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.bytes)
+        return PKV_ERR_WORKSPACE;
+    if (num_seqs == 0 || num_tokens == 0)
+        return PKV_OK;
+    if (!q || !q_start || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(q_start, 4) || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
+        return PKV_ERR_INVALID_ARG;
+
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    PrefillParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.q_start = q_start;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.out = out;
+    p.status = reinterpret_cast<int *>(ws);
+    p.counter = reinterpret_cast<unsigned *>(ws + 4);
+    p.part_o = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.part_o_off) : nullptr;
+    p.part_ml = pl.max_parts > 1 ? reinterpret_cast<float *>(ws + pl.part_ml_off) : nullptr;
+    p.out_dtype = out_dtype;
+    p.num_seqs = num_seqs;
+    p.num_tokens = num_tokens;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.head_dim = head_dim;
+    p.num_blocks = num_blocks;
+    p.max_blocks = max_blocks_per_seq;
+    p.max_len = max_seq_len;
+    p.max_q_len = max_q_len;
+    p.group = group;
+    p.score_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.partition = pl.partition > 0 ? pl.partition : max_blocks_per_seq * kBlockSize;
+    p.max_parts = pl.max_parts;
+    p.drop_first_copy = (flags & PKV_FLAG_TEST_DROP_FIRST_COPY) ? 1 : 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess)  // status word and work counter
+        return PKV_ERR_CUDA;
+    return launch_prefill(p, kv_dtype, st);
+}
+
 pkv_status pkv_read_status(void *workspace, int clear, int32_t *host_status, void *stream)
 {
     if (!workspace || !host_status)

@@ -47,6 +47,32 @@ struct DecodeParams {
     float k_scale, v_scale;
 };
 
+// Paged attention of several query tokens per sequence (chunked prefill,
+// speculative verification).  The queries of sequence s are rows
+// q_start[s] .. q_start[s+1]-1 of q [T, Hq, D], its last n_s positions.
+struct PrefillParams {
+    const void *q;
+    const int32_t *q_start;  // [S + 1]
+    const void *k_cache;
+    const void *v_cache;
+    const int32_t *block_tables;
+    const int32_t *seq_lens;
+    void *out;               // [T, Hq, D]
+    float *part_o;           // [T][Hq][max_parts][D] normalised partial outputs
+    float *part_ml;          // [T][Hq][max_parts][2]
+    int *status;             // workspace word 0
+    unsigned *counter;       // workspace word 1: next work item
+    int out_dtype;
+    int num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks;
+    int max_len;             // bound on seq_lens
+    int max_q_len;           // bound on n_s
+    int group;
+    float score_scale;       // scale * log2(e)
+    int partition;           // tokens per partition (multiple of 16)
+    int max_parts;           // 1: no split
+    int drop_first_copy;     // test hook: never issue the first copy of item 0
+};
+
 constexpr int kBlockSize = 16;
 constexpr size_t kWorkspaceHeader = 256;
 constexpr int kStreamKMaxCtas = 1024;  // partial slots of the stream-K schedule
@@ -58,6 +84,7 @@ pkv_status launch_decode_simt(const DecodeParams &p, int kv_dtype, cudaStream_t 
 pkv_status launch_decode_mma(const DecodeParams &p, int kv_dtype, cudaStream_t stream);
 pkv_status launch_merge(const DecodeParams &p, cudaStream_t stream);
 bool mma_supports(int kv_dtype, int q_dtype, int head_dim, int group);
+pkv_status launch_prefill(const PrefillParams &p, int kv_dtype, cudaStream_t stream);
 
 pkv_status launch_reshape_and_cache(const void *k, const void *v, int in_dtype,
                                     const int64_t *slot_mapping, int num_tokens,

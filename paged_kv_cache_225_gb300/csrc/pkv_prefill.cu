@@ -1,0 +1,655 @@
+// Paged attention of several query tokens per sequence for sm_103a: chunked
+// prefill and speculative verification.
+//
+// What is computed: the block-table walk of the PagedAttention kernel
+// pseudocode ("vLLM e PagedAttention: serving high-throughput") with the
+// causal mask of the "Inference optimization" lesson (Step 2,
+// scaled_dot_product_attention, triu mask of offset
+// seq_len_k - seq_len_q + 1).  The n queries of a sequence of L cached tokens
+// are its last n positions; query i attends the rows t <= L - n + i.
+//
+// How it is laid out on the GPU (not taken from the pages):
+//  * A row is one (query token, grouped query head) pair; the n * G rows of
+//    (sequence, KV head) are cut into blocks of up to 64.  A work item is
+//    (sequence, KV head, partition of the context, row block); every K/V
+//    page the item needs crosses HBM once for all of its rows.
+//  * A persistent grid pulls items from an atomic counter.  The CTA's four
+//    warps stream the item's pages through one shared ring of bulk (TMA)
+//    copies: lane 0 of warp 0 issues them in page order; a full barrier per
+//    stage carries the copied bytes, an empty barrier per stage counts the
+//    warps that have read it.  Every wait is bounded.
+//  * Each warp owns a 16-row tile (two 8-wide MMA N tiles).  With fewer than
+//    64 rows the spare warps split the pages instead: warp w takes row tile
+//    w % RT and every PG-th page, RT * PG = 4.
+//  * Per page and warp, S^T = K^T Q^T and O^T = V P^T run on mma.sync as in
+//    the decode kernel; the causal limit of each row masks its scores.
+//  * The warps' softmax states are merged through shared memory at the end
+//    of the item.  A row whose visible context fits one partition is written
+//    to `out`; the others leave normalised partials (o, m, l) that
+//    prefill_merge_kernel combines with log-sum-exp weights.
+#include "pkv_decode.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kRowTile = 16;                  // rows per warp tile
+constexpr int kRowBlock = kWarps * kRowTile;  // rows per work item
+constexpr int kPrefillRingBytes = 96 * 1024;  // two CTAs per SM
+
+template <int D> struct PrefillGeom {
+    static constexpr int kTileBytes = D * kBlockSize * 2;  // bf16 page tile
+    static constexpr int kStageBytes = 2 * kTileBytes;     // K then V
+    static constexpr int NS = kPrefillRingBytes / kStageBytes;
+    static constexpr int kRingBytes = NS * kStageBytes;
+    static constexpr int kScratchFloats = kRowTile * D + 2 * kRowTile;  // O, m, l of a warp
+    static constexpr int kSmem = kRingBytes + 2 * NS * 8;
+    static_assert(kWarps * kScratchFloats * 4 <= kRingBytes, "merge scratch fits in the ring");
+    static_assert((kScratchFloats * 4) % 16 == 0, "warp scratch keeps float4 alignment");
+};
+
+struct SeqInfo {
+    int L;   // cached tokens (the queries included)
+    int q0;  // first query row in q
+    int nq;  // queries (0 when the sequence's arguments are invalid)
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const PrefillParams &p, int s)
+{
+    SeqInfo si;
+    int L = __ldg(p.seq_lens + s);
+    if (L < 0 || L > p.max_len) {
+        set_status(p.status, PKV_ERR_OUT_OF_RANGE);
+        L = L < 0 ? 0 : p.max_len;
+    }
+    const int a = __ldg(p.q_start + s), b = __ldg(p.q_start + s + 1);
+    si.L = L;
+    si.q0 = a;
+    si.nq = b - a;
+    if (a < 0 || b > p.num_tokens || b < a || b - a > L || b - a > p.max_q_len) {
+        set_status(p.status, PKV_ERR_OUT_OF_RANGE);
+        si.q0 = 0;
+        si.nq = 0;
+    }
+    return si;
+}
+
+__device__ __forceinline__ int seq_parts(const PrefillParams &p, int L)
+{
+    return p.max_parts > 1 ? parts_of(L, p.partition) : 1;
+}
+
+// Items of sequence s: KV heads x partitions x row blocks.
+__device__ __forceinline__ int seq_item_count(const PrefillParams &p, const SeqInfo &si)
+{
+    const int blocks = (si.nq * p.group + kRowBlock - 1) / kRowBlock;
+    return p.num_kv_heads * seq_parts(p, si.L) * blocks;
+}
+
+struct PrefillItem {
+    int s, hkv, part, rb, L, q0, nq;
+};
+
+// Warp-collective: maps item index u to its (sequence, KV head, partition,
+// row block).  (cur_s, cur_base) keep the scan position between calls; u only
+// grows.  Returns false past the last item.
+__device__ bool find_prefill_item(const PrefillParams &p, int u, int &cur_s, int &cur_base,
+                                  int lane, PrefillItem &it)
+{
+    const int S = p.num_seqs;
+    for (;;) {
+        const int sl = cur_s + lane;
+        int n = 0;
+        SeqInfo si = {0, 0, 0};
+        if (sl < S) {
+            si = seq_info(p, sl);
+            n = seq_item_count(p, si);
+        }
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(kFullMask, incl, off);
+            if (lane >= off)
+                incl += t;
+        }
+        const int tot = __shfl_sync(kFullMask, incl, 31);
+        if (u < cur_base + tot) {
+            const unsigned bal = __ballot_sync(kFullMask, cur_base + incl > u);
+            const int ln = __ffs(bal) - 1;
+            const int excl = __shfl_sync(kFullMask, incl - n, ln);
+            it.s = cur_s + ln;
+            it.L = __shfl_sync(kFullMask, si.L, ln);
+            it.q0 = __shfl_sync(kFullMask, si.q0, ln);
+            it.nq = __shfl_sync(kFullMask, si.nq, ln);
+            const int k = u - cur_base - excl;
+            const int blocks = (it.nq * p.group + kRowBlock - 1) / kRowBlock;
+            const int parts = seq_parts(p, it.L);
+            it.rb = k % blocks;
+            it.part = (k / blocks) % parts;
+            it.hkv = k / (blocks * parts);
+            return true;
+        }
+        if (cur_s + 32 >= S)
+            return false;
+        cur_base += tot;
+        cur_s += 32;
+    }
+}
+
+__device__ __forceinline__ void mbar_inval(uint64_t *bar)
+{
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Online-softmax update of one N tile with a per-row visibility limit: token
+// tok of the page is seen by row column e when tok < lim[e].
+__device__ __forceinline__ bool causal_update(const float (&sacc)[4], int tokA, int tokB,
+                                              const int (&lim)[2], float c, float (&m)[2],
+                                              float (&l)[2], float (&pr)[4], float (&alpha)[2])
+{
+    const bool a0 = tokA < lim[0], a1 = tokA < lim[1];
+    const bool b0 = tokB < lim[0], b1 = tokB < lim[1];
+    const float s0 = a0 ? sacc[0] * c : -INFINITY;
+    const float s1 = a1 ? sacc[1] * c : -INFINITY;
+    const float s2 = b0 ? sacc[2] * c : -INFINITY;
+    const float s3 = b1 ? sacc[3] * c : -INFINITY;
+    constexpr float kLazy = MmaSoftmax::kLazy;
+    const bool fast = s0 <= m[0] + kLazy && s2 <= m[0] + kLazy && s1 <= m[1] + kLazy &&
+                      s3 <= m[1] + kLazy;
+    if (__all_sync(kFullMask, fast)) {
+        // A row that has seen nothing yet keeps m = -inf: its masked scores
+        // give p = 0 explicitly (never 2^(-inf - -inf)).
+        pr[0] = a0 ? MmaSoftmax::ex2(s0 - m[0]) : 0.f;
+        pr[1] = a1 ? MmaSoftmax::ex2(s1 - m[1]) : 0.f;
+        pr[2] = b0 ? MmaSoftmax::ex2(s2 - m[0]) : 0.f;
+        pr[3] = b1 ? MmaSoftmax::ex2(s3 - m[1]) : 0.f;
+        l[0] += pr[0] + pr[2];
+        l[1] += pr[1] + pr[3];
+        return false;
+    }
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFullMask, mx0, off));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFullMask, mx1, off));
+    }
+    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+    alpha[0] = (m[0] == -INFINITY) ? 0.f : MmaSoftmax::ex2(m[0] - mn0);
+    alpha[1] = (m[1] == -INFINITY) ? 0.f : MmaSoftmax::ex2(m[1] - mn1);
+    pr[0] = a0 ? MmaSoftmax::ex2(s0 - mn0) : 0.f;
+    pr[1] = a1 ? MmaSoftmax::ex2(s1 - mn1) : 0.f;
+    pr[2] = b0 ? MmaSoftmax::ex2(s2 - mn0) : 0.f;
+    pr[3] = b1 ? MmaSoftmax::ex2(s3 - mn1) : 0.f;
+    l[0] = l[0] * alpha[0] + pr[0] + pr[2];
+    l[1] = l[1] * alpha[1] + pr[1] + pr[3];
+    m[0] = mn0;
+    m[1] = mn1;
+    return true;
+}
+
+// One page for one warp's 16 rows: scores, causal softmax, P V.  `lim` holds
+// the visible-token count of the page for each of the lane's four row columns.
+template <int D>
+__device__ __forceinline__ void prefill_page(typename MmaStateBase<D, 2>::State &st,
+                                             typename MmaBf16Policy<D, 2>::Frags &f, int valid,
+                                             const int (&lim)[2][2], int lane, float c)
+{
+    using Base = MmaStateBase<D, 2>;
+    constexpr int KS = Base::KS, MT = Base::MT, NT = 2;
+    const int r = lane >> 2, cc = lane & 3;
+    float sacc[NT][4], sodd[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            sacc[n][e] = sodd[n][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+            mma_bf16((ks & 1) ? sodd[n] : sacc[n], f.k[ks], st.qf[ks][n][0], st.qf[ks][n][1]);
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            sacc[n][e] += sodd[n][e];
+
+    uint32_t bh0[NT], bh1[NT], bl0[NT], bl1[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        float pr[4], alpha[2];
+        if (causal_update(sacc[n], r, r + 8, lim[n], c, st.m[n], st.l[n], pr, alpha))
+            Base::rescale(st, n, alpha);
+        const uint32_t hx = pack_bf16(pr[0], pr[1]);
+        const uint32_t hy = pack_bf16(pr[2], pr[3]);
+        const uint32_t lx = pack_bf16(pr[0] - bf16_lo(hx), pr[1] - bf16_hi(hx));
+        const uint32_t ly = pack_bf16(pr[2] - bf16_lo(hy), pr[3] - bf16_hi(hy));
+        bh0[n] = movmatrix_t(hx);
+        bh1[n] = movmatrix_t(hy);
+        bl0[n] = movmatrix_t(lx);
+        bl1[n] = movmatrix_t(ly);
+    }
+    if (valid < kBlockSize) {  // past the sequence end: zero V (may hold NaN)
+        const uint32_t mlo = (2 * cc < valid ? 0x0000ffffu : 0u) |
+                             (2 * cc + 1 < valid ? 0xffff0000u : 0u);
+        const uint32_t mhi = (8 + 2 * cc < valid ? 0x0000ffffu : 0u) |
+                             (9 + 2 * cc < valid ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            f.v[mt][0] &= mlo;
+            f.v[mt][1] &= mlo;
+            f.v[mt][2] &= mhi;
+            f.v[mt][3] &= mhi;
+        }
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+            mma_bf16(st.o[mt][n], f.v[mt], bh0[n], bh1[n]);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+            mma_bf16(st.o[mt][n], f.v[mt], bl0[n], bl1[n]);
+}
+
+__device__ __forceinline__ void store_row4(const PrefillParams &p, int D, int token, int h,
+                                           int q4, float4 v)
+{
+    const size_t off = (static_cast<size_t>(token) * p.num_q_heads + h) * D + 4 * q4;
+    if (p.out_dtype == PKV_F32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) = v;
+    } else {
+        uint2 w;
+        w.x = pack_bf16(v.x, v.y);
+        w.y = pack_bf16(v.z, v.w);
+        *reinterpret_cast<uint2 *>(static_cast<unsigned short *>(p.out) + off) = w;
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParams p)
+{
+    using Geo = PrefillGeom<D>;
+    using Base = MmaStateBase<D, 2>;
+    using Pol = MmaBf16Policy<D, 2>;
+    constexpr int NS = Geo::NS;
+    constexpr int KS = Base::KS;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Geo::kRingBytes);
+    uint64_t *empty = full + NS;
+    __shared__ int s_item[8];
+    __shared__ int s_ok[NS];
+    __shared__ int s_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int G = p.group;
+    const float c = p.score_scale;
+    int cur_s = 0, cur_base = 0;  // warp 0's scan position
+    bool initialised = false;
+    bool first = true;
+
+    for (;;) {
+        if (threadIdx.x == 0) {
+            s_item[0] = static_cast<int>(atomicAdd(p.counter, 1u));
+            s_abort = 0;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            PrefillItem it;
+            const bool ok = find_prefill_item(p, s_item[0], cur_s, cur_base, lane, it);
+            if (lane == 0) {
+                s_item[1] = ok ? 1 : 0;
+                if (ok) {
+                    s_item[2] = it.s;
+                    s_item[3] = it.hkv;
+                    s_item[4] = it.part;
+                    s_item[5] = it.rb;
+                    s_item[6] = it.L;
+                    s_item[7] = it.nq;
+                    // Barriers restart for each item; the empty count is the
+                    // number of warps that read each page.
+                    const int rows = it.nq * G - it.rb * kRowBlock;
+                    const int nrows = rows < kRowBlock ? rows : kRowBlock;
+                    const int rt = (nrows + kRowTile - 1) / kRowTile;
+                    const int rtp = rt == 3 ? 4 : rt;
+                    for (int i = 0; i < NS; ++i) {
+                        if (initialised) {
+                            mbar_inval(&full[i]);
+                            mbar_inval(&empty[i]);
+                        }
+                        mbar_init(&full[i], 1);
+                        mbar_init(&empty[i], rtp);
+                    }
+                    fence_mbar_init();
+                }
+            }
+            if (__shfl_sync(kFullMask, ok ? 1 : 0, 0))
+                initialised = true;
+        }
+        __syncthreads();
+        if (!s_item[1])
+            break;
+        const int s = s_item[2], hkv = s_item[3], part = s_item[4], rb = s_item[5];
+        const int L = s_item[6], nq = s_item[7];
+        const int q0 = __ldg(p.q_start + s);  // validated by the scan
+
+        // ------------------------------------------------ item geometry
+        const int rows = nq * G;
+        const int row0 = rb * kRowBlock;
+        const int nrows = min(kRowBlock, rows - row0);
+        const int RT = (nrows + kRowTile - 1) / kRowTile;
+        const int RTp = RT == 3 ? 4 : RT;
+        const int PG = kWarps / RTp;
+        const int rt = warp % RTp, pg = warp / RTp;
+        const int q_first = L - nq;  // position of query 0
+        const int pos_max = q_first + (row0 + nrows - 1) / G;
+        const int P = p.partition;
+        const int t0 = part * P;
+        int t1 = t0 + P < L ? t0 + P : L;
+        t1 = t1 < pos_max + 1 ? t1 : pos_max + 1;
+        const int pg0 = t0 / kBlockSize;
+        const int npages = t1 > t0 ? (t1 - t0 + kBlockSize - 1) / kBlockSize : 0;
+
+        // ------------------------------------------- this warp's rows
+        typename Base::State st;
+        Base::reset(st);
+        const int tile0 = row0 + rt * kRowTile;  // first row of the warp's tile
+        int pos[2][2];
+        {
+            const int r = lane >> 2, cc = lane & 3;
+#pragma unroll
+            for (int n = 0; n < 2; ++n) {
+                const int R = tile0 + 8 * n + r;
+                const bool ok = R - row0 < nrows;
+                const int tok = q0 + (ok ? R / G : 0);
+                const int h = hkv * G + (ok ? R % G : 0);
+                const size_t qrow = (static_cast<size_t>(tok) * p.num_q_heads + h) * D;
+#pragma unroll
+                for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int d = 16 * ks + 8 * hh + 2 * cc;
+                        st.qf[ks][n][hh] =
+                            ok ? *reinterpret_cast<const uint32_t *>(
+                                     static_cast<const unsigned short *>(p.q) + qrow + d)
+                               : 0u;
+                    }
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int Rc = tile0 + 8 * n + 2 * cc + e;
+                    pos[n][e] = (Rc - row0 < nrows) ? q_first + Rc / G : -1;
+                }
+            }
+        }
+
+        // ------------------------------------------------ page stream
+        const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks + pg0;
+        const size_t tile_stride = static_cast<size_t>(D) * kBlockSize * 2;
+        const size_t block_stride = tile_stride * p.num_kv_heads;
+        int issued = 0;  // pages issued (warp 0)
+        bool aborted = false;
+        auto issue_one = [&](int k) {
+            const int stg = k % NS;
+            const int phys = __ldg(table + k);
+            const bool ok = phys >= 0 && phys < p.num_blocks;
+            s_ok[stg] = ok ? 1 : 0;
+            if (!ok) {
+                set_status(p.status, PKV_ERR_OUT_OF_RANGE);
+                mbar_arrive(&full[stg]);
+                return;
+            }
+            mbar_arrive_expect_tx(&full[stg], 2 * Geo::kTileBytes);
+            if (p.drop_first_copy && first && blockIdx.x == 0 && k == 0)
+                return;
+            const size_t off = static_cast<size_t>(phys) * block_stride + hkv * tile_stride;
+            unsigned char *dst = smem + stg * Geo::kStageBytes;
+            bulk_g2s(dst, static_cast<const unsigned char *>(p.k_cache) + off, Geo::kTileBytes,
+                     &full[stg]);
+            bulk_g2s(dst + Geo::kTileBytes, static_cast<const unsigned char *>(p.v_cache) + off,
+                     Geo::kTileBytes, &full[stg]);
+        };
+        // Warp 0 only: issue pages < limit; blocking waits for free stages
+        // when `block`, else stops at the first stage still in use.
+        auto issue_upto = [&](int limit, bool block) {
+            while (issued < npages && issued < limit) {
+                if (issued >= NS) {
+                    const int stg = issued % NS;
+                    const uint32_t par = static_cast<uint32_t>((issued / NS) - 1) & 1u;
+                    int ready = 0;
+                    if (lane == 0)
+                        ready = block ? mbar_wait_bounded(&empty[stg], par, kWaitLimitNs)
+                                      : mbar_try_wait(&empty[stg], par);
+                    ready = __shfl_sync(kFullMask, ready, 0);
+                    if (!ready) {
+                        if (block) {
+                            if (lane == 0) {
+                                set_status(p.status, PKV_ERR_TIMEOUT);
+                                atomicExch(&s_abort, 1);
+                            }
+                            aborted = true;
+                        }
+                        return;
+                    }
+                }
+                if (lane == 0)
+                    issue_one(issued);
+                ++issued;
+            }
+        };
+        if (warp == 0)
+            issue_upto(NS, false);
+
+        for (int j = pg; j < npages && !aborted; j += PG) {
+            if (warp == 0) {
+                issue_upto(j + 1, true);
+                if (aborted)
+                    break;
+            }
+            const int stg = j % NS;
+            const uint32_t par = static_cast<uint32_t>(j / NS) & 1u;
+            const bool ok = mbar_wait_bounded(&full[stg], par, kWaitLimitNs);
+            if (!__all_sync(kFullMask, ok)) {
+                if (lane == 0) {
+                    set_status(p.status, PKV_ERR_TIMEOUT);
+                    atomicExch(&s_abort, 1);
+                }
+                aborted = true;
+                break;
+            }
+            const bool have = s_ok[stg] != 0;
+            const unsigned char *sk = smem + stg * Geo::kStageBytes;
+            typename Pol::Frags f;
+            if (have)
+                Pol::load(f, sk, sk + Geo::kTileBytes, lane);
+            // The stage is free once every lane's reads are done.
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stg]);
+            if (warp == 0)
+                issue_upto(j + NS, false);
+            if (have) {
+                const int tb = (pg0 + j) * kBlockSize;  // position of the page's token 0
+                const int valid = min(kBlockSize, L - tb);
+                int lim[2][2];
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int v = pos[n][e] - tb + 1;
+                        lim[n][e] = v < valid ? v : valid;
+                    }
+                prefill_page<D>(st, f, valid, lim, lane, c);
+            }
+        }
+        // Warp 0 issues whatever the other warps still wait for.
+        if (warp == 0 && !aborted)
+            issue_upto(npages, true);
+        __syncthreads();
+        if (s_abort) {
+            // Let every copy still in flight land before the ring is reused.
+            if (warp == 0 && lane == 0)
+                for (int k = issued > NS ? issued - NS : 0; k < issued; ++k)
+                    mbar_wait_bounded(&full[k % NS], static_cast<uint32_t>(k / NS) & 1u,
+                                      kWaitLimitNs);
+            __syncthreads();
+        }
+
+        // ---------------------------------------------- merge the warps
+        float *scratch = reinterpret_cast<float *>(smem);
+        {
+            float *mine = scratch + warp * Geo::kScratchFloats;
+            Base::finish(st, mine, mine + kRowTile * D, mine + kRowTile * D + kRowTile, lane);
+        }
+        __syncthreads();
+        constexpr int Q4 = D / 4;
+        for (int idx = threadIdx.x; idx < nrows * Q4; idx += kThreads) {
+            const int r = idx / Q4, q4 = idx - r * Q4;
+            const int rtr = r / kRowTile, rr = r % kRowTile;
+            const int R = row0 + r;
+            const int i = R / G;
+            const int h = hkv * G + R % G;
+            const int pos_r = q_first + i;
+            const int nparts_r = p.max_parts > 1 ? parts_of(pos_r + 1, P) : 1;
+            if (part >= nparts_r)
+                continue;  // this partition is past the row's last visible token
+            float mw[kWarps], mx = -INFINITY;
+            for (int g = 0; g < PG; ++g) {
+                const float *sw = scratch + (rtr + RTp * g) * Geo::kScratchFloats;
+                mw[g] = sw[kRowTile * D + rr];
+                mx = fmaxf(mx, mw[g]);
+            }
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float lsum = 0.f;
+            for (int g = 0; g < PG; ++g) {
+                const float *sw = scratch + (rtr + RTp * g) * Geo::kScratchFloats;
+                const float fw = (mw[g] == -INFINITY) ? 0.f : exp2f(mw[g] - mx);
+                const float4 o = reinterpret_cast<const float4 *>(sw + rr * D)[q4];
+                acc.x += fw * o.x;
+                acc.y += fw * o.y;
+                acc.z += fw * o.z;
+                acc.w += fw * o.w;
+                lsum += fw * sw[kRowTile * D + kRowTile + rr];
+            }
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            const float4 o4 = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            if (nparts_r == 1) {
+                store_row4(p, D, q0 + i, h, q4, o4);
+            } else {
+                const size_t prow =
+                    (static_cast<size_t>(q0 + i) * p.num_q_heads + h) * p.max_parts + part;
+                reinterpret_cast<float4 *>(p.part_o + prow * D)[q4] = o4;
+                if (q4 == 0) {
+                    p.part_ml[2 * prow] = mx;
+                    p.part_ml[2 * prow + 1] = lsum;
+                }
+            }
+        }
+        __syncthreads();  // scratch (the ring) is read before the next item refills it
+        first = false;
+    }
+}
+
+// Log-sum-exp merge of the partials of one (query token, KV head): the rows
+// whose visible context spans more than one partition.
+template <int D>
+__global__ void __launch_bounds__(kThreads) prefill_merge_kernel(const PrefillParams p)
+{
+    const int t = blockIdx.x / p.num_kv_heads;
+    const int hkv = blockIdx.x - t * p.num_kv_heads;
+    int lo = 0, hi = p.num_seqs;  // q_start[lo] <= t < q_start[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(p.q_start + mid) <= t)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int s = lo;
+    int L = __ldg(p.seq_lens + s);
+    L = L < 0 ? 0 : (L > p.max_len ? p.max_len : L);
+    const int a = __ldg(p.q_start + s), b = __ldg(p.q_start + s + 1);
+    if (a < 0 || b > p.num_tokens || b < a || b - a > L || b - a > p.max_q_len || t < a || t >= b)
+        return;  // reported by the attention kernel
+    const int pos = L - (b - a) + (t - a);
+    const int nparts = parts_of(pos + 1, p.partition);
+    if (nparts <= 1)
+        return;  // written directly
+    constexpr int Q4 = D / 4;
+    const int G = p.group;
+    for (int idx = threadIdx.x; idx < G * Q4; idx += blockDim.x) {
+        const int g = idx / Q4, q4 = idx - g * Q4;
+        const int h = hkv * G + g;
+        const size_t row0 = (static_cast<size_t>(t) * p.num_q_heads + h) * p.max_parts;
+        const float *ml = p.part_ml + 2 * row0;
+        float mx = -INFINITY;
+        for (int i = 0; i < nparts; ++i)
+            mx = fmaxf(mx, __ldcg(ml + 2 * i));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float wsum = 0.f;
+        for (int i = 0; i < nparts; ++i) {
+            const float m = __ldcg(ml + 2 * i), l = __ldcg(ml + 2 * i + 1);
+            const float w = (m == -INFINITY) ? 0.f : l * exp2f(m - mx);
+            wsum += w;
+            const float4 o =
+                __ldcg(reinterpret_cast<const float4 *>(p.part_o + (row0 + i) * D) + q4);
+            acc.x += w * o.x;
+            acc.y += w * o.y;
+            acc.z += w * o.z;
+            acc.w += w * o.w;
+        }
+        const float sc = wsum > 0.f ? 1.f / wsum : 0.f;
+        store_row4(p, D, t, h, q4, make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
+    }
+}
+
+template <int D>
+pkv_status launch_prefill_d(const PrefillParams &p, cudaStream_t stream)
+{
+    using Geo = PrefillGeom<D>;
+    static int occ = -1;
+    if (occ < 0) {
+        if (cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Geo::kSmem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        int o = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, prefill_kernel<D>, kThreads,
+                                                          Geo::kSmem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        occ = o > 0 ? o : 1;
+    }
+    const long blocks = (static_cast<long>(p.max_q_len) * p.group + kRowBlock - 1) / kRowBlock;
+    const long items = static_cast<long>(p.num_seqs) * p.num_kv_heads * p.max_parts * blocks;
+    const long slots = static_cast<long>(occ) * device_sm_count();
+    const long grid = items < slots ? items : slots;
+    if (grid <= 0)
+        return PKV_OK;
+    prefill_kernel<D><<<static_cast<unsigned>(grid), kThreads, Geo::kSmem, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (p.max_parts > 1 && p.num_tokens > 0) {
+        const long mgrid = static_cast<long>(p.num_tokens) * p.num_kv_heads;
+        prefill_merge_kernel<D><<<static_cast<unsigned>(mgrid), kThreads, 0, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
+    return PKV_OK;
+}
+
+}  // namespace
+
+pkv_status launch_prefill(const PrefillParams &p, int kv_dtype, cudaStream_t stream)
+{
+    if (kv_dtype != PKV_BF16 || p.group < 1 || p.group > 16)
+        return PKV_ERR_UNSUPPORTED;
+    if (p.head_dim == 128)
+        return launch_prefill_d<128>(p, stream);
+    if (p.head_dim == 64)
+        return launch_prefill_d<64>(p, stream);
+    return PKV_ERR_UNSUPPORTED;
+}
+
+}  // namespace pkv

@@ -37,3 +37,28 @@ def algorithmic_bytes(w: Workload, seq_lens: Optional[np.ndarray] = None,
     table = pages * 4 + cfg.num_seqs * 4
     return {"tokens": tok, "kv": kv, "q": q, "out": out, "table": table,
             "total": kv + q + out + table, "kv_page_rounded": pages * cfg.block_size * row}
+
+
+def prefill_algorithmic(w, out_elem_bytes: int = 4) -> dict:
+    """Minimum HBM bytes and the flops of one several-queries attention launch.
+
+    Every (sequence, KV head) must read the K/V rows of its valid tokens once,
+    whatever its number of queries; q and out are read / written once; the
+    table entries and lengths are read once.  Flops count the multiply-adds of
+    q.k and p.v over each query's visible rows (causal), two flops each.
+    """
+    base = w.cfg.base
+    L = np.asarray(w.seq_lens, dtype=np.int64)
+    n = np.diff(np.asarray(w.q_start, dtype=np.int64))
+    row = base.num_kv_heads * 2 * base.head_dim * ELEM_BYTES[base.kv_dtype]
+    kv = int(L.sum()) * row
+    pages = int(((L + base.block_size - 1) // base.block_size).sum())
+    T = int(n.sum())
+    q = T * base.num_q_heads * base.head_dim * ELEM_BYTES[base.q_dtype]
+    out = T * base.num_q_heads * base.head_dim * out_elem_bytes
+    table = pages * 4 + (2 * L.size + 1) * 4
+    # Query i of a sequence sees L - n + i + 1 rows.
+    visible = int(((L - n) * n + n * (n + 1) // 2).sum())
+    flops = 4 * base.head_dim * base.num_q_heads * visible
+    return {"tokens": int(L.sum()), "queries": T, "kv": kv, "q": q, "out": out, "table": table,
+            "total": kv + q + out + table, "flops": flops, "visible_rows": visible}

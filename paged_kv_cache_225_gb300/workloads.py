@@ -271,3 +271,128 @@ def make_workload(cfg: DecodeConfig | str, seed: Optional[int] = None,
     return Workload(cfg=cfg, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=tables,
                     seq_lens=L, new_k=new_k, new_v=new_v, slot_mapping=slots,
                     scale=1.0 / math.sqrt(D))
+
+
+# ------------------------------------------------------------------ several queries per sequence
+
+@dataclasses.dataclass(frozen=True)
+class PrefillConfig:
+    """Recipe of one batch with several causal query tokens per sequence.
+
+    ``base`` fixes head shapes, dtypes and the context-length recipe; here a
+    sequence's length counts its queries, whose K/V are already in the cache.
+    Every sequence gets ``q_len`` queries (0 = all of its tokens), capped at
+    its length, unless ``q_lens`` lists them; the first ``chunk_seqs``
+    sequences instead run a prefill chunk of ``chunk_len`` queries at a
+    length drawn from U{chunk_ctx_lo..chunk_ctx_hi} (vLLM's chunked prefill
+    mixes such chunks with decoding sequences in one step).
+    """
+
+    name: str
+    base: DecodeConfig
+    q_len: int = 1
+    q_lens: tuple = ()
+    chunk_seqs: int = 0
+    chunk_len: int = 0
+    chunk_ctx_lo: int = 0
+    chunk_ctx_hi: int = 0
+
+
+PREFILL_CONFIGS = {
+    # Small mixed case the oracle finishes in well under a second: ragged
+    # lengths, a whole-prompt prefill, row counts that need one to four warp
+    # tiles and several row blocks, NaN in every slot no sequence owns.
+    "prefill_tiny": PrefillConfig(
+        name="prefill_tiny",
+        base=DecodeConfig(name="prefill_tiny", num_seqs=7, num_q_heads=8, num_kv_heads=2,
+                          head_dim=64, block_size=16, q_dtype=BF16, kv_dtype=BF16,
+                          len_dist="uniform", len_lo=1, len_hi=200, garbage="nan",
+                          new_tokens=False),
+        q_lens=(1, 3, 16, 33, 0, 10, 2)),
+    # Speculative verification on the Llama-3-70B layer: five draft tokens
+    # per sequence checked in one pass ("Inference optimization" lesson,
+    # speculative decoding: the target model scores the ~5 guesses at once).
+    "spec_verify_70b": PrefillConfig(
+        name="spec_verify_70b",
+        base=DecodeConfig(name="spec_verify_70b", num_seqs=128, num_q_heads=64,
+                          num_kv_heads=8, head_dim=128, block_size=16, q_dtype=BF16,
+                          kv_dtype=BF16, len_dist="lognormal", len_median=2048.0,
+                          len_sigma=0.8, len_lo=16, len_hi=32768, new_tokens=False),
+        q_len=5),
+    # Chunked prefill on the Llama-3-8B layer: four 256-token prompt chunks
+    # scheduled with 60 decoding sequences.
+    "chunked_prefill_8b": PrefillConfig(
+        name="chunked_prefill_8b",
+        base=DecodeConfig(name="chunked_prefill_8b", num_seqs=64, num_q_heads=32,
+                          num_kv_heads=8, head_dim=128, block_size=16, q_dtype=BF16,
+                          kv_dtype=BF16, len_dist="uniform", len_lo=512, len_hi=4096,
+                          new_tokens=False),
+        q_len=1, chunk_seqs=4, chunk_len=256, chunk_ctx_lo=1024, chunk_ctx_hi=4096),
+}
+PREFILL_SEED = {name: 100 + i for i, name in enumerate(PREFILL_CONFIGS)}
+
+
+@dataclasses.dataclass
+class PrefillWorkload:
+    cfg: PrefillConfig
+    q: np.ndarray             # [T, Hq, D]
+    q_start: np.ndarray       # int32 [S + 1]
+    k_cache: np.ndarray
+    v_cache: np.ndarray
+    block_tables: np.ndarray
+    seq_lens: np.ndarray      # int32 [S], queries included
+    scale: float
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.q_start[-1])
+
+    @property
+    def max_q_len(self) -> int:
+        return int(np.max(np.diff(self.q_start))) if self.seq_lens.size else 0
+
+
+def make_prefill_workload(cfg: PrefillConfig | str, seed: Optional[int] = None,
+                          seq_lens: Optional[np.ndarray] = None,
+                          q_lens: Optional[np.ndarray] = None) -> PrefillWorkload:
+    """Build the seeded several-queries workload of ``cfg``.
+
+    Draw order from ``default_rng(seed)``: lengths, chunk lengths, then the
+    cache (``make_workload`` of the base recipe with seed + 1), then q.
+    ``seq_lens`` / ``q_lens`` override the drawn values (edge-case tests).
+    """
+    if isinstance(cfg, str):
+        if seed is None:
+            seed = PREFILL_SEED[cfg]
+        cfg = PREFILL_CONFIGS[cfg]
+    if seed is None:
+        seed = 0
+    rng = np.random.default_rng(seed)
+    base = cfg.base
+    S = base.num_seqs
+    L = _draw_lengths(base, rng)
+    if cfg.chunk_seqs:
+        L[:cfg.chunk_seqs] = rng.integers(cfg.chunk_ctx_lo, cfg.chunk_ctx_hi,
+                                          size=cfg.chunk_seqs, endpoint=True)
+    if seq_lens is not None:
+        L = np.asarray(seq_lens, dtype=np.int32).copy()
+    if q_lens is not None:
+        n = np.asarray(q_lens, dtype=np.int64).copy()
+    elif cfg.q_lens:
+        n = np.asarray(cfg.q_lens, dtype=np.int64)
+        n = np.where(n == 0, L, n)
+    else:
+        n = np.full(S, cfg.q_len if cfg.q_len > 0 else 0, dtype=np.int64)
+        n = np.where(n == 0, L, n)
+        if cfg.chunk_seqs:
+            n[:cfg.chunk_seqs] = cfg.chunk_len
+    n = np.minimum(n, L).astype(np.int32)
+    w = make_workload(base, seed=seed + 1, seq_lens=L)
+    q_start = np.zeros(S + 1, dtype=np.int32)
+    q_start[1:] = np.cumsum(n)
+    T = int(q_start[-1])
+    q = round_to_storage(rng.standard_normal((T, base.num_q_heads, base.head_dim),
+                                             dtype=np.float32), base.q_dtype)
+    return PrefillWorkload(cfg=cfg, q=q, q_start=q_start, k_cache=w.k_cache,
+                           v_cache=w.v_cache, block_tables=w.block_tables, seq_lens=w.seq_lens,
+                           scale=w.scale)

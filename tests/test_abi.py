@@ -155,3 +155,75 @@ def test_binding_rejects_cpu_tensors_without_fallback():
     with pytest.raises((ValueError, RuntimeError, TypeError)):
         pkv.paged_attn_decode(q, kc, kc, torch.zeros(1, 1, dtype=torch.int32),
                               torch.ones(1, dtype=torch.int32), 0.125, torch.empty_like(q))
+
+
+# ------------------------------------------------- several queries per sequence
+
+def test_prefill_partition_plan():
+    P = pkv.prefill_partition_tokens
+    assert P(4, 20, 8, 2, 64, 8, 200, -1) == 0
+    assert P(4, 20, 8, 2, 64, 8, 200, 48) == 48
+    assert P(4, 20, 8, 2, 64, 8, 200, 40) == -1          # not a multiple of the block size
+    # Enough (KV head, 64-row block) items: no split for short contexts,
+    # 2048-token partitions for long ones.
+    assert P(128, 640, 64, 8, 128, 5, 2000, 0) == 0
+    assert P(128, 640, 64, 8, 128, 5, 14563, 0) == 2048
+    # Few items: split so that about four items per resident CTA exist.
+    assert P(2, 8, 64, 8, 128, 5, 32768, 0) == 1024       # 16 items -> 38 parts
+    assert P(2, 8, 64, 8, 128, 5, 300, 0) == 256
+    assert P(2, 8, 64, 8, 128, 5, 256, 0) == 0           # one partition covers it
+
+
+def test_prefill_workspace_size():
+    W = pkv.prefill_workspace_size
+    assert W(4, 20, 8, 2, 64, 8, 200, -1) == 256
+    T, Hq, D, P, L = 40, 64, 128, 512, 2049
+    parts = -(-L // P)
+    rows = T * Hq * parts
+
+    def a(x):
+        return (x + 255) // 256 * 256
+    assert W(8, T, Hq, 8, D, 5, L, P) == 256 + a(rows * D * 4) + a(rows * 8)
+    with pytest.raises(ValueError):
+        W(4, 20, 6, 4, 64, 8, 200, 0)                     # heads do not divide
+
+
+def _prefill(**kw):
+    args = dict(q=0x1000, q_dtype=BF16, qs=0x1800, k=0x2000, v=0x3000, kv_dtype=BF16, bt=0x4000,
+                sl=0x5000, S=2, T=6, Hq=8, Hkv=2, D=128, B=16, N=10, maxb=4, maxq=4, maxl=64,
+                scale=0.1, out=0x6000, out_dtype=F32, ws=0x7000, wsb=1 << 26, part=0, flags=0)
+    args.update(kw)
+    return pkv.lib().pkv_paged_attn_prefill(
+        args["q"], args["q_dtype"], args["qs"], args["k"], args["v"], args["kv_dtype"], 1.0, 1.0,
+        args["bt"], args["sl"], args["S"], args["T"], args["Hq"], args["Hkv"], args["D"],
+        args["B"], args["N"], args["maxb"], args["maxq"], args["maxl"], args["scale"],
+        args["out"], args["out_dtype"], args["ws"], args["wsb"], args["part"], args["flags"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hq=6, Hkv=4), INVALID),
+    (dict(D=96), UNSUPPORTED),
+    (dict(B=32), UNSUPPORTED),
+    (dict(Hq=34, Hkv=2), UNSUPPORTED),
+    (dict(q_dtype=F32), UNSUPPORTED),             # tensor-core path: bf16 q and KV
+    (dict(kv_dtype=FP8), UNSUPPORTED),
+    (dict(out_dtype=FP8), UNSUPPORTED),
+    (dict(maxl=65), INVALID),
+    (dict(T=-1), INVALID),
+    (dict(maxq=-1), INVALID),
+    (dict(ws=0), WORKSPACE),
+    (dict(ws=0x7010), WORKSPACE),
+    (dict(wsb=100, part=16), WORKSPACE),
+    (dict(q=0), INVALID),
+    (dict(qs=0), INVALID),
+    (dict(qs=0x1802), INVALID),                   # misaligned q_start
+    (dict(k=0x2008), INVALID),
+    (dict(part=40), INVALID),
+    (dict(flags=0x1), INVALID),                   # no CUDA-core variant
+    (dict(flags=0x4), INVALID),
+    (dict(scale=float("inf")), INVALID),
+    (dict(S=0), OK),
+    (dict(T=0), OK),
+])
+def test_prefill_argument_errors(kw, code):
+    assert _prefill(**kw) == code
