@@ -51,7 +51,8 @@ typedef enum {
     PKV_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed             */
     PKV_ERR_OUT_OF_RANGE = 4,  /* device side: block id / slot / seq_len invalid   */
     PKV_ERR_TIMEOUT = 5,       /* device side: a bounded wait gave up              */
-    PKV_ERR_WORKSPACE = 6      /* workspace missing or smaller than required       */
+    PKV_ERR_WORKSPACE = 6,     /* workspace missing or smaller than required       */
+    PKV_ERR_NO_BLOCKS = 7      /* block manager: the pool (or host memory) ran out */
 } pkv_status;
 
 typedef enum {
@@ -296,6 +297,71 @@ pkv_status pkv_reshape_and_cache(const void *k, const void *v, pkv_dtype in_dtyp
                                  int head_dim, int block_size, int num_blocks,
                                  void *k_cache, void *v_cache, pkv_dtype kv_dtype,
                                  float k_scale, float v_scale, int32_t *status, void *stream);
+
+/*
+ * Copy-on-write page copies ("Inference optimization" lesson, section
+ * "PagedAttention": pages of a shared prompt are stored once; a request that
+ * diverges gets its own copy).  For every i < num_pairs, with
+ * (src, dst) = (pairs[2i], pairs[2i+1]) (int32, device memory), block dst of
+ * k_cache and of v_cache becomes a copy of block src: all num_kv_heads x
+ * head_dim x block_size elements, copied bit for bit.  Pairs whose src or dst
+ * lies outside [0, num_blocks) are skipped and reported in *status
+ * (optional device int32, as for pkv_reshape_and_cache).  A dst must not be
+ * the src or dst of another pair of the same call (no chains).  The pairs
+ * come from pkv_bm_append.
+ */
+pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, pkv_dtype kv_dtype, int num_kv_heads,
+                           int head_dim, int block_size, int num_blocks, const int32_t *pairs,
+                           int num_pairs, int32_t *status, void *stream);
+
+/*
+ * Host-side block manager (no GPU calls; thread-safe).  It keeps the page
+ * pool of one cache: a free list, a reference count per page and one page
+ * table per sequence ("Inference optimization" lesson, section
+ * "PagedAttention"; "Continuous Batching e PagedAttention no vLLM", section 3:
+ * logical blocks of a sequence map to physical pages anywhere in the pool,
+ * the last page may be partly filled, shared pages are stored once).
+ * Token t of a sequence lives at slot table[t / block_size] * block_size +
+ * t % block_size.  The lowest free page id is always taken first.  Every call
+ * either succeeds completely or leaves the manager unchanged.
+ *
+ *   pkv_bm_create    a pool of num_blocks pages; *out receives the handle
+ *                    (release with pkv_bm_destroy).
+ *   pkv_bm_add       a new sequence seq_id holding num_tokens tokens (a
+ *                    prompt): ceil(num_tokens / block_size) fresh pages;
+ *                    slots (optional, [num_tokens]) receives each token's slot.
+ *   pkv_bm_fork      child_id starts as parent_id, sharing every page (the
+ *                    reference counts go up; nothing is copied).
+ *   pkv_bm_append    reserves the next token of each of the n listed
+ *                    sequences (distinct ids), in list order: a fresh page
+ *                    when the last page is full; when the last page is
+ *                    shared, a fresh page plus a (src, dst) copy appended to
+ *                    copy_pairs ([n][2], *num_copies of them filled).
+ *                    slots[i] receives the new token's slot.  Copy the pairs
+ *                    (pkv_copy_blocks) before writing the tokens
+ *                    (pkv_reshape_and_cache).
+ *   pkv_bm_free      releases a sequence; pages no longer referenced return
+ *                    to the pool.
+ *   pkv_bm_tables    dense block tables [n][max_blocks_per_seq] (-1 padded)
+ *                    and lengths of the listed sequences, for attention.
+ *   pkv_bm_num_free, pkv_bm_ref_count   inspection (-1 on bad arguments).
+ * Errors: PKV_ERR_INVALID_ARG (unknown or duplicate id, a sequence longer
+ * than max_blocks_per_seq pages, null pointers), PKV_ERR_NO_BLOCKS (not
+ * enough free pages for the whole call).
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+pkv_status pkv_bm_create(int num_blocks, int block_size, int max_blocks_per_seq,
+                         pkv_block_manager **out);
+void pkv_bm_destroy(pkv_block_manager *bm);
+pkv_status pkv_bm_add(pkv_block_manager *bm, int seq_id, int num_tokens, int64_t *slots);
+pkv_status pkv_bm_fork(pkv_block_manager *bm, int parent_id, int child_id);
+pkv_status pkv_bm_append(pkv_block_manager *bm, const int32_t *seq_ids, int n, int64_t *slots,
+                         int32_t *copy_pairs, int *num_copies);
+pkv_status pkv_bm_free(pkv_block_manager *bm, int seq_id);
+pkv_status pkv_bm_tables(pkv_block_manager *bm, const int32_t *seq_ids, int n,
+                         int max_blocks_per_seq, int32_t *tables, int32_t *seq_lens);
+int pkv_bm_num_free(pkv_block_manager *bm);
+int pkv_bm_ref_count(pkv_block_manager *bm, int block);
 
 /*
  * Waits for `stream`, then copies the status word of a decode workspace to

@@ -10,6 +10,8 @@ current stream and the workspace allocation.
     paged_attn_decode_append(q, new_k, new_v, k_cache, v_cache, ..., out)
     paged_attn_prefill(q, q_start, k_cache, v_cache, block_tables, seq_lens, scale, out)
     reshape_and_cache(k, v, slot_mapping, k_cache, v_cache)
+    copy_blocks(k_cache, v_cache, pairs)
+    BlockManager(num_blocks)   (host-side page pool: add / fork / append / free / tables)
 """
 from __future__ import annotations
 
@@ -24,7 +26,8 @@ from . import build as _build
 
 __all__ = ["paged_attn_decode", "paged_attn_decode_append", "paged_attn_prefill",
            "reshape_and_cache", "workspace_size", "partition_tokens",
-           "prefill_workspace_size", "prefill_partition_tokens",
+           "prefill_workspace_size", "prefill_partition_tokens", "copy_blocks",
+           "BlockManager",
            "read_status", "PkvError", "lib", "F32", "BF16", "FP8_E5M2"]
 
 F32, BF16, FP8_E5M2 = 0, 1, 2
@@ -32,7 +35,8 @@ IMPL = {"auto": 0x0, "simt": 0x1, "mma": 0x2}
 FLAG_SEPARATE_MERGE = 0x4
 FLAG_TEST_DROP_FIRST_COPY = 0x100
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
-          4: "PKV_ERR_OUT_OF_RANGE", 5: "PKV_ERR_TIMEOUT", 6: "PKV_ERR_WORKSPACE"}
+          4: "PKV_ERR_OUT_OF_RANGE", 5: "PKV_ERR_TIMEOUT", 6: "PKV_ERR_WORKSPACE",
+          7: "PKV_ERR_NO_BLOCKS"}
 
 _lock = threading.Lock()
 _lib = None
@@ -76,6 +80,28 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.pkv_paged_attn_prefill.argtypes = [vp, i, vp, vp, vp, i, f, f, vp, vp, i, i, i, i,
                                                  i, i, i, i, i, i, f, vp, i, vp, sz, i, i, vp]
             L.pkv_paged_attn_prefill.restype = i
+            L.pkv_copy_blocks.argtypes = [vp, vp, i, i, i, i, i, vp, i, vp, vp]
+            L.pkv_copy_blocks.restype = i
+            ip, i32p, i64p = (ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int32),
+                              ctypes.POINTER(ctypes.c_int64))
+            L.pkv_bm_create.argtypes = [i, i, i, ctypes.POINTER(vp)]
+            L.pkv_bm_create.restype = i
+            L.pkv_bm_destroy.argtypes = [vp]
+            L.pkv_bm_destroy.restype = None
+            L.pkv_bm_add.argtypes = [vp, i, i, i64p]
+            L.pkv_bm_add.restype = i
+            L.pkv_bm_fork.argtypes = [vp, i, i]
+            L.pkv_bm_fork.restype = i
+            L.pkv_bm_append.argtypes = [vp, i32p, i, i64p, i32p, ip]
+            L.pkv_bm_append.restype = i
+            L.pkv_bm_free.argtypes = [vp, i]
+            L.pkv_bm_free.restype = i
+            L.pkv_bm_tables.argtypes = [vp, i32p, i, i, i32p, i32p]
+            L.pkv_bm_tables.restype = i
+            L.pkv_bm_num_free.argtypes = [vp]
+            L.pkv_bm_num_free.restype = i
+            L.pkv_bm_ref_count.argtypes = [vp, i]
+            L.pkv_bm_ref_count.restype = i
             L.pkv_reshape_and_cache.argtypes = [vp, vp, i, vp, i, i, i, i, i, vp, vp, i, f, f, vp,
                                                 vp]
             L.pkv_reshape_and_cache.restype = i
@@ -357,6 +383,114 @@ def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tens
         float(k_scale), float(v_scale), st_ptr, _stream(dev, stream))
     if rc != 0:
         raise PkvError(rc, "pkv_reshape_and_cache")
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs: torch.Tensor, *,
+                status: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> None:
+    """Copy-on-write page copies: block pairs[i, 1] of both caches becomes a copy
+    of block pairs[i, 0] (pairs: int32 [n, 2] on the caches' device)."""
+    dev = k_cache.device
+    _check(k_cache, "k_cache", 4, dev)
+    _check(v_cache, "v_cache", 4, dev)
+    _check(pairs, "pairs", 2, dev)
+    if pairs.dtype != torch.int32 or pairs.shape[1] != 2:
+        raise ValueError("pairs must be int32 [n, 2]")
+    if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
+        raise ValueError("k_cache and v_cache must have the same shape and dtype")
+    N, Hkv, D, B = k_cache.shape
+    st_ptr = None
+    if status is not None:
+        _check(status, "status", 1, dev)
+        st_ptr = status.data_ptr()
+    rc = lib().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(),
+                               _dtype_code(k_cache, "k_cache"), Hkv, D, B, N, pairs.data_ptr(),
+                               pairs.shape[0], st_ptr, _stream(dev, stream))
+    if rc != 0:
+        raise PkvError(rc, "pkv_copy_blocks")
+
+
+class BlockManager:
+    """Host-side page pool of one paged cache (the C library's pkv_bm_* calls).
+
+    ``add`` a sequence with its prompt, ``fork`` a sequence that shares every
+    page of another, ``append`` one token to each listed sequence (returns the
+    slots and the copy-on-write page pairs to copy first), ``free`` a
+    sequence, and ``tables`` for the dense block tables attention reads.
+    """
+
+    def __init__(self, num_blocks: int, block_size: int = 16, max_blocks_per_seq: int = 1 << 20):
+        self._lib = lib()
+        h = ctypes.c_void_p()
+        rc = self._lib.pkv_bm_create(num_blocks, block_size, max_blocks_per_seq, ctypes.byref(h))
+        if rc != 0:
+            raise PkvError(rc, "pkv_bm_create")
+        self._h = h
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        self.max_blocks_per_seq = max_blocks_per_seq
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.pkv_bm_destroy(h)
+            self._h = None
+
+    @staticmethod
+    def _p(a, ct):
+        return a.ctypes.data_as(ctypes.POINTER(ct))
+
+    def add(self, seq_id: int, num_tokens: int):
+        import numpy as np
+        slots = np.empty(max(num_tokens, 1), dtype=np.int64)
+        rc = self._lib.pkv_bm_add(self._h, seq_id, num_tokens, self._p(slots, ctypes.c_int64))
+        if rc != 0:
+            raise PkvError(rc, "pkv_bm_add")
+        return slots[:num_tokens]
+
+    def fork(self, parent_id: int, child_id: int) -> None:
+        rc = self._lib.pkv_bm_fork(self._h, parent_id, child_id)
+        if rc != 0:
+            raise PkvError(rc, "pkv_bm_fork")
+
+    def append(self, seq_ids):
+        """One token for each sequence; returns (slots int64 [n], pairs int32 [c, 2])."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        n = ids.size
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        pairs = np.empty((max(n, 1), 2), dtype=np.int32)
+        nc = ctypes.c_int(0)
+        rc = self._lib.pkv_bm_append(self._h, self._p(ids, ctypes.c_int32), n,
+                                     self._p(slots, ctypes.c_int64),
+                                     self._p(pairs, ctypes.c_int32), ctypes.byref(nc))
+        if rc != 0:
+            raise PkvError(rc, "pkv_bm_append")
+        return slots[:n], pairs[:nc.value]
+
+    def free(self, seq_id: int) -> None:
+        rc = self._lib.pkv_bm_free(self._h, seq_id)
+        if rc != 0:
+            raise PkvError(rc, "pkv_bm_free")
+
+    def tables(self, seq_ids, max_blocks_per_seq: int):
+        """Dense block tables int32 [n, max_blocks_per_seq] (-1 padded) and lengths."""
+        import numpy as np
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int32)
+        tab = np.empty((max(ids.size, 1), max_blocks_per_seq), dtype=np.int32)
+        lens = np.empty(max(ids.size, 1), dtype=np.int32)
+        rc = self._lib.pkv_bm_tables(self._h, self._p(ids, ctypes.c_int32), ids.size,
+                                     max_blocks_per_seq, self._p(tab, ctypes.c_int32),
+                                     self._p(lens, ctypes.c_int32))
+        if rc != 0:
+            raise PkvError(rc, "pkv_bm_tables")
+        return tab[:ids.size], lens[:ids.size]
+
+    def num_free(self) -> int:
+        return int(self._lib.pkv_bm_num_free(self._h))
+
+    def ref_count(self, block: int) -> int:
+        return int(self._lib.pkv_bm_ref_count(self._h, block))
 
 
 def read_status(workspace: Optional[torch.Tensor] = None, clear: bool = True,

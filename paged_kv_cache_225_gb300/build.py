@@ -17,7 +17,7 @@ SRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 UNITS = ["pkv_api.cu", "pkv_cache.cu", "pkv_merge.cu", "pkv_decode_simt.cu", "pkv_decode_mma.cu",
-         "pkv_noalloc.cu", "pkv_prefill.cu"]
+         "pkv_noalloc.cu", "pkv_prefill.cu", "pkv_block_manager.cpp"]
 HEADERS = ["pkv_common.cuh", "pkv_convert.cuh", "pkv_decode.cuh", "pkv_merge.cuh",
            "pkv_streamk.cuh", "pkv_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -55,7 +55,7 @@ def build(force: bool = False, verbose: bool = False, defines=(), out: str = Non
     tag = f"{os.getpid()}"
 
     def compile_unit(unit: str):
-        obj = os.path.join(BUILD, unit.replace(".cu", f".{tag}.o"))
+        obj = os.path.join(BUILD, os.path.splitext(unit)[0] + f".{tag}.o")
         cmd = [nvcc, *ARCH, *FLAGS, *[f"-D{d}" for d in defines], "-c",
                os.path.join(SRC, unit), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)

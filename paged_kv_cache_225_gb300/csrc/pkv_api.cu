@@ -494,6 +494,29 @@ pkv_status pkv_paged_attn_prefill(const void *q, pkv_dtype q_dtype, const int32_
     return launch_prefill(p, kv_dtype, st);
 }
 
+pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, pkv_dtype kv_dtype, int num_kv_heads,
+                           int head_dim, int block_size, int num_blocks, const int32_t *pairs,
+                           int num_pairs, int32_t *status, void *stream)
+{
+    if (num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || num_pairs < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (block_size != kBlockSize)
+        return PKV_ERR_UNSUPPORTED;
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E5M2)
+        return PKV_ERR_UNSUPPORTED;
+    if (num_pairs == 0)
+        return PKV_OK;
+    if (!k_cache || !v_cache || !pairs)
+        return PKV_ERR_INVALID_ARG;
+    const size_t elem = kv_dtype == PKV_F32 ? 4 : (kv_dtype == PKV_BF16 ? 2 : 1);
+    const size_t block_bytes = static_cast<size_t>(num_kv_heads) * head_dim * kBlockSize * elem;
+    if (block_bytes % 16 != 0 || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(pairs, 4) || (status && !aligned(status, 4)))
+        return PKV_ERR_INVALID_ARG;
+    return launch_copy_blocks(k_cache, v_cache, block_bytes, pairs, num_pairs, num_blocks, status,
+                              static_cast<cudaStream_t>(stream));
+}
+
 pkv_status pkv_read_status(void *workspace, int clear, int32_t *host_status, void *stream)
 {
     if (!workspace || !host_status)
@@ -527,6 +550,8 @@ const char *pkv_status_string(pkv_status status)
         return "PKV_ERR_TIMEOUT: a bounded device wait gave up";
     case PKV_ERR_WORKSPACE:
         return "PKV_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case PKV_ERR_NO_BLOCKS:
+        return "PKV_ERR_NO_BLOCKS: the block pool (or host memory) is exhausted";
     default:
         return "PKV_ERR_?: unknown status";
     }

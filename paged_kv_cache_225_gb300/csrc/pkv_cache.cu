@@ -52,4 +52,64 @@ pkv_status launch_reshape_and_cache(const void *k, const void *v, int in_dtype,
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// Copy-on-write page copies ("Inference optimization" lesson, section
+// "PagedAttention": a request that diverges from a shared prompt gets its own
+// copy of the shared page).  pairs[i] = (src, dst) block ids; the whole block
+// of K and of V (every KV head's [D x 16] tile, `block_bytes` each) is copied
+// with 16-byte loads and stores.  Flattened grid: (pair, cache, chunk).
+constexpr int kCopyThreads = 256;
+constexpr int kCopyVecPerThread = 4;
+
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_blocks_kernel(unsigned char *k_cache, unsigned char *v_cache, size_t block_bytes,
+                       const int32_t *pairs, int num_blocks, int chunks, int32_t *status)
+{
+    const int chunk = blockIdx.x % chunks;
+    const int which = (blockIdx.x / chunks) & 1;
+    const int i = blockIdx.x / (2 * chunks);
+    const int32_t src = __ldg(pairs + 2 * i), dst = __ldg(pairs + 2 * i + 1);
+    if (src < 0 || dst < 0 || src >= num_blocks || dst >= num_blocks) {
+        if (threadIdx.x == 0 && chunk == 0 && which == 0)
+            set_status(status, PKV_ERR_OUT_OF_RANGE);
+        return;
+    }
+    unsigned char *base = which ? v_cache : k_cache;
+    const uint4 *s = reinterpret_cast<const uint4 *>(base + static_cast<size_t>(src) * block_bytes);
+    uint4 *d = reinterpret_cast<uint4 *>(base + static_cast<size_t>(dst) * block_bytes);
+    const size_t n16 = block_bytes / 16;
+    const size_t per_chunk = static_cast<size_t>(kCopyThreads) * kCopyVecPerThread;
+    const size_t lo = static_cast<size_t>(chunk) * per_chunk;
+    uint4 v[kCopyVecPerThread];
+#pragma unroll
+    for (int j = 0; j < kCopyVecPerThread; ++j) {
+        const size_t e = lo + static_cast<size_t>(j) * kCopyThreads + threadIdx.x;
+        if (e < n16)
+            v[j] = __ldcs(s + e);
+    }
+#pragma unroll
+    for (int j = 0; j < kCopyVecPerThread; ++j) {
+        const size_t e = lo + static_cast<size_t>(j) * kCopyThreads + threadIdx.x;
+        if (e < n16)
+            d[e] = v[j];
+    }
+}
+
+pkv_status launch_copy_blocks(void *k_cache, void *v_cache, size_t block_bytes,
+                              const int32_t *pairs, int num_pairs, int num_blocks,
+                              int32_t *status, cudaStream_t stream)
+{
+    if (num_pairs <= 0)
+        return PKV_OK;
+    const size_t per_chunk = static_cast<size_t>(kCopyThreads) * kCopyVecPerThread;
+    const size_t n16 = block_bytes / 16;
+    const long chunks = static_cast<long>((n16 + per_chunk - 1) / per_chunk);
+    const long grid = static_cast<long>(num_pairs) * 2 * chunks;
+    if (grid > 0x7fffffffL)
+        return PKV_ERR_INVALID_ARG;
+    copy_blocks_kernel<<<static_cast<unsigned>(grid), kCopyThreads, 0, stream>>>(
+        static_cast<unsigned char *>(k_cache), static_cast<unsigned char *>(v_cache),
+        block_bytes, pairs, num_blocks, static_cast<int>(chunks), status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 }  // namespace pkv

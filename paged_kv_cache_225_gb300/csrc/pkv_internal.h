@@ -92,6 +92,10 @@ pkv_status launch_reshape_and_cache(const void *k, const void *v, int in_dtype,
                                     void *k_cache, void *v_cache, int kv_dtype, float k_scale,
                                     float v_scale, int32_t *status, cudaStream_t stream);
 
+pkv_status launch_copy_blocks(void *k_cache, void *v_cache, size_t block_bytes,
+                              const int32_t *pairs, int num_pairs, int num_blocks,
+                              int32_t *status, cudaStream_t stream);
+
 int device_sm_count();
 
 }  // namespace pkv

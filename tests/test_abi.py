@@ -42,7 +42,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_status_strings_and_version():
     L = pkv.lib()
-    for code in range(7):
+    for code in range(8):
         assert L.pkv_status_string(code).decode().startswith(pkv.STATUS[code])
     assert L.pkv_version() >= 100
 
@@ -227,3 +227,27 @@ def _prefill(**kw):
 ])
 def test_prefill_argument_errors(kw, code):
     assert _prefill(**kw) == code
+
+
+def _copy(**kw):
+    args = dict(k=0x1000, v=0x2000, kv_dtype=BF16, Hkv=8, D=128, B=16, N=10, pairs=0x3000, n=4,
+                status=None)
+    args.update(kw)
+    return pkv.lib().pkv_copy_blocks(args["k"], args["v"], args["kv_dtype"], args["Hkv"], args["D"],
+                                     args["B"], args["N"], args["pairs"], args["n"], args["status"],
+                                     None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=32), UNSUPPORTED),
+    (dict(kv_dtype=9), UNSUPPORTED),
+    (dict(Hkv=0), INVALID),
+    (dict(N=0), INVALID),
+    (dict(n=-1), INVALID),
+    (dict(pairs=0), INVALID),
+    (dict(pairs=0x3002), INVALID),
+    (dict(k=0x1008), INVALID),
+    (dict(n=0), OK),
+])
+def test_copy_blocks_argument_errors(kw, code):
+    assert _copy(**kw) == code
