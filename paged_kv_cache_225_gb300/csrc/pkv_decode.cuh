@@ -704,11 +704,12 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
 
 // ==================================================================== kernel
 
-// Fused cache write: before the bulk copy of the page that holds a
-// sequence's new token (position L - 1) is issued, the warp that will issue it
-// writes the converted K/V row of KV head hkv into the cache slot (block
-// `phys`) and fences those generic writes against the copy engine's reads,
-// so the ordinary page copy brings the new token in with the rest.
+// Fused cache write.  The new token of a sequence is its position L - 1; its
+// converted K/V rows are written into the cache slot and fenced against the
+// copy engine's reads before the bulk copy of that page is issued, so the
+// ordinary page copy brings the new token in with the rest.  The item
+// kernel stages the rows at item start and writes them on the issue path of
+// the page; the stream-K kernel writes all tokens of its range at start.
 // Bytes of one warp's staging buffer for the new K and V rows (head_dim up
 // to 128 elements of up to 4 bytes each, K then V).
 constexpr int kNewRowBytes = 2 * 128 * 4;
@@ -731,8 +732,9 @@ __device__ __forceinline__ void prefetch_new_rows(const DecodeParams &p, int s, 
     cp_async_commit();
 }
 
-// write_new_token with the rows already staged in shared memory by
-// prefetch_new_rows.
+// Writes the new token of (s, hkv) from the rows prefetch_new_rows staged in
+// shared memory into slot (L - 1) % 16 of block phys, then fences the writes
+// against the bulk copy of that page that follows.
 __device__ __forceinline__ void write_new_token_from(const DecodeParams &p, int hkv, int L,
                                                      int phys, int D, const unsigned char *buf,
                                                      int lane)
@@ -753,21 +755,52 @@ __device__ __forceinline__ void write_new_token_from(const DecodeParams &p, int 
     __syncwarp();
 }
 
-__device__ __forceinline__ void write_new_token(const DecodeParams &p, int s, int hkv, int L,
-                                                int phys, int D, int lane)
+// The converted K/V rows of the listed new tokens stored into their slots,
+// without a fence (the caller fences before the copies it orders).  Entry e
+// of `w` is (s, hkv, L, phys): rows new_k/new_v[s, hkv] go to slot
+// (L - 1) % 16 of block phys.  Each lane handles head_dim elements
+// lane + 32j; all loads of a pair of entries are issued before their stores.
+__device__ __forceinline__ void write_token_rows(const DecodeParams &p, const int (*w)[4], int e0,
+                                                 int n, int step, int D, int lane)
 {
-    const int t = (L - 1) % kBlockSize;
-    const size_t src0 = (static_cast<size_t>(s) * p.num_kv_heads + hkv) * D;
-    const size_t dst0 = (static_cast<size_t>(phys) * p.num_kv_heads + hkv) * D;
+    constexpr int kJ = 4;  // head_dim <= 128
     void *kc = const_cast<void *>(p.k_cache);
     void *vc = const_cast<void *>(p.v_cache);
-    for (int d = lane; d < D; d += 32) {
-        const size_t g = (dst0 + d) * kBlockSize + t;
-        store_kv(kc, p.kv_dtype, g, p.new_k, p.new_dtype, src0 + d, p.k_scale);
-        store_kv(vc, p.kv_dtype, g, p.new_v, p.new_dtype, src0 + d, p.v_scale);
+    for (int e = e0; e < n; e += 2 * step) {
+        float kv[2][kJ], vv[2][kJ];
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            const int ee = e + x * step;
+            if (ee >= n)
+                break;
+            const size_t src0 = (static_cast<size_t>(w[ee][0]) * p.num_kv_heads + w[ee][1]) * D;
+#pragma unroll
+            for (int j = 0; j < kJ; ++j) {
+                const int d = lane + 32 * j;
+                if (d < D) {
+                    kv[x][j] = load_in(p.new_k, p.new_dtype, src0 + d);
+                    vv[x][j] = load_in(p.new_v, p.new_dtype, src0 + d);
+                }
+            }
+        }
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            const int ee = e + x * step;
+            if (ee >= n)
+                break;
+            const int t = (w[ee][2] - 1) % kBlockSize;
+            const size_t dst0 = (static_cast<size_t>(w[ee][3]) * p.num_kv_heads + w[ee][1]) * D;
+#pragma unroll
+            for (int j = 0; j < kJ; ++j) {
+                const int d = lane + 32 * j;
+                if (d < D) {
+                    const size_t g = (dst0 + d) * kBlockSize + t;
+                    store_kv_value(kc, p.kv_dtype, g, kv[x][j], p.k_scale);
+                    store_kv_value(vc, p.kv_dtype, g, vv[x][j], p.v_scale);
+                }
+            }
+        }
     }
-    fence_proxy_async_all();
-    __syncwarp();
 }
 
 

@@ -43,6 +43,9 @@ __device__ __forceinline__ long long block_sum(long long v, long long *red)
     return t;
 }
 
+// New tokens listed per round of the fused cache write.
+constexpr int kWriteBatch = 16;
+
 // A unit of the flattened page space and its global page offset.
 struct Unit {
     int s, hkv, L, np;
@@ -169,6 +172,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
     __shared__ long long s_start_off;
     __shared__ int s_abort;
     __shared__ int s_last;
+    __shared__ int s_w[kWriteBatch][4];  // fused write list: s, hkv, L, physical page
+    __shared__ int s_wn, s_wmore;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -318,20 +323,44 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
             issue_next();
     };
 
-    // Fused cache write: every new token whose page this warp will copy is
-    // written now, before the first copy and while HBM is still idle (a
-    // write on the issue path would wait behind the saturated queue).
+    // Fused cache write: the new tokens of the units whose last page lies in
+    // this CTA's range are written before any page copy is issued, while HBM
+    // is still idle.  Lane 0 of warp 0 lists them (with their physical page,
+    // kWriteBatch at a time); all four warps then write the rows and fence
+    // them against the copies the barrier releases.  (Writing them per warp,
+    // where the page is copied, serialised several dependent loads of the
+    // same warp under full memory load: about 7 us per token.)
     if (p.new_k) {
         Unit wu = start;
-        while (wu.off < b) {
-            const long long g_last = wu.off + wu.np - 1;
-            if (wu.L > 0 && g_last >= a && g_last < b && ((g_last - a) & 3) == warp) {
-                const int phys = __ldg(p.block_tables +
-                                       static_cast<size_t>(wu.s) * p.max_blocks + wu.np - 1);
-                if (phys >= 0 && phys < p.num_blocks)
-                    write_new_token(p, wu.s, wu.hkv, wu.L, phys, D, lane);
+        for (;;) {
+            if (threadIdx.x == 0) {
+                int n = 0;
+                while (wu.off < b && n < kWriteBatch) {
+                    const long long g_last = wu.off + wu.np - 1;
+                    if (wu.L > 0 && g_last >= a) {
+                        const int phys = __ldg(p.block_tables +
+                                               static_cast<size_t>(wu.s) * p.max_blocks + wu.np - 1);
+                        if (g_last < b && phys >= 0 && phys < p.num_blocks) {
+                            s_w[n][0] = wu.s;
+                            s_w[n][1] = wu.hkv;
+                            s_w[n][2] = wu.L;
+                            s_w[n][3] = phys;
+                            ++n;
+                        }
+                    }
+                    unit_next(p, wu);
+                }
+                s_wn = n;
+                s_wmore = (wu.off < b) ? 1 : 0;
             }
-            unit_next(p, wu);
+            __syncthreads();
+            const int n = s_wn;
+            write_token_rows(p, s_w, warp, n, kWarps, D, lane);
+            fence_proxy_async_all();
+            const int more = s_wmore;
+            __syncthreads();  // the list is reused; every write is fenced
+            if (!more)
+                break;
         }
     }
     refill();
