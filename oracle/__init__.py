@@ -26,7 +26,7 @@ _LIB_PATH = os.path.join(_BUILD, "libpkv_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, BF16, FP8_E5M2 = 0, 1, 2
+F32, BF16, FP8_E5M2, FP8_E4M3 = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -96,7 +96,8 @@ def decode_values(bits: np.ndarray, dtype: int) -> np.ndarray:
 def encode_values(x: np.ndarray, dtype: int, scale: float = 1.0) -> np.ndarray:
     """Encode float32 values to a stored dtype with the oracle's own encoders."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    storage = {F32: np.float32, BF16: np.uint16, FP8_E5M2: np.uint8}[dtype]
+    storage = {F32: np.float32, BF16: np.uint16, FP8_E5M2: np.uint8,
+               FP8_E4M3: np.uint8}[dtype]
     out = np.empty(x.shape, dtype=storage)
     rc = _load().pkvo_encode_values(_ptr(x, ctypes.c_float), x.size, dtype, scale, _ptr(out))
     if rc:

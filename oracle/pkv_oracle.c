@@ -10,7 +10,10 @@
  *  - Decoding of stored elements, written from the bit formats: IEEE float32;
  *    bf16 (the upper 16 bits of a float32); fp8-e5m2 (1 sign bit, 5 exponent
  *    bits with bias 15, 2 mantissa bits; exponent 0 is subnormal, 31 is
- *    Inf/NaN).  fp8 values are multiplied by the per-tensor dequant scale.
+ *    Inf/NaN); fp8-e4m3 (1 sign bit, 4 exponent bits with bias 7, 3 mantissa
+ *    bits; exponent 0 is subnormal, no infinities, the all-ones code is NaN,
+ *    largest magnitude 448).  fp8 values are multiplied by the per-tensor
+ *    dequant scale.
  *
  *  - Paged decode attention ("vLLM e PagedAttention: serving high-throughput",
  *    the simplified PagedAttention CUDA-kernel pseudocode; "Inference
@@ -42,7 +45,8 @@
  *    new row i with slot = slot_mapping[i] >= 0 lands in block slot / B at
  *    offset slot % B of every KV head.  Values are converted with this file's
  *    own encoders: float32 -> bf16 round-to-nearest-even; float32 ->
- *    fp8-e5m2 as RNE(x / scale) in float32 with saturation to +-57344.
+ *    fp8-e5m2 as RNE(x / scale) in float32 with saturation to +-57344;
+ *    float32 -> fp8-e4m3 the same with saturation to +-448.
  */
 #include <math.h>
 #include <stddef.h>
@@ -53,7 +57,7 @@
 #include <omp.h>
 #endif
 
-enum { PKVO_F32 = 0, PKVO_BF16 = 1, PKVO_FP8_E5M2 = 2 };
+enum { PKVO_F32 = 0, PKVO_BF16 = 1, PKVO_FP8_E5M2 = 2, PKVO_FP8_E4M3 = 3 };
 
 /* ------------------------------------------------------------------ decoders */
 
@@ -86,6 +90,25 @@ static double e5m2_value(uint8_t code)
     return sign ? -mag : mag;
 }
 
+/* fp8-e4m3 ("fn": finite, no infinities): 1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits.  Exponent 0 is subnormal (m/8 * 2^-6); the one
+ * code with every exponent and mantissa bit set is NaN; the largest finite
+ * magnitude is 1.75 * 2^8 = 448. */
+static double e4m3_value(uint8_t code)
+{
+    int sign = (code >> 7) & 1;
+    int expo = (code >> 3) & 0xf;
+    int mant = code & 0x7;
+    double mag;
+    if (expo == 0xf && mant == 0x7)
+        return NAN;
+    if (expo == 0)
+        mag = ldexp((double)mant / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)mant / 8.0, expo - 7);
+    return sign ? -mag : mag;
+}
+
 static double elem_value(const void *base, int dtype, size_t i)
 {
     switch (dtype) {
@@ -101,6 +124,8 @@ static double elem_value(const void *base, int dtype, size_t i)
     }
     case PKVO_FP8_E5M2:
         return e5m2_value(((const uint8_t *)base)[i]);
+    case PKVO_FP8_E4M3:
+        return e4m3_value(((const uint8_t *)base)[i]);
     default:
         return NAN;
     }
@@ -165,6 +190,37 @@ static uint8_t e5m2_encode_rne_satfinite(float x)
     return sign | (uint8_t)(((e + 15) << 2) | ((int)n - 4));
 }
 
+/* Round to the nearest e4m3 value, ties to even; magnitudes beyond 448
+ * (infinities included) saturate to +-448; NaN gives the NaN code. */
+static uint8_t e4m3_encode_rne_satfinite(float x)
+{
+    if (isnan(x))
+        return 0x7f;
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (isinf(a) || a >= 448.0)
+        return sign | 0x7e;
+    if (a < ldexp(1.0, -6)) {
+        /* Subnormal range: multiples of 2^-9. */
+        double n = round_half_even(a * 512.0);
+        if (n >= 8.0)
+            return sign | 0x08;                     /* rounds up to 2^-6 */
+        return sign | (uint8_t)n;
+    }
+    int k;
+    frexp(a, &k);
+    int e = k - 1;           /* a in [2^e, 2^(e+1)) */
+    double ulp = ldexp(1.0, e - 3);
+    double n = round_half_even(a / ulp);   /* in [8, 16] */
+    if (n >= 16.0) {
+        n = 8.0;
+        e += 1;
+    }
+    if (e > 8 || (e == 8 && n > 14.0))
+        return sign | 0x7e;                         /* saturate at 448 */
+    return sign | (uint8_t)(((e + 7) << 3) | ((int)n - 8));
+}
+
 /* ------------------------------------------------------- exported decoders */
 
 /* Widen n stored elements of `dtype` to double (no scale applied). */
@@ -192,6 +248,11 @@ int pkvo_encode_values(const float *src, size_t n, int dtype, float scale, void 
         case PKVO_FP8_E5M2: {
             float xs = x / scale;
             ((uint8_t *)dst)[i] = e5m2_encode_rne_satfinite(xs);
+            break;
+        }
+        case PKVO_FP8_E4M3: {
+            float xs = x / scale;
+            ((uint8_t *)dst)[i] = e4m3_encode_rne_satfinite(xs);
             break;
         }
         default:
@@ -227,8 +288,9 @@ static size_t cache_index(const pkvo_problem *P, int32_t blk, int hkv, int d, in
 static int gather_rows(const pkvo_problem *P, int s, int hkv, int L, double *K, double *V)
 {
     const int D = P->head_dim, B = P->block_size;
-    double ks = (P->kv_dtype == PKVO_FP8_E5M2) ? P->k_scale : 1.0;
-    double vs = (P->kv_dtype == PKVO_FP8_E5M2) ? P->v_scale : 1.0;
+    const int fp8 = P->kv_dtype == PKVO_FP8_E5M2 || P->kv_dtype == PKVO_FP8_E4M3;
+    double ks = fp8 ? P->k_scale : 1.0;
+    double vs = fp8 ? P->v_scale : 1.0;
     for (int t = 0; t < L; ++t) {
         int32_t blk = P->block_tables[(size_t)s * P->max_blocks_per_seq + t / B];
         if (blk < 0 || blk >= P->num_blocks)
@@ -522,7 +584,8 @@ int pkvo_reshape_and_cache(const void *k, const void *v, int in_dtype,
 {
     if (in_dtype != PKVO_F32 && in_dtype != PKVO_BF16)
         return 5;
-    if (kv_dtype != PKVO_F32 && kv_dtype != PKVO_BF16 && kv_dtype != PKVO_FP8_E5M2)
+    if (kv_dtype != PKVO_F32 && kv_dtype != PKVO_BF16 && kv_dtype != PKVO_FP8_E5M2 &&
+        kv_dtype != PKVO_FP8_E4M3)
         return 5;
     int rc = 0;
     for (int i = 0; i < num_tokens; ++i) {
@@ -549,9 +612,12 @@ int pkvo_reshape_and_cache(const void *k, const void *v, int in_dtype,
                     uint16_t kb = bf16_encode_rne(kx), vb = bf16_encode_rne(vx);
                     memcpy((uint8_t *)k_cache + 2 * dst, &kb, 2);
                     memcpy((uint8_t *)v_cache + 2 * dst, &vb, 2);
-                } else {
+                } else if (kv_dtype == PKVO_FP8_E5M2) {
                     ((uint8_t *)k_cache)[dst] = e5m2_encode_rne_satfinite(kx / k_scale);
                     ((uint8_t *)v_cache)[dst] = e5m2_encode_rne_satfinite(vx / v_scale);
+                } else {
+                    ((uint8_t *)k_cache)[dst] = e4m3_encode_rne_satfinite(kx / k_scale);
+                    ((uint8_t *)v_cache)[dst] = e4m3_encode_rne_satfinite(vx / v_scale);
                 }
             }
         }

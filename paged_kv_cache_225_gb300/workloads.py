@@ -30,10 +30,11 @@ from typing import Optional
 import numpy as np
 import torch
 
-F32, BF16, FP8_E5M2 = 0, 1, 2
-DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_E5M2: "fp8_e5m2"}
-ELEM_BYTES = {F32: 4, BF16: 2, FP8_E5M2: 1}
-NP_STORAGE = {F32: np.float32, BF16: np.uint16, FP8_E5M2: np.uint8}
+F32, BF16, FP8_E5M2, FP8_E4M3 = 0, 1, 2, 3
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_E5M2: "fp8_e5m2", FP8_E4M3: "fp8_e4m3"}
+ELEM_BYTES = {F32: 4, BF16: 2, FP8_E5M2: 1, FP8_E4M3: 1}
+NP_STORAGE = {F32: np.float32, BF16: np.uint16, FP8_E5M2: np.uint8, FP8_E4M3: np.uint8}
+FP8 = (FP8_E5M2, FP8_E4M3)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -123,7 +124,10 @@ def round_to_storage(x: np.ndarray, dtype: int) -> np.ndarray:
     if dtype == BF16:
         return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     if dtype == FP8_E5M2:
-        return t.to(torch.float8_e5m2).view(torch.uint8).numpy()
+        return t.clamp(-57344.0, 57344.0).to(torch.float8_e5m2).view(torch.uint8).numpy()
+    if dtype == FP8_E4M3:
+        # Clamp first: saturating to the largest finite value (448).
+        return t.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     raise ValueError(f"unknown dtype {dtype}")
 
 
@@ -136,6 +140,9 @@ def storage_to_float32(x: np.ndarray, dtype: int) -> np.ndarray:
         return t.float().numpy()
     if dtype == FP8_E5M2:
         t = torch.from_numpy(np.ascontiguousarray(x)).view(torch.float8_e5m2)
+        return t.float().numpy()
+    if dtype == FP8_E4M3:
+        t = torch.from_numpy(np.ascontiguousarray(x)).view(torch.float8_e4m3fn)
         return t.float().numpy()
     raise ValueError(f"unknown dtype {dtype}")
 
@@ -251,7 +258,7 @@ def make_workload(cfg: DecodeConfig | str, seed: Optional[int] = None,
                 owned[tables[s, j], :valid] = True
         k_pool[np.broadcast_to(~owned[:, None, None, :], k_pool.shape)] = np.nan
         v_pool[np.broadcast_to(~owned[:, None, None, :], v_pool.shape)] = np.nan
-    if cfg.kv_dtype == FP8_E5M2 and cfg.kv_scale != 1.0:
+    if cfg.kv_dtype in FP8 and cfg.kv_scale != 1.0:
         k_pool /= np.float32(cfg.kv_scale)
         v_pool /= np.float32(cfg.kv_scale)
     k_cache = _pool_to_storage(k_pool, cfg.kv_dtype)

@@ -17,7 +17,7 @@ import torch
 import oracle
 from paged_kv_cache_225_gb300 import workloads as W
 
-F32, BF16, FP8 = W.F32, W.BF16, W.FP8_E5M2
+F32, BF16, FP8, E4M3 = W.F32, W.BF16, W.FP8_E5M2, W.FP8_E4M3
 
 
 # ----------------------------------------------------------------- decoders
@@ -34,6 +34,25 @@ def test_e5m2_decode_all_codes_match_float16_high_byte_and_torch():
         assert np.array_equal(np.isnan(got), nan)
         assert np.array_equal(got[~nan], ref[~nan])
     assert got[0x7b] == 57344.0 and got[0x01] == 2.0 ** -16 and got[0x7c] == np.inf
+
+
+def test_e4m3_decode_all_codes_match_closed_form_and_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_values(codes, E4M3)
+    # From the format: sign | 4 exponent bits (bias 7) | 3 mantissa bits;
+    # exponent 0 is subnormal, the all-ones code is NaN, no infinities.
+    sign = np.where(codes >> 7, -1.0, 1.0)
+    e = (codes >> 3) & 15
+    m = (codes & 7).astype(np.float64)
+    closed = sign * np.where(e == 0, m / 8 * 2.0 ** -6, (1 + m / 8) * 2.0 ** (e.astype(float) - 7))
+    closed[(e == 15) & (m == 7)] = np.nan
+    via_torch = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    for ref in (closed, via_torch):
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(got), nan)
+        assert np.array_equal(got[~nan], ref[~nan])
+    assert got[0x7e] == 448.0 and got[0x01] == 2.0 ** -9 and np.isnan(got[0x7f])
+    assert np.isnan(got).sum() == 2
 
 
 def test_bf16_decode_matches_torch():
@@ -92,6 +111,37 @@ def test_e5m2_encode_matches_torch_rne_in_range_and_saturates():
     assert got[-3] == 0x7b and got[-2] == 0xfb and got[-1] == 0xfb
 
 
+def test_e4m3_encode_matches_torch_rne_in_range_and_saturates():
+    rng = np.random.default_rng(40)
+    finite = oracle.decode_values(np.arange(256, dtype=np.uint8), E4M3)
+    finite = np.unique(finite[np.isfinite(finite)])
+    mids = ((finite[1:] + finite[:-1]) / 2).astype(np.float32)       # exact ties
+    x = np.concatenate([
+        (rng.standard_normal(200_000) * 2.0 ** rng.integers(-12, 9, 200_000)).astype(np.float32),
+        mids, -mids, finite.astype(np.float32),
+        np.array([448.0, 460.0, 464.0, 470.0, 1e9, np.inf, -np.inf, -1000.0],
+                 dtype=np.float32)])
+    got = oracle.encode_values(x, E4M3)
+    ref = torch.from_numpy(np.clip(x, -448.0, 448.0)).to(torch.float8_e4m3fn)
+    assert np.array_equal(got, ref.view(torch.uint8).numpy())
+    assert got[-3] == 0x7e and got[-2] == 0xfe and got[-1] == 0xfe
+
+
+def test_e4m3_round_trip_and_scale():
+    codes = np.arange(256, dtype=np.uint8)
+    vals = oracle.decode_values(codes, E4M3)
+    finite = np.isfinite(vals)
+    back = oracle.encode_values(vals[finite].astype(np.float32), E4M3)
+    # +0 and -0 both come back; every finite code maps to itself.
+    assert np.array_equal(back, codes[finite])
+    x = np.random.default_rng(41).standard_normal(50_000).astype(np.float32) * 3
+    for scale in (2.0, 0.37):
+        got = oracle.encode_values(x, E4M3, scale=scale)
+        xs = (x / np.float32(scale)).astype(np.float32)
+        ref = torch.from_numpy(np.clip(xs, -448, 448)).to(torch.float8_e4m3fn)
+        assert np.array_equal(got, ref.view(torch.uint8).numpy())
+
+
 def test_e5m2_round_trip_of_every_finite_code():
     codes = np.arange(256, dtype=np.uint8)
     vals = oracle.decode_values(codes, FP8)
@@ -138,7 +188,7 @@ def _dense_kv(p):
     """Contiguous per-sequence K/V [Hkv, L, D] by numpy indexing, in float64."""
     k = W.storage_to_float32(p["k_cache"], p["kv_dtype"]).astype(np.float64)
     v = W.storage_to_float32(p["v_cache"], p["kv_dtype"]).astype(np.float64)
-    if p["kv_dtype"] == FP8:
+    if p["kv_dtype"] in (FP8, E4M3):
         k, v = k * p["k_scale"], v * p["v_scale"]
     out = []
     B = k.shape[3]
@@ -165,7 +215,8 @@ def _run(p, **kw):
 
 
 @pytest.mark.parametrize("kv_dtype,q_dtype,kv_scale",
-                         [(F32, F32, 1.0), (BF16, BF16, 1.0), (FP8, BF16, 1.0), (FP8, BF16, 0.5)])
+                         [(F32, F32, 1.0), (BF16, BF16, 1.0), (FP8, BF16, 1.0), (FP8, BF16, 0.5),
+                          (E4M3, BF16, 1.0), (E4M3, BF16, 0.25)])
 @pytest.mark.parametrize("identity", [True, False])
 def test_paged_equals_dense_sdpa(kv_dtype, q_dtype, kv_scale, identity):
     p = _tiny_problem(kv_dtype, q_dtype, identity=identity, kv_scale=kv_scale)
@@ -319,7 +370,8 @@ def test_decode_seqs_matches_full():
 
 @pytest.mark.parametrize("in_dtype,kv_dtype,scale", [(F32, F32, 1.0), (F32, BF16, 1.0),
                                                      (BF16, BF16, 1.0), (BF16, FP8, 1.0),
-                                                     (F32, FP8, 0.25)])
+                                                     (F32, FP8, 0.25), (BF16, E4M3, 1.0),
+                                                     (F32, E4M3, 0.5)])
 def test_reshape_and_cache_matches_numpy_scatter(in_dtype, kv_dtype, scale):
     rng = np.random.default_rng(21)
     N, Hkv, D, B, T = 9, 3, 16, 16, 7
@@ -339,9 +391,9 @@ def test_reshape_and_cache_matches_numpy_scatter(in_dtype, kv_dtype, scale):
         blk, off = divmod(int(slot), B)
         for src, dst in ((kin, ek), (vin, ev)):
             x = W.storage_to_float32(src[i], in_dtype)
-            if kv_dtype == FP8:
-                x = np.clip((x / np.float32(scale)).astype(np.float32), -57344, 57344)
-            dst[blk, :, :, off] = W.round_to_storage(x, kv_dtype)
+            if kv_dtype in (FP8, E4M3):
+                x = (x / np.float32(scale)).astype(np.float32)
+            dst[blk, :, :, off] = W.round_to_storage(x, kv_dtype)   # clamps fp8 to its range
     assert np.array_equal(kc.view(np.uint8), ek.view(np.uint8))
     assert np.array_equal(vc.view(np.uint8), ev.view(np.uint8))
 
