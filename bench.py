@@ -37,11 +37,11 @@ if ROOT not in sys.path:
 import numpy as np  # noqa: E402
 
 from paged_kv_cache_225_gb300 import workloads as W  # noqa: E402
-from paged_kv_cache_225_gb300.metrics import algorithmic_bytes  # noqa: E402
+from paged_kv_cache_225_gb300.metrics import algorithmic_bytes, prefill_algorithmic  # noqa: E402
 
 METRIC = "decode-attn KV GB/s & tokens/s on 1 GB300, % of HBM peak (70B-shape layer)"
 FALLBACK_HBM_GBS = 6800.0
-DTYPE_NAME = {W.F32: "f32", W.BF16: "bf16", W.FP8_E5M2: "fp8_e5m2"}
+DTYPE_NAME = {W.F32: "f32", W.BF16: "bf16", W.FP8_E5M2: "fp8_e5m2", W.FP8_E4M3: "fp8_e4m3"}
 CONFIG_TEXT = {
     "tiny_fp32": "tiny fp32 decode: 4 seqs, 4 q/4 kv heads, D=64, lengths U[1,64]",
     "llama3_8b": "Llama-3-8B-shaped decode layer: 64 seqs, 32 q/8 kv heads, D=128, bf16 KV, "
@@ -51,6 +51,19 @@ CONFIG_TEXT = {
     "long_split": "long-context split-KV: 8 seqs x 32768 tokens, 64 q/8 kv heads, D=128, bf16 KV",
     "fp8_chat": "fp8-e5m2 KV chat mix: 128 seqs, 64 q/8 kv heads, D=128, lengths U[256,512], "
                 "8-block shared prefixes",
+    "e4m3_70b": "Llama-3-70B-shaped decode layer with an fp8-e4m3 KV cache (per-tensor scale "
+                "1/8): 128 seqs, 64 q/8 kv heads, D=128, lognormal lengths (median 2048)",
+    "prefill_tiny": "several causal queries per sequence, tiny mix: 7 seqs, 8 q/2 kv heads, "
+                    "D=64, bf16 KV",
+    "spec_verify_70b": "speculative verification on the Llama-3-70B-shaped layer: 128 seqs x 5 "
+                       "causal queries, 64 q/8 kv heads, D=128, bf16 KV, lognormal lengths "
+                       "(median 2048, sigma 0.8)",
+    "cow_copy_70b": "copy-on-write page copies on the Llama-3-70B-shaped pool: 2048 (src, dst) "
+                    "block pairs, 8 kv heads x 128 x 16 bf16 per block and cache; plus the host "
+                    "block manager's append of 128 forked sequences",
+    "chunked_prefill_8b": "chunked prefill on the Llama-3-8B-shaped layer: 4 seqs with a "
+                          "256-token prompt chunk (context U[1024,4096]) + 60 decoding seqs "
+                          "(U[512,4096]), 32 q/8 kv heads, D=128, bf16 KV",
 }
 
 
@@ -60,7 +73,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="llama3_70b", choices=W.CONFIG_ORDER)
+    ap.add_argument("--config", default="llama3_70b",
+                    choices=W.CONFIG_ORDER + list(W.PREFILL_CONFIGS) + ["cow_copy_70b"])
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "mma"])
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
@@ -74,7 +88,7 @@ def parse_args(argv=None):
 
 
 # Sources that do not define or launch the decode kernels.
-_NOT_DECODE = {"pkv_cache.cu", "pkv_noalloc.cu"}
+_NOT_DECODE = {"pkv_cache.cu", "pkv_noalloc.cu", "pkv_prefill.cu"}
 
 
 def source_hash() -> str:
@@ -223,6 +237,8 @@ def run_ours(args):
             return torch.from_numpy(a)
         if dt == W.BF16:
             return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        if dt == W.FP8_E4M3:
+            return torch.from_numpy(a).view(torch.float8_e4m3fn)
         return torch.from_numpy(a).view(torch.float8_e5m2)
 
     host = {
@@ -513,12 +529,428 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------- several queries per sequence
+
+def _query_rows(w):
+    """Slots of every query token and the K/V rows the pool holds there."""
+    base = w.cfg.base
+    B = base.block_size
+    slots, ks, vs = [], [], []
+    for s in range(w.seq_lens.size):
+        L = int(w.seq_lens[s])
+        n = int(w.q_start[s + 1] - w.q_start[s])
+        for pos in range(L - n, L):
+            blk = int(w.block_tables[s, pos // B])
+            slots.append(blk * B + pos % B)
+            ks.append(w.k_cache[blk, :, :, pos % B])
+            vs.append(w.v_cache[blk, :, :, pos % B])
+    return (np.asarray(slots, dtype=np.int64), np.ascontiguousarray(np.stack(ks)),
+            np.ascontiguousarray(np.stack(vs)))
+
+
+def run_prefill(args):
+    """One step = the cache write of every query token's K/V, then causal paged
+    attention of all queries (chunked prefill / speculative verification)."""
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_225_gb300 as pkv
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    w = W.make_prefill_workload(args.config)
+    base = w.cfg.base
+    S, Hq, Hkv, D = base.num_seqs, base.num_q_heads, base.num_kv_heads, base.head_dim
+    T, max_q, max_len = w.num_tokens, w.max_q_len, int(w.seq_lens.max())
+    ab = prefill_algorithmic(w)
+    slots, new_k, new_v = _query_rows(w)
+    write_bytes = T * Hkv * D * 2 * (2 + W.ELEM_BYTES[base.kv_dtype])
+
+    def t(a, dt):
+        a = np.ascontiguousarray(a)
+        if dt == W.BF16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(a)
+
+    host = {"q": t(w.q, base.q_dtype), "q_start": torch.from_numpy(w.q_start),
+            "tables": torch.from_numpy(w.block_tables), "lens": torch.from_numpy(w.seq_lens),
+            "new_k": t(new_k, base.kv_dtype), "new_v": t(new_v, base.kv_dtype),
+            "slots": torch.from_numpy(slots)}
+    kc = t(w.k_cache, base.kv_dtype).to(dev)
+    vc = t(w.v_cache, base.kv_dtype).to(dev)
+    d = {k: v.to(dev) for k, v in host.items()}
+    out = torch.empty((T, Hq, D), dtype=torch.float32, device=dev)
+    part = pkv.prefill_partition_tokens(S, T, Hq, Hkv, D, max_q, max_len, args.partition)
+    ws = torch.empty(pkv.prefill_workspace_size(S, T, Hq, Hkv, D, max_q, max_len,
+                                                args.partition), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def attend(dd):
+        pkv.paged_attn_prefill(dd["q"], dd["q_start"], kc, vc, dd["tables"], dd["lens"],
+                               w.scale, out, max_q_len=max_q, max_seq_len=max_len,
+                               partition_tokens=args.partition, workspace=ws)
+
+    def step(dd):
+        pkv.reshape_and_cache(dd["new_k"], dd["new_v"], dd["slots"], kc, vc)
+        attend(dd)
+
+    for _ in range(max(args.warmup, 3)):
+        step(d)
+    torch.cuda.synchronize()
+    status = pkv.read_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {pkv.STATUS.get(status, status)} during warm-up")
+    K = args.steps
+    graph_stream = torch.cuda.Stream(dev)
+    graph_stream.wait_stream(stream)
+    g_step, g_call = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=graph_stream):
+        step(d)
+    with torch.cuda.graph(g_call, stream=graph_stream):
+        attend(d)
+    stream.wait_stream(graph_stream)
+    for _ in range(3):
+        g_step.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    if world > 1:
+        dist.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(K):
+        g_step.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1))
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    c0.record(stream)
+    for _ in range(K):
+        g_call.replay()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    call_ms = c0.elapsed_time(c1) / K
+    status = pkv.read_status(ws)
+    if status != 0:
+        raise RuntimeError(f"device status {pkv.STATUS.get(status, status)} in the timed run")
+
+    e2e = None
+    if not args.no_e2e:
+        pinned = {k: v.pin_memory() for k, v in host.items()}
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+        d2h = out_host.numel() * out_host.element_size()
+        Ke = max(1, min(K, 200))
+        for _ in range(3):
+            for k, v in pinned.items():
+                d[k].copy_(v, non_blocking=True)
+            step(d)
+            out_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            for k, v in pinned.items():
+                d[k].copy_(v, non_blocking=True)
+            step(d)
+            out_host.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / Ke
+        e2e = {"value": ab["kv"] * world / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_ms, "steps": Ke}
+
+    ms_step = elapsed_ms / K
+    peak, peak_kind = hbm_peak()
+    achieved = ab["total"] / (call_ms * 1e-3) / 1e9
+    tflops = ab["flops"] / (call_ms * 1e-3) / 1e12
+    bf16_peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            bf16_peak = float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        bf16_peak = 1900.0
+    launches = 2 + (1 if part > 0 and max_len > part else 0)
+    line = {
+        "metric": METRIC, "value": whole_job_rate(ab["kv"], world, ms_step * 1e-3) / 1e9,
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE_NAME[base.kv_dtype],
+        "data": "synthetic: seeded N(0,1) q/K/V, shuffled physical blocks (no dataset)",
+        "config": {"workload": workload_text(args.config), "name": args.config,
+                   "num_seqs": S, "num_queries": T, "num_q_heads": Hq, "num_kv_heads": Hkv,
+                   "head_dim": D, "block_size": base.block_size, "tokens": ab["tokens"],
+                   "kv_bytes_per_step": ab["kv"], "flops_per_step": ab["flops"],
+                   "partition": part,
+                   "l2": "no flush: KV read per step exceeds L2 (129 MB)",
+                   "step": "reshape_and_cache of every query token, then causal paged "
+                           "attention of all queries",
+                   "launch": "step captured once as a CUDA graph, replayed per step"},
+        "queries_per_s": whole_job_rate(T, world, ms_step * 1e-3),
+        "pct_hbm_peak": 100.0 * ab["total"] / (ms_step * 1e-3) / 1e9 / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": f"paged_attn_prefill call (mean of {K} CUDA-graph replays, "
+                               "CUDA events on the launch stream)",
+                     "algorithmic_bytes_per_launch": ab["total"],
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "tensor": {"achieved_tflops": tflops, "bf16_peak_tflops": bf16_peak,
+                                "frac": tflops / bf16_peak,
+                                "note": "mma.sync m16n8k16; P.V issued twice (bf16 high "
+                                        "part + residual)"}},
+        "gpu_launches": K * launches,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(w, budget_s=10.0)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _oracle_prefill_seqs(w, seqs, threads):
+    """The oracle's several-queries attention for the listed sequences only."""
+    import oracle
+    base = w.cfg.base
+    idx = list(seqs)
+    lens = w.seq_lens[idx]
+    qs = [w.q[w.q_start[s]:w.q_start[s + 1]] for s in idx]
+    q_start = np.zeros(len(idx) + 1, dtype=np.int32)
+    q_start[1:] = np.cumsum([x.shape[0] for x in qs])
+    return oracle.paged_prefill(np.ascontiguousarray(np.concatenate(qs)), base.q_dtype,
+                                q_start, w.k_cache, w.v_cache, base.kv_dtype,
+                                np.ascontiguousarray(w.block_tables[idx]), lens, w.scale,
+                                num_threads=threads)
+
+
+def prefill_cpu_baseline(w, budget_s=10.0):
+    import oracle
+    threads = oracle.max_threads()
+    base = w.cfg.base
+    row = base.num_kv_heads * 2 * base.head_dim * W.ELEM_BYTES[base.kv_dtype]
+    order = np.random.default_rng(1234).permutation(w.seq_lens.size)
+    done, kv, t_total = 0, 0, 0.0
+    t_start = time.perf_counter()
+    while t_total < budget_s and time.perf_counter() - t_start < 3 * budget_s:
+        for s in order:
+            t0 = time.perf_counter()
+            _oracle_prefill_seqs(w, [int(s)], threads)
+            t_total += time.perf_counter() - t0
+            done += 1
+            kv += int(w.seq_lens[s]) * row
+            if t_total >= budget_s:
+                break
+    return {"value": kv / t_total / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{done} sequences of this workload (random order, {kv / 1e9:.2f} GB of "
+                      f"KV) in {t_total:.1f} s, fp64 C oracle with OpenMP over (seq, kv head)"}
+
+
+def run_reference_prefill(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    w = W.make_prefill_workload(args.config)
+    base = w.cfg.base
+    threads = oracle.max_threads()
+    row = base.num_kv_heads * 2 * base.head_dim * W.ELEM_BYTES[base.kv_dtype]
+    S = w.seq_lens.size
+    order = np.random.default_rng(99).permutation(S)
+    t0 = time.perf_counter()
+    _oracle_prefill_seqs(w, [int(order[0])], threads)
+    per_seq = max(time.perf_counter() - t0, 1e-4)
+    total_steps = args.steps + max(args.warmup, 0)
+    n_seq = int(max(1, min(S, (120.0 / max(total_steps, 1)) / per_seq)))
+    cursor = 0
+
+    def one_step():
+        nonlocal cursor
+        seqs = [int(order[(cursor + i) % S]) for i in range(n_seq)]
+        cursor += n_seq
+        _oracle_prefill_seqs(w, seqs, threads)
+        return sum(int(w.seq_lens[s]) for s in seqs)
+
+    for _ in range(args.warmup):
+        one_step()
+    tok = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        tok += one_step()
+    el = time.perf_counter() - t0
+    value = tok * row / el / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded N(0,1) q/K/V, shuffled physical blocks",
+        "config": {"workload": workload_text(args.config), "name": args.config,
+                   "sample_seqs_per_step": n_seq},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_seq} of {S} sequences per step, fp64 C oracle"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------- copy-on-write copies
+
+def run_copy(args):
+    """One step = pkv_copy_blocks of 2048 disjoint page pairs on the 70B-shaped
+    pool (both caches); the host block manager's per-step append is timed
+    alongside (128 sequences forked from one prompt)."""
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_225_gb300 as pkv
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    N, Hkv, D, npairs = 8192, 8, 128, 2048
+    block_bytes = Hkv * D * 16 * 2
+    rng = np.random.default_rng(2024)
+    ids = rng.permutation(N)[:2 * npairs].astype(np.int32)
+    pairs_h = torch.from_numpy(ids.reshape(npairs, 2).copy())
+    kc = torch.randn((N, Hkv, D, 16), device=dev).to(torch.bfloat16)
+    vc = torch.randn((N, Hkv, D, 16), device=dev).to(torch.bfloat16)
+    pairs = pairs_h.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(args.warmup, 3)):
+        pkv.copy_blocks(kc, vc, pairs, status=status)
+    torch.cuda.synchronize()
+    K = args.steps
+    gs = torch.cuda.Stream(dev)
+    gs.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=gs):
+        pkv.copy_blocks(kc, vc, pairs, status=status)
+    stream.wait_stream(gs)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    if world > 1:
+        dist.barrier()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(K):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = max_over_ranks(t0.elapsed_time(t1)) / K
+    if int(status.item()) != 0:
+        raise RuntimeError("copy_blocks reported a bad pair")
+    moved = npairs * 2 * block_bytes * 2          # read + write, K and V
+    peak, peak_kind = hbm_peak()
+    achieved = moved / (ms * 1e-3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        pinned = pairs_h.pin_memory()
+        Ke = max(1, min(K, 500))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            pairs.copy_(pinned, non_blocking=True)
+            pkv.copy_blocks(kc, vc, pairs, status=status)
+        st_host = status.to("cpu", non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / Ke
+        e2e = {"value": moved * world / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(pairs_h.numel() * 4), "d2h_bytes_per_step": 4,
+               "ms_per_step": e_ms, "steps": Ke, "status": int(st_host.item())}
+
+    # Host block manager: 128 sequences forked from a 1000-token prompt, one
+    # append each per step (slots + copy pairs for the step).
+    bm = pkv.BlockManager(N, 16, 4096)
+    bm.add(0, 1000)
+    seqs = list(range(1, 129))
+    for sq in seqs:
+        bm.fork(0, sq)
+    steps_h = 200
+    h0 = time.perf_counter()
+    per_step = []
+    for _ in range(steps_h):
+        _, pr = bm.append(seqs)
+        per_step.append(len(pr))
+    host_us = (time.perf_counter() - h0) / steps_h * 1e6
+
+    line = {
+        "metric": METRIC, "value": whole_job_rate(moved, world, ms * 1e-3) / 1e9, "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: random bf16 pool, seeded disjoint block pairs (no dataset)",
+        "config": {"workload": workload_text("cow_copy_70b"), "name": "cow_copy_70b",
+                   "num_blocks": N, "pairs": npairs, "block_bytes_per_cache": block_bytes,
+                   "bytes_moved_per_step": moved,
+                   "l2": "no flush: 268 MB moved per step exceeds L2 (129 MB)",
+                   "launch": "copy captured once as a CUDA graph, replayed per step"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": f"copy_blocks_kernel (mean of {K} CUDA-graph replays)",
+                     "algorithmic_bytes_per_launch": moved,
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "host_block_manager": {"append_us_per_step": host_us, "sequences": len(seqs),
+                               "copies_first_step": per_step[0], "copies_total": sum(per_step),
+                               "note": "ctypes call from Python included"},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        # The plain copy on the host (numpy), on a sample of the pairs.
+        kh = np.random.default_rng(1).standard_normal((4096, Hkv, D, 16)).astype(np.float16)
+        sub = np.random.default_rng(2).permutation(4096)[:512].reshape(256, 2)
+        c0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - c0 < 5.0:
+            kh[sub[:, 1]] = kh[sub[:, 0]]
+            reps += 1
+        el = time.perf_counter() - c0
+        line["cpu_baseline"] = {"value": reps * 256 * block_bytes * 2 / el / 1e9, "unit": "GB/s",
+                                "cores": 1, "kind": "numpy page copy",
+                                "sample": f"{reps} x 256 page copies of one 16-bit cache in "
+                                          f"{el:.1f} s"}
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
+    prefill = args.config in W.PREFILL_CONFIGS
+    if args.config == "cow_copy_70b":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "no oracle arm for page copies: "
+                              "the copy is its own definition (numpy cpu_baseline reported)"}))
+            return
+        run_copy(args)
+        return
     if args.impl == "reference":
-        run_reference(args)
+        (run_reference_prefill if prefill else run_reference)(args)
     else:
-        run_ours(args)
+        (run_prefill if prefill else run_ours)(args)
 
 
 if __name__ == "__main__":

@@ -58,7 +58,9 @@ typedef enum {
 typedef enum {
     PKV_F32 = 0,       /* IEEE binary32                                   */
     PKV_BF16 = 1,      /* bfloat16                                        */
-    PKV_FP8_E5M2 = 2   /* OCP fp8 E5M2 (KV cache only), value = code * scale */
+    PKV_FP8_E5M2 = 2,  /* OCP fp8 E5M2 (KV cache only), value = code * scale */
+    PKV_FP8_E4M3 = 3   /* OCP fp8 E4M3, finite form: no infinities, +-448 max,
+                          the all-ones code is NaN (KV cache only), value = code * scale */
 } pkv_dtype;
 
 /* Flags of pkv_paged_attn_decode. */
@@ -114,10 +116,10 @@ int pkv_paged_attn_partition_tokens(int num_seqs, int num_q_heads, int num_kv_he
  *   q            [num_seqs, num_q_heads, head_dim], q_dtype in {F32, BF16}
  *   k_cache,
  *   v_cache      [num_blocks, num_kv_heads, head_dim, block_size], kv_dtype in
- *                {F32, BF16, FP8_E5M2}: tokens of a page are contiguous for
+ *                {F32, BF16, FP8_E5M2, FP8_E4M3}: tokens of a page are contiguous for
  *                each (head, dim), as in the pages' K_cache layout.
  *   k_scale,
- *   v_scale      dequant scales of FP8_E5M2 caches (value = code * scale);
+ *   v_scale      dequant scales of fp8 caches (value = code * scale);
  *                ignored for F32/BF16.
  *   block_tables int32 [num_seqs, max_blocks_per_seq]; entry j of row s is the
  *                physical block holding logical tokens [16j, 16j+16) of
@@ -284,9 +286,9 @@ pkv_status pkv_paged_attn_decode_noalloc(const void *q, pkv_dtype q_dtype,
  *   k_cache,
  *   v_cache       [num_blocks, num_kv_heads, head_dim, block_size] of kv_dtype.
  *   cvt           F32 -> F32 and BF16 -> BF16 copy the bits; F32 -> BF16 rounds
- *                 to nearest even; BF16 -> F32 widens exactly; -> FP8_E5M2
+ *                 to nearest even; BF16 -> F32 widens exactly; -> FP8_E5M2 / FP8_E4M3
  *                 stores round-to-nearest-even(x / scale) computed in float32
- *                 and saturated to +-57344.  NaN inputs give a NaN code of
+ *                 and saturated to +-57344 (e5m2) / +-448 (e4m3).  NaN inputs give a NaN code of
  *                 unspecified payload.
  *   status        optional device int32 (NULL = none): set to
  *                 PKV_ERR_OUT_OF_RANGE if a slot lies past the pool (that

@@ -28,9 +28,9 @@ __all__ = ["paged_attn_decode", "paged_attn_decode_append", "paged_attn_prefill"
            "reshape_and_cache", "workspace_size", "partition_tokens",
            "prefill_workspace_size", "prefill_partition_tokens", "copy_blocks",
            "BlockManager",
-           "read_status", "PkvError", "lib", "F32", "BF16", "FP8_E5M2"]
+           "read_status", "PkvError", "lib", "F32", "BF16", "FP8_E5M2", "FP8_E4M3"]
 
-F32, BF16, FP8_E5M2 = 0, 1, 2
+F32, BF16, FP8_E5M2, FP8_E4M3 = 0, 1, 2, 3
 IMPL = {"auto": 0x0, "simt": 0x1, "mma": 0x2}
 FLAG_SEPARATE_MERGE = 0x4
 FLAG_TEST_DROP_FIRST_COPY = 0x100
@@ -122,6 +122,8 @@ def _dtype_code(t: torch.Tensor, what: str) -> int:
         return BF16
     if t.dtype == torch.float8_e5m2:
         return FP8_E5M2
+    if t.dtype == torch.float8_e4m3fn:
+        return FP8_E4M3
     raise TypeError(f"{what}: unsupported dtype {t.dtype}")
 
 
@@ -183,7 +185,7 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     """PagedAttention decode: out[s, h] = softmax(scale q[s,h] K_s^T) V_s.
 
     q [S, Hq, D] (f32/bf16); k_cache, v_cache [N, Hkv, D, 16] (f32/bf16/
-    float8_e5m2); block_tables int32 [S, max_blocks]; seq_lens int32 [S];
+    float8_e5m2/float8_e4m3fn); block_tables int32 [S, max_blocks]; seq_lens int32 [S];
     out [S, Hq, D] (f32/bf16).  ``max_seq_len`` bounds seq_lens (default:
     max_blocks * 16, no device sync).  Returns ``out``.
     """

@@ -16,7 +16,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
-UNITS = ["pkv_api.cu", "pkv_cache.cu", "pkv_merge.cu", "pkv_decode_simt.cu", "pkv_decode_mma.cu",
+UNITS = ["pkv_api.cu", "pkv_cache.cu", "pkv_merge.cu", "pkv_decode_simt.cu",
+         "pkv_decode_simt_fp8.cu", "pkv_decode_mma.cu",
          "pkv_noalloc.cu", "pkv_prefill.cu", "pkv_block_manager.cpp"]
 HEADERS = ["pkv_common.cuh", "pkv_convert.cuh", "pkv_decode.cuh", "pkv_merge.cuh",
            "pkv_streamk.cuh", "pkv_internal.h"]

@@ -154,7 +154,7 @@ static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_ca
         return PKV_ERR_INVALID_ARG;
     if (q_dtype != PKV_F32 && q_dtype != PKV_BF16)
         return PKV_ERR_UNSUPPORTED;
-    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E5M2)
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && !is_fp8(kv_dtype))
         return PKV_ERR_UNSUPPORTED;
     if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
         return PKV_ERR_UNSUPPORTED;
@@ -216,9 +216,9 @@ static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_ca
     p.max_blocks = max_blocks_per_seq;
     p.max_len = max_seq_len;
     p.group = group;
-    const float k_mul = (kv_dtype == PKV_FP8_E5M2) ? k_scale : 1.0f;
+    const float k_mul = is_fp8(kv_dtype) ? k_scale : 1.0f;
     p.score_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * k_mul);
-    p.out_scale = (kv_dtype == PKV_FP8_E5M2) ? v_scale : 1.0f;
+    p.out_scale = is_fp8(kv_dtype) ? v_scale : 1.0f;
     p.partition = pl.partition > 0 ? pl.partition : max_blocks_per_seq * kBlockSize;
     p.max_parts = pl.max_parts;
     p.split = pl.partition > 0 ? 1 : 0;
@@ -279,7 +279,7 @@ pkv_status pkv_paged_attn_decode_append(const void *q, pkv_dtype q_dtype, const 
 {
     if (new_dtype != PKV_F32 && new_dtype != PKV_BF16)
         return PKV_ERR_UNSUPPORTED;
-    if (kv_dtype == PKV_FP8_E5M2 && (k_scale == 0.f || v_scale == 0.f))
+    if (is_fp8(kv_dtype) && (k_scale == 0.f || v_scale == 0.f))
         return PKV_ERR_INVALID_ARG;
     if (num_seqs > 0 && (!new_k || !new_v || !aligned(new_k, 16) || !aligned(new_v, 16)))
         return PKV_ERR_INVALID_ARG;
@@ -302,12 +302,9 @@ pkv_status pkv_reshape_and_cache(const void *k, const void *v, pkv_dtype in_dtyp
         return PKV_ERR_UNSUPPORTED;
     if (in_dtype != PKV_F32 && in_dtype != PKV_BF16)
         return PKV_ERR_UNSUPPORTED;
-    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E5M2)
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && !is_fp8(kv_dtype))
         return PKV_ERR_UNSUPPORTED;
-    if (kv_dtype == PKV_F32 && in_dtype == PKV_BF16) {
-        // widening is exact and supported
-    }
-    if (kv_dtype == PKV_FP8_E5M2 &&
+    if (is_fp8(kv_dtype) &&
         (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale == 0.f || v_scale == 0.f))
         return PKV_ERR_INVALID_ARG;
     if (num_tokens == 0)
@@ -502,7 +499,7 @@ pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, pkv_dtype kv_dtype, int
         return PKV_ERR_INVALID_ARG;
     if (block_size != kBlockSize)
         return PKV_ERR_UNSUPPORTED;
-    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && kv_dtype != PKV_FP8_E5M2)
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && !is_fp8(kv_dtype))
         return PKV_ERR_UNSUPPORTED;
     if (num_pairs == 0)
         return PKV_OK;

@@ -1,8 +1,8 @@
 // Element conversions of the paged cache write, shared by the cache-write
 // kernel and the fused write-and-decode path of the decode kernels.
 // F32 -> F32 and BF16 -> BF16 copy the bits; F32 -> BF16 rounds to nearest
-// even; BF16 -> F32 widens exactly; -> FP8_E5M2 stores
-// round-to-nearest-even(x / scale) in float32, saturated to +-57344.
+// even; BF16 -> F32 widens exactly; -> FP8_E5M2 / FP8_E4M3 store
+// round-to-nearest-even(x / scale) in float32, saturated to +-57344 / +-448.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -36,8 +36,8 @@ __device__ __forceinline__ void store_kv(void *cache, int dtype, size_t i, const
         static_cast<unsigned short *>(cache)[i] = b;
     } else {
         const float x = load_in(src, in_dtype, j) / scale;
-        static_cast<unsigned char *>(cache)[i] =
-            static_cast<unsigned char>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E5M2));
+        static_cast<unsigned char *>(cache)[i] = static_cast<unsigned char>(__nv_cvt_float_to_fp8(
+            x, __NV_SATFINITE, dtype == PKV_FP8_E4M3 ? __NV_E4M3 : __NV_E5M2));
     }
 }
 
@@ -51,8 +51,8 @@ __device__ __forceinline__ void store_kv_value(void *cache, int dtype, size_t i,
     else if (dtype == PKV_BF16)
         static_cast<unsigned short *>(cache)[i] = __bfloat16_as_ushort(__float2bfloat16_rn(x));
     else
-        static_cast<unsigned char *>(cache)[i] =
-            static_cast<unsigned char>(__nv_cvt_float_to_fp8(x / scale, __NV_SATFINITE, __NV_E5M2));
+        static_cast<unsigned char *>(cache)[i] = static_cast<unsigned char>(__nv_cvt_float_to_fp8(
+            x / scale, __NV_SATFINITE, dtype == PKV_FP8_E4M3 ? __NV_E4M3 : __NV_E5M2));
 }
 
 }  // namespace pkv

@@ -55,6 +55,7 @@ template <int KV> struct KvBytes;
 template <> struct KvBytes<PKV_F32> { static constexpr int v = 4; };
 template <> struct KvBytes<PKV_BF16> { static constexpr int v = 2; };
 template <> struct KvBytes<PKV_FP8_E5M2> { static constexpr int v = 1; };
+template <> struct KvBytes<PKV_FP8_E4M3> { static constexpr int v = 1; };
 
 // Per-CTA shared memory the stream-K kernel plans for (two CTAs per SM) and
 // the ring budget per warp it may use at most.
@@ -142,8 +143,10 @@ struct SimtPolicy {
         else if constexpr (KV == PKV_BF16)
             return __uint_as_float(
                 static_cast<uint32_t>(reinterpret_cast<const unsigned short *>(tile)[idx]) << 16);
-        else
+        else if constexpr (KV == PKV_FP8_E5M2)
             return e5m2_to_float(tile[idx]);
+        else
+            return e4m3_to_float(tile[idx]);
     }
 
     // One page row V[d][0..15] widened to floats.
@@ -178,7 +181,8 @@ struct SimtPolicy {
             for (int k = 0; k < 4; ++k)
 #pragma unroll
                 for (int b = 0; b < 4; ++b)
-                    v[4 * k + b] = e5m2_to_float(w[k] >> (8 * b));
+                    v[4 * k + b] = KV == PKV_FP8_E5M2 ? e5m2_to_float(w[k] >> (8 * b))
+                                                      : e4m3_to_float(w[k] >> (8 * b));
         }
     }
 
@@ -569,19 +573,20 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
     }
 };
 
-// fp8-e5m2 KV: the page tile is [D][16] bytes (16-byte rows), read by
-// ldmatrix as 16-bit pairs; byte_perm widens each code to an f16 (the code
-// is the f16's high byte, exactly).  Token order inside a fragment is
+// fp8 KV (e5m2 or e4m3): the page tile is [D][16] bytes (16-byte rows), read
+// by ldmatrix as 16-bit pairs; each code is widened to an f16, exactly (e5m2:
+// byte_perm places it as the f16's high byte; e4m3: cvt.f16x2.e4m3x2).  Token order inside a fragment is
 // permuted consistently on both operands (see the byte selectors).  Staged
 // like the bf16 policy: 32 registers hold a page's raw codes.
-template <int D, int NT, int Budget = PKV_RING_BYTES_PER_WARP, bool Staged = false>
+template <int D, int NT, int Budget = PKV_RING_BYTES_PER_WARP, bool Staged = false,
+          int KV = PKV_FP8_E5M2>
 struct MmaFp8Policy : MmaStateBase<D, NT> {
     using Base = MmaStateBase<D, NT>;
     using State = typename Base::State;
-    using RingT = Ring<PKV_FP8_E5M2, D, Budget>;
+    using RingT = Ring<KV, D, Budget>;
     // The same policy with a separate merge scratch and the ring that fits.
     // Stream-K stages pages in registers when G <= 8 (no spills there).
-    using StreamK = MmaFp8Policy<D, NT, ring_budget(scratch_bytes(8 * NT, D)), NT == 1>;
+    using StreamK = MmaFp8Policy<D, NT, ring_budget(scratch_bytes(8 * NT, D)), NT == 1, KV>;
     static constexpr int R = RingT::R;
     static constexpr int kTileBytes = RingT::kTileBytes;
     static constexpr int kStageBytes = RingT::kStageBytes;
@@ -594,6 +599,16 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
     static constexpr bool kSharedBegin = false;  // begin() only fills registers
     static constexpr uint32_t kSelEven = 0x2404u;  // bytes 0, 2 -> high bytes of two f16
     static constexpr uint32_t kSelOdd = 0x3414u;   // bytes 1, 3 -> high bytes of two f16
+
+    // Codes (bytes 0, 2) or (bytes 1, 3) of w as an f16x2 word: e5m2 is the
+    // high byte of the same binary16; e4m3 goes through the hardware convert.
+    __device__ static uint32_t widen(uint32_t w, bool odd)
+    {
+        if constexpr (KV == PKV_FP8_E5M2)
+            return e5m2x2_to_f16x2(w, odd ? kSelOdd : kSelEven);
+        else
+            return e4m3x2_to_f16x2(w, odd ? 0x4431u : 0x4420u);
+    }
 
     struct Frags {
         uint32_t k[KS / 2][4];  // raw codes of 32 head_dim rows of K per entry
@@ -638,10 +653,8 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
             const uint32_t *w = f.k[kp];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const uint32_t a[4] = {e5m2x2_to_f16x2(w[2 * h], kSelEven),
-                                       e5m2x2_to_f16x2(w[2 * h], kSelOdd),
-                                       e5m2x2_to_f16x2(w[2 * h + 1], kSelEven),
-                                       e5m2x2_to_f16x2(w[2 * h + 1], kSelOdd)};
+                const uint32_t a[4] = {widen(w[2 * h], false), widen(w[2 * h], true),
+                                       widen(w[2 * h + 1], false), widen(w[2 * h + 1], true)};
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
                     mma_f16(h ? sodd[n] : sacc[n], a, st.qf[2 * kp + h][n][0],
@@ -677,10 +690,8 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
             const uint32_t *w = f.v[mp];
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const uint32_t a[4] = {e5m2x2_to_f16x2(w[2 * h], kSelEven) & me,
-                                       e5m2x2_to_f16x2(w[2 * h + 1], kSelEven) & me,
-                                       e5m2x2_to_f16x2(w[2 * h], kSelOdd) & mo,
-                                       e5m2x2_to_f16x2(w[2 * h + 1], kSelOdd) & mo};
+                const uint32_t a[4] = {widen(w[2 * h], false) & me, widen(w[2 * h + 1], false) & me,
+                                       widen(w[2 * h], true) & mo, widen(w[2 * h + 1], true) & mo};
 #pragma unroll
                 for (int n = 0; n < NT; ++n)
                     mma_f16(st.o[2 * mp + h][n], a, b0[n], b1[n]);

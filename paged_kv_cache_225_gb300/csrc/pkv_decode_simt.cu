@@ -1,5 +1,6 @@
 // CUDA-core (FFMA) decode kernels: every KV dtype, head_dim 64/128, up to 16
-// query heads per KV head (padded to a power of two).
+// query heads per KV head (padded to a power of two).  The fp8 dtypes are
+// instantiated in pkv_decode_simt_fp8.cu.
 #include "pkv_streamk.cuh"
 
 namespace pkv {
@@ -39,7 +40,8 @@ pkv_status launch_decode_simt(const DecodeParams &p, int kv_dtype, cudaStream_t 
     case PKV_BF16:
         return dispatch_dim<PKV_BF16>(p, stream);
     case PKV_FP8_E5M2:
-        return dispatch_dim<PKV_FP8_E5M2>(p, stream);
+    case PKV_FP8_E4M3:
+        return launch_decode_simt_fp8(p, kv_dtype, stream);
     default:
         return PKV_ERR_UNSUPPORTED;
     }

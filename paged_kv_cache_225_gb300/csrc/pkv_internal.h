@@ -74,6 +74,9 @@ struct PrefillParams {
 };
 
 constexpr int kBlockSize = 16;
+
+// The 8-bit KV dtypes (value = code * scale).
+constexpr bool is_fp8(int dtype) { return dtype == PKV_FP8_E5M2 || dtype == PKV_FP8_E4M3; }
 constexpr size_t kWorkspaceHeader = 256;
 constexpr int kStreamKMaxCtas = 1024;  // partial slots of the stream-K schedule
 
@@ -81,6 +84,7 @@ constexpr int kStreamKMaxCtas = 1024;  // partial slots of the stream-K schedule
 // (PKV_OK, PKV_ERR_UNSUPPORTED for a shape with no kernel, PKV_ERR_CUDA).
 // `grid_items` is the number of CTAs to launch (0 = let the unit decide).
 pkv_status launch_decode_simt(const DecodeParams &p, int kv_dtype, cudaStream_t stream);
+pkv_status launch_decode_simt_fp8(const DecodeParams &p, int kv_dtype, cudaStream_t stream);
 pkv_status launch_decode_mma(const DecodeParams &p, int kv_dtype, cudaStream_t stream);
 pkv_status launch_merge(const DecodeParams &p, cudaStream_t stream);
 bool mma_supports(int kv_dtype, int q_dtype, int head_dim, int group);

@@ -35,7 +35,14 @@ namespace {
 
 constexpr int kRowTile = 16;                  // rows per warp tile
 constexpr int kRowBlock = kWarps * kRowTile;  // rows per work item
-constexpr int kPrefillRingBytes = 96 * 1024;  // two CTAs per SM
+// Page ring per CTA and the CTAs per SM the registers are bounded for.
+#ifndef PKV_PREFILL_RING_BYTES
+#define PKV_PREFILL_RING_BYTES (96 * 1024)
+#endif
+#ifndef PKV_PREFILL_MIN_CTAS
+#define PKV_PREFILL_MIN_CTAS 2
+#endif
+constexpr int kPrefillRingBytes = PKV_PREFILL_RING_BYTES;
 
 template <int D> struct PrefillGeom {
     static constexpr int kTileBytes = D * kBlockSize * 2;  // bf16 page tile
@@ -269,7 +276,8 @@ __device__ __forceinline__ void store_row4(const PrefillParams &p, int D, int to
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParams p)
+__global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
+    prefill_kernel(const PrefillParams p)
 {
     using Geo = PrefillGeom<D>;
     using Base = MmaStateBase<D, 2>;
@@ -462,7 +470,10 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
             const bool have = s_ok[stg] != 0;
             const unsigned char *sk = smem + stg * Geo::kStageBytes;
             typename Pol::Frags f;
-            if (have)
+            // A warp whose row tile is empty (three tiles of rows on four
+            // warps) only releases the stage.
+            const bool work = have && rt < RT;
+            if (work)
                 Pol::load(f, sk, sk + Geo::kTileBytes, lane);
             // The stage is free once every lane's reads are done.
             fence_proxy_async();
@@ -471,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_kernel(const PrefillParam
                 mbar_arrive(&empty[stg]);
             if (warp == 0)
                 issue_upto(j + NS, false);
-            if (have) {
+            if (work) {
                 const int tb = (pg0 + j) * kBlockSize;  // position of the page's token 0
                 const int valid = min(kBlockSize, L - tb);
                 int lim[2][2];

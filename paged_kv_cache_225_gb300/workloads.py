@@ -86,8 +86,15 @@ CONFIGS = {
         name="fp8_chat", num_seqs=128, num_q_heads=64, num_kv_heads=8, head_dim=128,
         block_size=16, q_dtype=BF16, kv_dtype=FP8_E5M2, len_dist="uniform", len_lo=256,
         len_hi=512, shared_prefix_group=8, shared_prefix_blocks=8),
+    # The 70B layer with an fp8-e4m3 cache and a per-tensor scale of 1/8
+    # (values stored as x * 8 before rounding, so N(0,1) data uses the
+    # format's finer upper range).
+    "e4m3_70b": DecodeConfig(
+        name="e4m3_70b", num_seqs=128, num_q_heads=64, num_kv_heads=8, head_dim=128,
+        block_size=16, q_dtype=BF16, kv_dtype=FP8_E4M3, len_dist="lognormal",
+        len_median=2048.0, len_sigma=0.8, len_lo=16, len_hi=32768, kv_scale=0.125),
 }
-CONFIG_ORDER = ["tiny_fp32", "llama3_8b", "llama3_70b", "long_split", "fp8_chat"]
+CONFIG_ORDER = ["tiny_fp32", "llama3_8b", "llama3_70b", "long_split", "fp8_chat", "e4m3_70b"]
 CONFIG_SEED = {name: i for i, name in enumerate(CONFIG_ORDER)}
 
 
