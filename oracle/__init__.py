@@ -61,6 +61,14 @@ def _load():
                       ip, ip, ip, ip, ip, ip, ip, ctypes.c_double]
             lib.pkvo_paged_decode.argtypes = common + [ip, dp, ip]
             lib.pkvo_paged_decode.restype = ip
+            fp = ctypes.POINTER(ctypes.c_float)
+            lib.pkvo_paged_decode_head_scaled.argtypes = (common[:7] + [fp, fp] + common[7:]
+                                                          + [ip, dp, ip])
+            lib.pkvo_paged_decode_head_scaled.restype = ip
+            lib.pkvo_reshape_and_cache_head_scaled.argtypes = [
+                vp, vp, ip, i64p, ip, ip, ip, ip, ip, vp, vp, ip, ctypes.c_float, ctypes.c_float,
+                fp, fp]
+            lib.pkvo_reshape_and_cache_head_scaled.restype = ip
             lib.pkvo_paged_decode_seqs.argtypes = common + [i32p, ip, dp, ip]
             lib.pkvo_paged_decode_seqs.restype = ip
             lib.pkvo_paged_prefill.argtypes = [vp, ip, i32p] + common[2:] + [ip, dp, ip]
@@ -123,17 +131,30 @@ def _attn_args(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_lens, s
 
 
 def paged_decode(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_lens, scale,
-                 k_scale=1.0, v_scale=1.0, partition_tokens=0, num_threads=0) -> np.ndarray:
+                 k_scale=1.0, v_scale=1.0, partition_tokens=0, num_threads=0,
+                 k_head_scales=None, v_head_scales=None) -> np.ndarray:
     """Paged decode attention of the whole batch in float64: out [S, Hq, D].
 
     ``partition_tokens > 0`` evaluates the split-sequence form with the
-    log-sum-exp merge instead of one softmax per sequence.
+    log-sum-exp merge instead of one softmax per sequence.  For fp8 caches,
+    ``k_head_scales`` / ``v_head_scales`` ([Hkv] float32) multiply the
+    dequant scale of each KV head.
     """
     args, keep, shape = _attn_args(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
                                    seq_lens, scale, k_scale, v_scale)
     out = np.zeros(shape, dtype=np.float64)
-    rc = _load().pkvo_paged_decode(*args, int(partition_tokens), _ptr(out, ctypes.c_double),
-                                   int(num_threads))
+    if k_head_scales is None and v_head_scales is None:
+        rc = _load().pkvo_paged_decode(*args, int(partition_tokens), _ptr(out, ctypes.c_double),
+                                       int(num_threads))
+    else:
+        Hkv = k_cache.shape[1]
+        ones = np.ones(Hkv, np.float32)
+        ksh = np.ascontiguousarray(ones if k_head_scales is None else k_head_scales, np.float32)
+        vsh = np.ascontiguousarray(ones if v_head_scales is None else v_head_scales, np.float32)
+        assert ksh.shape == (Hkv,) and vsh.shape == (Hkv,)
+        rc = _load().pkvo_paged_decode_head_scaled(
+            *args[:7], _ptr(ksh, ctypes.c_float), _ptr(vsh, ctypes.c_float), *args[7:],
+            int(partition_tokens), _ptr(out, ctypes.c_double), int(num_threads))
     del keep
     if rc:
         raise ValueError(f"oracle paged_decode failed ({rc})")
@@ -187,8 +208,12 @@ def paged_prefill(q, q_dtype, q_start, k_cache, v_cache, kv_dtype, block_tables,
 
 
 def reshape_and_cache(k, v, in_dtype, slot_mapping, k_cache, v_cache, kv_dtype,
-                      k_scale=1.0, v_scale=1.0) -> int:
-    """Scatter new K/V rows into host cache copies in place; returns the status code."""
+                      k_scale=1.0, v_scale=1.0, k_head_scales=None, v_head_scales=None) -> int:
+    """Scatter new K/V rows into host cache copies in place; returns the status code.
+
+    For fp8 caches ``k_head_scales`` / ``v_head_scales`` ([Hkv] float32)
+    multiply the quantisation scale of each KV head.
+    """
     T, Hkv, D = k.shape
     N, Hkv2, D2, B = k_cache.shape
     assert Hkv2 == Hkv and D2 == D and v.shape == k.shape
@@ -196,7 +221,15 @@ def reshape_and_cache(k, v, in_dtype, slot_mapping, k_cache, v_cache, kv_dtype,
     k = np.ascontiguousarray(k)
     v = np.ascontiguousarray(v)
     sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
-    return int(_load().pkvo_reshape_and_cache(_ptr(k), _ptr(v), in_dtype,
-                                              _ptr(sm, ctypes.c_int64), T, Hkv, D, B, N,
-                                              _ptr(k_cache), _ptr(v_cache), kv_dtype,
-                                              float(k_scale), float(v_scale)))
+    if k_head_scales is None and v_head_scales is None:
+        return int(_load().pkvo_reshape_and_cache(_ptr(k), _ptr(v), in_dtype,
+                                                  _ptr(sm, ctypes.c_int64), T, Hkv, D, B, N,
+                                                  _ptr(k_cache), _ptr(v_cache), kv_dtype,
+                                                  float(k_scale), float(v_scale)))
+    ones = np.ones(Hkv, np.float32)
+    ksh = np.ascontiguousarray(ones if k_head_scales is None else k_head_scales, np.float32)
+    vsh = np.ascontiguousarray(ones if v_head_scales is None else v_head_scales, np.float32)
+    return int(_load().pkvo_reshape_and_cache_head_scaled(
+        _ptr(k), _ptr(v), in_dtype, _ptr(sm, ctypes.c_int64), T, Hkv, D, B, N, _ptr(k_cache),
+        _ptr(v_cache), kv_dtype, float(k_scale), float(v_scale), _ptr(ksh, ctypes.c_float),
+        _ptr(vsh, ctypes.c_float)))

@@ -276,6 +276,8 @@ typedef struct {
     int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size;
     int num_blocks, max_blocks_per_seq;
     double scale;
+    const float *k_head_scales;   /* [num_kv_heads] or NULL: per-head factors of fp8 caches */
+    const float *v_head_scales;
 } pkvo_problem;
 
 static size_t cache_index(const pkvo_problem *P, int32_t blk, int hkv, int d, int off)
@@ -291,6 +293,10 @@ static int gather_rows(const pkvo_problem *P, int s, int hkv, int L, double *K, 
     const int fp8 = P->kv_dtype == PKVO_FP8_E5M2 || P->kv_dtype == PKVO_FP8_E4M3;
     double ks = fp8 ? P->k_scale : 1.0;
     double vs = fp8 ? P->v_scale : 1.0;
+    if (fp8 && P->k_head_scales)
+        ks *= (double)P->k_head_scales[hkv];
+    if (fp8 && P->v_head_scales)
+        vs *= (double)P->v_head_scales[hkv];
     for (int t = 0; t < L; ++t) {
         int32_t blk = P->block_tables[(size_t)s * P->max_blocks_per_seq + t / B];
         if (blk < 0 || blk >= P->num_blocks)
@@ -484,7 +490,28 @@ int pkvo_paged_decode(const void *q, int q_dtype, const void *k_cache, const voi
 {
     pkvo_problem P = {q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale,
                       block_tables, seq_lens, num_seqs, num_q_heads, num_kv_heads,
-                      head_dim, block_size, num_blocks, max_blocks_per_seq, scale};
+                      head_dim, block_size, num_blocks, max_blocks_per_seq, scale, NULL, NULL};
+    return run_attention(&P, partition_tokens, out, num_threads);
+}
+
+/*
+ * The same decode for fp8 caches with a dequant factor per KV head: element
+ * (block, h, d, t) of K stands for code * k_scale * k_head_scales[h] (V
+ * likewise).  NULL arrays mean a factor of 1.
+ */
+int pkvo_paged_decode_head_scaled(const void *q, int q_dtype, const void *k_cache,
+                                  const void *v_cache, int kv_dtype, double k_scale,
+                                  double v_scale, const float *k_head_scales,
+                                  const float *v_head_scales, const int32_t *block_tables,
+                                  const int32_t *seq_lens, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                  int max_blocks_per_seq, double scale, int partition_tokens,
+                                  double *out, int num_threads)
+{
+    pkvo_problem P = {q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                      block_tables, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                      head_dim, block_size, num_blocks, max_blocks_per_seq, scale,
+                      k_head_scales, v_head_scales};
     return run_attention(&P, partition_tokens, out, num_threads);
 }
 
@@ -502,7 +529,7 @@ int pkvo_paged_decode_seqs(const void *q, int q_dtype, const void *k_cache,
 {
     pkvo_problem P = {q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale,
                       block_tables, seq_lens, num_seqs, num_q_heads, num_kv_heads,
-                      head_dim, block_size, num_blocks, max_blocks_per_seq, scale};
+                      head_dim, block_size, num_blocks, max_blocks_per_seq, scale, NULL, NULL};
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
         return 4;
     long units = (long)num_listed * num_kv_heads;
@@ -546,7 +573,7 @@ int pkvo_paged_prefill(const void *q, int q_dtype, const int32_t *q_start,
 {
     pkvo_problem P = {q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale,
                       block_tables, seq_lens, num_seqs, num_q_heads, num_kv_heads,
-                      head_dim, block_size, num_blocks, max_blocks_per_seq, scale};
+                      head_dim, block_size, num_blocks, max_blocks_per_seq, scale, NULL, NULL};
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
         return 4;
     for (int s = 0; s < num_seqs; ++s)
@@ -577,10 +604,35 @@ int pkvo_paged_prefill(const void *q, int q_dtype, const int32_t *q_start,
  * skipped.  Returns 1 if a slot lies past the pool (nothing written for it),
  * 5 for an unsupported dtype.
  */
+int pkvo_reshape_and_cache_head_scaled(const void *k, const void *v, int in_dtype,
+                                       const int64_t *slot_mapping, int num_tokens,
+                                       int num_kv_heads, int head_dim, int block_size,
+                                       int num_blocks, void *k_cache, void *v_cache,
+                                       int kv_dtype, float k_scale, float v_scale,
+                                       const float *k_head_scales, const float *v_head_scales);
+
 int pkvo_reshape_and_cache(const void *k, const void *v, int in_dtype,
                            const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
                            int head_dim, int block_size, int num_blocks, void *k_cache,
                            void *v_cache, int kv_dtype, float k_scale, float v_scale)
+{
+    return pkvo_reshape_and_cache_head_scaled(k, v, in_dtype, slot_mapping, num_tokens,
+                                              num_kv_heads, head_dim, block_size, num_blocks,
+                                              k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                                              NULL, NULL);
+}
+
+/*
+ * The cache write with a quantisation factor per KV head for fp8 caches: the
+ * code stored for head h is RNE_satfinite(x / (k_scale * k_head_scales[h])),
+ * the divisor formed in float32 (V likewise).  NULL arrays mean 1.
+ */
+int pkvo_reshape_and_cache_head_scaled(const void *k, const void *v, int in_dtype,
+                                       const int64_t *slot_mapping, int num_tokens,
+                                       int num_kv_heads, int head_dim, int block_size,
+                                       int num_blocks, void *k_cache, void *v_cache,
+                                       int kv_dtype, float k_scale, float v_scale,
+                                       const float *k_head_scales, const float *v_head_scales)
 {
     if (in_dtype != PKVO_F32 && in_dtype != PKVO_BF16)
         return 5;
@@ -599,6 +651,8 @@ int pkvo_reshape_and_cache(const void *k, const void *v, int in_dtype,
             continue;
         }
         for (int h = 0; h < num_kv_heads; ++h) {
+            const float ksh = k_head_scales ? k_scale * k_head_scales[h] : k_scale;
+            const float vsh = v_head_scales ? v_scale * v_head_scales[h] : v_scale;
             for (int d = 0; d < head_dim; ++d) {
                 size_t src = ((size_t)i * num_kv_heads + h) * head_dim + d;
                 size_t dst = (((size_t)blk * num_kv_heads + h) * head_dim + d) * block_size + off;
@@ -613,11 +667,11 @@ int pkvo_reshape_and_cache(const void *k, const void *v, int in_dtype,
                     memcpy((uint8_t *)k_cache + 2 * dst, &kb, 2);
                     memcpy((uint8_t *)v_cache + 2 * dst, &vb, 2);
                 } else if (kv_dtype == PKVO_FP8_E5M2) {
-                    ((uint8_t *)k_cache)[dst] = e5m2_encode_rne_satfinite(kx / k_scale);
-                    ((uint8_t *)v_cache)[dst] = e5m2_encode_rne_satfinite(vx / v_scale);
+                    ((uint8_t *)k_cache)[dst] = e5m2_encode_rne_satfinite(kx / ksh);
+                    ((uint8_t *)v_cache)[dst] = e5m2_encode_rne_satfinite(vx / vsh);
                 } else {
-                    ((uint8_t *)k_cache)[dst] = e4m3_encode_rne_satfinite(kx / k_scale);
-                    ((uint8_t *)v_cache)[dst] = e4m3_encode_rne_satfinite(vx / v_scale);
+                    ((uint8_t *)k_cache)[dst] = e4m3_encode_rne_satfinite(kx / ksh);
+                    ((uint8_t *)v_cache)[dst] = e4m3_encode_rne_satfinite(vx / vsh);
                 }
             }
         }

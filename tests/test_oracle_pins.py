@@ -429,3 +429,53 @@ def test_kv_bytes_per_token_matches_page_worked_example():
     mha = kv_bytes_per_token(int(g["num_layers"]), int(g["num_q_heads"]), int(g["head_dim"]),
                              int(g["bytes_per_elem"]))
     assert mha / per_tok == g["gqa_reduction"]
+
+
+# ------------------------------------------------------ per-head fp8 scales
+
+@pytest.mark.parametrize("kv_dtype", [FP8, E4M3])
+def test_per_head_scales_reduce_to_per_tensor_runs(kv_dtype):
+    p = _tiny_problem(kv_dtype, BF16, S=3, Hq=6, Hkv=3, lens=(9, 40, 23), seed=30)
+    ks, vs = np.array([0.5, 2.0, 0.25], np.float32), np.array([3.0, 0.125, 1.0], np.float32)
+    got = _run(dict(p, k_scale=1.0, v_scale=1.0), k_head_scales=ks, v_head_scales=vs)
+    G = 2
+    for h in range(3):
+        ref = _run(dict(p, k_scale=float(ks[h]), v_scale=float(vs[h])))
+        assert np.array_equal(got[:, h * G:(h + 1) * G], ref[:, h * G:(h + 1) * G])
+    # Equal factors are the per-tensor scale; the tensor scale multiplies in.
+    same = _run(dict(p, k_scale=1.0, v_scale=1.0), k_head_scales=np.full(3, 0.5, np.float32),
+                v_head_scales=np.full(3, 0.5, np.float32))
+    assert np.array_equal(same, _run(dict(p, k_scale=0.5, v_scale=0.5)))
+    two = _run(dict(p, k_scale=2.0, v_scale=1.0), k_head_scales=np.full(3, 0.25, np.float32))
+    assert np.array_equal(two, _run(dict(p, k_scale=0.5, v_scale=1.0)))
+
+
+def test_per_head_v_scale_scales_only_that_heads_rows():
+    p = _tiny_problem(E4M3, BF16, S=2, Hq=4, Hkv=2, lens=(17, 33), seed=31)
+    base = _run(p)
+    got = _run(p, v_head_scales=np.array([1.0, 4.0], np.float32))
+    np.testing.assert_array_equal(got[:, :2], base[:, :2])
+    np.testing.assert_allclose(got[:, 2:], 4.0 * base[:, 2:], rtol=1e-14, atol=0)
+
+
+@pytest.mark.parametrize("kv_dtype", [FP8, E4M3])
+def test_reshape_with_per_head_scales_matches_numpy(kv_dtype):
+    rng = np.random.default_rng(32)
+    N, Hkv, D, B, T = 6, 3, 16, 16, 5
+    kc = np.zeros((N, Hkv, D, B), np.uint8)
+    vc = np.zeros_like(kc)
+    kin = rng.standard_normal((T, Hkv, D)).astype(np.float32) * 4
+    vin = rng.standard_normal((T, Hkv, D)).astype(np.float32)
+    slots = rng.choice(N * B, size=T, replace=False).astype(np.int64)
+    ks, vs = np.array([0.5, 2.0, 0.1], np.float32), np.array([0.25, 1.0, 8.0], np.float32)
+    assert oracle.reshape_and_cache(kin, vin, F32, slots, kc, vc, kv_dtype, 2.0, 1.0,
+                                    k_head_scales=ks, v_head_scales=vs) == 0
+    ek, ev = np.zeros_like(kc), np.zeros_like(vc)
+    for i, slot in enumerate(slots):
+        blk, off = divmod(int(slot), B)
+        for h in range(Hkv):
+            kd = np.float32(2.0) * ks[h]
+            vd = np.float32(1.0) * vs[h]
+            ek[blk, h, :, off] = W.round_to_storage((kin[i, h] / kd).astype(np.float32), kv_dtype)
+            ev[blk, h, :, off] = W.round_to_storage((vin[i, h] / vd).astype(np.float32), kv_dtype)
+    assert np.array_equal(kc, ek) and np.array_equal(vc, ev)
