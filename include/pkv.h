@@ -60,7 +60,10 @@ typedef enum {
     PKV_BF16 = 1,      /* bfloat16                                        */
     PKV_FP8_E5M2 = 2,  /* OCP fp8 E5M2 (KV cache only), value = code * scale */
     PKV_FP8_E4M3 = 3   /* OCP fp8 E4M3, finite form: no infinities, +-448 max,
-                          the all-ones code is NaN (KV cache only), value = code * scale */
+                          the all-ones code is NaN (KV cache only), value = code * scale.
+                          The tensor-core decode reads a NaN code in a valid slot
+                          as 480 (the cache write never stores one for finite
+                          inputs). */
 } pkv_dtype;
 
 /* Flags of pkv_paged_attn_decode. */
@@ -182,6 +185,22 @@ pkv_status pkv_paged_attn_decode_append(const void *q, pkv_dtype q_dtype, const 
                                         int partition_tokens, int flags, void *stream);
 
 /*
+ * Decode over an fp8 cache (FP8_E5M2 or FP8_E4M3) quantised with one scale per
+ * KV head: element (block, h, d, t) stands for code * k_head_scales[h] (K) and
+ * code * v_head_scales[h] (V).  k_head_scales, v_head_scales: float32
+ * [num_kv_heads] in device memory, non-zero and finite.  Everything else as
+ * for pkv_paged_attn_decode (whose scalar k_scale / v_scale are the special
+ * case of equal factors).  Other KV dtypes: PKV_ERR_UNSUPPORTED.
+ */
+pkv_status pkv_paged_attn_decode_head_scaled(
+    const void *q, pkv_dtype q_dtype, const void *k_cache, const void *v_cache, pkv_dtype kv_dtype,
+    const float *k_head_scales, const float *v_head_scales, const int32_t *block_tables,
+    const int32_t *seq_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, int max_blocks_per_seq, int max_seq_len, float scale,
+    void *out, pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
+    int partition_tokens, int flags, void *stream);
+
+/*
  * Paged attention of several query tokens per sequence: chunked prefill
  * ("vLLM e PagedAttention: serving high-throughput", the
  * --enable-chunked-prefill flag) and speculative verification of draft
@@ -299,6 +318,21 @@ pkv_status pkv_reshape_and_cache(const void *k, const void *v, pkv_dtype in_dtyp
                                  int head_dim, int block_size, int num_blocks,
                                  void *k_cache, void *v_cache, pkv_dtype kv_dtype,
                                  float k_scale, float v_scale, int32_t *status, void *stream);
+
+/*
+ * The cache write of pkv_reshape_and_cache for an fp8 cache quantised with one
+ * scale per KV head: head h's codes are RNE_satfinite(x / k_head_scales[h])
+ * (V likewise), the division done in float32.  k_head_scales, v_head_scales:
+ * float32 [num_kv_heads] in device memory.  Other KV dtypes:
+ * PKV_ERR_UNSUPPORTED.
+ */
+pkv_status pkv_reshape_and_cache_head_scaled(const void *k, const void *v, pkv_dtype in_dtype,
+                                             const int64_t *slot_mapping, int num_tokens,
+                                             int num_kv_heads, int head_dim, int block_size,
+                                             int num_blocks, void *k_cache, void *v_cache,
+                                             pkv_dtype kv_dtype, const float *k_head_scales,
+                                             const float *v_head_scales, int32_t *status,
+                                             void *stream);
 
 /*
  * Copy-on-write page copies ("Inference optimization" lesson, section

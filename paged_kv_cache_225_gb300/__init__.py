@@ -25,6 +25,7 @@ import torch
 from . import build as _build
 
 __all__ = ["paged_attn_decode", "paged_attn_decode_append", "paged_attn_prefill",
+           "paged_attn_decode_head_scaled", "reshape_and_cache_head_scaled",
            "reshape_and_cache", "workspace_size", "partition_tokens",
            "prefill_workspace_size", "prefill_partition_tokens", "copy_blocks",
            "BlockManager",
@@ -80,6 +81,13 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
             L.pkv_paged_attn_prefill.argtypes = [vp, i, vp, vp, vp, i, f, f, vp, vp, i, i, i, i,
                                                  i, i, i, i, i, i, f, vp, i, vp, sz, i, i, vp]
             L.pkv_paged_attn_prefill.restype = i
+            L.pkv_paged_attn_decode_head_scaled.argtypes = [vp, i, vp, vp, i, vp, vp, vp, vp, i,
+                                                            i, i, i, i, i, i, i, f, vp, i, vp,
+                                                            sz, i, i, vp]
+            L.pkv_paged_attn_decode_head_scaled.restype = i
+            L.pkv_reshape_and_cache_head_scaled.argtypes = [vp, vp, i, vp, i, i, i, i, i, vp, vp,
+                                                            i, vp, vp, vp, vp]
+            L.pkv_reshape_and_cache_head_scaled.restype = i
             L.pkv_copy_blocks.argtypes = [vp, vp, i, i, i, i, i, vp, i, vp, vp]
             L.pkv_copy_blocks.restype = i
             ip, i32p, i64p = (ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int32),
@@ -224,6 +232,85 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     if rc != 0:
         raise PkvError(rc, "pkv_paged_attn_decode")
     return out
+
+
+def paged_attn_decode_head_scaled(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  k_head_scales: torch.Tensor, v_head_scales: torch.Tensor,
+                                  block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                                  scale: float, out: torch.Tensor, *,
+                                  max_seq_len: Optional[int] = None, partition_tokens: int = 0,
+                                  impl: str = "auto", workspace: Optional[torch.Tensor] = None,
+                                  stream: Optional[torch.cuda.Stream] = None,
+                                  flags: int = 0) -> torch.Tensor:
+    """Decode over an fp8 cache with one dequant scale per KV head
+    (k_head_scales, v_head_scales: float32 [Hkv] on the device)."""
+    dev = q.device
+    for t, name, nd in ((q, "q", 3), (k_cache, "k_cache", 4), (v_cache, "v_cache", 4),
+                        (k_head_scales, "k_head_scales", 1), (v_head_scales, "v_head_scales", 1),
+                        (block_tables, "block_tables", 2), (seq_lens, "seq_lens", 1),
+                        (out, "out", 3)):
+        _check(t, name, nd, dev)
+    if k_head_scales.dtype != torch.float32 or v_head_scales.dtype != torch.float32:
+        raise TypeError("per-head scales must be float32")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    S, Hq, D = q.shape
+    N, Hkv, D2, B = k_cache.shape
+    if (D2 != D or out.shape != q.shape or k_cache.shape != v_cache.shape
+            or k_head_scales.shape[0] != Hkv or v_head_scales.shape[0] != Hkv):
+        raise ValueError("inconsistent shapes")
+    max_blocks = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_blocks * B
+    L = lib()
+    need = L.pkv_paged_attn_workspace_size(S, Hq, Hkv, D, B, max_seq_len, partition_tokens)
+    if need == 0:
+        raise ValueError("invalid sizes or partition_tokens")
+    if workspace is None:
+        workspace = get_workspace(need, dev)
+    rc = L.pkv_paged_attn_decode_head_scaled(
+        q.data_ptr(), _dtype_code(q, "q"), k_cache.data_ptr(), v_cache.data_ptr(),
+        _dtype_code(k_cache, "k_cache"), k_head_scales.data_ptr(), v_head_scales.data_ptr(),
+        block_tables.data_ptr(), seq_lens.data_ptr(), S, Hq, Hkv, D, B, N, max_blocks,
+        int(max_seq_len), float(scale), out.data_ptr(), _dtype_code(out, "out"),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        int(partition_tokens), int(flags) | IMPL[impl], _stream(dev, stream))
+    if rc != 0:
+        raise PkvError(rc, "pkv_paged_attn_decode_head_scaled")
+    return out
+
+
+def reshape_and_cache_head_scaled(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                                  k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                  k_head_scales: torch.Tensor, v_head_scales: torch.Tensor, *,
+                                  status: Optional[torch.Tensor] = None,
+                                  stream: Optional[torch.cuda.Stream] = None) -> None:
+    """The cache write into an fp8 cache with one quantisation scale per KV head."""
+    dev = k.device
+    for t, name, nd in ((k, "k", 3), (v, "v", 3), (slot_mapping, "slot_mapping", 1),
+                        (k_cache, "k_cache", 4), (v_cache, "v_cache", 4),
+                        (k_head_scales, "k_head_scales", 1), (v_head_scales, "v_head_scales", 1)):
+        _check(t, name, nd, dev)
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    if k_head_scales.dtype != torch.float32 or v_head_scales.dtype != torch.float32:
+        raise TypeError("per-head scales must be float32")
+    T, Hkv, D = k.shape
+    N, Hkv2, D2, B = k_cache.shape
+    if (v.shape != k.shape or Hkv2 != Hkv or D2 != D or v_cache.shape != k_cache.shape
+            or slot_mapping.shape[0] != T or k_head_scales.shape[0] != Hkv
+            or v_head_scales.shape[0] != Hkv):
+        raise ValueError("inconsistent shapes")
+    st_ptr = None
+    if status is not None:
+        _check(status, "status", 1, dev)
+        st_ptr = status.data_ptr()
+    rc = lib().pkv_reshape_and_cache_head_scaled(
+        k.data_ptr(), v.data_ptr(), _dtype_code(k, "k"), slot_mapping.data_ptr(), T, Hkv, D, B,
+        N, k_cache.data_ptr(), v_cache.data_ptr(), _dtype_code(k_cache, "k_cache"),
+        k_head_scales.data_ptr(), v_head_scales.data_ptr(), st_ptr, _stream(dev, stream))
+    if rc != 0:
+        raise PkvError(rc, "pkv_reshape_and_cache_head_scaled")
 
 
 def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.Tensor,

@@ -143,7 +143,9 @@ static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_ca
                               int max_blocks_per_seq, int max_seq_len, float scale, void *out,
                               pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
                               int partition_tokens, int flags, void *stream, const void *new_k,
-                              const void *new_v, pkv_dtype new_dtype)
+                              const void *new_v, pkv_dtype new_dtype,
+                              const float *k_head_scales = nullptr,
+                              const float *v_head_scales = nullptr)
 {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
         max_blocks_per_seq <= 0 || max_seq_len < 0)
@@ -219,6 +221,10 @@ static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_ca
     const float k_mul = is_fp8(kv_dtype) ? k_scale : 1.0f;
     p.score_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * k_mul);
     p.out_scale = is_fp8(kv_dtype) ? v_scale : 1.0f;
+    if (use_mma && kv_dtype == PKV_FP8_E4M3) {
+        p.score_scale *= kE4m3Shift;
+        p.out_scale *= kE4m3Shift;
+    }
     p.partition = pl.partition > 0 ? pl.partition : max_blocks_per_seq * kBlockSize;
     p.max_parts = pl.max_parts;
     p.split = pl.partition > 0 ? 1 : 0;
@@ -232,6 +238,8 @@ static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_ca
     p.kv_dtype = kv_dtype;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.k_head_scale = k_head_scales;
+    p.v_head_scale = v_head_scales;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // Status word, work counter and arrival counters start at zero.
@@ -290,11 +298,68 @@ pkv_status pkv_paged_attn_decode_append(const void *q, pkv_dtype q_dtype, const 
                        new_dtype);
 }
 
+pkv_status pkv_paged_attn_decode_head_scaled(
+    const void *q, pkv_dtype q_dtype, const void *k_cache, const void *v_cache, pkv_dtype kv_dtype,
+    const float *k_head_scales, const float *v_head_scales, const int32_t *block_tables,
+    const int32_t *seq_lens, int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+    int block_size, int num_blocks, int max_blocks_per_seq, int max_seq_len, float scale,
+    void *out, pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
+    int partition_tokens, int flags, void *stream)
+{
+    if (!is_fp8(kv_dtype))
+        return PKV_ERR_UNSUPPORTED;
+    if (num_seqs > 0 && (!k_head_scales || !v_head_scales || !aligned(k_head_scales, 4) ||
+                         !aligned(v_head_scales, 4)))
+        return PKV_ERR_INVALID_ARG;
+    return decode_impl(q, q_dtype, k_cache, v_cache, kv_dtype, 1.0f, 1.0f, block_tables,
+                       seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, max_blocks_per_seq, max_seq_len, scale, out, out_dtype,
+                       workspace, workspace_bytes, partition_tokens, flags, stream, nullptr,
+                       nullptr, PKV_F32, k_head_scales, v_head_scales);
+}
+
+static pkv_status reshape_impl(const void *k, const void *v, pkv_dtype in_dtype,
+                               const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks, void *k_cache,
+                               void *v_cache, pkv_dtype kv_dtype, float k_scale, float v_scale,
+                               const float *k_head_scales, const float *v_head_scales,
+                               int32_t *status, void *stream);
+
 pkv_status pkv_reshape_and_cache(const void *k, const void *v, pkv_dtype in_dtype,
                                  const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
                                  int head_dim, int block_size, int num_blocks, void *k_cache,
                                  void *v_cache, pkv_dtype kv_dtype, float k_scale, float v_scale,
                                  int32_t *status, void *stream)
+{
+    return reshape_impl(k, v, in_dtype, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                        block_size, num_blocks, k_cache, v_cache, kv_dtype, k_scale, v_scale,
+                        nullptr, nullptr, status, stream);
+}
+
+pkv_status pkv_reshape_and_cache_head_scaled(const void *k, const void *v, pkv_dtype in_dtype,
+                                             const int64_t *slot_mapping, int num_tokens,
+                                             int num_kv_heads, int head_dim, int block_size,
+                                             int num_blocks, void *k_cache, void *v_cache,
+                                             pkv_dtype kv_dtype, const float *k_head_scales,
+                                             const float *v_head_scales, int32_t *status,
+                                             void *stream)
+{
+    if (!is_fp8(kv_dtype))
+        return PKV_ERR_UNSUPPORTED;
+    if (num_tokens > 0 && (!k_head_scales || !v_head_scales || !aligned(k_head_scales, 4) ||
+                           !aligned(v_head_scales, 4)))
+        return PKV_ERR_INVALID_ARG;
+    return reshape_impl(k, v, in_dtype, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                        block_size, num_blocks, k_cache, v_cache, kv_dtype, 1.0f, 1.0f,
+                        k_head_scales, v_head_scales, status, stream);
+}
+
+static pkv_status reshape_impl(const void *k, const void *v, pkv_dtype in_dtype,
+                               const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                               int head_dim, int block_size, int num_blocks, void *k_cache,
+                               void *v_cache, pkv_dtype kv_dtype, float k_scale, float v_scale,
+                               const float *k_head_scales, const float *v_head_scales,
+                               int32_t *status, void *stream)
 {
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || num_blocks <= 0)
         return PKV_ERR_INVALID_ARG;
@@ -316,7 +381,8 @@ pkv_status pkv_reshape_and_cache(const void *k, const void *v, pkv_dtype in_dtyp
         return PKV_ERR_INVALID_ARG;
     return launch_reshape_and_cache(k, v, in_dtype, slot_mapping, num_tokens, num_kv_heads,
                                     head_dim, num_blocks, k_cache, v_cache, kv_dtype, k_scale,
-                                    v_scale, status, static_cast<cudaStream_t>(stream));
+                                    v_scale, k_head_scales, v_head_scales, status,
+                                    static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

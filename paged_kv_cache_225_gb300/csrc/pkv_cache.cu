@@ -14,7 +14,8 @@ __global__ void __launch_bounds__(256)
     reshape_and_cache_kernel(const void *k, const void *v, int in_dtype,
                              const int64_t *slot_mapping, int num_kv_heads, int head_dim,
                              int num_blocks, void *k_cache, void *v_cache, int kv_dtype,
-                             float k_scale, float v_scale, int32_t *status)
+                             float k_scale, float v_scale, const float *k_head_scale,
+                             const float *v_head_scale, int32_t *status)
 {
     const int i = blockIdx.x;
     const int64_t slot = __ldg(slot_mapping + i);
@@ -31,8 +32,11 @@ __global__ void __launch_bounds__(256)
     for (int e = threadIdx.x; e < n; e += blockDim.x) {
         const size_t src = static_cast<size_t>(i) * n + e;
         const size_t dst = (static_cast<size_t>(blk) * n + e) * kBlockSize + off;
-        store_kv(k_cache, kv_dtype, dst, k, in_dtype, src, k_scale);
-        store_kv(v_cache, kv_dtype, dst, v, in_dtype, src, v_scale);
+        const int h = e / head_dim;
+        const float ks = k_head_scale ? k_scale * __ldg(k_head_scale + h) : k_scale;
+        const float vs = v_head_scale ? v_scale * __ldg(v_head_scale + h) : v_scale;
+        store_kv(k_cache, kv_dtype, dst, k, in_dtype, src, ks);
+        store_kv(v_cache, kv_dtype, dst, v, in_dtype, src, vs);
     }
 }
 
@@ -40,7 +44,9 @@ pkv_status launch_reshape_and_cache(const void *k, const void *v, int in_dtype,
                                     const int64_t *slot_mapping, int num_tokens,
                                     int num_kv_heads, int head_dim, int num_blocks,
                                     void *k_cache, void *v_cache, int kv_dtype, float k_scale,
-                                    float v_scale, int32_t *status, cudaStream_t stream)
+                                    float v_scale, const float *k_head_scale,
+                                    const float *v_head_scale, int32_t *status,
+                                    cudaStream_t stream)
 {
     if (num_tokens <= 0)
         return PKV_OK;
@@ -48,7 +54,7 @@ pkv_status launch_reshape_and_cache(const void *k, const void *v, int in_dtype,
     const int threads = n >= 256 ? 256 : ((n + 31) / 32) * 32;
     reshape_and_cache_kernel<<<num_tokens, threads, 0, stream>>>(
         k, v, in_dtype, slot_mapping, num_kv_heads, head_dim, num_blocks, k_cache, v_cache,
-        kv_dtype, k_scale, v_scale, status);
+        kv_dtype, k_scale, v_scale, k_head_scale, v_head_scale, status);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

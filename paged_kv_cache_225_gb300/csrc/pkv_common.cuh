@@ -218,15 +218,6 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t code)
     return __half2float(__half(h));
 }
 
-// Two e4m3 codes of w (the bytes a byte_perm selector picks: low half from
-// selector nibble 0, high half from nibble 1) widened to an f16x2 word.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w, uint32_t sel)
-{
-    const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>(__byte_perm(w, 0u, sel));
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-}
-
 __device__ __forceinline__ void set_status(int *status, int code)
 {
     if (status)

@@ -132,6 +132,7 @@ struct SimtPolicy {
     };
     static constexpr bool kStaged = false;  // reads K/V straight from the stage
     static constexpr bool kSharedBegin = true;  // begin() writes the query to shared memory
+    static constexpr int kMinBlocks = 2;        // CTAs per SM the registers are bounded for
     struct Frags {};
     __device__ static void load(Frags &, const unsigned char *, const unsigned char *, int) {}
     __device__ static void compute(State &, Frags &, int, int, float) {}
@@ -466,6 +467,7 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
     static constexpr int KS = Base::KS, MT = Base::MT;
     static constexpr bool kStaged = Staged;
     static constexpr bool kSharedBegin = false;  // begin() only fills registers
+    static constexpr int kMinBlocks = 2;
 
     struct Frags {
         uint32_t k[KS][4];  // K^T A fragments, one per 16-wide k step
@@ -578,7 +580,16 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
 // byte_perm places it as the f16's high byte; e4m3: cvt.f16x2.e4m3x2).  Token order inside a fragment is
 // permuted consistently on both operands (see the byte selectors).  Staged
 // like the bf16 policy: 32 registers hold a page's raw codes.
-template <int D, int NT, int Budget = PKV_RING_BYTES_PER_WARP, bool Staged = false,
+// Ring bytes per warp and CTAs per SM of the fp8 item kernel (its pages are
+// half the bytes of bf16 pages, so more, smaller rings fit).
+#ifndef PKV_FP8_RING_BYTES_PER_WARP
+#define PKV_FP8_RING_BYTES_PER_WARP PKV_RING_BYTES_PER_WARP
+#endif
+#ifndef PKV_FP8_MIN_BLOCKS
+#define PKV_FP8_MIN_BLOCKS 2
+#endif
+
+template <int D, int NT, int Budget = PKV_FP8_RING_BYTES_PER_WARP, bool Staged = false,
           int KV = PKV_FP8_E5M2>
 struct MmaFp8Policy : MmaStateBase<D, NT> {
     using Base = MmaStateBase<D, NT>;
@@ -597,17 +608,23 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
     static constexpr int KS = Base::KS, MT = Base::MT;
     static constexpr bool kStaged = Staged;
     static constexpr bool kSharedBegin = false;  // begin() only fills registers
+    static constexpr int kMinBlocks = Staged ? 2 : PKV_FP8_MIN_BLOCKS;
     static constexpr uint32_t kSelEven = 0x2404u;  // bytes 0, 2 -> high bytes of two f16
     static constexpr uint32_t kSelOdd = 0x3414u;   // bytes 1, 3 -> high bytes of two f16
 
-    // Codes (bytes 0, 2) or (bytes 1, 3) of w as an f16x2 word: e5m2 is the
-    // high byte of the same binary16; e4m3 goes through the hardware convert.
+    // Codes (bytes 0, 2) or (bytes 1, 3) of w as an f16x2 word.  e5m2 is the
+    // high byte of the binary16 with the same value.  e4m3: the code's sign
+    // to bit 15 and its 7 exponent/mantissa bits to bits 13..7 make a binary16
+    // of exactly 2^-8 times the code's value, normal and subnormal codes alike
+    // (both formats have 3 ... 10 mantissa bits and biases 7 / 15); the host
+    // folds the 2^8 into the score and output scales (kE4m3Shift).
     __device__ static uint32_t widen(uint32_t w, bool odd)
     {
+        const uint32_t h = e5m2x2_to_f16x2(w, odd ? kSelOdd : kSelEven);  // codes in high bytes
         if constexpr (KV == PKV_FP8_E5M2)
-            return e5m2x2_to_f16x2(w, odd ? kSelOdd : kSelEven);
+            return h;
         else
-            return e4m3x2_to_f16x2(w, odd ? 0x4431u : 0x4420u);
+            return (h & 0x80008000u) | ((h >> 1) & 0x3f803f80u);
     }
 
     struct Frags {
@@ -757,10 +774,11 @@ __device__ __forceinline__ void write_new_token_from(const DecodeParams &p, int 
     const size_t dst0 = (static_cast<size_t>(phys) * p.num_kv_heads + hkv) * D;
     void *kc = const_cast<void *>(p.k_cache);
     void *vc = const_cast<void *>(p.v_cache);
+    const float kq = unit_k_quant(p, hkv), vq = unit_v_quant(p, hkv);
     for (int d = lane; d < D; d += 32) {
         const size_t g = (dst0 + d) * kBlockSize + t;
-        store_kv(kc, p.kv_dtype, g, buf, p.new_dtype, d, p.k_scale);
-        store_kv(vc, p.kv_dtype, g, buf + row_bytes, p.new_dtype, d, p.v_scale);
+        store_kv(kc, p.kv_dtype, g, buf, p.new_dtype, d, kq);
+        store_kv(vc, p.kv_dtype, g, buf + row_bytes, p.new_dtype, d, vq);
     }
     fence_proxy_async_all();
     __syncwarp();
@@ -801,13 +819,14 @@ __device__ __forceinline__ void write_token_rows(const DecodeParams &p, const in
                 break;
             const int t = (w[ee][2] - 1) % kBlockSize;
             const size_t dst0 = (static_cast<size_t>(w[ee][3]) * p.num_kv_heads + w[ee][1]) * D;
+            const float kq = unit_k_quant(p, w[ee][1]), vq = unit_v_quant(p, w[ee][1]);
 #pragma unroll
             for (int j = 0; j < kJ; ++j) {
                 const int d = lane + 32 * j;
                 if (d < D) {
                     const size_t g = (dst0 + d) * kBlockSize + t;
-                    store_kv_value(kc, p.kv_dtype, g, kv[x][j], p.k_scale);
-                    store_kv_value(vc, p.kv_dtype, g, vv[x][j], p.v_scale);
+                    store_kv_value(kc, p.kv_dtype, g, kv[x][j], kq);
+                    store_kv_value(vc, p.kv_dtype, g, vv[x][j], vq);
                 }
             }
         }
@@ -912,7 +931,7 @@ __device__ void merge_item(const DecodeParams &p, const unsigned char *smem, int
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
         const int h = hkv * G + g;
         if (nparts == 1) {
-            const float sc = inv * p.out_scale;
+            const float sc = inv * unit_out_scale(p, hkv);
             store_out4(p, D, s, h, q4, make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
         } else {
             const size_t row = (static_cast<size_t>(s) * p.num_q_heads + h) * p.max_parts + part;
@@ -927,7 +946,7 @@ __device__ void merge_item(const DecodeParams &p, const unsigned char *smem, int
 }
 
 template <class Pol>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(kThreads, Pol::kMinBlocks) decode_kernel(const DecodeParams p)
 {
     constexpr int D = Pol::kDim;
     static_assert((Pol::GP * D + 2 * Pol::GP) * 4 <= Pol::kRingBytes,
@@ -957,7 +976,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
     const int P = p.partition;
     const size_t tile_stride = static_cast<size_t>(Pol::kTileBytes);
     const size_t block_stride = static_cast<size_t>(Hkv) * tile_stride;
-    const float c = p.score_scale;
 
     uint32_t pages_done = 0;  // pages this warp has consumed (ring position / phase)
     // Warp 0 only: scan cursors of the two item phases and the phase-1 size.
@@ -1014,6 +1032,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
             break;
         const int s = s_item[0], part = s_item[1], hkv = s_item[2], L = s_item[3];
         const int nparts = s_item[4], item = s_item[5];
+        const float c = unit_score_scale(p, hkv);
 
         // ---------------------------------------------- this warp's pages
         const int t0 = part * P;

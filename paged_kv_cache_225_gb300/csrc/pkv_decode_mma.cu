@@ -19,7 +19,7 @@ static pkv_status dispatch(const DecodeParams &p, int kv_dtype, cudaStream_t str
         return two ? launch_any<MmaBf16Policy<D, 2>>(p, stream)
                    : launch_any<MmaBf16Policy<D, 1>>(p, stream);
     if (kv_dtype == PKV_FP8_E4M3) {
-        constexpr int kRing = PKV_RING_BYTES_PER_WARP;
+        constexpr int kRing = PKV_FP8_RING_BYTES_PER_WARP;
         return two ? launch_any<MmaFp8Policy<D, 2, kRing, false, PKV_FP8_E4M3>>(p, stream)
                    : launch_any<MmaFp8Policy<D, 1, kRing, false, PKV_FP8_E4M3>>(p, stream);
     }

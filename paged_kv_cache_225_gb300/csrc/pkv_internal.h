@@ -45,6 +45,10 @@ struct DecodeParams {
     int new_dtype;
     int kv_dtype;
     float k_scale, v_scale;
+    // Per-KV-head factors of fp8 caches ([num_kv_heads], device; null = 1):
+    // a code of head h stands for code * k_scale * k_head_scale[h].
+    const float *k_head_scale;
+    const float *v_head_scale;
 };
 
 // Paged attention of several query tokens per sequence (chunked prefill,
@@ -77,6 +81,10 @@ constexpr int kBlockSize = 16;
 
 // The 8-bit KV dtypes (value = code * scale).
 constexpr bool is_fp8(int dtype) { return dtype == PKV_FP8_E5M2 || dtype == PKV_FP8_E4M3; }
+
+// The tensor-core e4m3 policy widens a code to a binary16 holding 2^-8 times
+// its value; the host multiplies the score and output scales by 2^8.
+constexpr float kE4m3Shift = 256.0f;
 constexpr size_t kWorkspaceHeader = 256;
 constexpr int kStreamKMaxCtas = 1024;  // partial slots of the stream-K schedule
 
@@ -94,7 +102,9 @@ pkv_status launch_reshape_and_cache(const void *k, const void *v, int in_dtype,
                                     const int64_t *slot_mapping, int num_tokens,
                                     int num_kv_heads, int head_dim, int num_blocks,
                                     void *k_cache, void *v_cache, int kv_dtype, float k_scale,
-                                    float v_scale, int32_t *status, cudaStream_t stream);
+                                    float v_scale, const float *k_head_scale,
+                                    const float *v_head_scale, int32_t *status,
+                                    cudaStream_t stream);
 
 pkv_status launch_copy_blocks(void *k_cache, void *v_cache, size_t block_bytes,
                               const int32_t *pairs, int num_pairs, int num_blocks,

@@ -25,6 +25,26 @@ __device__ __forceinline__ int clamp_len(const DecodeParams &p, int L)
     return L;
 }
 
+// Score scale (log2 domain) and output scale of the units of KV head hkv:
+// the per-head factors of an fp8 cache multiply the per-tensor ones.
+__device__ __forceinline__ float unit_score_scale(const DecodeParams &p, int hkv)
+{
+    return p.k_head_scale ? p.score_scale * __ldg(p.k_head_scale + hkv) : p.score_scale;
+}
+__device__ __forceinline__ float unit_out_scale(const DecodeParams &p, int hkv)
+{
+    return p.v_head_scale ? p.out_scale * __ldg(p.v_head_scale + hkv) : p.out_scale;
+}
+// The divisors the fused cache write quantises head hkv's new rows with.
+__device__ __forceinline__ float unit_k_quant(const DecodeParams &p, int hkv)
+{
+    return p.k_head_scale ? p.k_scale * __ldg(p.k_head_scale + hkv) : p.k_scale;
+}
+__device__ __forceinline__ float unit_v_quant(const DecodeParams &p, int hkv)
+{
+    return p.v_head_scale ? p.v_scale * __ldg(p.v_head_scale + hkv) : p.v_scale;
+}
+
 // Partitions of a sequence of L tokens (an empty sequence still has one item,
 // which writes its zero row).
 __device__ __forceinline__ int parts_of(int L, int P) { return L > P ? (L + P - 1) / P : 1; }
@@ -76,7 +96,7 @@ __device__ void merge_partials(const DecodeParams &p, int s, int hkv, int nparts
             acc.z += w * o.z;
             acc.w += w * o.w;
         }
-        const float sc = (wsum > 0.f ? 1.f / wsum : 0.f) * p.out_scale;
+        const float sc = (wsum > 0.f ? 1.f / wsum : 0.f) * unit_out_scale(p, hkv);
         store_out4(p, D, s, h, q4, make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
     }
 }

@@ -105,7 +105,7 @@ __device__ void merge_streamk_partials(const DecodeParams &p, int s, int hkv, lo
             acc.z += w * o.z;
             acc.w += w * o.w;
         }
-        const float sc = (wsum > 0.f ? 1.f / wsum : 0.f) * p.out_scale;
+        const float sc = (wsum > 0.f ? 1.f / wsum : 0.f) * unit_out_scale(p, hkv);
         store_out4(p, D, s, hkv * G + g, q4,
                    make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
     }
@@ -143,7 +143,7 @@ __device__ void merge_segment(const DecodeParams &p, const float *scratch, int s
         }
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
         if (complete) {
-            const float sc = inv * p.out_scale;
+            const float sc = inv * unit_out_scale(p, hkv);
             store_out4(p, D, s, hkv * G + g, q4,
                        make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
         } else {
@@ -265,7 +265,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
 
     const size_t tile_stride = static_cast<size_t>(Pol::kTileBytes);
     const size_t block_stride = static_cast<size_t>(Hkv) * tile_stride;
-    const float c = p.score_scale;
 
     // ---------------------------------------------- issue side (per warp)
     // This warp's pages are global pages a + warp + 4i, ring position i.
@@ -372,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
     Pol::begin(st, p, su.s, su.hkv, lane, extra);
     __syncthreads();  // policy shared data (SIMT query) is ready
     for (int k = 0;; ++k) {
+        const float c = unit_score_scale(p, su.hkv);
         const long long lo = su.off > a ? su.off : a;
         const long long hi = (su.off + su.np < b) ? su.off + su.np : b;
         const bool complete = (lo == su.off) && (hi == su.off + su.np);

@@ -251,3 +251,21 @@ def _copy(**kw):
 ])
 def test_copy_blocks_argument_errors(kw, code):
     assert _copy(**kw) == code
+
+
+def test_head_scaled_entries_reject_non_fp8_and_missing_scales():
+    L = pkv.lib()
+    args = [0x1000, BF16, 0x2000, 0x3000, BF16, 0x4000, 0x4100, 0x5000, 0x6000, 2, 8, 2, 128, 16,
+            10, 4, 64, 0.1, 0x7000, F32, 0x8000, 1 << 26, 0, 0, None]
+    assert L.pkv_paged_attn_decode_head_scaled(*args) == UNSUPPORTED
+    args[4] = FP8
+    args[5] = None
+    assert L.pkv_paged_attn_decode_head_scaled(*args) == INVALID
+    args[5] = 0x4002                                  # misaligned scales
+    assert L.pkv_paged_attn_decode_head_scaled(*args) == INVALID
+    r = [0x1000, 0x2000, BF16, 0x3000, 4, 2, 128, 16, 8, 0x4000, 0x5000, BF16, 0x6000, 0x6100,
+         None, None]
+    assert L.pkv_reshape_and_cache_head_scaled(*r) == UNSUPPORTED
+    r[11] = FP8
+    r[12] = None
+    assert L.pkv_reshape_and_cache_head_scaled(*r) == INVALID

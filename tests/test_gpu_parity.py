@@ -349,3 +349,57 @@ def test_bounded_wait_reports_timeout_and_context_survives(part):
     ref = oracle.paged_decode(w.q, w.cfg.q_dtype, w.k_cache, w.v_cache, w.cfg.kv_dtype,
                               w.block_tables, w.seq_lens, w.scale)
     assert status == 0 and max_abs(out2, ref) <= 4e-3
+
+
+# ------------------------------------------------------ per-head fp8 scales
+
+@pytest.mark.parametrize("kv_dtype", [W.FP8_E5M2, W.FP8_E4M3])
+@pytest.mark.parametrize("impl", ["auto", "simt"])
+@pytest.mark.parametrize("part", [0, -2, -1, 64])
+def test_per_head_scaled_decode(kv_dtype, impl, part):
+    w = _custom(num_seqs=6, num_q_heads=16, num_kv_heads=4, kv_dtype=kv_dtype, garbage="nan",
+                lens=np.array([1, 17, 300, 45, 0, 1000]), seed=41)
+    ks = np.array([0.5, 2.0, 0.125, 1.0], np.float32)
+    vs = np.array([4.0, 0.25, 1.0, 0.5], np.float32)
+    ref = oracle.paged_decode(w.q, w.cfg.q_dtype, w.k_cache, w.v_cache, kv_dtype, w.block_tables,
+                              w.seq_lens, w.scale, k_head_scales=ks, v_head_scales=vs)
+    d = device_workload(w, DEV)
+    out = torch.empty(d["q"].shape, dtype=torch.float32, device=DEV)
+    pkv.paged_attn_decode_head_scaled(d["q"], d["k_cache"], d["v_cache"],
+                                      torch.from_numpy(ks).to(DEV), torch.from_numpy(vs).to(DEV),
+                                      d["block_tables"], d["seq_lens"], w.scale, out,
+                                      max_seq_len=1000, partition_tokens=part, impl=impl)
+    torch.cuda.synchronize()
+    assert pkv.read_status(device=DEV) == 0
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    # Outputs scale with v: compare relative to each head's factor.
+    G = 4
+    for h in range(4):
+        err = max_abs(got[:, h * G:(h + 1) * G] / vs[h], ref[:, h * G:(h + 1) * G] / vs[h])
+        assert err <= TOL[kv_dtype], (h, err)
+
+
+@pytest.mark.parametrize("kv_dtype", [W.FP8_E5M2, W.FP8_E4M3])
+@pytest.mark.parametrize("in_dtype", [W.F32, W.BF16])
+def test_per_head_scaled_cache_write_is_bit_exact(kv_dtype, in_dtype):
+    rng = np.random.default_rng(42)
+    N, Hkv, D, B, T = 30, 4, 128, 16, 61
+    ks = np.array([0.5, 2.0, 0.1, 8.0], np.float32)
+    vs = np.array([0.25, 1.0, 3.0, 0.05], np.float32)
+    k_cache = np.zeros((N, Hkv, D, B), np.uint8)
+    v_cache = np.zeros_like(k_cache)
+    kin = W.round_to_storage(rng.standard_normal((T, Hkv, D)).astype(np.float32) * 6, in_dtype)
+    vin = W.round_to_storage(rng.standard_normal((T, Hkv, D)).astype(np.float32), in_dtype)
+    slots = rng.choice(N * B, size=T, replace=False).astype(np.int64)
+    kc, vc = k_cache.copy(), v_cache.copy()
+    assert oracle.reshape_and_cache(kin, vin, in_dtype, slots, kc, vc, kv_dtype,
+                                    k_head_scales=ks, v_head_scales=vs) == 0
+    dk, dv = to_torch(k_cache, kv_dtype).to(DEV), to_torch(v_cache, kv_dtype).to(DEV)
+    pkv.reshape_and_cache_head_scaled(to_torch(kin, in_dtype).to(DEV),
+                                      to_torch(vin, in_dtype).to(DEV),
+                                      torch.from_numpy(slots).to(DEV), dk, dv,
+                                      torch.from_numpy(ks).to(DEV), torch.from_numpy(vs).to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(dk), kc.view(np.uint8).reshape(-1))
+    assert np.array_equal(bits(dv), vc.view(np.uint8).reshape(-1))
