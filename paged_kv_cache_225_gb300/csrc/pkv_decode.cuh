@@ -580,13 +580,16 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
 // byte_perm places it as the f16's high byte; e4m3: cvt.f16x2.e4m3x2).  Token order inside a fragment is
 // permuted consistently on both operands (see the byte selectors).  Staged
 // like the bf16 policy: 32 registers hold a page's raw codes.
-// Ring bytes per warp and CTAs per SM of the fp8 item kernel (its pages are
-// half the bytes of bf16 pages, so more, smaller rings fit).
+// Ring bytes per warp and CTAs per SM of the fp8 item kernel.  Its pages are
+// half the bytes of bf16 pages and it is bound by pages per second rather
+// than bytes, so four CTAs with three 4 KB stages per warp (registers capped
+// at 128, no spills) beat three CTAs with four stages: measured on GB300,
+// fp8 chat layer 34.7 -> 29.8 us, 70B e4m3 layer 171 -> 160 us.
 #ifndef PKV_FP8_RING_BYTES_PER_WARP
-#define PKV_FP8_RING_BYTES_PER_WARP PKV_RING_BYTES_PER_WARP
+#define PKV_FP8_RING_BYTES_PER_WARP (12 * 1024)
 #endif
 #ifndef PKV_FP8_MIN_BLOCKS
-#define PKV_FP8_MIN_BLOCKS 2
+#define PKV_FP8_MIN_BLOCKS 4
 #endif
 
 template <int D, int NT, int Budget = PKV_FP8_RING_BYTES_PER_WARP, bool Staged = false,
@@ -608,7 +611,9 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
     static constexpr int KS = Base::KS, MT = Base::MT;
     static constexpr bool kStaged = Staged;
     static constexpr bool kSharedBegin = false;  // begin() only fills registers
-    static constexpr int kMinBlocks = Staged ? 2 : PKV_FP8_MIN_BLOCKS;
+    // Two N tiles (more than 8 heads per KV head) need more registers than
+    // four CTAs per SM leave: three there.
+    static constexpr int kMinBlocks = Staged ? 2 : (NT == 1 ? PKV_FP8_MIN_BLOCKS : 3);
     static constexpr uint32_t kSelEven = 0x2404u;  // bytes 0, 2 -> high bytes of two f16
     static constexpr uint32_t kSelOdd = 0x3414u;   // bytes 1, 3 -> high bytes of two f16
 

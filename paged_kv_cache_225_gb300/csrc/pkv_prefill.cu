@@ -196,13 +196,15 @@ __device__ __forceinline__ bool causal_update(const float (&sacc)[4], int tokA, 
 
 // One page for one warp's 16 rows: scores, causal softmax, P V.  `lim` holds
 // the visible-token count of the page for each of the lane's four row columns.
-template <int D>
+// NT = 1 when the tile's rows all sit in its first 8-row N tile (the second
+// tile's state then stays empty).
+template <int D, int NT>
 __device__ __forceinline__ void prefill_page(typename MmaStateBase<D, 2>::State &st,
                                              typename MmaBf16Policy<D, 2>::Frags &f, int valid,
                                              const int (&lim)[2][2], int lane, float c)
 {
     using Base = MmaStateBase<D, 2>;
-    constexpr int KS = Base::KS, MT = Base::MT, NT = 2;
+    constexpr int KS = Base::KS, MT = Base::MT;
     const int r = lane >> 2, cc = lane & 3;
     float sacc[NT][4], sodd[NT][4];
 #pragma unroll
@@ -365,6 +367,7 @@ __global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
         typename Base::State st;
         Base::reset(st);
         const int tile0 = row0 + rt * kRowTile;  // first row of the warp's tile
+        const bool two_tiles = nrows - rt * kRowTile > 8;  // rows in the second N tile
         int pos[2][2];
         {
             const int r = lane >> 2, cc = lane & 3;
@@ -493,7 +496,10 @@ __global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
                         const int v = pos[n][e] - tb + 1;
                         lim[n][e] = v < valid ? v : valid;
                     }
-                prefill_page<D>(st, f, valid, lim, lane, c);
+                if (two_tiles)
+                    prefill_page<D, 2>(st, f, valid, lim, lane, c);
+                else
+                    prefill_page<D, 1>(st, f, valid, lim, lane, c);
             }
         }
         // Warp 0 issues whatever the other warps still wait for.
