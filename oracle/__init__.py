@@ -26,7 +26,7 @@ _LIB_PATH = os.path.join(_BUILD, "libpkv_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, BF16, FP8_E5M2, FP8_E4M3 = 0, 1, 2, 3
+F32, BF16, FP8_E5M2, FP8_E4M3, INT4 = 0, 1, 2, 3, 4
 
 
 def build(force: bool = False) -> str:
@@ -94,29 +94,45 @@ def max_threads() -> int:
 
 
 def decode_values(bits: np.ndarray, dtype: int) -> np.ndarray:
-    """Widen stored elements to float64 with the oracle's own decoders."""
+    """Widen stored elements to float64 with the oracle's own decoders.
+
+    INT4 storage holds two elements per byte: the result has twice the last
+    dimension.
+    """
     bits = np.ascontiguousarray(bits)
-    out = np.empty(bits.size, dtype=np.float64)
-    _load().pkvo_decode_values(_ptr(bits), dtype, bits.size, _ptr(out, ctypes.c_double))
-    return out.reshape(bits.shape)
+    n = bits.size * (2 if dtype == INT4 else 1)
+    out = np.empty(n, dtype=np.float64)
+    _load().pkvo_decode_values(_ptr(bits), dtype, n, _ptr(out, ctypes.c_double))
+    shape = bits.shape[:-1] + (bits.shape[-1] * 2,) if dtype == INT4 else bits.shape
+    return out.reshape(shape)
 
 
 def encode_values(x: np.ndarray, dtype: int, scale: float = 1.0) -> np.ndarray:
     """Encode float32 values to a stored dtype with the oracle's own encoders."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     storage = {F32: np.float32, BF16: np.uint16, FP8_E5M2: np.uint8,
-               FP8_E4M3: np.uint8}[dtype]
-    out = np.empty(x.shape, dtype=storage)
+               FP8_E4M3: np.uint8, INT4: np.uint8}[dtype]
+    if dtype == INT4:
+        assert x.shape[-1] % 2 == 0, "INT4 packs pairs along the last axis"
+        out = np.zeros(x.shape[:-1] + (x.shape[-1] // 2,), dtype=storage)
+    else:
+        out = np.empty(x.shape, dtype=storage)
     rc = _load().pkvo_encode_values(_ptr(x, ctypes.c_float), x.size, dtype, scale, _ptr(out))
     if rc:
         raise ValueError(f"encode_values failed ({rc})")
     return out
 
 
+def _pool_dims(cache, kv_dtype):
+    """(N, Hkv, D, block_size) of a cache array (INT4 holds two tokens per byte)."""
+    N, Hkv, D, B = cache.shape
+    return N, Hkv, D, (2 * B if kv_dtype == INT4 else B)
+
+
 def _attn_args(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_lens, scale,
                k_scale, v_scale):
     S, Hq, D = q.shape
-    N, Hkv, D2, B = k_cache.shape
+    N, Hkv, D2, B = _pool_dims(k_cache, kv_dtype)
     assert D2 == D and v_cache.shape == k_cache.shape
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
@@ -186,7 +202,7 @@ def paged_prefill(q, q_dtype, q_start, k_cache, v_cache, kv_dtype, block_tables,
     ``seq_lens[s]`` cached tokens.
     """
     T, Hq, D = q.shape
-    N, Hkv, D2, B = k_cache.shape
+    N, Hkv, D2, B = _pool_dims(k_cache, kv_dtype)
     assert D2 == D and v_cache.shape == k_cache.shape
     qs = np.ascontiguousarray(q_start, dtype=np.int32)
     bt = np.ascontiguousarray(block_tables, dtype=np.int32)
@@ -215,7 +231,7 @@ def reshape_and_cache(k, v, in_dtype, slot_mapping, k_cache, v_cache, kv_dtype,
     multiply the quantisation scale of each KV head.
     """
     T, Hkv, D = k.shape
-    N, Hkv2, D2, B = k_cache.shape
+    N, Hkv2, D2, B = _pool_dims(k_cache, kv_dtype)
     assert Hkv2 == Hkv and D2 == D and v.shape == k.shape
     assert k_cache.flags["C_CONTIGUOUS"] and v_cache.flags["C_CONTIGUOUS"]
     k = np.ascontiguousarray(k)

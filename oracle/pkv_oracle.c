@@ -12,8 +12,9 @@
  *    bits with bias 15, 2 mantissa bits; exponent 0 is subnormal, 31 is
  *    Inf/NaN); fp8-e4m3 (1 sign bit, 4 exponent bits with bias 7, 3 mantissa
  *    bits; exponent 0 is subnormal, no infinities, the all-ones code is NaN,
- *    largest magnitude 448).  fp8 values are multiplied by the per-tensor
- *    dequant scale.
+ *    largest magnitude 448); INT4 (signed 4-bit integers, two per byte, the
+ *    even element in the low nibble).  fp8 and INT4 values are multiplied by
+ *    the per-tensor dequant scale (and an optional per-KV-head factor).
  *
  *  - Paged decode attention ("vLLM e PagedAttention: serving high-throughput",
  *    the simplified PagedAttention CUDA-kernel pseudocode; "Inference
@@ -46,7 +47,8 @@
  *    offset slot % B of every KV head.  Values are converted with this file's
  *    own encoders: float32 -> bf16 round-to-nearest-even; float32 ->
  *    fp8-e5m2 as RNE(x / scale) in float32 with saturation to +-57344;
- *    float32 -> fp8-e4m3 the same with saturation to +-448.
+ *    float32 -> fp8-e4m3 the same with saturation to +-448; float32 -> INT4
+ *    as RNE(x / scale) clamped to -8..7 (NaN -> 0).
  */
 #include <math.h>
 #include <stddef.h>
@@ -57,7 +59,7 @@
 #include <omp.h>
 #endif
 
-enum { PKVO_F32 = 0, PKVO_BF16 = 1, PKVO_FP8_E5M2 = 2, PKVO_FP8_E4M3 = 3 };
+enum { PKVO_F32 = 0, PKVO_BF16 = 1, PKVO_FP8_E5M2 = 2, PKVO_FP8_E4M3 = 3, PKVO_INT4 = 4 };
 
 /* ------------------------------------------------------------------ decoders */
 
@@ -109,6 +111,17 @@ static double e4m3_value(uint8_t code)
     return sign ? -mag : mag;
 }
 
+/* INT4: a signed 4-bit integer (two's complement, -8..7).  Two elements share
+ * a byte: element i is the low nibble of byte i / 2 when i is even, the high
+ * nibble when it is odd (in the [.., 16] page layout: tokens 2j and 2j+1 of
+ * a row share byte j). */
+static double int4_value(const void *base, size_t i)
+{
+    uint8_t byte = ((const uint8_t *)base)[i >> 1];
+    int nib = (i & 1) ? (byte >> 4) : (byte & 0xf);
+    return (double)(nib >= 8 ? nib - 16 : nib);
+}
+
 static double elem_value(const void *base, int dtype, size_t i)
 {
     switch (dtype) {
@@ -126,6 +139,8 @@ static double elem_value(const void *base, int dtype, size_t i)
         return e5m2_value(((const uint8_t *)base)[i]);
     case PKVO_FP8_E4M3:
         return e4m3_value(((const uint8_t *)base)[i]);
+    case PKVO_INT4:
+        return int4_value(base, i);
     default:
         return NAN;
     }
@@ -221,6 +236,30 @@ static uint8_t e4m3_encode_rne_satfinite(float x)
     return sign | (uint8_t)(((e + 7) << 3) | ((int)n - 8));
 }
 
+/* Round to the nearest integer, ties to even, clamped to -8..7; NaN gives 0. */
+static int int4_encode_rne(float x)
+{
+    if (isnan(x))
+        return 0;
+    double a = (double)x;
+    if (a >= 7.0)
+        return 7;
+    if (a <= -8.0)
+        return -8;
+    double r = (a >= 0) ? round_half_even(a) : -round_half_even(-a);
+    return (int)r;
+}
+
+static void int4_store(void *base, size_t i, int q)
+{
+    uint8_t *b = (uint8_t *)base + (i >> 1);
+    uint8_t nib = (uint8_t)(q & 0xf);
+    if (i & 1)
+        *b = (uint8_t)((*b & 0x0f) | (nib << 4));
+    else
+        *b = (uint8_t)((*b & 0xf0) | nib);
+}
+
 /* ------------------------------------------------------- exported decoders */
 
 /* Widen n stored elements of `dtype` to double (no scale applied). */
@@ -255,6 +294,9 @@ int pkvo_encode_values(const float *src, size_t n, int dtype, float scale, void 
             ((uint8_t *)dst)[i] = e4m3_encode_rne_satfinite(xs);
             break;
         }
+        case PKVO_INT4:
+            int4_store(dst, i, int4_encode_rne(x / scale));
+            break;
         default:
             return 1;
         }
@@ -290,7 +332,8 @@ static size_t cache_index(const pkvo_problem *P, int32_t blk, int hkv, int d, in
 static int gather_rows(const pkvo_problem *P, int s, int hkv, int L, double *K, double *V)
 {
     const int D = P->head_dim, B = P->block_size;
-    const int fp8 = P->kv_dtype == PKVO_FP8_E5M2 || P->kv_dtype == PKVO_FP8_E4M3;
+    const int fp8 = P->kv_dtype == PKVO_FP8_E5M2 || P->kv_dtype == PKVO_FP8_E4M3 ||
+                    P->kv_dtype == PKVO_INT4;
     double ks = fp8 ? P->k_scale : 1.0;
     double vs = fp8 ? P->v_scale : 1.0;
     if (fp8 && P->k_head_scales)
@@ -637,7 +680,7 @@ int pkvo_reshape_and_cache_head_scaled(const void *k, const void *v, int in_dtyp
     if (in_dtype != PKVO_F32 && in_dtype != PKVO_BF16)
         return 5;
     if (kv_dtype != PKVO_F32 && kv_dtype != PKVO_BF16 && kv_dtype != PKVO_FP8_E5M2 &&
-        kv_dtype != PKVO_FP8_E4M3)
+        kv_dtype != PKVO_FP8_E4M3 && kv_dtype != PKVO_INT4)
         return 5;
     int rc = 0;
     for (int i = 0; i < num_tokens; ++i) {
@@ -669,6 +712,9 @@ int pkvo_reshape_and_cache_head_scaled(const void *k, const void *v, int in_dtyp
                 } else if (kv_dtype == PKVO_FP8_E5M2) {
                     ((uint8_t *)k_cache)[dst] = e5m2_encode_rne_satfinite(kx / ksh);
                     ((uint8_t *)v_cache)[dst] = e5m2_encode_rne_satfinite(vx / vsh);
+                } else if (kv_dtype == PKVO_INT4) {
+                    int4_store(k_cache, dst, int4_encode_rne(kx / ksh));
+                    int4_store(v_cache, dst, int4_encode_rne(vx / vsh));
                 } else {
                     ((uint8_t *)k_cache)[dst] = e4m3_encode_rne_satfinite(kx / ksh);
                     ((uint8_t *)v_cache)[dst] = e4m3_encode_rne_satfinite(vx / vsh);

@@ -30,11 +30,14 @@ from typing import Optional
 import numpy as np
 import torch
 
-F32, BF16, FP8_E5M2, FP8_E4M3 = 0, 1, 2, 3
-DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_E5M2: "fp8_e5m2", FP8_E4M3: "fp8_e4m3"}
-ELEM_BYTES = {F32: 4, BF16: 2, FP8_E5M2: 1, FP8_E4M3: 1}
-NP_STORAGE = {F32: np.float32, BF16: np.uint16, FP8_E5M2: np.uint8, FP8_E4M3: np.uint8}
+F32, BF16, FP8_E5M2, FP8_E4M3, INT4 = 0, 1, 2, 3, 4
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", FP8_E5M2: "fp8_e5m2", FP8_E4M3: "fp8_e4m3",
+               INT4: "int4"}
+ELEM_BYTES = {F32: 4, BF16: 2, FP8_E5M2: 1, FP8_E4M3: 1, INT4: 0.5}
+NP_STORAGE = {F32: np.float32, BF16: np.uint16, FP8_E5M2: np.uint8, FP8_E4M3: np.uint8,
+              INT4: np.uint8}
 FP8 = (FP8_E5M2, FP8_E4M3)
+SCALED = (FP8_E5M2, FP8_E4M3, INT4)   # stored codes times a dequant scale
 
 
 @dataclasses.dataclass(frozen=True)
@@ -135,6 +138,12 @@ def round_to_storage(x: np.ndarray, dtype: int) -> np.ndarray:
     if dtype == FP8_E4M3:
         # Clamp first: saturating to the largest finite value (448).
         return t.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    if dtype == INT4:
+        # Round half to even, clamp to -8..7 (NaN -> 0), pack pairs along the
+        # last axis: even element in the low nibble.
+        qv = np.clip(np.rint(np.nan_to_num(x, nan=0.0, posinf=7.0, neginf=-8.0)), -8, 7)
+        nib = (qv.astype(np.int8).astype(np.uint8) & 0xF)
+        return (nib[..., 0::2] | (nib[..., 1::2] << 4)).astype(np.uint8)
     raise ValueError(f"unknown dtype {dtype}")
 
 
@@ -151,6 +160,14 @@ def storage_to_float32(x: np.ndarray, dtype: int) -> np.ndarray:
     if dtype == FP8_E4M3:
         t = torch.from_numpy(np.ascontiguousarray(x)).view(torch.float8_e4m3fn)
         return t.float().numpy()
+    if dtype == INT4:
+        b = np.ascontiguousarray(x, dtype=np.uint8)
+        lo = (b & 0xF).astype(np.int16)
+        hi = (b >> 4).astype(np.int16)
+        out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), dtype=np.float32)
+        out[..., 0::2] = np.where(lo >= 8, lo - 16, lo)
+        out[..., 1::2] = np.where(hi >= 8, hi - 16, hi)
+        return out
     raise ValueError(f"unknown dtype {dtype}")
 
 
@@ -179,11 +196,13 @@ def _normal_pool(rng: np.random.Generator, shape, chunk: int = 1 << 24) -> np.nd
 
 def _pool_to_storage(pool_f32: np.ndarray, dtype: int, chunk: int = 1 << 24) -> np.ndarray:
     flat = pool_f32.reshape(-1)
-    out = np.empty(flat.size, dtype=NP_STORAGE[dtype])
-    for lo in range(0, flat.size, chunk):
+    per = 2 if dtype == INT4 else 1          # elements per stored byte
+    out = np.empty(flat.size // per, dtype=NP_STORAGE[dtype])
+    for lo in range(0, flat.size, chunk):    # chunk is even: INT4 pairs stay together
         hi = min(flat.size, lo + chunk)
-        out[lo:hi] = round_to_storage(flat[lo:hi], dtype)
-    return out.reshape(pool_f32.shape)
+        out[lo // per:hi // per] = round_to_storage(flat[lo:hi], dtype)
+    shape = pool_f32.shape[:-1] + (pool_f32.shape[-1] // per,)
+    return out.reshape(shape)
 
 
 def make_workload(cfg: DecodeConfig | str, seed: Optional[int] = None,
@@ -265,7 +284,7 @@ def make_workload(cfg: DecodeConfig | str, seed: Optional[int] = None,
                 owned[tables[s, j], :valid] = True
         k_pool[np.broadcast_to(~owned[:, None, None, :], k_pool.shape)] = np.nan
         v_pool[np.broadcast_to(~owned[:, None, None, :], v_pool.shape)] = np.nan
-    if cfg.kv_dtype in FP8 and cfg.kv_scale != 1.0:
+    if cfg.kv_dtype in SCALED and cfg.kv_scale != 1.0:
         k_pool /= np.float32(cfg.kv_scale)
         v_pool /= np.float32(cfg.kv_scale)
     k_cache = _pool_to_storage(k_pool, cfg.kv_dtype)

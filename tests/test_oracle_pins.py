@@ -17,7 +17,7 @@ import torch
 import oracle
 from paged_kv_cache_225_gb300 import workloads as W
 
-F32, BF16, FP8, E4M3 = W.F32, W.BF16, W.FP8_E5M2, W.FP8_E4M3
+F32, BF16, FP8, E4M3, INT4 = W.F32, W.BF16, W.FP8_E5M2, W.FP8_E4M3, W.INT4
 
 
 # ----------------------------------------------------------------- decoders
@@ -188,7 +188,7 @@ def _dense_kv(p):
     """Contiguous per-sequence K/V [Hkv, L, D] by numpy indexing, in float64."""
     k = W.storage_to_float32(p["k_cache"], p["kv_dtype"]).astype(np.float64)
     v = W.storage_to_float32(p["v_cache"], p["kv_dtype"]).astype(np.float64)
-    if p["kv_dtype"] in (FP8, E4M3):
+    if p["kv_dtype"] in (FP8, E4M3, INT4):
         k, v = k * p["k_scale"], v * p["v_scale"]
     out = []
     B = k.shape[3]
@@ -479,3 +479,65 @@ def test_reshape_with_per_head_scales_matches_numpy(kv_dtype):
             ek[blk, h, :, off] = W.round_to_storage((kin[i, h] / kd).astype(np.float32), kv_dtype)
             ev[blk, h, :, off] = W.round_to_storage((vin[i, h] / vd).astype(np.float32), kv_dtype)
     assert np.array_equal(kc, ek) and np.array_equal(vc, ev)
+
+
+# ------------------------------------------------------------------ INT4 KV
+
+def test_int4_codes_decode_to_signed_nibbles():
+    b = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_values(b, INT4)
+    assert got.shape == (512,)
+    lo, hi = got[0::2], got[1::2]
+    assert np.array_equal(lo, [((x & 15) ^ 8) - 8 for x in range(256)])
+    assert np.array_equal(hi, [((x >> 4) ^ 8) - 8 for x in range(256)])
+    assert np.array_equal(got, W.storage_to_float32(b, INT4).astype(np.float64))
+
+
+def test_int4_encode_rounds_half_even_and_clamps():
+    x = np.array([0.0, 0.5, 1.5, 2.5, -0.5, -1.5, -2.5, 6.49, 6.5, 7.5, 100.0, -7.5, -8.5,
+                  -100.0, np.nan, 3.25], dtype=np.float32)
+    got = oracle.encode_values(x, INT4)
+    ref = np.array([0, 0, 2, 2, 0, -2, -2, 6, 6, 7, 7, -8, -8, -8, 0, 3], np.float64)
+    assert np.array_equal(oracle.decode_values(got, INT4), ref)
+    assert np.array_equal(got, W.round_to_storage(x, INT4))
+    # The scale divides first (float32); every code round-trips.
+    y = np.random.default_rng(50).standard_normal(4096).astype(np.float32) * 3
+    for s in (0.5, 0.37):
+        got = oracle.encode_values(y, INT4, scale=s)
+        assert np.array_equal(got, W.round_to_storage((y / np.float32(s)).astype(np.float32),
+                                                      INT4))
+    codes = np.arange(256, dtype=np.uint8)
+    assert np.array_equal(oracle.encode_values(oracle.decode_values(codes, INT4)
+                                               .astype(np.float32), INT4), codes)
+
+
+@pytest.mark.parametrize("identity", [True, False])
+def test_int4_paged_equals_dense_sdpa(identity):
+    p = _tiny_problem(INT4, BF16, identity=identity, kv_scale=0.5)
+    got = _run(p)
+    qd = W.storage_to_float32(p["q"], BF16).astype(np.float64)
+    G = qd.shape[1] // p["k_cache"].shape[1]
+    for s, (ks, vs) in enumerate(_dense_kv(p)):
+        for h in range(qd.shape[1]):
+            ref = _numpy_sdpa(qd[s, h], ks[h // G], vs[h // G], p["scale"])
+            np.testing.assert_allclose(got[s, h], ref, rtol=0, atol=1e-12)
+
+
+def test_int4_cache_write_matches_numpy_scatter():
+    rng = np.random.default_rng(51)
+    N, Hkv, D, B, T = 9, 3, 16, 16, 11
+    kc = W.round_to_storage(rng.standard_normal((N, Hkv, D, B)).astype(np.float32) * 3, INT4)
+    vc = W.round_to_storage(rng.standard_normal((N, Hkv, D, B)).astype(np.float32) * 3, INT4)
+    kin = rng.standard_normal((T, Hkv, D)).astype(np.float32) * 2
+    vin = rng.standard_normal((T, Hkv, D)).astype(np.float32) * 2
+    slots = rng.choice(N * B, size=T, replace=False).astype(np.int64)
+    k2, v2 = kc.copy(), vc.copy()
+    assert oracle.reshape_and_cache(kin, vin, F32, slots, k2, v2, INT4, 0.5, 0.25) == 0
+    ek = W.storage_to_float32(kc, INT4)
+    ev = W.storage_to_float32(vc, INT4)
+    for i, slot in enumerate(slots):
+        blk, off = divmod(int(slot), B)
+        ek[blk, :, :, off] = np.clip(np.rint(kin[i] / np.float32(0.5)), -8, 7)
+        ev[blk, :, :, off] = np.clip(np.rint(vin[i] / np.float32(0.25)), -8, 7)
+    assert np.array_equal(k2, W.round_to_storage(ek, INT4))
+    assert np.array_equal(v2, W.round_to_storage(ev, INT4))
