@@ -41,7 +41,8 @@ from paged_kv_cache_225_gb300.metrics import algorithmic_bytes, prefill_algorith
 
 METRIC = "decode-attn KV GB/s & tokens/s on 1 GB300, % of HBM peak (70B-shape layer)"
 FALLBACK_HBM_GBS = 6800.0
-DTYPE_NAME = {W.F32: "f32", W.BF16: "bf16", W.FP8_E5M2: "fp8_e5m2", W.FP8_E4M3: "fp8_e4m3"}
+DTYPE_NAME = {W.F32: "f32", W.BF16: "bf16", W.FP8_E5M2: "fp8_e5m2", W.FP8_E4M3: "fp8_e4m3",
+              W.INT4: "int4"}
 CONFIG_TEXT = {
     "tiny_fp32": "tiny fp32 decode: 4 seqs, 4 q/4 kv heads, D=64, lengths U[1,64]",
     "llama3_8b": "Llama-3-8B-shaped decode layer: 64 seqs, 32 q/8 kv heads, D=128, bf16 KV, "
@@ -53,6 +54,8 @@ CONFIG_TEXT = {
                 "8-block shared prefixes",
     "e4m3_70b": "Llama-3-70B-shaped decode layer with an fp8-e4m3 KV cache (per-tensor scale "
                 "1/8): 128 seqs, 64 q/8 kv heads, D=128, lognormal lengths (median 2048)",
+    "int4_70b": "Llama-3-70B-shaped decode layer with an INT4 KV cache (scale 1/2, two tokens "
+                "per byte): 128 seqs, 64 q/8 kv heads, D=128, lognormal lengths (median 2048)",
     "prefill_tiny": "several causal queries per sequence, tiny mix: 7 seqs, 8 q/2 kv heads, "
                     "D=64, bf16 KV",
     "spec_verify_70b": "speculative verification on the Llama-3-70B-shaped layer: 128 seqs x 5 "
@@ -239,6 +242,8 @@ def run_ours(args):
             return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
         if dt == W.FP8_E4M3:
             return torch.from_numpy(a).view(torch.float8_e4m3fn)
+        if dt == W.INT4:
+            return torch.from_numpy(a)                  # packed nibbles as uint8
         return torch.from_numpy(a).view(torch.float8_e5m2)
 
     host = {

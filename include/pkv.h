@@ -59,11 +59,16 @@ typedef enum {
     PKV_F32 = 0,       /* IEEE binary32                                   */
     PKV_BF16 = 1,      /* bfloat16                                        */
     PKV_FP8_E5M2 = 2,  /* OCP fp8 E5M2 (KV cache only), value = code * scale */
-    PKV_FP8_E4M3 = 3   /* OCP fp8 E4M3, finite form: no infinities, +-448 max,
+    PKV_FP8_E4M3 = 3,  /* OCP fp8 E4M3, finite form: no infinities, +-448 max,
                           the all-ones code is NaN (KV cache only), value = code * scale.
                           The tensor-core decode reads a NaN code in a valid slot
                           as 480 (the cache write never stores one for finite
                           inputs). */
+    PKV_INT4 = 4       /* signed 4-bit integers -8..7 (KV cache only), value =
+                          code * scale; two tokens per byte: a cache is
+                          [num_blocks, num_kv_heads, head_dim, block_size / 2]
+                          bytes, token 2j of a row in the low nibble of byte j,
+                          token 2j+1 in the high nibble. */
 } pkv_dtype;
 
 /* Flags of pkv_paged_attn_decode. */
@@ -119,10 +124,10 @@ int pkv_paged_attn_partition_tokens(int num_seqs, int num_q_heads, int num_kv_he
  *   q            [num_seqs, num_q_heads, head_dim], q_dtype in {F32, BF16}
  *   k_cache,
  *   v_cache      [num_blocks, num_kv_heads, head_dim, block_size], kv_dtype in
- *                {F32, BF16, FP8_E5M2, FP8_E4M3}: tokens of a page are contiguous for
+ *                {F32, BF16, FP8_E5M2, FP8_E4M3, INT4}: tokens of a page are contiguous for
  *                each (head, dim), as in the pages' K_cache layout.
  *   k_scale,
- *   v_scale      dequant scales of fp8 caches (value = code * scale);
+ *   v_scale      dequant scales of fp8 and INT4 caches (value = code * scale);
  *                ignored for F32/BF16.
  *   block_tables int32 [num_seqs, max_blocks_per_seq]; entry j of row s is the
  *                physical block holding logical tokens [16j, 16j+16) of
@@ -185,7 +190,7 @@ pkv_status pkv_paged_attn_decode_append(const void *q, pkv_dtype q_dtype, const 
                                         int partition_tokens, int flags, void *stream);
 
 /*
- * Decode over an fp8 cache (FP8_E5M2 or FP8_E4M3) quantised with one scale per
+ * Decode over an fp8 or INT4 cache quantised with one scale per
  * KV head: element (block, h, d, t) stands for code * k_head_scales[h] (K) and
  * code * v_head_scales[h] (V).  k_head_scales, v_head_scales: float32
  * [num_kv_heads] in device memory, non-zero and finite.  Everything else as
@@ -307,8 +312,9 @@ pkv_status pkv_paged_attn_decode_noalloc(const void *q, pkv_dtype q_dtype,
  *   cvt           F32 -> F32 and BF16 -> BF16 copy the bits; F32 -> BF16 rounds
  *                 to nearest even; BF16 -> F32 widens exactly; -> FP8_E5M2 / FP8_E4M3
  *                 stores round-to-nearest-even(x / scale) computed in float32
- *                 and saturated to +-57344 (e5m2) / +-448 (e4m3).  NaN inputs give a NaN code of
- *                 unspecified payload.
+ *                 and saturated to +-57344 (e5m2) / +-448 (e4m3); -> INT4 the same
+ *                 rounding clamped to -8..7.  NaN inputs give a NaN code of
+ *                 unspecified payload (INT4: 0).
  *   status        optional device int32 (NULL = none): set to
  *                 PKV_ERR_OUT_OF_RANGE if a slot lies past the pool (that
  *                 token is skipped).  It is never cleared by this call.
@@ -320,7 +326,7 @@ pkv_status pkv_reshape_and_cache(const void *k, const void *v, pkv_dtype in_dtyp
                                  float k_scale, float v_scale, int32_t *status, void *stream);
 
 /*
- * The cache write of pkv_reshape_and_cache for an fp8 cache quantised with one
+ * The cache write of pkv_reshape_and_cache for an fp8 or INT4 cache quantised with one
  * scale per KV head: head h's codes are RNE_satfinite(x / k_head_scales[h])
  * (V likewise), the division done in float32.  k_head_scales, v_head_scales:
  * float32 [num_kv_heads] in device memory.  Other KV dtypes:

@@ -29,9 +29,10 @@ __all__ = ["paged_attn_decode", "paged_attn_decode_append", "paged_attn_prefill"
            "reshape_and_cache", "workspace_size", "partition_tokens",
            "prefill_workspace_size", "prefill_partition_tokens", "copy_blocks",
            "BlockManager",
-           "read_status", "PkvError", "lib", "F32", "BF16", "FP8_E5M2", "FP8_E4M3"]
+           "read_status", "PkvError", "lib", "F32", "BF16", "FP8_E5M2", "FP8_E4M3",
+           "INT4"]
 
-F32, BF16, FP8_E5M2, FP8_E4M3 = 0, 1, 2, 3
+F32, BF16, FP8_E5M2, FP8_E4M3, INT4 = 0, 1, 2, 3, 4
 IMPL = {"auto": 0x0, "simt": 0x1, "mma": 0x2}
 FLAG_SEPARATE_MERGE = 0x4
 FLAG_TEST_DROP_FIRST_COPY = 0x100
@@ -132,6 +133,8 @@ def _dtype_code(t: torch.Tensor, what: str) -> int:
         return FP8_E5M2
     if t.dtype == torch.float8_e4m3fn:
         return FP8_E4M3
+    if t.dtype == torch.uint8:
+        return INT4          # packed signed nibbles, two tokens per byte
     raise TypeError(f"{what}: unsupported dtype {t.dtype}")
 
 
@@ -146,6 +149,13 @@ def _check(t: torch.Tensor, what: str, ndim: int, device: torch.device):
         raise ValueError(f"{what} must have {ndim} dims, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{what} must be contiguous")
+
+
+def _pool_dims(cache: torch.Tensor):
+    """(N, Hkv, D, block_size) of a cache tensor; INT4 caches (uint8) hold two
+    tokens per byte in the last dimension."""
+    N, Hkv, D, B = cache.shape
+    return N, Hkv, D, (2 * B if cache.dtype == torch.uint8 else B)
 
 
 def _stream(device: torch.device, stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
@@ -209,7 +219,7 @@ def paged_attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Ten
     if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
         raise ValueError("k_cache and v_cache must have the same shape and dtype")
     S, Hq, D = q.shape
-    N, Hkv, D2, B = k_cache.shape
+    N, Hkv, D2, B = _pool_dims(k_cache)
     if D2 != D or out.shape != q.shape or block_tables.shape[0] != S or seq_lens.shape[0] != S:
         raise ValueError("inconsistent shapes")
     max_blocks = block_tables.shape[1]
@@ -255,7 +265,7 @@ def paged_attn_decode_head_scaled(q: torch.Tensor, k_cache: torch.Tensor, v_cach
     if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
         raise TypeError("block_tables and seq_lens must be int32")
     S, Hq, D = q.shape
-    N, Hkv, D2, B = k_cache.shape
+    N, Hkv, D2, B = _pool_dims(k_cache)
     if (D2 != D or out.shape != q.shape or k_cache.shape != v_cache.shape
             or k_head_scales.shape[0] != Hkv or v_head_scales.shape[0] != Hkv):
         raise ValueError("inconsistent shapes")
@@ -296,7 +306,7 @@ def reshape_and_cache_head_scaled(k: torch.Tensor, v: torch.Tensor, slot_mapping
     if k_head_scales.dtype != torch.float32 or v_head_scales.dtype != torch.float32:
         raise TypeError("per-head scales must be float32")
     T, Hkv, D = k.shape
-    N, Hkv2, D2, B = k_cache.shape
+    N, Hkv2, D2, B = _pool_dims(k_cache)
     if (v.shape != k.shape or Hkv2 != Hkv or D2 != D or v_cache.shape != k_cache.shape
             or slot_mapping.shape[0] != T or k_head_scales.shape[0] != Hkv
             or v_head_scales.shape[0] != Hkv):
@@ -339,7 +349,7 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
     if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
         raise ValueError("k_cache and v_cache must have the same shape and dtype")
     S, Hq, D = q.shape
-    N, Hkv, D2, B = k_cache.shape
+    N, Hkv, D2, B = _pool_dims(k_cache)
     if (D2 != D or out.shape != q.shape or block_tables.shape[0] != S
             or seq_lens.shape[0] != S or new_k.shape != (S, Hkv, D)
             or new_v.shape != new_k.shape or new_v.dtype != new_k.dtype):
@@ -414,7 +424,7 @@ def paged_attn_prefill(q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Te
     if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
         raise ValueError("k_cache and v_cache must have the same shape and dtype")
     T, Hq, D = q.shape
-    N, Hkv, D2, B = k_cache.shape
+    N, Hkv, D2, B = _pool_dims(k_cache)
     S = seq_lens.shape[0]
     if (D2 != D or out.shape != q.shape or block_tables.shape[0] != S
             or q_start.shape[0] != S + 1):
@@ -457,7 +467,7 @@ def reshape_and_cache(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tens
     if slot_mapping.dtype != torch.int64:
         raise TypeError("slot_mapping must be int64")
     T, Hkv, D = k.shape
-    N, Hkv2, D2, B = k_cache.shape
+    N, Hkv2, D2, B = _pool_dims(k_cache)
     if v.shape != k.shape or Hkv2 != Hkv or D2 != D or v_cache.shape != k_cache.shape:
         raise ValueError("inconsistent shapes")
     if slot_mapping.shape[0] != T:
@@ -487,7 +497,7 @@ def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, pairs: torch.Tenso
         raise ValueError("pairs must be int32 [n, 2]")
     if k_cache.shape != v_cache.shape or k_cache.dtype != v_cache.dtype:
         raise ValueError("k_cache and v_cache must have the same shape and dtype")
-    N, Hkv, D, B = k_cache.shape
+    N, Hkv, D, B = _pool_dims(k_cache)
     st_ptr = None
     if status is not None:
         _check(status, "status", 1, dev)

@@ -156,7 +156,7 @@ static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_ca
         return PKV_ERR_INVALID_ARG;
     if (q_dtype != PKV_F32 && q_dtype != PKV_BF16)
         return PKV_ERR_UNSUPPORTED;
-    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && !is_fp8(kv_dtype))
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && !is_scaled(kv_dtype))
         return PKV_ERR_UNSUPPORTED;
     if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
         return PKV_ERR_UNSUPPORTED;
@@ -218,9 +218,9 @@ static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_ca
     p.max_blocks = max_blocks_per_seq;
     p.max_len = max_seq_len;
     p.group = group;
-    const float k_mul = is_fp8(kv_dtype) ? k_scale : 1.0f;
+    const float k_mul = is_scaled(kv_dtype) ? k_scale : 1.0f;
     p.score_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 * k_mul);
-    p.out_scale = is_fp8(kv_dtype) ? v_scale : 1.0f;
+    p.out_scale = is_scaled(kv_dtype) ? v_scale : 1.0f;
     if (use_mma && kv_dtype == PKV_FP8_E4M3) {
         p.score_scale *= kE4m3Shift;
         p.out_scale *= kE4m3Shift;
@@ -287,7 +287,7 @@ pkv_status pkv_paged_attn_decode_append(const void *q, pkv_dtype q_dtype, const 
 {
     if (new_dtype != PKV_F32 && new_dtype != PKV_BF16)
         return PKV_ERR_UNSUPPORTED;
-    if (is_fp8(kv_dtype) && (k_scale == 0.f || v_scale == 0.f))
+    if (is_scaled(kv_dtype) && (k_scale == 0.f || v_scale == 0.f))
         return PKV_ERR_INVALID_ARG;
     if (num_seqs > 0 && (!new_k || !new_v || !aligned(new_k, 16) || !aligned(new_v, 16)))
         return PKV_ERR_INVALID_ARG;
@@ -306,7 +306,7 @@ pkv_status pkv_paged_attn_decode_head_scaled(
     void *out, pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
     int partition_tokens, int flags, void *stream)
 {
-    if (!is_fp8(kv_dtype))
+    if (!is_scaled(kv_dtype))
         return PKV_ERR_UNSUPPORTED;
     if (num_seqs > 0 && (!k_head_scales || !v_head_scales || !aligned(k_head_scales, 4) ||
                          !aligned(v_head_scales, 4)))
@@ -344,7 +344,7 @@ pkv_status pkv_reshape_and_cache_head_scaled(const void *k, const void *v, pkv_d
                                              const float *v_head_scales, int32_t *status,
                                              void *stream)
 {
-    if (!is_fp8(kv_dtype))
+    if (!is_scaled(kv_dtype))
         return PKV_ERR_UNSUPPORTED;
     if (num_tokens > 0 && (!k_head_scales || !v_head_scales || !aligned(k_head_scales, 4) ||
                            !aligned(v_head_scales, 4)))
@@ -367,9 +367,9 @@ static pkv_status reshape_impl(const void *k, const void *v, pkv_dtype in_dtype,
         return PKV_ERR_UNSUPPORTED;
     if (in_dtype != PKV_F32 && in_dtype != PKV_BF16)
         return PKV_ERR_UNSUPPORTED;
-    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && !is_fp8(kv_dtype))
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && !is_scaled(kv_dtype))
         return PKV_ERR_UNSUPPORTED;
-    if (is_fp8(kv_dtype) &&
+    if (is_scaled(kv_dtype) &&
         (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale == 0.f || v_scale == 0.f))
         return PKV_ERR_INVALID_ARG;
     if (num_tokens == 0)
@@ -565,14 +565,14 @@ pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, pkv_dtype kv_dtype, int
         return PKV_ERR_INVALID_ARG;
     if (block_size != kBlockSize)
         return PKV_ERR_UNSUPPORTED;
-    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && !is_fp8(kv_dtype))
+    if (kv_dtype != PKV_F32 && kv_dtype != PKV_BF16 && !is_scaled(kv_dtype))
         return PKV_ERR_UNSUPPORTED;
     if (num_pairs == 0)
         return PKV_OK;
     if (!k_cache || !v_cache || !pairs)
         return PKV_ERR_INVALID_ARG;
-    const size_t elem = kv_dtype == PKV_F32 ? 4 : (kv_dtype == PKV_BF16 ? 2 : 1);
-    const size_t block_bytes = static_cast<size_t>(num_kv_heads) * head_dim * kBlockSize * elem;
+    const size_t block_bytes =
+        static_cast<size_t>(num_kv_heads) * static_cast<size_t>(tile_bytes(kv_dtype, head_dim));
     if (block_bytes % 16 != 0 || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(pairs, 4) || (status && !aligned(status, 4)))
         return PKV_ERR_INVALID_ARG;

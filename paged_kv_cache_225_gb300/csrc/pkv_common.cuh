@@ -218,6 +218,13 @@ __device__ __forceinline__ float e4m3_to_float(uint32_t code)
     return __half2float(__half(h));
 }
 
+// Nibble `hi` (0: low, 1: high) of an INT4 byte as a signed value -8..7.
+__device__ __forceinline__ float int4_to_float(uint32_t byte, int hi)
+{
+    const uint32_t nib = (byte >> (hi ? 4 : 0)) & 0xfu;
+    return static_cast<float>(static_cast<int>(nib ^ 0x8u) - 8);
+}
+
 __device__ __forceinline__ void set_status(int *status, int code)
 {
     if (status)

@@ -89,7 +89,7 @@ __host__ __device__ constexpr int ring_budget(int other)
 
 // Per-warp ring geometry: `Budget` bytes of page stages per warp.
 template <int KV, int D, int Budget> struct Ring {
-    static constexpr int kTileBytes = D * kBlockSize * KvBytes<KV>::v;  // one K or V page tile
+    static constexpr int kTileBytes = tile_bytes(KV, D);  // one K or V page tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRaw = Budget / kStageBytes;
     static constexpr int R = kRaw < 2 ? 2 : (kRaw > 8 ? 8 : kRaw);
@@ -146,8 +146,10 @@ struct SimtPolicy {
                 static_cast<uint32_t>(reinterpret_cast<const unsigned short *>(tile)[idx]) << 16);
         else if constexpr (KV == PKV_FP8_E5M2)
             return e5m2_to_float(tile[idx]);
-        else
+        else if constexpr (KV == PKV_FP8_E4M3)
             return e4m3_to_float(tile[idx]);
+        else
+            return int4_to_float(tile[idx >> 1], idx & 1);
     }
 
     // One page row V[d][0..15] widened to floats.
@@ -175,6 +177,15 @@ struct SimtPolicy {
                     v[8 * i + 2 * k + 1] = bf16_hi(w[k]);
                 }
             }
+        } else if constexpr (KV == PKV_INT4) {
+            const uint2 x = *reinterpret_cast<const uint2 *>(tile + d * (kBlockSize / 2));
+            const uint32_t w[2] = {x.x, x.y};
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+#pragma unroll
+                for (int b = 0; b < 8; ++b)
+                    v[8 * k + b] = static_cast<float>(
+                        static_cast<int>(((w[k] >> (4 * b)) & 0xfu) ^ 0x8u) - 8);
         } else {
             const uint4 x = *reinterpret_cast<const uint4 *>(tile + d * kBlockSize);
             const uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -719,6 +730,132 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
                     mma_f16(st.o[2 * mp + h][n], a, b0[n], b1[n]);
             }
         }
+    }
+
+    __device__ static void page(State &st, const unsigned char *sK, const unsigned char *sV,
+                                int valid, int lane, int, unsigned char *, float c)
+    {
+        Frags f;
+        load(f, sK, sV, lane);
+        compute(st, f, valid, lane, c);
+    }
+
+    __device__ static void finish(State &st, float *so, float *sm, float *sl, int lane)
+    {
+        Base::finish(st, so, sm, sl, lane);
+    }
+};
+
+// INT4 KV: the page tile is [D][8] bytes (token 2j of a head_dim row in the
+// low nibble of byte j).  Fragments are gathered with byte / halfword loads
+// in the fp8 policy's token order (fragment row r <-> token 2r, row r+8 <->
+// token 2r+1), so one byte holds the two tokens a lane needs for a head_dim
+// row; nibbles become exact binary16 integers with the 0x6400 exponent trick
+// (1024 + (n ^ 8) - 1032 = the signed nibble).  Scales multiply outside.
+template <int D, int NT, int Budget = PKV_FP8_RING_BYTES_PER_WARP, bool Staged = false>
+struct MmaInt4Policy : MmaStateBase<D, NT> {
+    using Base = MmaStateBase<D, NT>;
+    using State = typename Base::State;
+    using RingT = Ring<PKV_INT4, D, Budget>;
+    using StreamK = MmaInt4Policy<D, NT, ring_budget(scratch_bytes(8 * NT, D)), NT == 1>;
+    static constexpr int R = RingT::R;
+    static constexpr int kTileBytes = RingT::kTileBytes;
+    static constexpr int kStageBytes = RingT::kStageBytes;
+    static constexpr int kRingBytes = RingT::kRingBytes;
+    static constexpr int kDim = D;
+    static constexpr int GP = 8 * NT;
+    static constexpr int kExtraBytes = 0;
+    static constexpr int KS = Base::KS, MT = Base::MT;
+    static constexpr bool kStaged = Staged;
+    static constexpr bool kSharedBegin = false;
+    static constexpr int kMinBlocks = Staged ? 2 : (NT == 1 ? PKV_FP8_MIN_BLOCKS : 3);
+    static constexpr int kRow = kBlockSize / 2;  // bytes of one head_dim row
+
+    // Low (odd = false) or high nibbles of the two bytes of x (bits 0-7 and
+    // 8-15) as an f16x2 word of signed integers.
+    __device__ static uint32_t widen(uint32_t x, bool odd)
+    {
+        const uint32_t y = x | (x << 8);  // byte 1 also at bits 16-23
+        const uint32_t h = ((odd ? y >> 4 : y) & 0x000f000fu) ^ 0x64086408u;
+        const __half2 v = __hsub2(*reinterpret_cast<const __half2 *>(&h),
+                                  __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
+        return *reinterpret_cast<const uint32_t *>(&v);
+    }
+
+    struct Frags {
+        uint32_t k[KS][2];  // per k step: bytes g of rows (d0, d0+1) and (d0+8, d0+9)
+        uint32_t v[MT][2];  // per head_dim tile: halfword 2c of rows g and g + 8
+    };
+
+    __device__ static void begin(State &st, const DecodeParams &p, int s, int hkv, int lane,
+                                 unsigned char *)
+    {
+        Base::reset(st);
+        Base::template load_q_frags<true>(st, p, s, hkv, lane);
+    }
+
+    __device__ static void load(Frags &f, const unsigned char *sK, const unsigned char *sV,
+                                int lane)
+    {
+        const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const unsigned char *r = sK + (16 * ks + 2 * c) * kRow + g;
+            f.k[ks][0] = static_cast<uint32_t>(r[0]) | (static_cast<uint32_t>(r[kRow]) << 8);
+            f.k[ks][1] =
+                static_cast<uint32_t>(r[8 * kRow]) | (static_cast<uint32_t>(r[9 * kRow]) << 8);
+        }
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const unsigned char *r = sV + (16 * mt + g) * kRow + 2 * c;
+            f.v[mt][0] = *reinterpret_cast<const unsigned short *>(r);
+            f.v[mt][1] = *reinterpret_cast<const unsigned short *>(r + 8 * kRow);
+        }
+    }
+
+    __device__ static void compute(State &st, Frags &f, int valid, int lane, float c)
+    {
+        const int r = lane >> 2, cc = lane & 3;
+        float sacc[NT][4], sodd[NT][4];
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sacc[n][e] = sodd[n][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+            const uint32_t a[4] = {widen(f.k[ks][0], false), widen(f.k[ks][0], true),
+                                   widen(f.k[ks][1], false), widen(f.k[ks][1], true)};
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                mma_f16((ks & 1) ? sodd[n] : sacc[n], a, st.qf[ks][n][0], st.qf[ks][n][1]);
+        }
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                sacc[n][e] += sodd[n][e];
+
+        uint32_t b0[NT], b1[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            float pr[4], alpha[2];
+            if (MmaSoftmax::update(sacc[n], 2 * r, 2 * r + 1, valid, c, st.m[n], st.l[n], pr,
+                                   alpha))
+                Base::rescale(st, n, alpha);
+            b0[n] = movmatrix_t(pack_f16(pr[0], pr[1]));
+            b1[n] = movmatrix_t(pack_f16(pr[2], pr[3]));
+        }
+        // Past the sequence end the codes are finite and P is 0: no V mask.
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+            const uint32_t a[4] = {widen(f.v[mt][0], false), widen(f.v[mt][1], false),
+                                   widen(f.v[mt][0], true), widen(f.v[mt][1], true)};
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                mma_f16(st.o[mt][n], a, b0[n], b1[n]);
+        }
+        (void)cc;
     }
 
     __device__ static void page(State &st, const unsigned char *sK, const unsigned char *sV,

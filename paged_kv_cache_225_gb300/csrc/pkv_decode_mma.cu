@@ -1,4 +1,4 @@
-// Tensor-core (mma.sync) decode kernels: bf16 and fp8 (e5m2, e4m3) KV with a bf16
+// Tensor-core (mma.sync) decode kernels: bf16, fp8 (e5m2, e4m3) and INT4 KV with a bf16
 // query, head_dim 64/128, up to 16 query heads per KV head (one or two
 // 8-wide N tiles).
 #include "pkv_streamk.cuh"
@@ -7,7 +7,7 @@ namespace pkv {
 
 bool mma_supports(int kv_dtype, int q_dtype, int head_dim, int group)
 {
-    return (kv_dtype == PKV_BF16 || is_fp8(kv_dtype)) && q_dtype == PKV_BF16 &&
+    return (kv_dtype == PKV_BF16 || is_scaled(kv_dtype)) && q_dtype == PKV_BF16 &&
            (head_dim == 64 || head_dim == 128) && group >= 1 && group <= 16;
 }
 
@@ -18,6 +18,9 @@ static pkv_status dispatch(const DecodeParams &p, int kv_dtype, cudaStream_t str
     if (kv_dtype == PKV_BF16)
         return two ? launch_any<MmaBf16Policy<D, 2>>(p, stream)
                    : launch_any<MmaBf16Policy<D, 1>>(p, stream);
+    if (kv_dtype == PKV_INT4)
+        return two ? launch_any<MmaInt4Policy<D, 2>>(p, stream)
+                   : launch_any<MmaInt4Policy<D, 1>>(p, stream);
     if (kv_dtype == PKV_FP8_E4M3) {
         constexpr int kRing = PKV_FP8_RING_BYTES_PER_WARP;
         return two ? launch_any<MmaFp8Policy<D, 2, kRing, false, PKV_FP8_E4M3>>(p, stream)

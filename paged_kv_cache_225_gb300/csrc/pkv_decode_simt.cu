@@ -41,6 +41,7 @@ pkv_status launch_decode_simt(const DecodeParams &p, int kv_dtype, cudaStream_t 
         return dispatch_dim<PKV_BF16>(p, stream);
     case PKV_FP8_E5M2:
     case PKV_FP8_E4M3:
+    case PKV_INT4:
         return launch_decode_simt_fp8(p, kv_dtype, stream);
     default:
         return PKV_ERR_UNSUPPORTED;

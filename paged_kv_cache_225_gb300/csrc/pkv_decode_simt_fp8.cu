@@ -1,5 +1,6 @@
-// CUDA-core (FFMA) decode kernels for the fp8 KV dtypes (e5m2, e4m3), in a
-// translation unit of their own so the build compiles them in parallel.
+// CUDA-core (FFMA) decode kernels for the 8- and 4-bit KV dtypes (fp8 e5m2,
+// fp8 e4m3, INT4), in a translation unit of their own so the build compiles
+// them in parallel.
 #include "pkv_streamk.cuh"
 
 namespace pkv {
@@ -38,6 +39,8 @@ pkv_status launch_decode_simt_fp8(const DecodeParams &p, int kv_dtype, cudaStrea
         return dispatch_dim<PKV_FP8_E5M2>(p, stream);
     case PKV_FP8_E4M3:
         return dispatch_dim<PKV_FP8_E4M3>(p, stream);
+    case PKV_INT4:
+        return dispatch_dim<PKV_INT4>(p, stream);
     default:
         return PKV_ERR_UNSUPPORTED;
     }

@@ -81,6 +81,15 @@ constexpr int kBlockSize = 16;
 
 // The 8-bit KV dtypes (value = code * scale).
 constexpr bool is_fp8(int dtype) { return dtype == PKV_FP8_E5M2 || dtype == PKV_FP8_E4M3; }
+// Every KV dtype whose stored codes are multiplied by a dequant scale.
+constexpr bool is_scaled(int dtype) { return is_fp8(dtype) || dtype == PKV_INT4; }
+// Bytes of one [head_dim x 16] page tile of a KV dtype.
+constexpr int tile_bytes(int dtype, int head_dim)
+{
+    return dtype == PKV_F32 ? head_dim * 64
+                            : dtype == PKV_BF16 ? head_dim * 32
+                                                : dtype == PKV_INT4 ? head_dim * 8 : head_dim * 16;
+}
 
 // The tensor-core e4m3 policy widens a code to a binary16 holding 2^-8 times
 // its value; the host multiplies the score and output scales by 2^8.

@@ -96,8 +96,15 @@ CONFIGS = {
         name="e4m3_70b", num_seqs=128, num_q_heads=64, num_kv_heads=8, head_dim=128,
         block_size=16, q_dtype=BF16, kv_dtype=FP8_E4M3, len_dist="lognormal",
         len_median=2048.0, len_sigma=0.8, len_lo=16, len_hi=32768, kv_scale=0.125),
+    # The 70B layer with an INT4 cache (scale 1/2: N(0,1) data spans the
+    # codes -8..7 at +-3.5 sigma).
+    "int4_70b": DecodeConfig(
+        name="int4_70b", num_seqs=128, num_q_heads=64, num_kv_heads=8, head_dim=128,
+        block_size=16, q_dtype=BF16, kv_dtype=INT4, len_dist="lognormal",
+        len_median=2048.0, len_sigma=0.8, len_lo=16, len_hi=32768, kv_scale=0.5),
 }
-CONFIG_ORDER = ["tiny_fp32", "llama3_8b", "llama3_70b", "long_split", "fp8_chat", "e4m3_70b"]
+CONFIG_ORDER = ["tiny_fp32", "llama3_8b", "llama3_70b", "long_split", "fp8_chat", "e4m3_70b",
+                "int4_70b"]
 CONFIG_SEED = {name: i for i, name in enumerate(CONFIG_ORDER)}
 
 

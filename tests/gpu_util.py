@@ -9,7 +9,7 @@ import paged_kv_cache_225_gb300 as pkv
 from paged_kv_cache_225_gb300 import workloads as W
 
 # Max-abs tolerances against the fp64 oracle on identically rounded inputs.
-TOL = {W.F32: 1e-5, W.BF16: 4e-3, W.FP8_E5M2: 3e-2, W.FP8_E4M3: 3e-2}
+TOL = {W.F32: 1e-5, W.BF16: 4e-3, W.FP8_E5M2: 3e-2, W.FP8_E4M3: 3e-2, W.INT4: 4e-3}
 
 
 def to_torch(a: np.ndarray, dtype: int) -> torch.Tensor:
@@ -22,6 +22,8 @@ def to_torch(a: np.ndarray, dtype: int) -> torch.Tensor:
         return torch.from_numpy(a).view(torch.float8_e5m2)
     if dtype == W.FP8_E4M3:
         return torch.from_numpy(a).view(torch.float8_e4m3fn)
+    if dtype == W.INT4:
+        return torch.from_numpy(a)                   # packed nibbles as uint8
     raise ValueError(dtype)
 
 

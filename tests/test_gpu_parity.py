@@ -92,7 +92,7 @@ def _custom(base="llama3_8b", seed=100, lens=None, **kw):
 EDGE_LENS = [0, 1, 15, 16, 17, 31, 33, 100, 511, 512, 513, 1000]
 
 
-@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2, W.FP8_E4M3, W.F32])
+@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2, W.FP8_E4M3, W.INT4, W.F32])
 @pytest.mark.parametrize("impl", ["auto", "simt"])
 @pytest.mark.parametrize("part", [0, -1, 32, 48])
 def test_edge_lengths_with_nan_garbage(kv_dtype, impl, part):
@@ -108,7 +108,7 @@ def test_edge_lengths_with_nan_garbage(kv_dtype, impl, part):
 
 
 @pytest.mark.parametrize("group", [1, 2, 3, 4, 5, 8, 12, 16])
-@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2, W.FP8_E4M3])
+@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2, W.FP8_E4M3, W.INT4])
 @pytest.mark.parametrize("head_dim", [64, 128])
 @pytest.mark.parametrize("impl", ["mma", "simt"])
 def test_head_groups_and_dims(group, kv_dtype, head_dim, impl):
@@ -179,7 +179,7 @@ def test_long_sequence_32768_single_pass_and_split():
 
 @pytest.mark.parametrize("lens", [[1], [0], [0, 0, 5], [3] * 300, [16] * 7 + [4000],
                                   [1] * 50 + [20000], [700, 0, 1, 33, 9000, 2]])
-@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2, W.FP8_E4M3])
+@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2, W.FP8_E4M3, W.INT4])
 def test_streamk_ranges_cut_units_anywhere(lens, kv_dtype):
     """Few pages (fewer than CTAs), empty sequences, many tiny units, and one
     long unit cut across many CTAs next to short ones."""
@@ -194,7 +194,7 @@ def test_streamk_ranges_cut_units_anywhere(lens, kv_dtype):
         assert max_abs(out, ref) <= TOL[kv_dtype]
 
 
-@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2, W.FP8_E4M3])
+@pytest.mark.parametrize("kv_dtype", [W.BF16, W.FP8_E5M2, W.FP8_E4M3, W.INT4])
 @pytest.mark.parametrize("direction", [1.0, -1.0])
 def test_scores_ramping_across_the_running_max(kv_dtype, direction):
     """Keys scaled so each query head's scores drift steadily along the sequence
@@ -240,7 +240,7 @@ def test_fused_step_matches_write_then_decode_bitwise(name, part):
     assert max_abs(b, ref) <= TOL[w.cfg.kv_dtype]
 
 
-@pytest.mark.parametrize("kv_dtype", [W.F32, W.BF16, W.FP8_E5M2, W.FP8_E4M3])
+@pytest.mark.parametrize("kv_dtype", [W.F32, W.BF16, W.FP8_E5M2, W.FP8_E4M3, W.INT4])
 def test_fused_step_cuda_cores_and_edge_lengths(kv_dtype):
     q_dtype = W.F32 if kv_dtype == W.F32 else W.BF16
     lens = np.array(EDGE_LENS)
@@ -268,7 +268,8 @@ def test_results_are_deterministic():
 @pytest.mark.parametrize("in_dtype,kv_dtype,scale", [
     (W.F32, W.F32, 1.0), (W.F32, W.BF16, 1.0), (W.BF16, W.BF16, 1.0), (W.BF16, W.F32, 1.0),
     (W.BF16, W.FP8_E5M2, 1.0), (W.F32, W.FP8_E5M2, 0.25), (W.BF16, W.FP8_E5M2, 3.0),
-    (W.BF16, W.FP8_E4M3, 1.0), (W.F32, W.FP8_E4M3, 0.125), (W.BF16, W.FP8_E4M3, 3.0)])
+    (W.BF16, W.FP8_E4M3, 1.0), (W.F32, W.FP8_E4M3, 0.125), (W.BF16, W.FP8_E4M3, 3.0),
+    (W.BF16, W.INT4, 1.0), (W.F32, W.INT4, 0.25), (W.BF16, W.INT4, 3.0)])
 def test_reshape_and_cache_bit_exact(in_dtype, kv_dtype, scale):
     rng = np.random.default_rng(31)
     N, Hkv, D, B, T = 40, 4, 128, 16, 97
@@ -353,7 +354,7 @@ def test_bounded_wait_reports_timeout_and_context_survives(part):
 
 # ------------------------------------------------------ per-head fp8 scales
 
-@pytest.mark.parametrize("kv_dtype", [W.FP8_E5M2, W.FP8_E4M3])
+@pytest.mark.parametrize("kv_dtype", [W.FP8_E5M2, W.FP8_E4M3, W.INT4])
 @pytest.mark.parametrize("impl", ["auto", "simt"])
 @pytest.mark.parametrize("part", [0, -2, -1, 64])
 def test_per_head_scaled_decode(kv_dtype, impl, part):
@@ -380,14 +381,14 @@ def test_per_head_scaled_decode(kv_dtype, impl, part):
         assert err <= TOL[kv_dtype], (h, err)
 
 
-@pytest.mark.parametrize("kv_dtype", [W.FP8_E5M2, W.FP8_E4M3])
+@pytest.mark.parametrize("kv_dtype", [W.FP8_E5M2, W.FP8_E4M3, W.INT4])
 @pytest.mark.parametrize("in_dtype", [W.F32, W.BF16])
 def test_per_head_scaled_cache_write_is_bit_exact(kv_dtype, in_dtype):
     rng = np.random.default_rng(42)
     N, Hkv, D, B, T = 30, 4, 128, 16, 61
     ks = np.array([0.5, 2.0, 0.1, 8.0], np.float32)
     vs = np.array([0.25, 1.0, 3.0, 0.05], np.float32)
-    k_cache = np.zeros((N, Hkv, D, B), np.uint8)
+    k_cache = np.zeros((N, Hkv, D, B // 2 if kv_dtype == W.INT4 else B), np.uint8)
     v_cache = np.zeros_like(k_cache)
     kin = W.round_to_storage(rng.standard_normal((T, Hkv, D)).astype(np.float32) * 6, in_dtype)
     vin = W.round_to_storage(rng.standard_normal((T, Hkv, D)).astype(np.float32), in_dtype)
