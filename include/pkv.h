@@ -1,7 +1,7 @@
 /*
  * pkv.h - C ABI of the GB300 (sm_103a) paged KV-cache decode library.
  *
- * Two operations, both from the pages' statement of the problem:
+ * The operations, all from the pages' statement of the problem:
  *
  *  - pkv_paged_attn_decode: PagedAttention decode ("vLLM e PagedAttention:
  *    serving high-throughput", simplified PagedAttention CUDA-kernel
@@ -12,17 +12,30 @@
  *    softmax(scale * q K^T) V over the first seq_lens[s] logical rows, i.e.
  *    the dense single-query attention of the "Inference optimization" lesson
  *    (Step 2, scaled_dot_product_attention) on the gathered rows.
+ *    Variants: with the cache write fused in (pkv_paged_attn_decode_append),
+ *    with per-KV-head scales of quantised caches
+ *    (pkv_paged_attn_decode_head_scaled), without a caller workspace
+ *    (pkv_paged_attn_decode_noalloc).
  *
- *  - pkv_reshape_and_cache: the KV-cache update ("Inference optimization"
- *    lesson, section "Caches de KV": only the new token's K and V are computed
- *    and appended; section "PagedAttention": fixed-size pages anywhere in GPU
- *    memory, mapped by a per-request table).  Each new token's K/V row is
- *    written into its slot of the paged pool.
+ *  - pkv_paged_attn_prefill: the same attention for several causal query
+ *    tokens per sequence (chunked prefill, speculative verification).
+ *
+ *  - pkv_reshape_and_cache (and _head_scaled): the KV-cache update
+ *    ("Inference optimization" lesson, section "Caches de KV": only the new
+ *    token's K and V are computed and appended; section "PagedAttention":
+ *    fixed-size pages anywhere in GPU memory, mapped by a per-request table).
+ *    Each new token's K/V row is written into its slot of the paged pool.
+ *
+ *  - pkv_bm_* and pkv_copy_blocks: the page pool's bookkeeping on the host
+ *    (per-sequence page tables, shared pages stored once, copy-on-write) and
+ *    the page copies it asks for.
  *
  * Conventions shared by every entry point:
  *  - Every pointer argument is a DEVICE pointer owned by the caller, unless a
- *    comment says "host".  The library allocates no memory and keeps no
- *    device state between calls; scratch space is the caller's `workspace`.
+ *    comment says "host".  The library allocates no device memory and keeps
+ *    no device state between calls; scratch space is the caller's
+ *    `workspace` (pkv_paged_attn_decode_noalloc uses one fixed array instead;
+ *    the block manager keeps its tables in host memory).
  *  - All tensors are dense, row-major, with the shapes given below, and every
  *    device pointer must be 16-byte aligned.
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
