@@ -603,7 +603,14 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
 #define PKV_FP8_MIN_BLOCKS 4
 #endif
 
-template <int D, int NT, int Budget = PKV_FP8_RING_BYTES_PER_WARP, bool Staged = false,
+// Two-tile head groups keep three CTAs per SM and a 12 KB ring (their merge
+// scratch needs more than 8 KB per warp).
+constexpr int compact_ring_budget(int nt)
+{
+    return nt == 1 ? PKV_FP8_RING_BYTES_PER_WARP : 12 * 1024;
+}
+
+template <int D, int NT, int Budget = compact_ring_budget(NT), bool Staged = false,
           int KV = PKV_FP8_E5M2>
 struct MmaFp8Policy : MmaStateBase<D, NT> {
     using Base = MmaStateBase<D, NT>;
@@ -752,7 +759,7 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
 // token 2r+1), so one byte holds the two tokens a lane needs for a head_dim
 // row; nibbles become exact binary16 integers with the 0x6400 exponent trick
 // (1024 + (n ^ 8) - 1032 = the signed nibble).  Scales multiply outside.
-template <int D, int NT, int Budget = PKV_FP8_RING_BYTES_PER_WARP, bool Staged = false>
+template <int D, int NT, int Budget = compact_ring_budget(NT), bool Staged = false>
 struct MmaInt4Policy : MmaStateBase<D, NT> {
     using Base = MmaStateBase<D, NT>;
     using State = typename Base::State;

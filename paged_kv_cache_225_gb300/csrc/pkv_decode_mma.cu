@@ -21,11 +21,11 @@ static pkv_status dispatch(const DecodeParams &p, int kv_dtype, cudaStream_t str
     if (kv_dtype == PKV_INT4)
         return two ? launch_any<MmaInt4Policy<D, 2>>(p, stream)
                    : launch_any<MmaInt4Policy<D, 1>>(p, stream);
-    if (kv_dtype == PKV_FP8_E4M3) {
-        constexpr int kRing = PKV_FP8_RING_BYTES_PER_WARP;
-        return two ? launch_any<MmaFp8Policy<D, 2, kRing, false, PKV_FP8_E4M3>>(p, stream)
-                   : launch_any<MmaFp8Policy<D, 1, kRing, false, PKV_FP8_E4M3>>(p, stream);
-    }
+    if (kv_dtype == PKV_FP8_E4M3)
+        return two ? launch_any<MmaFp8Policy<D, 2, compact_ring_budget(2), false, PKV_FP8_E4M3>>(
+                         p, stream)
+                   : launch_any<MmaFp8Policy<D, 1, compact_ring_budget(1), false, PKV_FP8_E4M3>>(
+                         p, stream);
     return two ? launch_any<MmaFp8Policy<D, 2>>(p, stream)
                : launch_any<MmaFp8Policy<D, 1>>(p, stream);
 }
