@@ -778,20 +778,20 @@ struct MmaInt4Policy : MmaStateBase<D, NT> {
     static constexpr int kMinBlocks = Staged ? 2 : (NT == 1 ? PKV_FP8_MIN_BLOCKS : 3);
     static constexpr int kRow = kBlockSize / 2;  // bytes of one head_dim row
 
-    // Low (odd = false) or high nibbles of the two bytes of x (bits 0-7 and
-    // 8-15) as an f16x2 word of signed integers.
-    __device__ static uint32_t widen(uint32_t x, bool odd)
+    // Low (odd = false) or high nibbles of the two bytes of y (bits 0-7 and
+    // 16-23) as an f16x2 word of signed integers.
+    __device__ static uint32_t widen(uint32_t y, bool odd)
     {
-        const uint32_t y = x | (x << 8);  // byte 1 also at bits 16-23
         const uint32_t h = ((odd ? y >> 4 : y) & 0x000f000fu) ^ 0x64086408u;
         const __half2 v = __hsub2(*reinterpret_cast<const __half2 *>(&h),
                                   __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
         return *reinterpret_cast<const uint32_t *>(&v);
     }
 
+    // Each entry holds two bytes, at bits 0-7 and 16-23.
     struct Frags {
         uint32_t k[KS][2];  // per k step: bytes g of rows (d0, d0+1) and (d0+8, d0+9)
-        uint32_t v[MT][2];  // per head_dim tile: halfword 2c of rows g and g + 8
+        uint32_t v[MT][2];  // per head_dim tile: bytes 2c, 2c+1 of rows g and g + 8
     };
 
     __device__ static void begin(State &st, const DecodeParams &p, int s, int hkv, int lane,
@@ -808,15 +808,16 @@ struct MmaInt4Policy : MmaStateBase<D, NT> {
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
             const unsigned char *r = sK + (16 * ks + 2 * c) * kRow + g;
-            f.k[ks][0] = static_cast<uint32_t>(r[0]) | (static_cast<uint32_t>(r[kRow]) << 8);
+            f.k[ks][0] = static_cast<uint32_t>(r[0]) | (static_cast<uint32_t>(r[kRow]) << 16);
             f.k[ks][1] =
-                static_cast<uint32_t>(r[8 * kRow]) | (static_cast<uint32_t>(r[9 * kRow]) << 8);
+                static_cast<uint32_t>(r[8 * kRow]) | (static_cast<uint32_t>(r[9 * kRow]) << 16);
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
             const unsigned char *r = sV + (16 * mt + g) * kRow + 2 * c;
-            f.v[mt][0] = *reinterpret_cast<const unsigned short *>(r);
-            f.v[mt][1] = *reinterpret_cast<const unsigned short *>(r + 8 * kRow);
+            f.v[mt][0] = __byte_perm(*reinterpret_cast<const unsigned short *>(r), 0u, 0x4140u);
+            f.v[mt][1] =
+                __byte_perm(*reinterpret_cast<const unsigned short *>(r + 8 * kRow), 0u, 0x4140u);
         }
     }
 
