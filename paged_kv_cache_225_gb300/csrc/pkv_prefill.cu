@@ -34,13 +34,21 @@ namespace pkv {
 namespace {
 
 constexpr int kRowTile = 16;                  // rows per warp tile
-constexpr int kRowBlock = kWarps * kRowTile;  // rows per work item
+// Rows per work item (a multiple of 16, at most four warp tiles).
+#ifndef PKV_PREFILL_ROW_BLOCK
+#define PKV_PREFILL_ROW_BLOCK (kWarps * kRowTile)
+#endif
+constexpr int kRowBlock = PKV_PREFILL_ROW_BLOCK;
+static_assert(kRowBlock % kRowTile == 0 && kRowBlock <= kWarps * kRowTile, "row block");
 // Page ring per CTA and the CTAs per SM the registers are bounded for.
+// Three CTAs with 64 KB rings (168 registers, fragments read from the stage)
+// beat two with 96 KB rings by 20-25% (measured on GB300: 70B layer with five
+// queries per sequence 894 -> 695 us); four would spill.
 #ifndef PKV_PREFILL_RING_BYTES
-#define PKV_PREFILL_RING_BYTES (96 * 1024)
+#define PKV_PREFILL_RING_BYTES (64 * 1024)
 #endif
 #ifndef PKV_PREFILL_MIN_CTAS
-#define PKV_PREFILL_MIN_CTAS 2
+#define PKV_PREFILL_MIN_CTAS 3
 #endif
 constexpr int kPrefillRingBytes = PKV_PREFILL_RING_BYTES;
 
@@ -194,18 +202,25 @@ __device__ __forceinline__ bool causal_update(const float (&sacc)[4], int tokA, 
     return true;
 }
 
-// One page for one warp's 16 rows: scores, causal softmax, P V.  `lim` holds
-// the visible-token count of the page for each of the lane's four row columns.
+// One page for one warp's 16 rows: scores, causal softmax, P V, with the
+// fragments read straight from the stage: K per k step while S^T
+// accumulates, V after the softmax, so the two sets are never live together
+// (the caller holds the stage until this returns).  `lim` holds the
+// visible-token count of the page for each of the lane's four row columns;
 // NT = 1 when the tile's rows all sit in its first 8-row N tile (the second
 // tile's state then stays empty).
 template <int D, int NT>
-__device__ __forceinline__ void prefill_page(typename MmaStateBase<D, 2>::State &st,
-                                             typename MmaBf16Policy<D, 2>::Frags &f, int valid,
-                                             const int (&lim)[2][2], int lane, float c)
+__device__ __forceinline__ void prefill_page_smem(typename MmaStateBase<D, 2>::State &st,
+                                                  const unsigned char *sK,
+                                                  const unsigned char *sV, int valid,
+                                                  const int (&lim)[2][2], int lane, float c)
 {
     using Base = MmaStateBase<D, 2>;
     constexpr int KS = Base::KS, MT = Base::MT;
     const int r = lane >> 2, cc = lane & 3;
+    const int mi = lane >> 3, ri = lane & 7;
+    const uint32_t ka = smem_u32(sK) + (ri + 8 * (mi >> 1)) * 32 + (mi & 1) * 16;
+    const uint32_t va = smem_u32(sV) + (ri + 8 * (mi & 1)) * 32 + (mi >> 1) * 16;
     float sacc[NT][4], sodd[NT][4];
 #pragma unroll
     for (int n = 0; n < NT; ++n)
@@ -213,10 +228,13 @@ __device__ __forceinline__ void prefill_page(typename MmaStateBase<D, 2>::State 
         for (int e = 0; e < 4; ++e)
             sacc[n][e] = sodd[n][e] = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < KS; ++ks)
+    for (int ks = 0; ks < KS; ++ks) {
+        uint32_t kf[4];
+        ldsm_x4_t(kf, ka + ks * 16 * 32);
 #pragma unroll
         for (int n = 0; n < NT; ++n)
-            mma_bf16((ks & 1) ? sodd[n] : sacc[n], f.k[ks], st.qf[ks][n][0], st.qf[ks][n][1]);
+            mma_bf16((ks & 1) ? sodd[n] : sacc[n], kf, st.qf[ks][n][0], st.qf[ks][n][1]);
+    }
 #pragma unroll
     for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -238,6 +256,10 @@ __device__ __forceinline__ void prefill_page(typename MmaStateBase<D, 2>::State 
         bl0[n] = movmatrix_t(lx);
         bl1[n] = movmatrix_t(ly);
     }
+    uint32_t vf[MT][4];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+        ldsm_x4(vf[mt], va + mt * 16 * 32);
     if (valid < kBlockSize) {  // past the sequence end: zero V (may hold NaN)
         const uint32_t mlo = (2 * cc < valid ? 0x0000ffffu : 0u) |
                              (2 * cc + 1 < valid ? 0xffff0000u : 0u);
@@ -245,22 +267,22 @@ __device__ __forceinline__ void prefill_page(typename MmaStateBase<D, 2>::State 
                              (9 + 2 * cc < valid ? 0xffff0000u : 0u);
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {
-            f.v[mt][0] &= mlo;
-            f.v[mt][1] &= mlo;
-            f.v[mt][2] &= mhi;
-            f.v[mt][3] &= mhi;
+            vf[mt][0] &= mlo;
+            vf[mt][1] &= mlo;
+            vf[mt][2] &= mhi;
+            vf[mt][3] &= mhi;
         }
     }
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
-            mma_bf16(st.o[mt][n], f.v[mt], bh0[n], bh1[n]);
+            mma_bf16(st.o[mt][n], vf[mt], bh0[n], bh1[n]);
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
         for (int n = 0; n < NT; ++n)
-            mma_bf16(st.o[mt][n], f.v[mt], bl0[n], bl1[n]);
+            mma_bf16(st.o[mt][n], vf[mt], bl0[n], bl1[n]);
 }
 
 __device__ __forceinline__ void store_row4(const PrefillParams &p, int D, int token, int h,
@@ -283,7 +305,6 @@ __global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
 {
     using Geo = PrefillGeom<D>;
     using Base = MmaStateBase<D, 2>;
-    using Pol = MmaBf16Policy<D, 2>;
     constexpr int NS = Geo::NS;
     constexpr int KS = Base::KS;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -472,19 +493,9 @@ __global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
             }
             const bool have = s_ok[stg] != 0;
             const unsigned char *sk = smem + stg * Geo::kStageBytes;
-            typename Pol::Frags f;
             // A warp whose row tile is empty (three tiles of rows on four
             // warps) only releases the stage.
             const bool work = have && rt < RT;
-            if (work)
-                Pol::load(f, sk, sk + Geo::kTileBytes, lane);
-            // The stage is free once every lane's reads are done.
-            fence_proxy_async();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&empty[stg]);
-            if (warp == 0)
-                issue_upto(j + NS, false);
             if (work) {
                 const int tb = (pg0 + j) * kBlockSize;  // position of the page's token 0
                 const int valid = min(kBlockSize, L - tb);
@@ -497,10 +508,17 @@ __global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
                         lim[n][e] = v < valid ? v : valid;
                     }
                 if (two_tiles)
-                    prefill_page<D, 2>(st, f, valid, lim, lane, c);
+                    prefill_page_smem<D, 2>(st, sk, sk + Geo::kTileBytes, valid, lim, lane, c);
                 else
-                    prefill_page<D, 1>(st, f, valid, lim, lane, c);
+                    prefill_page_smem<D, 1>(st, sk, sk + Geo::kTileBytes, valid, lim, lane, c);
             }
+            // The stage is free once every lane's reads are done.
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stg]);
+            if (warp == 0)
+                issue_upto(j + NS, false);
         }
         // Warp 0 issues whatever the other warps still wait for.
         if (warp == 0 && !aborted)
