@@ -88,6 +88,7 @@ typedef enum {
 #define PKV_FLAG_IMPL_AUTO 0x0      /* tensor-core path when it applies, else CUDA cores */
 #define PKV_FLAG_IMPL_SIMT 0x1      /* force the CUDA-core (FFMA) kernel                 */
 #define PKV_FLAG_IMPL_MMA  0x2      /* force the tensor-core (mma.sync) kernel           */
+#define PKV_FLAG_IMPL_TC   0x3      /* pkv_paged_attn_prefill only: the tcgen05 kernel   */
 #define PKV_FLAG_IMPL_MASK 0x3
 /* Split sequences are merged by the decode kernel itself (the CTA finishing a
  * sequence's last partition merges it).  This flag merges them in a second

@@ -33,7 +33,7 @@ __all__ = ["paged_attn_decode", "paged_attn_decode_append", "paged_attn_prefill"
            "INT4"]
 
 F32, BF16, FP8_E5M2, FP8_E4M3, INT4 = 0, 1, 2, 3, 4
-IMPL = {"auto": 0x0, "simt": 0x1, "mma": 0x2}
+IMPL = {"auto": 0x0, "simt": 0x1, "mma": 0x2, "tc": 0x3}  # "tc": several-queries kernel only
 FLAG_SEPARATE_MERGE = 0x4
 FLAG_TEST_DROP_FIRST_COPY = 0x100
 STATUS = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",

@@ -18,9 +18,9 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libpkv.so")
 UNITS = ["pkv_api.cu", "pkv_cache.cu", "pkv_merge.cu", "pkv_decode_simt.cu",
          "pkv_decode_simt_fp8.cu", "pkv_decode_mma.cu",
-         "pkv_noalloc.cu", "pkv_prefill.cu", "pkv_block_manager.cpp"]
+         "pkv_noalloc.cu", "pkv_prefill.cu", "pkv_prefill_tc.cu", "pkv_block_manager.cpp"]
 HEADERS = ["pkv_common.cuh", "pkv_convert.cuh", "pkv_decode.cuh", "pkv_merge.cuh",
-           "pkv_streamk.cuh", "pkv_internal.h"]
+           "pkv_streamk.cuh", "pkv_prefill.cuh", "pkv_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 

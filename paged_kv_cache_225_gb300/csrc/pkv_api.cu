@@ -505,8 +505,7 @@ pkv_status pkv_paged_attn_prefill(const void *q, pkv_dtype q_dtype, const int32_
     if (!std::isfinite(scale))
         return PKV_ERR_INVALID_ARG;
     if ((flags & ~(PKV_FLAG_IMPL_MASK | PKV_FLAG_TEST_DROP_FIRST_COPY)) != 0 ||
-        (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_SIMT ||
-        (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_MASK)
+        (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_SIMT)
         return PKV_ERR_INVALID_ARG;
     PrefillPlan pl;
     if (!make_prefill_plan(num_seqs, num_tokens, num_q_heads, num_kv_heads, head_dim, block_size,
@@ -551,6 +550,7 @@ pkv_status pkv_paged_attn_prefill(const void *q, pkv_dtype q_dtype, const int32_
     p.partition = pl.partition > 0 ? pl.partition : max_blocks_per_seq * kBlockSize;
     p.max_parts = pl.max_parts;
     p.drop_first_copy = (flags & PKV_FLAG_TEST_DROP_FIRST_COPY) ? 1 : 0;
+    p.impl = (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_TC ? PKV_FLAG_IMPL_TC : PKV_FLAG_IMPL_MMA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess)  // status word and work counter
         return PKV_ERR_CUDA;

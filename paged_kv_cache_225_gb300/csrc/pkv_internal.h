@@ -75,6 +75,7 @@ struct PrefillParams {
     int partition;           // tokens per partition (multiple of 16)
     int max_parts;           // 1: no split
     int drop_first_copy;     // test hook: never issue the first copy of item 0
+    int impl;                // PKV_FLAG_IMPL_MMA (mma.sync) or PKV_FLAG_IMPL_TC (tcgen05)
 };
 
 constexpr int kBlockSize = 16;
@@ -106,6 +107,8 @@ pkv_status launch_decode_mma(const DecodeParams &p, int kv_dtype, cudaStream_t s
 pkv_status launch_merge(const DecodeParams &p, cudaStream_t stream);
 bool mma_supports(int kv_dtype, int q_dtype, int head_dim, int group);
 pkv_status launch_prefill(const PrefillParams &p, int kv_dtype, cudaStream_t stream);
+// The tcgen05 form of the several-queries kernel (bf16, head_dim 64 / 128).
+pkv_status launch_prefill_tc(const PrefillParams &p, cudaStream_t stream);
 
 pkv_status launch_reshape_and_cache(const void *k, const void *v, int in_dtype,
                                     const int64_t *slot_mapping, int num_tokens,

@@ -27,7 +27,7 @@
 //    of the item.  A row whose visible context fits one partition is written
 //    to `out`; the others leave normalised partials (o, m, l) that
 //    prefill_merge_kernel combines with log-sum-exp weights.
-#include "pkv_decode.cuh"
+#include "pkv_prefill.cuh"
 
 namespace pkv {
 
@@ -62,94 +62,6 @@ template <int D> struct PrefillGeom {
     static_assert(kWarps * kScratchFloats * 4 <= kRingBytes, "merge scratch fits in the ring");
     static_assert((kScratchFloats * 4) % 16 == 0, "warp scratch keeps float4 alignment");
 };
-
-struct SeqInfo {
-    int L;   // cached tokens (the queries included)
-    int q0;  // first query row in q
-    int nq;  // queries (0 when the sequence's arguments are invalid)
-};
-
-__device__ __forceinline__ SeqInfo seq_info(const PrefillParams &p, int s)
-{
-    SeqInfo si;
-    int L = __ldg(p.seq_lens + s);
-    if (L < 0 || L > p.max_len) {
-        set_status(p.status, PKV_ERR_OUT_OF_RANGE);
-        L = L < 0 ? 0 : p.max_len;
-    }
-    const int a = __ldg(p.q_start + s), b = __ldg(p.q_start + s + 1);
-    si.L = L;
-    si.q0 = a;
-    si.nq = b - a;
-    if (a < 0 || b > p.num_tokens || b < a || b - a > L || b - a > p.max_q_len) {
-        set_status(p.status, PKV_ERR_OUT_OF_RANGE);
-        si.q0 = 0;
-        si.nq = 0;
-    }
-    return si;
-}
-
-__device__ __forceinline__ int seq_parts(const PrefillParams &p, int L)
-{
-    return p.max_parts > 1 ? parts_of(L, p.partition) : 1;
-}
-
-// Items of sequence s: KV heads x partitions x row blocks.
-__device__ __forceinline__ int seq_item_count(const PrefillParams &p, const SeqInfo &si)
-{
-    const int blocks = (si.nq * p.group + kRowBlock - 1) / kRowBlock;
-    return p.num_kv_heads * seq_parts(p, si.L) * blocks;
-}
-
-struct PrefillItem {
-    int s, hkv, part, rb, L, q0, nq;
-};
-
-// Warp-collective: maps item index u to its (sequence, KV head, partition,
-// row block).  (cur_s, cur_base) keep the scan position between calls; u only
-// grows.  Returns false past the last item.
-__device__ bool find_prefill_item(const PrefillParams &p, int u, int &cur_s, int &cur_base,
-                                  int lane, PrefillItem &it)
-{
-    const int S = p.num_seqs;
-    for (;;) {
-        const int sl = cur_s + lane;
-        int n = 0;
-        SeqInfo si = {0, 0, 0};
-        if (sl < S) {
-            si = seq_info(p, sl);
-            n = seq_item_count(p, si);
-        }
-        int incl = n;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int t = __shfl_up_sync(kFullMask, incl, off);
-            if (lane >= off)
-                incl += t;
-        }
-        const int tot = __shfl_sync(kFullMask, incl, 31);
-        if (u < cur_base + tot) {
-            const unsigned bal = __ballot_sync(kFullMask, cur_base + incl > u);
-            const int ln = __ffs(bal) - 1;
-            const int excl = __shfl_sync(kFullMask, incl - n, ln);
-            it.s = cur_s + ln;
-            it.L = __shfl_sync(kFullMask, si.L, ln);
-            it.q0 = __shfl_sync(kFullMask, si.q0, ln);
-            it.nq = __shfl_sync(kFullMask, si.nq, ln);
-            const int k = u - cur_base - excl;
-            const int blocks = (it.nq * p.group + kRowBlock - 1) / kRowBlock;
-            const int parts = seq_parts(p, it.L);
-            it.rb = k % blocks;
-            it.part = (k / blocks) % parts;
-            it.hkv = k / (blocks * parts);
-            return true;
-        }
-        if (cur_s + 32 >= S)
-            return false;
-        cur_base += tot;
-        cur_s += 32;
-    }
-}
 
 __device__ __forceinline__ void mbar_inval(uint64_t *bar)
 {
@@ -330,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
         __syncthreads();
         if (warp == 0) {
             PrefillItem it;
-            const bool ok = find_prefill_item(p, s_item[0], cur_s, cur_base, lane, it);
+            const bool ok = find_prefill_item<kRowBlock>(p, s_item[0], cur_s, cur_base, lane, it);
             if (lane == 0) {
                 s_item[1] = ok ? 1 : 0;
                 if (ok) {
@@ -665,26 +577,32 @@ pkv_status launch_prefill_d(const PrefillParams &p, cudaStream_t stream)
     prefill_kernel<D><<<static_cast<unsigned>(grid), kThreads, Geo::kSmem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess)
         return PKV_ERR_CUDA;
-    if (p.max_parts > 1 && p.num_tokens > 0) {
-        const long mgrid = static_cast<long>(p.num_tokens) * p.num_kv_heads;
-        prefill_merge_kernel<D><<<static_cast<unsigned>(mgrid), kThreads, 0, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess)
-            return PKV_ERR_CUDA;
-    }
-    return PKV_OK;
+    return launch_prefill_merge(p, stream);
 }
 
 }  // namespace
+
+pkv_status launch_prefill_merge(const PrefillParams &p, cudaStream_t stream)
+{
+    if (p.max_parts <= 1 || p.num_tokens <= 0)
+        return PKV_OK;
+    const long mgrid = static_cast<long>(p.num_tokens) * p.num_kv_heads;
+    if (p.head_dim == 128)
+        prefill_merge_kernel<128><<<static_cast<unsigned>(mgrid), kThreads, 0, stream>>>(p);
+    else
+        prefill_merge_kernel<64><<<static_cast<unsigned>(mgrid), kThreads, 0, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 pkv_status launch_prefill(const PrefillParams &p, int kv_dtype, cudaStream_t stream)
 {
     if (kv_dtype != PKV_BF16 || p.group < 1 || p.group > 16)
         return PKV_ERR_UNSUPPORTED;
-    if (p.head_dim == 128)
-        return launch_prefill_d<128>(p, stream);
-    if (p.head_dim == 64)
-        return launch_prefill_d<64>(p, stream);
-    return PKV_ERR_UNSUPPORTED;
+    if (p.head_dim != 128 && p.head_dim != 64)
+        return PKV_ERR_UNSUPPORTED;
+    if (p.impl == PKV_FLAG_IMPL_TC)
+        return launch_prefill_tc(p, stream);
+    return p.head_dim == 128 ? launch_prefill_d<128>(p, stream) : launch_prefill_d<64>(p, stream);
 }
 
 }  // namespace pkv

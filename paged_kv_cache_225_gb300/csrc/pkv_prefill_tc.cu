@@ -1,0 +1,810 @@
+// Paged attention of several query tokens per sequence on the tcgen05 tensor
+// cores of sm_103a (chunked prefill, speculative verification).
+//
+// What is computed is the same as the mma.sync form in pkv_prefill.cu: the
+// block-table walk of the PagedAttention kernel pseudocode ("vLLM e
+// PagedAttention: serving high-throughput") with the causal mask of the
+// "Inference optimization" lesson (Step 2, scaled_dot_product_attention,
+// triu mask of offset seq_len_k - seq_len_q + 1); query i of the n queries of
+// a sequence of L cached tokens attends the rows t <= L - n + i.
+//
+// How it is laid out on the GPU (not taken from the pages):
+//  * An item is (sequence, KV head, context partition, block of up to 128
+//    rows), a row being one (query token, grouped query head) pair.  Every
+//    K/V page crosses HBM once per item.
+//  * Six warps with fixed roles.  Warp 4 (producer) pulls items from an
+//    atomic counter, hands them to the others through a two-slot queue, and
+//    copies K and V with tensor-map (TMA) loads into a ring of stages of two
+//    pages each.  Warp 5 (one thread) issues the MMAs.  Warps 0-3 own one row
+//    per thread (TMEM lane = row): Q, softmax, P, rescaling, output.
+//  * Tensor memory holds O (128 x head_dim f32), two score buffers of 32
+//    columns and the item's Q (bf16 pairs, the A operand of S).  Per chunk of
+//    two pages: S = Q K^T (M = 128, N = 32 tokens, head_dim / 16 MMAs of
+//    K = 16); each row's thread reads its 32 scores, applies the causal limit
+//    and the online softmax, and writes P back over its consumed scores as a
+//    bf16 high part and a bf16 residual; then O += P_hi V + P_lo V (M = 128,
+//    N = head_dim, K = 16 per page) with P read from tensor memory.  The
+//    scores of chunk i + 1 are issued before P V of chunk i.
+//  * The running max is updated lazily (only when a score exceeds it by
+//    2^8); O is then rescaled in TMEM by the rows' threads once the previous
+//    P V has completed.
+//  * Each page tile [head_dim][16 tokens] is copied as two halves of 8
+//    tokens, so that it lands as [half][head_dim][8]: the interleaved
+//    (no-swizzle) layout of 8-row x 16-byte core matrices.  The two K tiles
+//    of a stage are adjacent, so one MMA with N = 32 reads both (MN-major);
+//    V tiles are read K-major.
+//  * Every wait is bounded; a timeout records PKV_ERR_TIMEOUT, stops every
+//    role, lets copies and MMAs in flight finish and frees TMEM.
+#include <cuda.h>  // CUtensorMap and its enums; the encoder is looked up at run time
+
+#include "pkv_prefill.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kTcRows = 128;  // rows per item = the MMA's M
+constexpr int kTcThreads = 192;
+constexpr int kProducerWarp = 4;
+constexpr int kMmaWarp = 5;
+
+constexpr int kChunk = 2;  // pages per softmax step
+
+template <int D> struct TcGeom {
+    static constexpr int kTile = D * kBlockSize * 2;  // one K or V page tile (bf16)
+    static constexpr int kHalf = kTile / 2;           // 8 tokens of every head_dim row
+    static constexpr int kVOff = kChunk * kTile;      // V tiles follow the K tiles
+    static constexpr int kStage = 2 * kChunk * kTile;
+    static constexpr int NS = (96 * 1024) / kStage;
+    static constexpr int kSmem = NS * kStage;
+    static constexpr int kSCols = kChunk * kBlockSize;  // score columns per buffer
+    static constexpr int kSCol = D;                     // two score buffers after O
+    static constexpr int kQCol = D + 2 * kSCols;        // Q as bf16 pairs: D / 2 columns
+    static constexpr int kTmemCols = 256;
+    static_assert(kQCol + D / 2 <= kTmemCols, "O, scores and Q fit the allocation");
+    static_assert(NS >= 4, "ring holds the two chunks in use and copies ahead");
+};
+
+// ------------------------------------------------------------ tcgen05 / TMA
+
+__device__ __forceinline__ void tc_fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, interleaved (no swizzle) layout: start
+// address, byte distance between core matrices along K (leading) and along
+// M / N (stride), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = static_cast<uint64_t>((addr >> 4) & 0x3fffu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3fffu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3fffu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
+// Instruction descriptor of kind::f16: f32 accumulator, bf16 A and B, A
+// K-major, B K-major or MN-major, N and M.
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N, bool b_mn_major)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D (+)= A B with A read from tensor memory (row m in lane m, elements 2c
+// and 2c + 1 of a row in the low and high halves of column c) and B from a
+// shared-memory descriptor; D is overwritten when accumulate is false.
+__device__ __forceinline__ void tc_mma_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                          uint32_t idesc, bool accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate ? 1u : 0u));
+}
+
+// Arrives on bar once every MMA this thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+        "%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 3-D tensor-map load of one box into shared memory, completing on bar.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Bounded wait that also gives up once another role has aborted.
+__device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, const volatile int *abort)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort)
+            return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
+// Every lane waits (each needs the barrier's ordering); the warp agrees on
+// the outcome so that it stays converged for the .sync.aligned TMEM accesses.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const volatile int *abort)
+{
+    const bool ok = tc_wait(bar, parity, abort);
+    return __all_sync(kFullMask, ok);
+}
+
+__device__ __forceinline__ void tc_fail(const PrefillParams &p, volatile int *abort)
+{
+    set_status(p.status, PKV_ERR_TIMEOUT);
+    *abort = 1;
+}
+
+__device__ __forceinline__ void store_out4(const PrefillParams &p, int D, size_t orow, int q4,
+                                           float4 v)
+{
+    const size_t off = orow * D + 4 * q4;
+    if (p.out_dtype == PKV_F32) {
+        *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) = v;
+    } else {
+        uint2 w;
+        w.x = pack_bf16(v.x, v.y);
+        w.y = pack_bf16(v.z, v.w);
+        *reinterpret_cast<uint2 *>(static_cast<unsigned short *>(p.out) + off) = w;
+    }
+}
+
+struct TcMaps {
+    CUtensorMap k0, k1, v0, v1;  // K / V caches, token halves 0 and 1
+};
+
+struct TcItem {
+    int valid, s, hkv, part, rb, L, nq;
+};
+
+__device__ __forceinline__ TcItem read_item(const int *slot)
+{
+    TcItem it;
+    it.valid = slot[0];
+    it.s = slot[1];
+    it.hkv = slot[2];
+    it.part = slot[3];
+    it.rb = slot[4];
+    it.L = slot[5];
+    it.nq = slot[6];
+    return it;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const PrefillParams p, const __grid_constant__ TcMaps maps)
+{
+    using Geo = TcGeom<D>;
+    constexpr int NS = Geo::NS;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[NS], empty[NS];
+    __shared__ __align__(8) uint64_t s_full[2], p_full[2], pv_done[2];
+    __shared__ __align__(8) uint64_t item_full[2], item_empty[2];
+    __shared__ __align__(8) uint64_t q_full, o_free, drain;
+    __shared__ int s_item[2][8];
+    __shared__ int s_ok[NS][kChunk];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    volatile int *abort = &s_abort;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], 4);
+            mbar_init(&pv_done[i], 1);
+            mbar_init(&item_full[i], 1);
+            mbar_init(&item_empty[i], 5);  // the MMA thread and the four softmax warps
+        }
+        mbar_init(&q_full, 4);
+        mbar_init(&o_free, 4);
+        mbar_init(&drain, 1);
+        s_abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        asm volatile(
+            "tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                smem_u32(&s_tmem)),
+            "r"(Geo::kTmemCols)
+            : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    const int G = p.group;
+    const uint32_t smem0 = smem_u32(smem);
+
+    if (warp == kProducerWarp) {
+        // ------------------------------------------------------- producer
+        int cur_s = 0, cur_base = 0;
+        uint32_t gc = 0;  // chunks issued by this CTA
+        bool stop = false;
+        for (int k = 0; !stop; ++k) {
+            unsigned u = 0;
+            if (lane == 0)
+                u = atomicAdd(p.counter, 1u);
+            u = __shfl_sync(kFullMask, u, 0);
+            PrefillItem it;
+            const bool ok = find_prefill_item<kTcRows>(p, static_cast<int>(u), cur_s, cur_base,
+                                                       lane, it);
+            const int slot = k & 1;
+            int free_ok = 1;
+            if (k >= 2 && lane == 0)
+                free_ok = tc_wait(&item_empty[slot], ((k - 2) >> 1) & 1, abort);
+            free_ok = __shfl_sync(kFullMask, free_ok, 0);
+            if (!free_ok) {
+                if (lane == 0)
+                    tc_fail(p, abort);
+                break;
+            }
+            if (lane == 0) {
+                int *w = s_item[slot];
+                w[0] = ok ? 1 : 0;
+                w[1] = it.s;
+                w[2] = it.hkv;
+                w[3] = it.part;
+                w[4] = it.rb;
+                w[5] = it.L;
+                w[6] = it.nq;
+                mbar_arrive(&item_full[slot]);
+            }
+            if (!ok)
+                break;
+            const int row0 = it.rb * kTcRows;
+            const int nrows = min(kTcRows, it.nq * G - row0);
+            int pg0, npages;
+            item_pages(p, it.L, it.nq, row0, nrows, it.part, pg0, npages);
+            const int32_t *table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks + pg0;
+            for (int j0 = 0; j0 < npages && !stop; j0 += 32) {
+                const int ent = j0 + lane < npages ? __ldg(table + j0 + lane) : -1;
+                const int n = min(32, npages - j0);  // even unless it ends the item
+                for (int jj = 0; jj < n; jj += kChunk, ++gc) {
+                    const int stg = static_cast<int>(gc % NS);
+                    int ready = 1;
+                    if (gc >= NS && lane == 0)
+                        ready = tc_wait(&empty[stg], ((gc / NS) - 1) & 1, abort);
+                    ready = __shfl_sync(kFullMask, ready, 0);
+                    if (!ready) {
+                        if (lane == 0)
+                            tc_fail(p, abort);
+                        stop = true;
+                        break;
+                    }
+                    int phys[kChunk];
+#pragma unroll
+                    for (int x = 0; x < kChunk; ++x)
+                        phys[x] = __shfl_sync(kFullMask, ent, (jj + x) & 31);
+                    if (lane == 0) {
+                        int good[kChunk], ngood = 0;
+#pragma unroll
+                        for (int x = 0; x < kChunk; ++x) {
+                            const bool present = jj + x < n;
+                            good[x] = present && phys[x] >= 0 && phys[x] < p.num_blocks;
+                            if (present && !good[x])
+                                set_status(p.status, PKV_ERR_OUT_OF_RANGE);
+                            s_ok[stg][x] = good[x];
+                            ngood += good[x];
+                        }
+                        if (ngood == 0) {
+                            mbar_arrive(&full[stg]);
+                        } else {
+                            mbar_arrive_expect_tx(&full[stg], ngood * 2 * Geo::kTile);
+                            unsigned char *st = smem + stg * Geo::kStage;
+#pragma unroll
+                            for (int x = 0; x < kChunk; ++x) {
+                                if (!good[x] ||
+                                    (p.drop_first_copy && blockIdx.x == 0 && gc == 0 && x == 0))
+                                    continue;
+                                unsigned char *dk = st + x * Geo::kTile;
+                                unsigned char *dv = st + Geo::kVOff + x * Geo::kTile;
+                                const int c2 = phys[x] * p.num_kv_heads + it.hkv;
+                                tma_load_3d(dk, &maps.k0, 0, 0, c2, &full[stg]);
+                                tma_load_3d(dk + Geo::kHalf, &maps.k1, 0, 0, c2, &full[stg]);
+                                tma_load_3d(dv, &maps.v0, 0, 0, c2, &full[stg]);
+                                tma_load_3d(dv + Geo::kHalf, &maps.v1, 0, 0, c2, &full[stg]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        if (*abort && lane == 0) {
+            // Let every copy still in flight land before the CTA exits.
+            const uint32_t lo = gc > NS ? gc - NS : 0;
+            for (uint32_t q = lo; q < gc; ++q)
+                mbar_wait_bounded(&full[q % NS], (q / NS) & 1, kWaitLimitNs);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t kIdS = tc_idesc(kTcRows, Geo::kSCols, true);
+            constexpr uint32_t kIdPV = tc_idesc(kTcRows, D, false);
+            uint32_t gc = 0;       // chunks
+            uint32_t counted = 0;  // items with pages
+            bool failed = false;
+            bool o_started = false, o_wait = false;
+            // P V of chunk c: waits for its P, and before the first P V of an
+            // item for the previous item's output to have been read.
+            auto issue_pv = [&](uint32_t c) -> bool {
+                if (!tc_wait(&p_full[c & 1], (c >> 1) & 1, abort))
+                    return false;
+                if (o_wait) {
+                    if (!tc_wait(&o_free, (counted - 2) & 1, abort))
+                        return false;
+                    o_wait = false;
+                }
+                tc_fence_after();
+                const int stg = static_cast<int>(c % NS);
+                const uint32_t pcol = tmem + Geo::kSCol + Geo::kSCols * (c & 1);
+#pragma unroll
+                for (int x = 0; x < kChunk; ++x) {
+                    if (!s_ok[stg][x])
+                        continue;
+                    const uint64_t vdesc = smem_desc(
+                        smem0 + stg * Geo::kStage + Geo::kVOff + x * Geo::kTile, Geo::kHalf, 128);
+                    tc_mma_ta(tmem, pcol + 8 * x, vdesc, kIdPV, o_started);
+                    tc_mma_ta(tmem, pcol + Geo::kSCols / 2 + 8 * x, vdesc, kIdPV, true);
+                    o_started = true;
+                }
+                tc_commit(&pv_done[c & 1]);
+                tc_commit(&empty[stg]);
+                return true;
+            };
+            for (int k = 0; !failed; ++k) {
+                const int slot = k & 1;
+                if (!tc_wait(&item_full[slot], (k >> 1) & 1, abort)) {
+                    failed = true;
+                    break;
+                }
+                const TcItem it = read_item(s_item[slot]);
+                mbar_arrive(&item_empty[slot]);
+                if (!it.valid)
+                    break;
+                const int row0 = it.rb * kTcRows;
+                const int nrows = min(kTcRows, it.nq * G - row0);
+                int pg0, npages;
+                item_pages(p, it.L, it.nq, row0, nrows, it.part, pg0, npages);
+                if (npages == 0)
+                    continue;
+                if (!tc_wait(&q_full, counted & 1, abort)) {
+                    failed = true;
+                    break;
+                }
+                ++counted;
+                o_started = false;
+                o_wait = counted >= 2;
+                const int nchunks = (npages + kChunk - 1) / kChunk;
+                for (int j = 0; j < nchunks; ++j, ++gc) {
+                    const int stg = static_cast<int>(gc % NS);
+                    if (!tc_wait(&full[stg], (gc / NS) & 1, abort)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    // Scores of both pages in one MMA per k step (absent or
+                    // bad pages leave stale columns that the softmax masks).
+                    const uint32_t scol = tmem + Geo::kSCol + Geo::kSCols * (gc & 1);
+                    const uint32_t kaddr = smem0 + stg * Geo::kStage;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        tc_mma_ta(scol, tmem + Geo::kQCol + 8 * ks,
+                                  smem_desc(kaddr + ks * 256, 128, Geo::kHalf), kIdS, ks > 0);
+                    tc_commit(&s_full[gc & 1]);
+                    if (j > 0 && !issue_pv(gc - 1)) {
+                        failed = true;
+                        break;
+                    }
+                }
+                if (failed || !issue_pv(gc - 1)) {
+                    failed = true;
+                    break;
+                }
+            }
+            if (failed)
+                tc_fail(p, abort);
+            // Every MMA issued has completed before TMEM is freed.
+            tc_commit(&drain);
+            mbar_wait_bounded(&drain, 0, kWaitLimitNs);
+        }
+    } else {
+        // ---------------------------------------- Q, softmax and output
+        const int t = threadIdx.x;  // row of the item = TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+        const float c = p.score_scale;
+        constexpr float kLazy = MmaSoftmax::kLazy;
+        constexpr int kTok = Geo::kSCols;  // tokens per chunk
+        uint32_t gc = 0;
+        for (int k = 0;; ++k) {
+            const int slot = k & 1;
+            if (!warp_wait(&item_full[slot], (k >> 1) & 1, abort))
+                break;
+            const TcItem it = read_item(s_item[slot]);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&item_empty[slot]);
+            if (!it.valid)
+                break;
+            const int row0 = it.rb * kTcRows;
+            const int nrows = min(kTcRows, it.nq * G - row0);
+            int pg0, npages;
+            item_pages(p, it.L, it.nq, row0, nrows, it.part, pg0, npages);
+            if (npages == 0)
+                continue;
+            const int q0 = __ldg(p.q_start + it.s);  // validated by the item scan
+            const bool row_ok = t < nrows;
+            const int R = row0 + (row_ok ? t : 0);
+            const int qi = R / G;
+            const int h = it.hkv * G + R % G;
+            const int pos = it.L - it.nq + qi;  // position of this row's query
+
+            // Q row into tensor memory as bf16 pairs (zero past the item).
+            // The previous item's scores have all been read, so every MMA
+            // that used the old Q has completed.
+            {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    static_cast<const unsigned short *>(p.q) +
+                    (static_cast<size_t>(q0 + qi) * p.num_q_heads + h) * D);
+#pragma unroll 1
+                for (int c0 = 0; c0 < D / 2; c0 += 16) {
+                    uint32_t r[16];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint4 v = row_ok ? __ldg(src + c0 / 4 + e) : make_uint4(0, 0, 0, 0);
+                        r[4 * e] = v.x;
+                        r[4 * e + 1] = v.y;
+                        r[4 * e + 2] = v.z;
+                        r[4 * e + 3] = v.w;
+                    }
+                    tmem_st16u(tmem + lane_base + Geo::kQCol + c0, r);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&q_full);
+
+            float m = -INFINITY, l = 0.f;
+            bool o_valid = false;
+            bool failed = false;
+            const int32_t *table =
+                p.block_tables + static_cast<size_t>(it.s) * p.max_blocks + pg0;
+            int ent = -1;
+            const int nchunks = (npages + kChunk - 1) / kChunk;
+            for (int j = 0; j < nchunks; ++j, ++gc) {
+                const int jp = j * kChunk;  // first page of the chunk
+                if ((jp & 31) == 0)
+                    ent = jp + lane < npages ? __ldg(table + jp + lane) : -1;
+                bool good[kChunk];
+                bool any_good = false;
+#pragma unroll
+                for (int x = 0; x < kChunk; ++x) {
+                    const int phys = __shfl_sync(kFullMask, ent, (jp + x) & 31);
+                    good[x] = jp + x < npages && phys >= 0 && phys < p.num_blocks;
+                    any_good = any_good || good[x];
+                }
+                if (!warp_wait(&s_full[gc & 1], (gc >> 1) & 1, abort)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t scol = tmem + lane_base + Geo::kSCol + Geo::kSCols * (gc & 1);
+                float sv[kTok];
+#pragma unroll
+                for (int x = 0; x < kChunk; ++x) {
+                    float part[16];
+                    tmem_ld16(scol + 16 * x, part);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        sv[16 * x + e] = part[e];
+                }
+                const int tb = (pg0 + jp) * kBlockSize;  // position of the chunk's token 0
+                int lim[kChunk];                          // tokens of each page this row sees
+#pragma unroll
+                for (int x = 0; x < kChunk; ++x) {
+                    int v = pos - (tb + 16 * x) + 1;
+                    v = v < 0 ? 0 : (v > kBlockSize ? kBlockSize : v);
+                    lim[x] = (row_ok && good[x]) ? v : 0;
+                }
+                float mx = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < kTok; ++e)
+                    if ((e & 15) < lim[e >> 4])
+                        mx = fmaxf(mx, sv[e] * c);
+                const bool need = mx > m + kLazy;  // false when nothing is visible
+                float alpha = 1.f;
+                if (need) {
+                    alpha = m == -INFINITY ? 0.f : MmaSoftmax::ex2(m - mx);
+                    l *= alpha;
+                    m = mx;
+                }
+                if (o_valid && __any_sync(kFullMask, need)) {
+                    // O holds earlier chunks: rescale it once their P V is done.
+                    if (!warp_wait(&pv_done[(gc - 1) & 1], ((gc - 1) >> 1) & 1, abort)) {
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 16) {
+                        float ov[16];
+                        tmem_ld16(tmem + lane_base + c0, ov);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            ov[e] *= alpha;
+                        tmem_st16(tmem + lane_base + c0, ov);
+                    }
+                    tmem_wait_st();
+                }
+                // P over the consumed scores: high parts in the first half of
+                // the buffer, residuals in the second (bf16 pairs).
+                uint32_t hi[kTok / 2], lo[kTok / 2];
+                float psum = 0.f;
+#pragma unroll
+                for (int e = 0; e < kTok; e += 2) {
+                    const float a = (e & 15) < lim[e >> 4] ? MmaSoftmax::ex2(sv[e] * c - m) : 0.f;
+                    const float b =
+                        ((e + 1) & 15) < lim[(e + 1) >> 4] ? MmaSoftmax::ex2(sv[e + 1] * c - m) : 0.f;
+                    psum += a + b;
+                    hi[e / 2] = pack_bf16(a, b);
+                    lo[e / 2] = pack_bf16(a - bf16_lo(hi[e / 2]), b - bf16_hi(hi[e / 2]));
+                }
+                l += psum;
+                tmem_st16u(scol, hi);
+                tmem_st16u(scol + kTok / 2, lo);
+                tmem_wait_st();
+                // Past the sequence end the V tile may hold anything (NaN):
+                // zero those tokens, since P = 0 does not cancel NaN.
+                bool zeroed = false;
+#pragma unroll
+                for (int x = 0; x < kChunk; ++x) {
+                    const int valid = it.L - (tb + 16 * x);
+                    if (good[x] && valid > 0 && valid < kBlockSize) {
+                        if (t < D) {
+                            unsigned short *vt = reinterpret_cast<unsigned short *>(
+                                smem + (gc % NS) * Geo::kStage + Geo::kVOff + x * Geo::kTile);
+                            for (int e = valid; e < kBlockSize; ++e)
+                                vt[(e >> 3) * (Geo::kHalf / 2) + t * 8 + (e & 7)] = 0;
+                        }
+                        zeroed = true;
+                    }
+                }
+                if (zeroed)
+                    fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&p_full[gc & 1]);
+                o_valid = o_valid || any_good;
+            }
+            if (failed) {
+                tc_fail(p, abort);
+                break;
+            }
+
+            // ------------------------------------------------ output rows
+            if (o_valid) {
+                if (!warp_wait(&pv_done[(gc - 1) & 1], ((gc - 1) >> 1) & 1, abort)) {
+                    tc_fail(p, abort);
+                    break;
+                }
+                tc_fence_after();
+            }
+            const int nparts_r = p.max_parts > 1 ? parts_of(pos + 1, p.partition) : 1;
+            const bool write = row_ok && it.part < nparts_r;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const size_t orow = static_cast<size_t>(q0 + qi) * p.num_q_heads + h;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 16) {
+                float ov[16];
+                if (o_valid) {
+                    tmem_ld16(tmem + lane_base + c0, ov);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        ov[e] = 0.f;
+                }
+                if (!write)
+                    continue;
+                if (nparts_r == 1) {
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        store_out4(p, D, orow, c0 / 4 + q4,
+                                   make_float4(ov[4 * q4] * inv, ov[4 * q4 + 1] * inv,
+                                               ov[4 * q4 + 2] * inv, ov[4 * q4 + 3] * inv));
+                } else {
+                    const size_t prow = orow * p.max_parts + it.part;
+                    float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * D + c0);
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4)
+                        dst[q4] = make_float4(ov[4 * q4] * inv, ov[4 * q4 + 1] * inv,
+                                              ov[4 * q4 + 2] * inv, ov[4 * q4 + 3] * inv);
+                }
+            }
+            if (write && nparts_r > 1) {
+                const size_t prow = orow * p.max_parts + it.part;
+                p.part_ml[2 * prow] = m;
+                p.part_ml[2 * prow + 1] = l;
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&o_free);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(Geo::kTmemCols)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder()
+{
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// Token half `half` of every [head_dim][16] tile of a bf16 cache, viewed as
+// [num_blocks * num_kv_heads][head_dim][8]: one box is a page's half tile.
+bool encode_half(EncodeTiledFn enc, CUtensorMap *map, const void *cache, int half, int D,
+                 long tiles)
+{
+    const cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(tiles)};
+    const cuuint64_t strides[2] = {kBlockSize * 2, static_cast<cuuint64_t>(D) * kBlockSize * 2};
+    const cuuint32_t box[3] = {8, static_cast<cuuint32_t>(D), 1};
+    const cuuint32_t es[3] = {1, 1, 1};
+    void *base = const_cast<unsigned char *>(static_cast<const unsigned char *>(cache) + 16 * half);
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
+{
+    using Geo = TcGeom<D>;
+    static int occ = -1;
+    if (occ < 0) {
+        if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Geo::kSmem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        int o = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, prefill_tc_kernel<D>, kTcThreads,
+                                                          Geo::kSmem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        // Two CTAs' TMEM columns fill an SM's 512.
+        occ = o < 1 ? 1 : (o > 512 / Geo::kTmemCols ? 512 / Geo::kTmemCols : o);
+    }
+    EncodeTiledFn enc = encoder();
+    if (!enc)
+        return PKV_ERR_CUDA;
+    const long tiles = static_cast<long>(p.num_blocks) * p.num_kv_heads;
+    if (tiles >= (1L << 31))
+        return PKV_ERR_UNSUPPORTED;
+    TcMaps maps;
+    if (!encode_half(enc, &maps.k0, p.k_cache, 0, D, tiles) ||
+        !encode_half(enc, &maps.k1, p.k_cache, 1, D, tiles) ||
+        !encode_half(enc, &maps.v0, p.v_cache, 0, D, tiles) ||
+        !encode_half(enc, &maps.v1, p.v_cache, 1, D, tiles))
+        return PKV_ERR_CUDA;
+    const long blocks = (static_cast<long>(p.max_q_len) * p.group + kTcRows - 1) / kTcRows;
+    const long items = static_cast<long>(p.num_seqs) * p.num_kv_heads * p.max_parts * blocks;
+    const long slots = static_cast<long>(occ) * device_sm_count();
+    const long grid = items < slots ? items : slots;
+    if (grid <= 0)
+        return PKV_OK;
+    prefill_tc_kernel<D><<<static_cast<unsigned>(grid), kTcThreads, Geo::kSmem, stream>>>(p, maps);
+    if (cudaGetLastError() != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return launch_prefill_merge(p, stream);
+}
+
+}  // namespace
+
+pkv_status launch_prefill_tc(const PrefillParams &p, cudaStream_t stream)
+{
+    return p.head_dim == 128 ? launch_tc_d<128>(p, stream) : launch_tc_d<64>(p, stream);
+}
+
+}  // namespace pkv

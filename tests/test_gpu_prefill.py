@@ -1,7 +1,8 @@
 """GPU parity of causal paged attention with several queries per sequence.
 
 The CUDA path (pkv_paged_attn_prefill, through the C ABI) against the fp64
-oracle element by element: the small mixed case under every split setting,
+oracle element by element, for both kernels (mma.sync and tcgen05): the
+small mixed case under every split setting,
 the speculative-verification and chunked-prefill layers at full size, edge
 shapes (whole-prompt prefill, one-token sequences, sequences without queries,
 row counts that fill one to four warp tiles and several row blocks, long
@@ -23,6 +24,13 @@ from gpu_util import TOL, max_abs, to_torch
 pytestmark = pytest.mark.gpu
 
 DEV = torch.device("cuda", 0)
+_IMPL = {"flags": 0}
+
+
+@pytest.fixture(params=["mma", "tc"], autouse=True)
+def impl(request):
+    _IMPL["flags"] = pkv.IMPL[request.param]
+    yield request.param
 
 
 def _device(w: W.PrefillWorkload) -> dict:
@@ -46,7 +54,7 @@ def _gpu(w, d, *, partition_tokens=0, out_dtype=torch.float32, flags=0, max_q_le
     pkv.paged_attn_prefill(d["q"], d["q_start"], d["k_cache"], d["v_cache"], d["block_tables"],
                            d["seq_lens"], w.scale, out, max_q_len=max_q_len or w.max_q_len,
                            max_seq_len=int(w.seq_lens.max()), partition_tokens=partition_tokens,
-                           workspace=ws, flags=flags)
+                           workspace=ws, flags=flags | _IMPL["flags"])
     torch.cuda.synchronize()
     status = pkv.read_status(ws)
     return out.float().cpu().numpy().astype(np.float64), status
@@ -154,6 +162,19 @@ def test_more_queries_than_tokens_is_reported():
     ref = _oracle(w)
     # Sequence 0 is still computed correctly.
     assert max_abs(out[:4], ref[:4]) <= TOL[W.BF16]
+
+
+def test_out_of_pool_page_is_reported_and_skipped():
+    w = _edge([40, 90, 33], [3, 5, 2], seed=13, Hq=16, Hkv=2, D=128)
+    d = _device(w)
+    tables = d["block_tables"].clone()
+    tables[1, 2] = w.k_cache.shape[0] + 7            # a page of sequence 1 outside the pool
+    d["block_tables"] = tables
+    out, status = _gpu(w, d)
+    assert status == 4  # PKV_ERR_OUT_OF_RANGE
+    ref = _oracle(w)
+    rows = np.r_[0:3, 8:10]                           # sequences 0 and 2
+    assert max_abs(out[rows], ref[rows]) <= TOL[W.BF16]
 
 
 def test_bounded_wait_reports_timeout_and_recovers():
