@@ -91,7 +91,8 @@ def parse_args(argv=None):
 
 
 # Sources that do not define or launch the decode kernels.
-_NOT_DECODE = {"pkv_cache.cu", "pkv_noalloc.cu", "pkv_prefill.cu"}
+_NOT_DECODE = {"pkv_cache.cu", "pkv_noalloc.cu", "pkv_prefill.cu", "pkv_prefill_tc.cu",
+               "pkv_prefill.cuh"}
 
 
 def source_hash() -> str:
@@ -747,8 +748,8 @@ def run_prefill(args):
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "tensor": {"achieved_tflops": tflops, "bf16_peak_tflops": bf16_peak,
                                 "frac": tflops / bf16_peak,
-                                "note": "mma.sync m16n8k16; P.V issued twice (bf16 high "
-                                        "part + residual)"}},
+                                "note": "tcgen05.mma kind::f16 (M = 128 rows, padded); "
+                                        "P.V issued twice (bf16 high part + residual)"}},
         "gpu_launches": K * launches,
         "clocks": clocks,
     }

@@ -250,7 +250,8 @@ pkv_status pkv_paged_attn_decode_head_scaled(
  *   partition_tokens   0 automatic, -1 never split a context, > 0 (multiple
  *                of 16) split every context into partitions of that many
  *                tokens merged with log-sum-exp weights.
- *   flags        PKV_FLAG_IMPL_AUTO or PKV_FLAG_IMPL_MMA, optionally
+ *   flags        PKV_FLAG_IMPL_AUTO (= PKV_FLAG_IMPL_TC, the tcgen05 kernel) or
+ *                PKV_FLAG_IMPL_MMA (the mma.sync kernel), optionally
  *                PKV_FLAG_TEST_DROP_FIRST_COPY.
  * head_dim 64 or 128, up to 16 query heads per KV head.  Errors as for
  * pkv_paged_attn_decode; on the device a sequence with n_s > L_s, n_s >

@@ -550,7 +550,8 @@ pkv_status pkv_paged_attn_prefill(const void *q, pkv_dtype q_dtype, const int32_
     p.partition = pl.partition > 0 ? pl.partition : max_blocks_per_seq * kBlockSize;
     p.max_parts = pl.max_parts;
     p.drop_first_copy = (flags & PKV_FLAG_TEST_DROP_FIRST_COPY) ? 1 : 0;
-    p.impl = (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_TC ? PKV_FLAG_IMPL_TC : PKV_FLAG_IMPL_MMA;
+    // Automatic: the tcgen05 kernel (faster on every measured layer).
+    p.impl = (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_MMA ? PKV_FLAG_IMPL_MMA : PKV_FLAG_IMPL_TC;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess)  // status word and work counter
         return PKV_ERR_CUDA;
