@@ -18,13 +18,14 @@
 //    pages each.  Warp 5 (one thread) issues the MMAs.  Warps 0-3 own one row
 //    per thread (TMEM lane = row): Q, softmax, P, rescaling, output.
 //  * Tensor memory holds O (128 x head_dim f32), two score buffers of 32
-//    columns and the item's Q (bf16 pairs, the A operand of S).  Per chunk of
-//    two pages: S = Q K^T (M = 128, N = 32 tokens, head_dim / 16 MMAs of
-//    K = 16); each row's thread reads its 32 scores, applies the causal limit
-//    and the online softmax, and writes P back over its consumed scores as a
-//    bf16 high part and a bf16 residual; then O += P_hi V + P_lo V (M = 128,
-//    N = head_dim, K = 16 per page) with P read from tensor memory.  The
-//    scores of chunk i + 1 are issued before P V of chunk i.
+//    columns and the item's Q (bf16 pairs, the A operand of S).
+//    Per chunk of two pages: S = Q K^T (M = 128, N = 32 tokens, head_dim / 16
+//    MMAs of K = 16); each row's thread reads its 32 scores, applies the
+//    causal limit and the online softmax, and writes P back over its
+//    consumed scores as a bf16 high part and a bf16 residual; then
+//    O += P_hi V + P_lo V (M = 128, N = head_dim, K = 16 per page) with P
+//    read from tensor memory.  The scores of chunk i + 1 are issued before
+//    P V of chunk i.
 //  * The running max is updated lazily (only when a score exceeds it by
 //    2^8); O is then rescaled in TMEM by the rows' threads once the previous
 //    P V has completed.
@@ -57,12 +58,16 @@ template <int D> struct TcGeom {
     static constexpr int kStage = 2 * kChunk * kTile;
     static constexpr int NS = (96 * 1024) / kStage;
     static constexpr int kSmem = NS * kStage;
+    // Two score / P buffers; a third (scores two chunks ahead) would push Q
+    // out of tensor memory and cut the ring to four stages: measured slower
+    // (70B verification 419 -> 496 us).
+    static constexpr int kSBufs = 2;
     static constexpr int kSCols = kChunk * kBlockSize;  // score columns per buffer
-    static constexpr int kSCol = D;                     // two score buffers after O
-    static constexpr int kQCol = D + 2 * kSCols;        // Q as bf16 pairs: D / 2 columns
+    static constexpr int kSCol = D;                     // score buffers after O
+    static constexpr int kQCol = D + kSBufs * kSCols;   // Q as bf16 pairs: D / 2 columns
     static constexpr int kTmemCols = 256;
     static_assert(kQCol + D / 2 <= kTmemCols, "O, scores and Q fit the allocation");
-    static_assert(NS >= 4, "ring holds the two chunks in use and copies ahead");
+    static_assert(NS >= 4, "ring holds the chunks in use and copies ahead");
 };
 
 // ------------------------------------------------------------ tcgen05 / TMA
@@ -240,14 +245,15 @@ __device__ __forceinline__ TcItem read_item(const int *slot)
 }
 
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ TcMaps maps)
 {
     using Geo = TcGeom<D>;
     constexpr int NS = Geo::NS;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[NS], empty[NS];
-    __shared__ __align__(8) uint64_t s_full[2], p_full[2], pv_done[2];
+    constexpr int SB = Geo::kSBufs;
+    __shared__ __align__(8) uint64_t s_full[SB], p_full[SB], pv_done[SB];
     __shared__ __align__(8) uint64_t item_full[2], item_empty[2];
     __shared__ __align__(8) uint64_t q_full, o_free, drain;
     __shared__ int s_item[2][8];
@@ -263,10 +269,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < SB; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&item_full[i], 1);
             mbar_init(&item_empty[i], 5);  // the MMA thread and the four softmax warps
         }
@@ -403,7 +411,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // P V of chunk c: waits for its P, and before the first P V of an
             // item for the previous item's output to have been read.
             auto issue_pv = [&](uint32_t c) -> bool {
-                if (!tc_wait(&p_full[c & 1], (c >> 1) & 1, abort))
+                if (!tc_wait(&p_full[c % SB], (c / SB) & 1, abort))
                     return false;
                 if (o_wait) {
                     if (!tc_wait(&o_free, (counted - 2) & 1, abort))
@@ -412,7 +420,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 tc_fence_after();
                 const int stg = static_cast<int>(c % NS);
-                const uint32_t pcol = tmem + Geo::kSCol + Geo::kSCols * (c & 1);
+                const uint32_t pcol = tmem + Geo::kSCol + Geo::kSCols * (c % SB);
 #pragma unroll
                 for (int x = 0; x < kChunk; ++x) {
                     if (!s_ok[stg][x])
@@ -423,7 +431,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_mma_ta(tmem, pcol + Geo::kSCols / 2 + 8 * x, vdesc, kIdPV, true);
                     o_started = true;
                 }
-                tc_commit(&pv_done[c & 1]);
+                tc_commit(&pv_done[c % SB]);
                 tc_commit(&empty[stg]);
                 return true;
             };
@@ -451,6 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 o_started = false;
                 o_wait = counted >= 2;
                 const int nchunks = (npages + kChunk - 1) / kChunk;
+                // Scores run SB - 1 chunks ahead of P V.
                 for (int j = 0; j < nchunks; ++j, ++gc) {
                     const int stg = static_cast<int>(gc % NS);
                     if (!tc_wait(&full[stg], (gc / NS) & 1, abort)) {
@@ -460,22 +469,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tc_fence_after();
                     // Scores of both pages in one MMA per k step (absent or
                     // bad pages leave stale columns that the softmax masks).
-                    const uint32_t scol = tmem + Geo::kSCol + Geo::kSCols * (gc & 1);
+                    const uint32_t scol = tmem + Geo::kSCol + Geo::kSCols * (gc % SB);
                     const uint32_t kaddr = smem0 + stg * Geo::kStage;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
                         tc_mma_ta(scol, tmem + Geo::kQCol + 8 * ks,
                                   smem_desc(kaddr + ks * 256, 128, Geo::kHalf), kIdS, ks > 0);
-                    tc_commit(&s_full[gc & 1]);
-                    if (j > 0 && !issue_pv(gc - 1)) {
+                    tc_commit(&s_full[gc % SB]);
+                    if (j >= SB - 1 && !issue_pv(gc - (SB - 1))) {
                         failed = true;
                         break;
                     }
                 }
-                if (failed || !issue_pv(gc - 1)) {
-                    failed = true;
+                if (failed)
                     break;
-                }
+                for (int r = nchunks < SB - 1 ? nchunks : SB - 1; r >= 1 && !failed; --r)
+                    failed = !issue_pv(gc - r);
+                if (failed)
+                    break;
             }
             if (failed)
                 tc_fail(p, abort);
@@ -491,67 +502,103 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         constexpr float kLazy = MmaSoftmax::kLazy;
         constexpr int kTok = Geo::kSCols;  // tokens per chunk
         uint32_t gc = 0;
-        for (int k = 0;; ++k) {
-            const int slot = k & 1;
-            if (!warp_wait(&item_full[slot], (k >> 1) & 1, abort))
-                break;
-            const TcItem it = read_item(s_item[slot]);
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(&item_empty[slot]);
-            if (!it.valid)
-                break;
-            const int row0 = it.rb * kTcRows;
-            const int nrows = min(kTcRows, it.nq * G - row0);
-            int pg0, npages;
-            item_pages(p, it.L, it.nq, row0, nrows, it.part, pg0, npages);
-            if (npages == 0)
-                continue;
-            const int q0 = __ldg(p.q_start + it.s);  // validated by the item scan
-            const bool row_ok = t < nrows;
-            const int R = row0 + (row_ok ? t : 0);
-            const int qi = R / G;
-            const int h = it.hkv * G + R % G;
-            const int pos = it.L - it.nq + qi;  // position of this row's query
+        int k = 0;  // queue entries read
 
-            // Q row into tensor memory as bf16 pairs (zero past the item).
-            // The previous item's scores have all been read, so every MMA
-            // that used the old Q has completed.
-            {
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    static_cast<const unsigned short *>(p.q) +
-                    (static_cast<size_t>(q0 + qi) * p.num_q_heads + h) * D);
-#pragma unroll 1
-                for (int c0 = 0; c0 < D / 2; c0 += 16) {
-                    uint32_t r[16];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint4 v = row_ok ? __ldg(src + c0 / 4 + e) : make_uint4(0, 0, 0, 0);
-                        r[4 * e] = v.x;
-                        r[4 * e + 1] = v.y;
-                        r[4 * e + 2] = v.z;
-                        r[4 * e + 3] = v.w;
-                    }
-                    tmem_st16u(tmem + lane_base + Geo::kQCol + c0, r);
+        struct RowItem {
+            TcItem it;
+            int pg0, npages, q0, qi, h, pos;
+            bool row_ok;
+        };
+        // Next queue item with pages (true), or the end of the work (false,
+        // ended) or an abort (false, !ended).
+        auto next_item = [&](RowItem &ri, bool &ended) -> bool {
+            for (;;) {
+                const int slot = k & 1;
+                if (!warp_wait(&item_full[slot], (k >> 1) & 1, abort)) {
+                    ended = false;
+                    return false;
                 }
-                tmem_wait_st();
+                const TcItem it = read_item(s_item[slot]);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&item_empty[slot]);
+                ++k;
+                if (!it.valid) {
+                    ended = true;
+                    return false;
+                }
+                const int row0 = it.rb * kTcRows;
+                const int nrows = min(kTcRows, it.nq * G - row0);
+                int pg0, npages;
+                item_pages(p, it.L, it.nq, row0, nrows, it.part, pg0, npages);
+                if (npages == 0)
+                    continue;
+                ri.it = it;
+                ri.pg0 = pg0;
+                ri.npages = npages;
+                ri.q0 = __ldg(p.q_start + it.s);  // validated by the item scan
+                ri.row_ok = t < nrows;
+                const int R = row0 + (ri.row_ok ? t : 0);
+                ri.qi = R / G;
+                ri.h = it.hkv * G + R % G;
+                ri.pos = it.L - it.nq + ri.qi;  // position of this row's query
+                return true;
             }
+        };
+        // Q row (zero past the item) into tensor memory, every load issued
+        // before the first store.  Callers have seen the scores of every
+        // chunk of the previous item, so no MMA still reads the old Q.
+        auto load_q = [&](const RowItem &ri) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                static_cast<const unsigned short *>(p.q) +
+                (static_cast<size_t>(ri.q0 + ri.qi) * p.num_q_heads + ri.h) * D);
+            uint4 v[D / 8];
+#pragma unroll
+            for (int e = 0; e < D / 8; ++e)
+                v[e] = ri.row_ok ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
+            // bf16 pairs, element 2c of the row in the low half of column c.
+#pragma unroll
+            for (int c0 = 0; c0 < D / 2; c0 += 16) {
+                uint32_t r[16];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    r[4 * e] = v[c0 / 4 + e].x;
+                    r[4 * e + 1] = v[c0 / 4 + e].y;
+                    r[4 * e + 2] = v[c0 / 4 + e].z;
+                    r[4 * e + 3] = v[c0 / 4 + e].w;
+                }
+                tmem_st16u(tmem + lane_base + Geo::kQCol + c0, r);
+            }
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&q_full);
+        };
 
+        RowItem cur;
+        bool ended = false;
+        bool have = next_item(cur, ended);
+        bool failed = !have && !ended;
+        if (have)
+            load_q(cur);
+        while (have) {
             float m = -INFINITY, l = 0.f;
             bool o_valid = false;
-            bool failed = false;
+            const int npages = cur.npages;
             const int32_t *table =
-                p.block_tables + static_cast<size_t>(it.s) * p.max_blocks + pg0;
-            int ent = -1;
+                p.block_tables + static_cast<size_t>(cur.it.s) * p.max_blocks + cur.pg0;
+            // Block-table entries of pages [32w, 32w + 32) in `ent`, the next
+            // window already on its way in `ent_next`.
+            int ent = lane < npages ? __ldg(table + lane) : -1;
+            int ent_next = 32 + lane < npages ? __ldg(table + 32 + lane) : -1;
             const int nchunks = (npages + kChunk - 1) / kChunk;
             for (int j = 0; j < nchunks; ++j, ++gc) {
                 const int jp = j * kChunk;  // first page of the chunk
-                if ((jp & 31) == 0)
-                    ent = jp + lane < npages ? __ldg(table + jp + lane) : -1;
+                if (jp > 0 && (jp & 31) == 0) {
+                    ent = ent_next;
+                    ent_next = jp + 32 + lane < npages ? __ldg(table + jp + 32 + lane) : -1;
+                }
                 bool good[kChunk];
                 bool any_good = false;
 #pragma unroll
@@ -560,34 +607,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     good[x] = jp + x < npages && phys >= 0 && phys < p.num_blocks;
                     any_good = any_good || good[x];
                 }
-                if (!warp_wait(&s_full[gc & 1], (gc >> 1) & 1, abort)) {
+                if (!warp_wait(&s_full[gc % SB], (gc / SB) & 1, abort)) {
                     failed = true;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t scol = tmem + lane_base + Geo::kSCol + Geo::kSCols * (gc & 1);
-                float sv[kTok];
+                const uint32_t scol = tmem + lane_base + Geo::kSCol + Geo::kSCols * (gc % SB);
+                const int tb = (cur.pg0 + jp) * kBlockSize;  // position of the chunk's token 0
+                // Scaled scores, -inf where the row does not see the token.
+                float xs[kTok];
 #pragma unroll
                 for (int x = 0; x < kChunk; ++x) {
                     float part[16];
                     tmem_ld16(scol + 16 * x, part);
+                    int v = cur.pos - (tb + 16 * x) + 1;
+                    v = v < 0 ? 0 : (v > kBlockSize ? kBlockSize : v);
+                    const int lim = (cur.row_ok && good[x]) ? v : 0;
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        sv[16 * x + e] = part[e];
+                        xs[16 * x + e] = e < lim ? part[e] * c : -INFINITY;
                 }
-                const int tb = (pg0 + jp) * kBlockSize;  // position of the chunk's token 0
-                int lim[kChunk];                          // tokens of each page this row sees
+                float mx;
+                {
+                    float r[kTok / 2];
 #pragma unroll
-                for (int x = 0; x < kChunk; ++x) {
-                    int v = pos - (tb + 16 * x) + 1;
-                    v = v < 0 ? 0 : (v > kBlockSize ? kBlockSize : v);
-                    lim[x] = (row_ok && good[x]) ? v : 0;
+                    for (int e = 0; e < kTok / 2; ++e)
+                        r[e] = fmaxf(xs[e], xs[e + kTok / 2]);
+#pragma unroll
+                    for (int w = kTok / 4; w >= 1; w >>= 1)
+#pragma unroll
+                        for (int e = 0; e < w; ++e)
+                            r[e] = fmaxf(r[e], r[e + w]);
+                    mx = r[0];
                 }
-                float mx = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < kTok; ++e)
-                    if ((e & 15) < lim[e >> 4])
-                        mx = fmaxf(mx, sv[e] * c);
                 const bool need = mx > m + kLazy;  // false when nothing is visible
                 float alpha = 1.f;
                 if (need) {
@@ -597,7 +649,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 if (o_valid && __any_sync(kFullMask, need)) {
                     // O holds earlier chunks: rescale it once their P V is done.
-                    if (!warp_wait(&pv_done[(gc - 1) & 1], ((gc - 1) >> 1) & 1, abort)) {
+                    if (!warp_wait(&pv_done[(gc - 1) % SB], ((gc - 1) / SB) & 1, abort)) {
                         failed = true;
                         break;
                     }
@@ -614,14 +666,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_wait_st();
                 }
                 // P over the consumed scores: high parts in the first half of
-                // the buffer, residuals in the second (bf16 pairs).
+                // the buffer, residuals in the second (bf16 pairs).  A row
+                // that has seen nothing keeps m = -inf and P = 0.
+                const bool seen = m != -INFINITY;
                 uint32_t hi[kTok / 2], lo[kTok / 2];
                 float psum = 0.f;
 #pragma unroll
                 for (int e = 0; e < kTok; e += 2) {
-                    const float a = (e & 15) < lim[e >> 4] ? MmaSoftmax::ex2(sv[e] * c - m) : 0.f;
-                    const float b =
-                        ((e + 1) & 15) < lim[(e + 1) >> 4] ? MmaSoftmax::ex2(sv[e + 1] * c - m) : 0.f;
+                    const float a = seen ? MmaSoftmax::ex2(xs[e] - m) : 0.f;
+                    const float b = seen ? MmaSoftmax::ex2(xs[e + 1] - m) : 0.f;
                     psum += a + b;
                     hi[e / 2] = pack_bf16(a, b);
                     lo[e / 2] = pack_bf16(a - bf16_lo(hi[e / 2]), b - bf16_hi(hi[e / 2]));
@@ -635,7 +688,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 bool zeroed = false;
 #pragma unroll
                 for (int x = 0; x < kChunk; ++x) {
-                    const int valid = it.L - (tb + 16 * x);
+                    const int valid = cur.it.L - (tb + 16 * x);
                     if (good[x] && valid > 0 && valid < kBlockSize) {
                         if (t < D) {
                             unsigned short *vt = reinterpret_cast<unsigned short *>(
@@ -651,26 +704,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
-                    mbar_arrive(&p_full[gc & 1]);
+                    mbar_arrive(&p_full[gc % SB]);
                 o_valid = o_valid || any_good;
             }
-            if (failed) {
-                tc_fail(p, abort);
+            if (failed)
+                break;
+
+            // The next item's Q first, so that its scores and copies run
+            // while this item's output rows are written.
+            RowItem nxt;
+            bool nended = false;
+            const bool have_next = next_item(nxt, nended);
+            if (!have_next && !nended) {
+                failed = true;
                 break;
             }
+            if (have_next)
+                load_q(nxt);
 
             // ------------------------------------------------ output rows
             if (o_valid) {
-                if (!warp_wait(&pv_done[(gc - 1) & 1], ((gc - 1) >> 1) & 1, abort)) {
-                    tc_fail(p, abort);
+                if (!warp_wait(&pv_done[(gc - 1) % SB], ((gc - 1) / SB) & 1, abort)) {
+                    failed = true;
                     break;
                 }
                 tc_fence_after();
             }
-            const int nparts_r = p.max_parts > 1 ? parts_of(pos + 1, p.partition) : 1;
-            const bool write = row_ok && it.part < nparts_r;
+            const int nparts_r = p.max_parts > 1 ? parts_of(cur.pos + 1, p.partition) : 1;
+            const bool write = cur.row_ok && cur.it.part < nparts_r;
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const size_t orow = static_cast<size_t>(q0 + qi) * p.num_q_heads + h;
+            const size_t orow = static_cast<size_t>(cur.q0 + cur.qi) * p.num_q_heads + cur.h;
 #pragma unroll 1
             for (int c0 = 0; c0 < D; c0 += 16) {
                 float ov[16];
@@ -690,7 +753,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                    make_float4(ov[4 * q4] * inv, ov[4 * q4 + 1] * inv,
                                                ov[4 * q4 + 2] * inv, ov[4 * q4 + 3] * inv));
                 } else {
-                    const size_t prow = orow * p.max_parts + it.part;
+                    const size_t prow = orow * p.max_parts + cur.it.part;
                     float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * D + c0);
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4)
@@ -699,7 +762,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             if (write && nparts_r > 1) {
-                const size_t prow = orow * p.max_parts + it.part;
+                const size_t prow = orow * p.max_parts + cur.it.part;
                 p.part_ml[2 * prow] = m;
                 p.part_ml[2 * prow + 1] = l;
             }
@@ -707,7 +770,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&o_free);
+            cur = nxt;
+            have = have_next;
         }
+        if (failed)
+            tc_fail(p, abort);
     }
 
     tc_fence_before();
