@@ -127,6 +127,19 @@ def test_edge_shapes(case, part):
     assert max_abs(out, ref) <= TOL[W.BF16]
 
 
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 64), (16, 8, 128), (40, 8, 128), (96, 8, 128),
+                                       (24, 2, 64)])
+def test_head_groups(Hq, Hkv, D):
+    # G = 1, 2, 5, 12, 12: row counts that are not multiples of 8 or 16, and
+    # (16 queries x 12 heads = 192 rows) more than one 128-row block.
+    w = _edge([70, 300, 16, 129], [3, 7, 16, 1], seed=Hq + D, Hq=Hq, Hkv=Hkv, D=D)
+    d = _device(w)
+    for part in (0, 64):
+        out, status = _gpu(w, d, partition_tokens=part)
+        assert status == 0
+        assert max_abs(out, _oracle(w)) <= TOL[W.BF16]
+
+
 def test_long_context_split_path():
     # Few sequences with long contexts: the automatic plan splits them.
     w = _edge([32768, 20000], [5, 3], seed=5, Hq=64, Hkv=8, D=128)
