@@ -111,7 +111,7 @@ def _decode(**kw):
     (dict(k=0x2008), INVALID),                    # misaligned cache
     (dict(bt=0x4002), INVALID),
     (dict(part=40), INVALID),
-    (dict(flags=0x3), INVALID),
+    (dict(flags=0x3), INVALID),                   # the tcgen05 kernel is several-queries only
     (dict(flags=0x40), INVALID),
     (dict(flags=0x8), INVALID),
     (dict(flags=0x2, kv_dtype=F32), UNSUPPORTED),  # tensor cores need bf16/fp8 KV
@@ -221,6 +221,10 @@ def _prefill(**kw):
     (dict(part=40), INVALID),
     (dict(flags=0x1), INVALID),                   # no CUDA-core variant
     (dict(flags=0x4), INVALID),
+    (dict(flags=0x2, ws=0), WORKSPACE),           # mma.sync kernel accepted
+    (dict(flags=0x3, ws=0), WORKSPACE),           # tcgen05 kernel accepted
+    (dict(flags=0x103, ws=0), WORKSPACE),         # with the test hook
+    (dict(flags=0x3, S=0), OK),
     (dict(scale=float("inf")), INVALID),
     (dict(S=0), OK),
     (dict(T=0), OK),
