@@ -49,23 +49,31 @@ constexpr int kTcThreads = 192;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 
-constexpr int kChunk = 2;  // pages per softmax step
+// Pages per softmax step.  Two keeps O, two score buffers and Q inside 256
+// TMEM columns (two CTAs per SM); four needs 320 (one CTA per SM, a 192 KB
+// ring): measured slower on GB300 (70B verification 420 -> 455 us).
+#ifndef PKV_TC_CHUNK
+#define PKV_TC_CHUNK 2
+#endif
+constexpr int kChunk = PKV_TC_CHUNK;
+static_assert(kChunk == 2 || kChunk == 4, "two or four pages per step");
 
 template <int D> struct TcGeom {
     static constexpr int kTile = D * kBlockSize * 2;  // one K or V page tile (bf16)
     static constexpr int kHalf = kTile / 2;           // 8 tokens of every head_dim row
     static constexpr int kVOff = kChunk * kTile;      // V tiles follow the K tiles
     static constexpr int kStage = 2 * kChunk * kTile;
-    static constexpr int NS = (96 * 1024) / kStage;
+    static constexpr int kSCols = kChunk * kBlockSize;  // score columns per buffer
+    static constexpr int kTmemUsed = D + 2 * kSCols + D / 2;  // O, two score buffers, Q
+    static constexpr int kTmemCols = kTmemUsed <= 256 ? 256 : 512;
+    static constexpr int NS = (kTmemCols == 256 ? 96 * 1024 : 192 * 1024) / kStage;
     static constexpr int kSmem = NS * kStage;
     // Two score / P buffers; a third (scores two chunks ahead) would push Q
     // out of tensor memory and cut the ring to four stages: measured slower
     // (70B verification 419 -> 496 us).
     static constexpr int kSBufs = 2;
-    static constexpr int kSCols = kChunk * kBlockSize;  // score columns per buffer
     static constexpr int kSCol = D;                     // score buffers after O
     static constexpr int kQCol = D + kSBufs * kSCols;   // Q as bf16 pairs: D / 2 columns
-    static constexpr int kTmemCols = 256;
     static_assert(kQCol + D / 2 <= kTmemCols, "O, scores and Q fit the allocation");
     static_assert(NS >= 4, "ring holds the chunks in use and copies ahead");
 };
@@ -245,7 +253,7 @@ __device__ __forceinline__ TcItem read_item(const int *slot)
 }
 
 template <int D>
-__global__ void __launch_bounds__(kTcThreads, 2)
+__global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ TcMaps maps)
 {
     using Geo = TcGeom<D>;
@@ -680,8 +688,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
                     lo[e / 2] = pack_bf16(a - bf16_lo(hi[e / 2]), b - bf16_hi(hi[e / 2]));
                 }
                 l += psum;
-                tmem_st16u(scol, hi);
-                tmem_st16u(scol + kTok / 2, lo);
+#pragma unroll
+                for (int c0 = 0; c0 < kTok / 2; c0 += 16) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = hi[c0 + e];
+                    tmem_st16u(scol + c0, w);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        w[e] = lo[c0 + e];
+                    tmem_st16u(scol + kTok / 2 + c0, w);
+                }
                 tmem_wait_st();
                 // Past the sequence end the V tile may hold anything (NaN):
                 // zero those tokens, since P = 0 does not cancel NaN.
