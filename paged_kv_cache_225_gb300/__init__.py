@@ -411,7 +411,9 @@ def paged_attn_prefill(q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Te
     [N, Hkv, D, 16] bf16 already holding the queries' K/V; block_tables int32
     [S, max_blocks]; seq_lens int32 [S] (queries included); out [T, Hq, D]
     f32/bf16.  ``max_q_len`` defaults to T, ``max_seq_len`` to max_blocks*16.
-    Returns ``out``.
+    ``flags``: ``IMPL["auto"]`` / ``IMPL["tc"]`` run the tcgen05 kernel,
+    ``IMPL["mma"]`` the mma.sync one (same results within the bf16
+    tolerance).  Returns ``out``.
     """
     dev = q.device
     for t, name, nd in ((q, "q", 3), (q_start, "q_start", 1), (k_cache, "k_cache", 4),
