@@ -49,7 +49,7 @@ def _dense(p, s):
     """Logical K, V [Hkv, L, D] of sequence s by numpy fancy indexing (float64)."""
     k = W.storage_to_float32(p["k_cache"], p["kv_dtype"]).astype(np.float64)
     v = W.storage_to_float32(p["v_cache"], p["kv_dtype"]).astype(np.float64)
-    if p["kv_dtype"] == FP8:
+    if p["kv_dtype"] in W.SCALED:
         k, v = k * p["k_scale"], v * p["v_scale"]
     L = int(p["seq_lens"][s])
     B = k.shape[3]
@@ -73,7 +73,8 @@ def _masked_sdpa(query, keys, values, scale):
 
 
 @pytest.mark.parametrize("kv_dtype,q_dtype,kv_scale",
-                         [(F32, F32, 1.0), (BF16, BF16, 1.0), (FP8, BF16, 0.5)])
+                         [(F32, F32, 1.0), (BF16, BF16, 1.0), (FP8, BF16, 0.5),
+                          (W.FP8_E4M3, BF16, 0.25), (W.INT4, BF16, 0.5)])
 def test_prefill_equals_dense_masked_sdpa(kv_dtype, q_dtype, kv_scale):
     lens, nq = (1, 17, 40, 33), (1, 5, 40, 16)
     p = _problem(kv_dtype, q_dtype, lens, nq, kv_scale=kv_scale, seed=1)
