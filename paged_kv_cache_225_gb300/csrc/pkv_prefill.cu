@@ -1,5 +1,8 @@
 // Paged attention of several query tokens per sequence for sm_103a: chunked
-// prefill and speculative verification.
+// prefill and speculative verification, on mma.sync tensor-core fragments.
+// The automatic kernel is the tcgen05 form in pkv_prefill_tc.cu; this one
+// runs with PKV_FLAG_IMPL_MMA.  launch_prefill (end of file) picks between
+// them; the log-sum-exp merge of split rows serves both.
 //
 // What is computed: the block-table walk of the PagedAttention kernel
 // pseudocode ("vLLM e PagedAttention: serving high-throughput") with the
