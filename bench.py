@@ -165,49 +165,97 @@ def whole_job_rate(units_per_rank: float, world: int, elapsed_s: float) -> float
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+    """nvidia-smi sampling of SM clocks and throttle reasons while running.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+    Started before the warm-up; each sample carries nvidia-smi's own
+    timestamp, so the summary covers exactly the window asked for (the
+    soak before the timed steps through their end) even if the tool's output
+    reaches us late."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index: int, enabled: bool = True):
+    def __init__(self, gpu_index: int, enabled: bool = True, interval_ms: int = 100):
+        import threading
         self.proc = None
         self.gpu = gpu_index
+        self.rows = []
+        self.lock = threading.Lock()
+        self.thread = None
         if enabled:
             try:
                 self.proc = subprocess.Popen(
                     ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                     "--format=csv,noheader,nounits", "-lms", "100"],
-                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                     "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
             except OSError:
                 self.proc = None
+        if self.proc is not None:
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
 
-    def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
-        rows = []
-        for line in out.splitlines():
+    @staticmethod
+    def now() -> float:
+        return time.time()
+
+    def _read(self):
+        import datetime
+        for line in self.proc.stdout:
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) != 7:
+            if len(parts) != 8:
                 continue
             try:
-                rows.append((float(parts[0]), float(parts[1]), parts[2], parts[3:]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                row = (ts, float(parts[1]), float(parts[2]), parts[4:])
             except ValueError:
                 continue
+            with self.lock:
+                self.rows.append(row)
+
+    def count_since(self, t0: float) -> int:
+        with self.lock:
+            return sum(1 for r in self.rows if r[0] >= t0)
+
+    def stop(self, since: float = 0.0, until: float = float("inf")):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        import signal
+        self.proc.send_signal(signal.SIGINT)
+        try:
+            self.proc.wait(timeout=3)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            self.proc.wait()
+        self.thread.join(timeout=3)
+        with self.lock:
+            rows = [r for r in self.rows if since <= r[0] <= until]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3])
+        reasons = sorted({self.REASONS[i] for r in rows for i, v in enumerate(r[3])
                           if v.lower().startswith("active")})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": rows[0][1],
-                "reasons": reasons, "samples": len(rows)}
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": rows[0][2],
+                "reasons": reasons, "samples": len(rows),
+                "window_s": round(min(until, self.now()) - since, 3)}
+
+
+def soak(run, sampler: ClockSampler, min_s: float = 1.0, min_samples: int = 5,
+         max_s: float = 6.0) -> float:
+    """Replays `run` (one step, no sync) for at least min_s seconds and until the
+    sampler holds min_samples clock samples (at most max_s seconds), so that
+    the clocks are read under the same load the timed steps see.  Returns the
+    soak's start time; the clock window runs from there to the timed end."""
+    import torch
+    t0 = ClockSampler.now()
+    while True:
+        for _ in range(16):
+            run()
+        torch.cuda.synchronize()
+        el = ClockSampler.now() - t0
+        if el >= max_s or (el >= min_s and (sampler.proc is None or
+                                             sampler.count_since(t0) >= min_samples)):
+            return t0
 
 
 # --------------------------------------------------------------- GPU arm
@@ -285,6 +333,7 @@ def run_ours(args):
         if ev is not None:
             ev[1].record(stream)
 
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
     for _ in range(max(args.warmup, 3)):
         step(d)
     torch.cuda.synchronize()
@@ -317,7 +366,7 @@ def run_ours(args):
         for _ in range(3):
             g_step.replay()
         torch.cuda.synchronize()
-    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    clock_t0 = soak((lambda: step(d)) if args.eager else g_step.replay, sampler)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -331,7 +380,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(since=clock_t0)
     elapsed_ms = t0.elapsed_time(t1)
     if args.eager:
         decode_ms = [a.elapsed_time(b) for a, b in evs]
@@ -494,31 +543,58 @@ def _oracle_step(w, lens, seqs, threads):
                                     num_threads=threads)
 
 
+def _timed_oracle(run, budget_s):
+    """Calls run() (returns the KV bytes it attended) until budget_s seconds of
+    oracle time have passed (bounded at 3x in wall time); (bytes, seconds, calls)."""
+    kv, t_total, calls = 0, 0.0, 0
+    t_start = time.perf_counter()
+    while t_total < budget_s and time.perf_counter() - t_start < 3 * budget_s:
+        t0 = time.perf_counter()
+        kv += run(calls)
+        t_total += time.perf_counter() - t0
+        calls += 1
+    return kv, t_total, calls
+
+
 def cpu_baseline(w, lens, budget_s=10.0):
-    """The oracle on this host's cores on a bounded sample of the workload."""
+    """The oracle on this host's cores, on bounded samples of the workload.
+
+    All cores: whole decode steps (the cache write and attention of every
+    sequence of the batch in one oracle call, OpenMP over its (sequence, KV
+    head) units).  One thread: chunks of 16 sequences in a seeded random
+    order.  Each leg runs for about budget_s seconds."""
     import oracle
     threads = oracle.max_threads()
     cfg = w.cfg
+    S = cfg.num_seqs
     row = cfg.num_kv_heads * 2 * cfg.head_dim * W.ELEM_BYTES[cfg.kv_dtype]
-    order = np.random.default_rng(1234).permutation(cfg.num_seqs)
-    done_seqs, kv_bytes, t_total, reps = 0, 0, 0.0, 0
-    t_start = time.perf_counter()
-    while t_total < budget_s and time.perf_counter() - t_start < 3 * budget_s:
-        for s in order:
-            t0 = time.perf_counter()
-            _oracle_step(w, lens, [int(s)], threads)
-            t_total += time.perf_counter() - t0
-            done_seqs += 1
-            kv_bytes += int(lens[s]) * row
-            if t_total >= budget_s:
-                break
-        reps += 1
-    return {"value": kv_bytes / t_total / 1e9, "unit": "GB/s", "cores": threads,
+    every = list(range(S))
+    step_kv = int(lens.sum()) * row
+
+    def whole(_):
+        _oracle_step(w, lens, every, threads)
+        return step_kv
+
+    kv_all, t_all, n_all = _timed_oracle(whole, budget_s)
+    order = np.random.default_rng(1234).permutation(S)
+    chunk = min(16, S)
+
+    def one_thread(i):
+        seqs = [int(order[(i * chunk + j) % S]) for j in range(chunk)]
+        _oracle_step(w, lens, seqs, 1)
+        return sum(int(lens[x]) for x in seqs) * row
+
+    kv_one, t_one, n_one = _timed_oracle(one_thread, budget_s)
+    return {"value": kv_all / t_all / 1e9, "unit": "GB/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"{done_seqs} sequence-steps of this workload (random order, "
-                      f"{kv_bytes / 1e9:.2f} GB of KV) in {t_total:.1f} s, fp64 C oracle "
-                      f"with OpenMP over (seq, kv head)",
-            "tokens_per_s": done_seqs / t_total}
+            "sample": f"{n_all} whole decode steps ({S} sequences each, cache write + "
+                      f"attention, {kv_all / 1e9:.2f} GB of KV) in {t_all:.1f} s, fp64 C "
+                      f"oracle with OpenMP over (sequence, KV head) on {threads} threads",
+            "tokens_per_s": n_all * S / t_all,
+            "single_thread": {"value": kv_one / t_one / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"{n_one} chunks of {chunk} sequences (random order, "
+                                        f"{kv_one / 1e9:.2f} GB of KV) in {t_one:.1f} s on "
+                                        "one thread"}}
 
 
 def run_reference(args):
@@ -533,9 +609,10 @@ def run_reference(args):
     row = cfg.num_kv_heads * 2 * cfg.head_dim * W.ELEM_BYTES[cfg.kv_dtype]
     # Size each step's sample so the whole run stays near two minutes.
     order = np.random.default_rng(99).permutation(cfg.num_seqs)
+    probe = [int(x) for x in order[:min(16, cfg.num_seqs)]]
     t0 = time.perf_counter()
-    _oracle_step(w, lens, [int(order[0])], threads)
-    per_seq = max(time.perf_counter() - t0, 1e-4)
+    _oracle_step(w, lens, probe, threads)
+    per_seq = max((time.perf_counter() - t0) / len(probe), 1e-5)
     total_steps = args.steps + max(args.warmup, 0)
     per_step_budget = 120.0 / max(total_steps, 1)
     n_seq = int(max(1, min(cfg.num_seqs, per_step_budget / per_seq)))
@@ -642,6 +719,7 @@ def run_prefill(args):
         pkv.reshape_and_cache(dd["new_k"], dd["new_v"], dd["slots"], kc, vc)
         attend(dd)
 
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
     for _ in range(max(args.warmup, 3)):
         step(d)
     torch.cuda.synchronize()
@@ -660,7 +738,7 @@ def run_prefill(args):
     for _ in range(3):
         g_step.replay()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    clock_t0 = soak(g_step.replay, sampler)
     if world > 1:
         dist.barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -672,7 +750,7 @@ def run_prefill(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(since=clock_t0)
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1))
     c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     c0.record(stream)
@@ -779,25 +857,39 @@ def _oracle_prefill_seqs(w, seqs, threads):
 
 
 def prefill_cpu_baseline(w, budget_s=10.0):
+    """The oracle's several-queries attention on this host: whole steps (every
+    sequence in one call) on all cores, and chunks of 16 sequences on one
+    thread, about budget_s seconds each."""
     import oracle
     threads = oracle.max_threads()
     base = w.cfg.base
+    S = w.seq_lens.size
     row = base.num_kv_heads * 2 * base.head_dim * W.ELEM_BYTES[base.kv_dtype]
-    order = np.random.default_rng(1234).permutation(w.seq_lens.size)
-    done, kv, t_total = 0, 0, 0.0
-    t_start = time.perf_counter()
-    while t_total < budget_s and time.perf_counter() - t_start < 3 * budget_s:
-        for s in order:
-            t0 = time.perf_counter()
-            _oracle_prefill_seqs(w, [int(s)], threads)
-            t_total += time.perf_counter() - t0
-            done += 1
-            kv += int(w.seq_lens[s]) * row
-            if t_total >= budget_s:
-                break
-    return {"value": kv / t_total / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{done} sequences of this workload (random order, {kv / 1e9:.2f} GB of "
-                      f"KV) in {t_total:.1f} s, fp64 C oracle with OpenMP over (seq, kv head)"}
+    every = list(range(S))
+    step_kv = int(w.seq_lens.sum()) * row
+
+    def whole(_):
+        _oracle_prefill_seqs(w, every, threads)
+        return step_kv
+
+    kv_all, t_all, n_all = _timed_oracle(whole, budget_s)
+    order = np.random.default_rng(1234).permutation(S)
+    chunk = min(16, S)
+
+    def one_thread(i):
+        seqs = [int(order[(i * chunk + j) % S]) for j in range(chunk)]
+        _oracle_prefill_seqs(w, seqs, 1)
+        return sum(int(w.seq_lens[x]) for x in seqs) * row
+
+    kv_one, t_one, n_one = _timed_oracle(one_thread, budget_s)
+    return {"value": kv_all / t_all / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n_all} whole steps ({S} sequences each, {kv_all / 1e9:.2f} GB of KV) "
+                      f"in {t_all:.1f} s, fp64 C oracle with OpenMP over (sequence, KV head) "
+                      f"on {threads} threads",
+            "single_thread": {"value": kv_one / t_one / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": f"{n_one} chunks of {chunk} sequences "
+                                        f"({kv_one / 1e9:.2f} GB of KV) in {t_one:.1f} s on "
+                                        "one thread"}}
 
 
 def run_reference_prefill(args):
@@ -811,9 +903,10 @@ def run_reference_prefill(args):
     row = base.num_kv_heads * 2 * base.head_dim * W.ELEM_BYTES[base.kv_dtype]
     S = w.seq_lens.size
     order = np.random.default_rng(99).permutation(S)
+    probe = [int(x) for x in order[:min(16, S)]]
     t0 = time.perf_counter()
-    _oracle_prefill_seqs(w, [int(order[0])], threads)
-    per_seq = max(time.perf_counter() - t0, 1e-4)
+    _oracle_prefill_seqs(w, probe, threads)
+    per_seq = max((time.perf_counter() - t0) / len(probe), 1e-5)
     total_steps = args.steps + max(args.warmup, 0)
     n_seq = int(max(1, min(S, (120.0 / max(total_steps, 1)) / per_seq)))
     cursor = 0
@@ -874,6 +967,7 @@ def run_copy(args):
     pairs = pairs_h.to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
     for _ in range(max(args.warmup, 3)):
         pkv.copy_blocks(kc, vc, pairs, status=status)
     torch.cuda.synchronize()
@@ -887,7 +981,7 @@ def run_copy(args):
     for _ in range(3):
         g.replay()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    clock_t0 = soak(g.replay, sampler)
     if world > 1:
         dist.barrier()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -898,7 +992,7 @@ def run_copy(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    clocks = sampler.stop()
+    clocks = sampler.stop(since=clock_t0)
     ms = max_over_ranks(t0.elapsed_time(t1)) / K
     if int(status.item()) != 0:
         raise RuntimeError("copy_blocks reported a bad pair")

@@ -292,8 +292,10 @@ pkv_status pkv_paged_attn_prefill(const void *q, pkv_dtype q_dtype, const int32_
  *  - Sizes whose pkv_paged_attn_workspace_size(...) exceeds
  *    PKV_NOALLOC_SCRATCH_BYTES are rejected with PKV_ERR_WORKSPACE before
  *    anything is enqueued (pass a larger partition_tokens, or -1, to need less).
- *  - The first call on a device looks up the array's device address with
- *    cudaGetSymbolAddress while that device is current; make that first call
+ *  - The first call in each CUDA context (the device's primary context, or
+ *    a context the caller made current) looks up the array's device address
+ *    with cudaGetSymbolAddress and remembers it for that context only, since
+ *    each context holds its own copy of the array; make that first call
  *    before any stream capture.
  *  - All calls share the one array and it keeps the previous call's contents
  *    (each call clears the parts that must start at zero).  Calls that can

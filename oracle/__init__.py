@@ -179,17 +179,18 @@ def paged_decode(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_lens,
 
 def paged_decode_seqs(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables, seq_lens, scale,
                       seqs, k_scale=1.0, v_scale=1.0, num_threads=0) -> np.ndarray:
-    """Like ``paged_decode`` but only for the listed sequences: returns [len(seqs), Hq, D]."""
+    """Like ``paged_decode`` but only for the listed sequences: returns [len(seqs), Hq, D]
+    (row i is sequence ``seqs[i]``; nothing is computed or allocated for the others)."""
     args, keep, shape = _attn_args(q, q_dtype, k_cache, v_cache, kv_dtype, block_tables,
                                    seq_lens, scale, k_scale, v_scale)
     seqs = np.ascontiguousarray(seqs, dtype=np.int32)
-    out = np.zeros(shape, dtype=np.float64)
+    out = np.empty((seqs.size,) + shape[1:], dtype=np.float64)
     rc = _load().pkvo_paged_decode_seqs(*args, _ptr(seqs, ctypes.c_int32), seqs.size,
                                         _ptr(out, ctypes.c_double), int(num_threads))
     del keep
     if rc:
         raise ValueError(f"oracle paged_decode_seqs failed ({rc})")
-    return out[seqs]
+    return out
 
 
 def paged_prefill(q, q_dtype, q_start, k_cache, v_cache, kv_dtype, block_tables, seq_lens,

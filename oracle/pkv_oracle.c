@@ -446,10 +446,11 @@ static int attend_row(const double *qrow, const double *K, const double *V, int 
 
 /* Attention of the n_q query tokens q_row0 .. q_row0 + n_q - 1 (rows of q
  * [T, Hq, D]) of sequence s for every query head of KV head hkv, written into
- * out [T, Hq, D].  Query i sits at logical position L - n_q + i and sees the
- * rows t <= that position.  Decode is n_q = 1, q_row0 = s. */
+ * rows out_row0 .. out_row0 + n_q - 1 of out [*, Hq, D].  Query i sits at
+ * logical position L - n_q + i and sees the rows t <= that position.  Decode
+ * is n_q = 1, q_row0 = s. */
 static int attend_group_rows(const pkvo_problem *P, int s, int hkv, int q_row0, int n_q,
-                             int partition_tokens, double *out)
+                             int out_row0, int partition_tokens, double *out)
 {
     const int D = P->head_dim;
     const int G = P->num_q_heads / P->num_kv_heads;
@@ -478,7 +479,7 @@ static int attend_group_rows(const pkvo_problem *P, int s, int hkv, int q_row0, 
         const int t_end = (L > 0) ? L - n_q + i + 1 : 0;
         for (int g = 0; g < G; ++g) {
             int h = hkv * G + g;
-            double *dst = out + ((size_t)(q_row0 + i) * P->num_q_heads + h) * D;
+            double *dst = out + ((size_t)(out_row0 + i) * P->num_q_heads + h) * D;
             load_q_row(P, q_row0 + i, h, qrow);
             rc |= attend_row(qrow, K, V, D, t_end, P->scale, partition_tokens, z, o, acc, dst);
         }
@@ -488,11 +489,11 @@ done:
     return rc;
 }
 
-/* Decode: one query per sequence, row s of q. */
-static int attend_group(const pkvo_problem *P, int s, int hkv, int partition_tokens,
+/* Decode: one query per sequence, row s of q, written to row out_row of out. */
+static int attend_group(const pkvo_problem *P, int s, int hkv, int out_row, int partition_tokens,
                         double *out)
 {
-    return attend_group_rows(P, s, hkv, s, 1, partition_tokens, out);
+    return attend_group_rows(P, s, hkv, s, 1, out_row, partition_tokens, out);
 }
 
 static int run_attention(const pkvo_problem *P, int partition_tokens, double *out,
@@ -510,7 +511,7 @@ static int run_attention(const pkvo_problem *P, int partition_tokens, double *ou
     for (long u = 0; u < units; ++u) {
         int s = (int)(u / P->num_kv_heads);
         int hkv = (int)(u % P->num_kv_heads);
-        rc |= attend_group(P, s, hkv, partition_tokens, out);
+        rc |= attend_group(P, s, hkv, s, partition_tokens, out);
     }
     (void)num_threads;
     return rc;
@@ -559,9 +560,9 @@ int pkvo_paged_decode_head_scaled(const void *q, int q_dtype, const void *k_cach
 }
 
 /*
- * The same attention for a subset of sequences only: rows of out for the
- * sequences listed in `seqs` are written (out keeps the full [S, Hq, D]
- * shape; other rows are untouched).  Used to sample large batches.
+ * The same attention for a subset of sequences only: out is
+ * [num_listed, Hq, D] and row i holds sequence seqs[i].  Used to sample
+ * large batches.
  */
 int pkvo_paged_decode_seqs(const void *q, int q_dtype, const void *k_cache,
                            const void *v_cache, int kv_dtype, double k_scale, double v_scale,
@@ -589,7 +590,7 @@ int pkvo_paged_decode_seqs(const void *q, int q_dtype, const void *k_cache,
             rc |= 2;
             continue;
         }
-        rc |= attend_group(&P, s, hkv, 0, out);
+        rc |= attend_group(&P, s, hkv, (int)(u / num_kv_heads), 0, out);
     }
     (void)num_threads;
     return rc;
@@ -633,7 +634,7 @@ int pkvo_paged_prefill(const void *q, int q_dtype, const int32_t *q_start,
         int s = (int)(u / num_kv_heads);
         int hkv = (int)(u % num_kv_heads);
         rc |= attend_group_rows(&P, s, hkv, q_start[s], q_start[s + 1] - q_start[s],
-                                partition_tokens, out);
+                                q_start[s], partition_tokens, out);
     }
     (void)num_threads;
     return rc;

@@ -5,9 +5,45 @@
 #include <cstring>
 #include <mutex>
 
+#include <cuda.h>  // CUcontext; the two driver calls below are looked up at run time
+
 #include "pkv_internal.h"
 
 namespace pkv {
+
+namespace {
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+std::once_flag g_ctx_once;
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+}  // namespace
+
+uint64_t current_context_id()
+{
+    std::call_once(g_ctx_once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    if (!g_ctx_current || !g_ctx_id)
+        return 0;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+        return 0;
+    unsigned long long id = 0;
+    if (g_ctx_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return static_cast<uint64_t>(id) + 1;  // never 0 for a real context
+}
 
 int device_sm_count()
 {

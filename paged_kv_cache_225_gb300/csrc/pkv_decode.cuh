@@ -18,11 +18,16 @@
 //  * Each warp keeps its own softmax state; at the end of an item the four
 //    states are merged through shared memory with log-sum-exp weights.  A
 //    sequence that fits one partition is written straight to `out`;
-//    otherwise normalised partials go to the workspace and a second kernel
-//    merges them.
+//    otherwise the item writes a normalised partial to the workspace and the
+//    CTA whose partial completes the sequence (an arrival counter per
+//    sequence and KV head) merges them all in partition order.  With
+//    PKV_FLAG_SEPARATE_MERGE the merge runs as a second kernel instead
+//    (pkv_merge.cu); both give the same bits.
 //  * In split mode the grid is persistent: CTAs pull items from an atomic
 //    counter and map the item index to (sequence, partition) with a warp
 //    prefix scan over the per-sequence partition counts.
+//  * With few (sequence, KV head) units the automatic schedule is stream-K
+//    instead (pkv_streamk.cuh): equal page ranges per CTA, same policies.
 //  * Per page, scores and the value accumulation run either on CUDA cores
 //    (SimtPolicy) or on tensor cores with mma.sync (MmaBf16Policy,
 //    MmaFp8Policy): S^T = K^T Q^T puts the page's 16 tokens on the MMA's M
@@ -1342,23 +1347,24 @@ template <class Pol>
 pkv_status launch_policy(const DecodeParams &p, cudaStream_t stream)
 {
     constexpr int smem = decode_smem_bytes<Pol>();
-    static int occ = -1;  // resident CTAs per SM (per process; one device type)
-    static bool attr_set = false;
-    if (!attr_set) {
+    // Resident CTAs per SM, once the shared-memory attribute is set (per context).
+    static ContextCache cache;
+    int occ = 1;
+    const pkv_status rc = cache.get(&occ, [](int *v) -> pkv_status {
         if (cudaFuncSetAttribute(decode_kernel<Pol>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem) != cudaSuccess)
             return PKV_ERR_CUDA;
-        attr_set = true;
-    }
+        int o = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<Pol>, kThreads,
+                                                          smem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        *v = o > 0 ? o : 1;
+        return PKV_OK;
+    });
+    if (rc != PKV_OK)
+        return rc;
     long grid;
     if (p.split) {
-        if (occ < 0) {
-            int o = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<Pol>, kThreads,
-                                                              smem) != cudaSuccess)
-                return PKV_ERR_CUDA;
-            occ = o > 0 ? o : 1;
-        }
         const long items = static_cast<long>(p.num_seqs) * p.num_kv_heads * p.max_parts;
         const long slots = static_cast<long>(occ) * device_sm_count();
         grid = items < slots ? items : slots;

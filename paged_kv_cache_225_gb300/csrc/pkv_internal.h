@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 
 #include <cuda_runtime.h>
 
@@ -123,5 +124,50 @@ pkv_status launch_copy_blocks(void *k_cache, void *v_cache, size_t block_bytes,
                               int32_t *status, cudaStream_t stream);
 
 int device_sm_count();
+
+// A process-unique id of the CUDA context current on the calling thread (0 when
+// there is none or the driver cannot tell).  Kernel attributes, module symbols
+// and occupancy facts belong to a context, which a device reset or a second
+// context on the same device replaces: caches of them are keyed on this id.
+uint64_t current_context_id();
+
+// One int per CUDA context, computed by make(&value) the first time a host
+// thread asks with that context current (e.g. a kernel's resident CTAs per SM,
+// after its shared-memory attribute is set).  Thread-safe; a few contexts are
+// remembered at once, others are recomputed.
+class ContextCache {
+  public:
+    template <class F> pkv_status get(int *value, F &&make)
+    {
+        const uint64_t ctx = current_context_id();
+        if (ctx != 0) {
+            std::lock_guard<std::mutex> lock(mu_);
+            for (int i = 0; i < kSlots; ++i)
+                if (id_[i] == ctx) {
+                    *value = val_[i];
+                    return PKV_OK;
+                }
+        }
+        int v = 0;
+        const pkv_status rc = make(&v);
+        if (rc != PKV_OK)
+            return rc;
+        if (ctx != 0) {
+            std::lock_guard<std::mutex> lock(mu_);
+            id_[next_] = ctx;
+            val_[next_] = v;
+            next_ = (next_ + 1) % kSlots;
+        }
+        *value = v;
+        return PKV_OK;
+    }
+
+  private:
+    static constexpr int kSlots = 16;
+    std::mutex mu_;
+    uint64_t id_[kSlots] = {};
+    int val_[kSlots] = {};
+    int next_ = 0;
+};
 
 }  // namespace pkv

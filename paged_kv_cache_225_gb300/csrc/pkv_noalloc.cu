@@ -11,8 +11,12 @@
 // library's module is loaded holds PKV_NOALLOC_SCRATCH_BYTES of it until the
 // process exits.  Host code cannot use the array's name as a device address
 // (on the host it is only a stand-in symbol), so the entry point looks the
-// address up once per device with cudaGetSymbolAddress, with that device
-// current, and passes it on like any workspace pointer.
+// address up with cudaGetSymbolAddress, with the caller's device current, and
+// passes it on like any workspace pointer.  The address belongs to the CUDA
+// context the module was loaded into: a plugin that pushes its own context on
+// a device, or a caller that resets the device between calls, gets a new copy
+// of the array at a new address.  The lookup is therefore remembered per
+// context (keyed on the driver's unique context id), never per device ordinal.
 #include <mutex>
 
 #include "pkv_internal.h"
@@ -21,26 +25,36 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[PKV_NOALLOC_SCR
 
 namespace {
 
-constexpr int kMaxDevices = 256;
+constexpr int kSlots = 32;
 std::mutex g_scratch_mu;
-void *g_scratch_addr[kMaxDevices];  // device address of g_noalloc_scratch, per ordinal
+uint64_t g_scratch_ctx[kSlots];  // context id of each remembered address (0 = empty)
+void *g_scratch_addr[kSlots];    // device address of g_noalloc_scratch in that context
+int g_scratch_next = 0;
 
-// Device address of the scratch array on the current device (looked up on the
-// first call for that device).
-pkv_status scratch_on_current_device(void **addr)
+// Device address of the scratch array in the current context (looked up the
+// first time this context calls).
+pkv_status scratch_in_current_context(void **addr)
 {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return PKV_ERR_CUDA;
+    const uint64_t ctx = pkv::current_context_id();
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (err != cudaSuccess || p == nullptr)
-            return PKV_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+    if (ctx != 0)
+        for (int i = 0; i < kSlots; ++i)
+            if (g_scratch_ctx[i] == ctx) {
+                *addr = g_scratch_addr[i];
+                return PKV_OK;
+            }
+    void *p = nullptr;
+    const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (err != cudaSuccess || p == nullptr)
+        return PKV_ERR_CUDA;
+    // The lookup itself may have made the device's primary context current.
+    const uint64_t now = ctx != 0 ? ctx : pkv::current_context_id();
+    if (now != 0) {
+        g_scratch_ctx[g_scratch_next] = now;
+        g_scratch_addr[g_scratch_next] = p;
+        g_scratch_next = (g_scratch_next + 1) % kSlots;
     }
-    *addr = g_scratch_addr[dev];
+    *addr = p;
     return PKV_OK;
 }
 
@@ -61,7 +75,7 @@ extern "C" pkv_status pkv_paged_attn_decode_noalloc(
     if (need > static_cast<size_t>(PKV_NOALLOC_SCRATCH_BYTES))
         return PKV_ERR_WORKSPACE;  // these sizes need more scratch than the fixed array
     void *scratch = nullptr;
-    const pkv_status rc = scratch_on_current_device(&scratch);
+    const pkv_status rc = scratch_in_current_context(&scratch);
     if (rc != PKV_OK)
         return rc;
     return pkv_paged_attn_decode(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale,

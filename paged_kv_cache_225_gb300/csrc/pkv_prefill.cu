@@ -560,8 +560,10 @@ template <int D>
 pkv_status launch_prefill_d(const PrefillParams &p, cudaStream_t stream)
 {
     using Geo = PrefillGeom<D>;
-    static int occ = -1;
-    if (occ < 0) {
+    // Resident CTAs per SM, once the shared-memory attribute is set (per context).
+    static ContextCache cache;
+    int occ = 1;
+    const pkv_status rc = cache.get(&occ, [](int *v) -> pkv_status {
         if (cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Geo::kSmem) != cudaSuccess)
             return PKV_ERR_CUDA;
@@ -569,8 +571,11 @@ pkv_status launch_prefill_d(const PrefillParams &p, cudaStream_t stream)
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, prefill_kernel<D>, kThreads,
                                                           Geo::kSmem) != cudaSuccess)
             return PKV_ERR_CUDA;
-        occ = o > 0 ? o : 1;
-    }
+        *v = o > 0 ? o : 1;
+        return PKV_OK;
+    });
+    if (rc != PKV_OK)
+        return rc;
     const long blocks = (static_cast<long>(p.max_q_len) * p.group + kRowBlock - 1) / kRowBlock;
     const long items = static_cast<long>(p.num_seqs) * p.num_kv_heads * p.max_parts * blocks;
     const long slots = static_cast<long>(occ) * device_sm_count();

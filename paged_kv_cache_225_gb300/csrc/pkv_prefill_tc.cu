@@ -815,17 +815,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t
 
 EncodeTiledFn encoder()
 {
+    static std::once_flag once;
     static EncodeTiledFn fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    std::call_once(once, [] {
         void *f = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
             fn = reinterpret_cast<EncodeTiledFn>(f);
-    }
+    });
     return fn;
 }
 
@@ -849,8 +848,10 @@ template <int D>
 pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
 {
     using Geo = TcGeom<D>;
-    static int occ = -1;
-    if (occ < 0) {
+    // Resident CTAs per SM, once the attributes are set (per context).
+    static ContextCache cache;
+    int occ = 1;
+    const pkv_status crc = cache.get(&occ, [](int *out_occ) -> pkv_status {
         // Two CTAs per SM need the largest shared-memory carveout.
         if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Geo::kSmem) != cudaSuccess ||
@@ -879,8 +880,11 @@ pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
         long o = 512 / Geo::kTmemCols;
         o = o < by_smem ? o : by_smem;
         o = o < by_regs ? o : by_regs;
-        occ = o < 1 ? 1 : static_cast<int>(o);
-    }
+        *out_occ = o < 1 ? 1 : static_cast<int>(o);
+        return PKV_OK;
+    });
+    if (crc != PKV_OK)
+        return crc;
     EncodeTiledFn enc = encoder();
     if (!enc)
         return PKV_ERR_CUDA;

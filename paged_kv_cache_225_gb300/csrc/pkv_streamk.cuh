@@ -469,21 +469,22 @@ pkv_status launch_streamk(const DecodeParams &p, cudaStream_t stream)
 {
     constexpr int smem = kWarps * Pol::kRingBytes + kWarps * Pol::R * 8 + Pol::kExtraBytes +
                          scratch_bytes(Pol::GP, Pol::kDim);
-    static int occ = -1;
-    static bool attr_set = false;
-    if (!attr_set) {
+    // Resident CTAs per SM, once the shared-memory attribute is set (per context).
+    static ContextCache cache;
+    int occ = 1;
+    const pkv_status rc = cache.get(&occ, [](int *v) -> pkv_status {
         if (cudaFuncSetAttribute(decode_streamk_kernel<Pol>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return PKV_ERR_CUDA;
-        attr_set = true;
-    }
-    if (occ < 0) {
         int o = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_streamk_kernel<Pol>, kThreads,
                                                           smem) != cudaSuccess)
             return PKV_ERR_CUDA;
-        occ = o > 0 ? o : 1;
-    }
+        *v = o > 0 ? o : 1;
+        return PKV_OK;
+    });
+    if (rc != PKV_OK)
+        return rc;
     long grid = static_cast<long>(occ) * device_sm_count();
     if (grid > p.streamk_max_ctas)
         grid = p.streamk_max_ctas;
