@@ -87,6 +87,9 @@ def parse_args(argv=None):
                     help="cache write and decode as two launches instead of one")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step from Python instead of replaying a CUDA graph")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="decode this many layers of the workload (shared tables and lengths, "
+                         "own caches) in one launch, against as many separate launches")
     return ap.parse_args(argv)
 
 
@@ -1075,9 +1078,225 @@ def run_copy(args):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------ several layers per launch
+
+def run_layers(args):
+    """One step = the decode of args.layers layers of one batch (shared block
+    tables and lengths, each layer with its own caches, query, new token rows
+    and output) in one pkv_paged_attn_decode_layers launch, the cache write of
+    every layer's new token fused in.  The same work as args.layers separate
+    fused launches (one CUDA graph holding them back to back) is timed beside
+    it."""
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_225_gb300 as pkv
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    NL = args.layers
+    ws = W.make_layers(args.config, NL)
+    w0 = ws[0]
+    cfg = w0.cfg
+    S, Hq, Hkv, D = cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
+    lens = (w0.seq_lens + 1).astype(np.int32)
+    max_len = int(lens.max())
+    ab = algorithmic_bytes(w0, lens)                     # per layer
+    new_rows = S * Hkv * D * 2
+    append_bytes = new_rows * (W.ELEM_BYTES[cfg.q_dtype] + W.ELEM_BYTES[cfg.kv_dtype])
+    launch_bytes = NL * (ab["total"] + append_bytes)
+
+    def t(a, dt):
+        a = np.ascontiguousarray(a)
+        if dt == W.F32:
+            return torch.from_numpy(a)
+        if dt == W.BF16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        if dt == W.FP8_E4M3:
+            return torch.from_numpy(a).view(torch.float8_e4m3fn)
+        if dt == W.INT4:
+            return torch.from_numpy(a)
+        return torch.from_numpy(a).view(torch.float8_e5m2)
+
+    layers = []
+    for w in ws:
+        layers.append({"q": t(w.q, cfg.q_dtype).to(dev), "new_k": t(w.new_k, cfg.q_dtype).to(dev),
+                       "new_v": t(w.new_v, cfg.q_dtype).to(dev),
+                       "k_cache": t(w.k_cache, cfg.kv_dtype).to(dev),
+                       "v_cache": t(w.v_cache, cfg.kv_dtype).to(dev),
+                       "out": torch.empty((S, Hq, D), dtype=torch.float32, device=dev)})
+    table = pkv.layer_table(layers)
+    tables = torch.from_numpy(w0.block_tables).to(dev)
+    lens_dev = torch.from_numpy(lens).to(dev)
+    part = pkv.layers_partition_tokens(NL, S, Hq, Hkv, D, max_len, args.partition)
+    wsp = torch.empty(pkv.layers_workspace_size(NL, S, Hq, Hkv, D, max_len, args.partition),
+                      dtype=torch.uint8, device=dev)
+    single_part = pkv.partition_tokens(S, Hq, Hkv, D, max_len, args.partition)
+    ws1 = [torch.empty(pkv.workspace_size(S, Hq, Hkv, D, max_len, args.partition),
+                       dtype=torch.uint8, device=dev) for _ in range(NL)]
+    stream = torch.cuda.current_stream(dev)
+    ks = cfg.kv_scale
+
+    def fused():
+        pkv.paged_attn_decode_layers(layers, tables, lens_dev, w0.scale, k_scale=ks, v_scale=ks,
+                                     max_seq_len=max_len, partition_tokens=args.partition,
+                                     impl=args.kernel, workspace=wsp, table=table)
+
+    def separate():
+        for lay, wsx in zip(layers, ws1):
+            pkv.paged_attn_decode_append(lay["q"], lay["new_k"], lay["new_v"], lay["k_cache"],
+                                         lay["v_cache"], tables, lens_dev, w0.scale, lay["out"],
+                                         k_scale=ks, v_scale=ks, max_seq_len=max_len,
+                                         partition_tokens=args.partition, impl=args.kernel,
+                                         workspace=wsx)
+
+    sampler = ClockSampler(local, enabled=not args.no_clocks)
+    for _ in range(max(args.warmup, 3)):
+        fused()
+        separate()
+    torch.cuda.synchronize()
+    for x in [wsp] + ws1:
+        status = pkv.read_status(x)
+        if status != 0:
+            raise RuntimeError(f"device status {pkv.STATUS.get(status, status)} during warm-up")
+    gs = torch.cuda.Stream(dev)
+    gs.wait_stream(stream)
+    g_fused, g_sep = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_fused, stream=gs):
+        fused()
+    with torch.cuda.graph(g_sep, stream=gs):
+        separate()
+    stream.wait_stream(gs)
+    for _ in range(3):
+        g_fused.replay()
+        g_sep.replay()
+    torch.cuda.synchronize()
+    K = args.steps
+    clock_t0 = soak(g_fused.replay, sampler)
+    if world > 1:
+        dist.barrier()
+
+    def timed(g):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(K):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    ms_fused = timed(g_fused)
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop(since=clock_t0)
+    ms_sep = timed(g_sep)
+    ms_fused = max_over_ranks(ms_fused)
+    for x in [wsp] + ws1:
+        status = pkv.read_status(x)
+        if status != 0:
+            raise RuntimeError(f"device status {pkv.STATUS.get(status, status)} in the timed run")
+
+    # End to end: every layer's q and new rows and the shared tables and
+    # lengths copied in from pinned host memory, every output copied back,
+    # serialised on the launch stream.
+    e2e = None
+    if not args.no_e2e:
+        pins = [{k: layers[i][k].cpu().pin_memory() for k in ("q", "new_k", "new_v")}
+                for i in range(NL)]
+        pin_tab = torch.from_numpy(w0.block_tables).pin_memory()
+        pin_len = torch.from_numpy(lens).pin_memory()
+        outs_h = [torch.empty((S, Hq, D), dtype=torch.float32).pin_memory() for _ in range(NL)]
+        h2d = sum(v.numel() * v.element_size() for p_ in pins for v in p_.values()) + \
+            pin_tab.numel() * 4 + pin_len.numel() * 4
+        d2h = NL * S * Hq * D * 4
+        Ke = max(1, min(K, 200))
+
+        def e2e_step():
+            for i in range(NL):
+                for k, v in pins[i].items():
+                    layers[i][k].copy_(v, non_blocking=True)
+            tables.copy_(pin_tab, non_blocking=True)
+            lens_dev.copy_(pin_len, non_blocking=True)
+            fused()
+            for i in range(NL):
+                outs_h[i].copy_(layers[i]["out"], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / Ke
+        e2e = {"value": NL * ab["kv"] * world / (e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_ms, "steps": Ke, "pipeline": "copies serialised on one stream"}
+
+    peak, peak_kind = hbm_peak()
+    achieved = launch_bytes / (ms_fused * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": whole_job_rate(NL * ab["kv"], world, ms_fused * 1e-3) / 1e9,
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_fused, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": DTYPE_NAME[cfg.kv_dtype],
+        "data": "synthetic: seeded N(0,1) q/K/V per layer, shuffled physical blocks (no dataset)",
+        "config": {"workload": f"{NL} layers of: " + workload_text(args.config),
+                   "name": args.config, "layers": NL, "num_seqs": S, "num_q_heads": Hq,
+                   "num_kv_heads": Hkv, "head_dim": D, "tokens_per_layer": ab["tokens"],
+                   "kv_bytes_per_step": NL * ab["kv"],
+                   "schedule": ("stream-K (equal page ranges per CTA)"
+                                if part == pkv.SCHEDULE_STREAMK else
+                                f"{part}-token partitions" if part > 0 else
+                                "one CTA per (layer, sequence, KV head)"),
+                   "l2": f"no flush: {NL} layers' caches ({NL * (w0.k_cache.nbytes * 2) / 1e9:.2f}"
+                         " GB) cycle through L2 (129 MB)",
+                   "step": "one launch: every layer's cache write fused into its paged decode "
+                           "over L+1",
+                   "launch": "step captured once as a CUDA graph, replayed per step"},
+        "ms_per_layer": ms_fused / NL,
+        "tokens_per_s": whole_job_rate(NL * S, world, ms_fused * 1e-3),
+        "separate_launches": {
+            "ms_per_step": ms_sep, "ms_per_layer": ms_sep / NL,
+            "value": NL * ab["kv"] / (ms_sep * 1e-3) / 1e9,
+            "schedule": (f"{single_part}-token partitions" if single_part > 0 else
+                         "stream-K" if single_part == pkv.SCHEDULE_STREAMK else
+                         "one CTA per (sequence, KV head)"),
+            "note": f"{NL} pkv_paged_attn_decode_append launches back to back in one CUDA graph"},
+        "pct_hbm_peak": 100.0 * NL * ab["total"] / (ms_fused * 1e-3) / 1e9 / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": f"paged_attn_decode_layers call (mean of {K} CUDA-graph replays, "
+                               "CUDA events on the launch stream)",
+                     "algorithmic_bytes_per_launch": launch_bytes,
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "gpu_launches": K,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     prefill = args.config in W.PREFILL_CONFIGS
+    if args.layers > 1 and not prefill and args.config != "cow_copy_70b":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
+                              "oracle on one layer (run without --layers)"}))
+            return
+        run_layers(args)
+        return
     if args.config == "cow_copy_70b":
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "no oracle arm for page copies: "

@@ -13,7 +13,8 @@
  *    the dense single-query attention of the "Inference optimization" lesson
  *    (Step 2, scaled_dot_product_attention) on the gathered rows.
  *    Variants: with the cache write fused in (pkv_paged_attn_decode_append),
- *    with per-KV-head scales of quantised caches
+ *    several layers in one launch (pkv_paged_attn_decode_layers), with
+ *    per-KV-head scales of quantised caches
  *    (pkv_paged_attn_decode_head_scaled), without a caller workspace
  *    (pkv_paged_attn_decode_noalloc).
  *
@@ -202,6 +203,71 @@ pkv_status pkv_paged_attn_decode_append(const void *q, pkv_dtype q_dtype, const 
                                         float scale, void *out, pkv_dtype out_dtype,
                                         void *workspace, size_t workspace_bytes,
                                         int partition_tokens, int flags, void *stream);
+
+/*
+ * Several decode layers in one launch.  A decoder stack repeats the same
+ * attention in every layer over the same sequences: the block tables and
+ * lengths are shared, while each layer has its own caches, query, new rows
+ * and output ("Inference optimization" lesson, section "Caches de KV": the
+ * cache holds K and V of every layer, 2 * layers * KV heads * head_dim *
+ * bytes per token).  Decode is bound by memory reads
+ * (section "O framework de operacoes:byte"), so on small layers (a chat
+ * batch of short sequences) the fixed cost of each launch -- grid fill and
+ * drain -- is a large share of the time; this entry point runs the decode of
+ * num_layers layers as one persistent grid, the work of all layers
+ * scheduled together, with the fused cache write of
+ * pkv_paged_attn_decode_append in every layer that has new rows.
+ *
+ *   layers       DEVICE array of num_layers pkv_layer entries (8-byte
+ *                aligned), read by the kernels.  Per layer:
+ *                  q        [num_seqs, num_q_heads, head_dim] of q_dtype
+ *                  new_k,
+ *                  new_v    [num_seqs, num_kv_heads, head_dim] of new_dtype
+ *                           (F32 or BF16), or both NULL: no cache write in
+ *                           that layer (then seq_lens[s] counts only cached
+ *                           tokens, as for pkv_paged_attn_decode)
+ *                  k_cache,
+ *                  v_cache  [num_blocks, num_kv_heads, head_dim, block_size]
+ *                           of kv_dtype
+ *                  out      [num_seqs, num_q_heads, head_dim] of out_dtype
+ *                Every pointer must be 16-byte aligned device memory.  An
+ *                entry with a null or misaligned tensor is skipped (nothing
+ *                is read through it or written to it) and reported as
+ *                PKV_ERR_INVALID_ARG in the status word.
+ *   block_tables, seq_lens, sizes, scales, scale: shared by every layer, as
+ *                for pkv_paged_attn_decode_append.
+ *   workspace    >= pkv_paged_attn_layers_workspace_size(num_layers, ...)
+ *                bytes, 256-byte aligned.
+ * Every layer's result is bit-identical to pkv_paged_attn_decode_append (or
+ * pkv_paged_attn_decode for a layer without new rows) of that layer alone
+ * with the partition size this call uses (pkv_paged_attn_layers_partition_
+ * tokens; the automatic choice counts the (layer, sequence, KV head) units).
+ * Other arguments and errors as for pkv_paged_attn_decode.
+ */
+typedef struct pkv_layer {
+    const void *q;
+    const void *new_k;
+    const void *new_v;
+    void *k_cache;
+    void *v_cache;
+    void *out;
+} pkv_layer;
+size_t pkv_paged_attn_layers_workspace_size(int num_layers, int num_seqs, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size,
+                                            int max_seq_len, int partition_tokens);
+int pkv_paged_attn_layers_partition_tokens(int num_layers, int num_seqs, int num_q_heads,
+                                           int num_kv_heads, int head_dim, int block_size,
+                                           int max_seq_len, int partition_tokens);
+pkv_status pkv_paged_attn_decode_layers(const pkv_layer *layers, int num_layers,
+                                        pkv_dtype q_dtype, pkv_dtype new_dtype,
+                                        pkv_dtype kv_dtype, float k_scale, float v_scale,
+                                        const int32_t *block_tables, const int32_t *seq_lens,
+                                        int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int num_blocks,
+                                        int max_blocks_per_seq, int max_seq_len, float scale,
+                                        pkv_dtype out_dtype, void *workspace,
+                                        size_t workspace_bytes, int partition_tokens, int flags,
+                                        void *stream);
 
 /*
  * Decode over an fp8 or INT4 cache quantised with one scale per

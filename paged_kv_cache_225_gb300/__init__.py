@@ -75,6 +75,13 @@ def lib(build_if_missing: bool = True) -> ctypes.CDLL:
                                                        i, i, i, i, i, i, i, i, f, vp, i, vp, sz, i,
                                                        i, vp]
             L.pkv_paged_attn_decode_append.restype = i
+            L.pkv_paged_attn_layers_workspace_size.argtypes = [i] * 8
+            L.pkv_paged_attn_layers_workspace_size.restype = sz
+            L.pkv_paged_attn_layers_partition_tokens.argtypes = [i] * 8
+            L.pkv_paged_attn_layers_partition_tokens.restype = i
+            L.pkv_paged_attn_decode_layers.argtypes = [vp, i, i, i, i, f, f, vp, vp, i, i, i, i,
+                                                       i, i, i, i, f, i, vp, sz, i, i, vp]
+            L.pkv_paged_attn_decode_layers.restype = i
             L.pkv_paged_attn_prefill_workspace_size.argtypes = [i] * 9
             L.pkv_paged_attn_prefill_workspace_size.restype = sz
             L.pkv_paged_attn_prefill_partition_tokens.argtypes = [i] * 9
@@ -375,6 +382,112 @@ def paged_attn_decode_append(q: torch.Tensor, new_k: torch.Tensor, new_v: torch.
     if rc != 0:
         raise PkvError(rc, "pkv_paged_attn_decode_append")
     return out
+
+
+def layers_workspace_size(num_layers: int, num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                          head_dim: int, max_seq_len: int, partition_tokens: int = 0) -> int:
+    """Workspace bytes of ``paged_attn_decode_layers`` (pkv_paged_attn_layers_workspace_size)."""
+    n = lib().pkv_paged_attn_layers_workspace_size(num_layers, num_seqs, num_q_heads,
+                                                   num_kv_heads, head_dim, 16, max_seq_len,
+                                                   partition_tokens)
+    if n == 0:
+        raise ValueError("invalid sizes or partition_tokens")
+    return int(n)
+
+
+def layers_partition_tokens(num_layers: int, num_seqs: int, num_q_heads: int, num_kv_heads: int,
+                            head_dim: int, max_seq_len: int, partition_tokens: int = 0) -> int:
+    """The schedule ``paged_attn_decode_layers`` uses (as ``partition_tokens``)."""
+    return int(lib().pkv_paged_attn_layers_partition_tokens(
+        num_layers, num_seqs, num_q_heads, num_kv_heads, head_dim, 16, max_seq_len,
+        partition_tokens))
+
+
+# Field order of one pkv_layer entry.
+LAYER_FIELDS = ("q", "new_k", "new_v", "k_cache", "v_cache", "out")
+
+
+def layer_table(layers, device: Optional[torch.device] = None) -> torch.Tensor:
+    """The device table of pkv_layer entries (int64 [L, 6]) for ``layers``, a list
+    of dicts with keys LAYER_FIELDS (new_k / new_v may be None or absent)."""
+    rows = [[(lay[k].data_ptr() if lay.get(k) is not None else 0) for k in LAYER_FIELDS]
+            for lay in layers]
+    dev = device if device is not None else layers[0]["q"].device
+    return torch.tensor(rows, dtype=torch.int64).to(dev)
+
+
+def paged_attn_decode_layers(layers, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                             scale: float, *, k_scale: float = 1.0, v_scale: float = 1.0,
+                             max_seq_len: Optional[int] = None, partition_tokens: int = 0,
+                             impl: str = "auto", workspace: Optional[torch.Tensor] = None,
+                             table: Optional[torch.Tensor] = None,
+                             stream: Optional[torch.cuda.Stream] = None, flags: int = 0):
+    """Decode of several layers in one launch (pkv_paged_attn_decode_layers).
+
+    ``layers``: list of dicts with keys LAYER_FIELDS: per layer q [S, Hq, D],
+    optional new_k / new_v [S, Hkv, D] (the fused cache write of
+    ``paged_attn_decode_append``; seq_lens then include the new token),
+    k_cache / v_cache [N, Hkv, D, 16] and out [S, Hq, D].  All layers share
+    block_tables and seq_lens, and the dtypes and shapes of the first layer.
+    ``table`` is a prebuilt ``layer_table(layers)`` (needed under CUDA-graph
+    capture; otherwise built here).  Returns the list of outputs.
+    """
+    dev = layers[0]["q"].device
+    first = layers[0]
+    for lay in layers:
+        for name, nd in (("q", 3), ("k_cache", 4), ("v_cache", 4), ("out", 3)):
+            _check(lay[name], name, nd, dev)
+            if lay[name].shape != first[name].shape or lay[name].dtype != first[name].dtype:
+                raise ValueError(f"layer {name} differs from the first layer's")
+        for name in ("new_k", "new_v"):
+            if lay.get(name) is not None:
+                _check(lay[name], name, 3, dev)
+    _check(block_tables, "block_tables", 2, dev)
+    _check(seq_lens, "seq_lens", 1, dev)
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    q, kc = first["q"], first["k_cache"]
+    S, Hq, D = q.shape
+    N, Hkv, D2, B = _pool_dims(kc)
+    if D2 != D or first["out"].shape != q.shape or block_tables.shape[0] != S \
+            or seq_lens.shape[0] != S:
+        raise ValueError("inconsistent shapes")
+    new_dtype = F32
+    for lay in layers:
+        nk, nv = lay.get("new_k"), lay.get("new_v")
+        if (nk is None) != (nv is None):
+            raise ValueError("new_k and new_v must both be given or both be None")
+        if nk is not None:
+            if nk.shape != (S, Hkv, D) or nv.shape != nk.shape or nv.dtype != nk.dtype:
+                raise ValueError("inconsistent new row shapes")
+            new_dtype = _dtype_code(nk, "new_k")
+    max_blocks = block_tables.shape[1]
+    if max_seq_len is None:
+        max_seq_len = max_blocks * B
+    NL = len(layers)
+    L = lib()
+    need = L.pkv_paged_attn_layers_workspace_size(NL, S, Hq, Hkv, D, B, max_seq_len,
+                                                  partition_tokens)
+    if need == 0:
+        raise ValueError("invalid sizes or partition_tokens")
+    if workspace is None:
+        workspace = get_workspace(need, dev)
+    if table is None:
+        table = layer_table(layers, dev)
+    if table.dtype != torch.int64 or tuple(table.shape) != (NL, len(LAYER_FIELDS)) \
+            or table.device != dev or not table.is_contiguous():
+        raise ValueError("table must be a contiguous int64 [num_layers, 6] tensor on q's device")
+    flags |= IMPL[impl]
+    rc = L.pkv_paged_attn_decode_layers(
+        table.data_ptr(), NL, _dtype_code(q, "q"), new_dtype, _dtype_code(kc, "k_cache"),
+        float(k_scale), float(v_scale), block_tables.data_ptr(), seq_lens.data_ptr(), S, Hq,
+        Hkv, D, B, N, max_blocks, int(max_seq_len), float(scale),
+        _dtype_code(first["out"], "out"), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), int(partition_tokens), int(flags),
+        _stream(dev, stream))
+    if rc != 0:
+        raise PkvError(rc, "pkv_paged_attn_decode_layers")
+    return [lay["out"] for lay in layers]
 
 
 def prefill_workspace_size(num_seqs: int, num_tokens: int, num_q_heads: int, num_kv_heads: int,

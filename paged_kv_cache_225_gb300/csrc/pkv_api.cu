@@ -72,12 +72,13 @@ constexpr int kStreamK = -2;  // plan code of the stream-K schedule
 
 // Schedule for these sizes: > 0 fixed partitions of that many tokens, 0 one
 // pass per (sequence, KV head), kStreamK equal page ranges per CTA (the
-// automatic choice), -1 invalid.
-static int resolve_partition(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                             int block_size, int max_seq_len, int requested)
+// automatic choice), -1 invalid.  num_layers layers share the lengths.
+static int resolve_partition(int num_layers, int num_seqs, int num_q_heads, int num_kv_heads,
+                             int head_dim, int block_size, int max_seq_len, int requested)
 {
-    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
-        block_size != kBlockSize || max_seq_len < 0 || num_q_heads % num_kv_heads != 0)
+    if (num_layers <= 0 || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim <= 0 || block_size != kBlockSize || max_seq_len < 0 ||
+        num_q_heads % num_kv_heads != 0)
         return -1;
     if (requested == -1)
         return 0;
@@ -94,7 +95,7 @@ static int resolve_partition(int num_seqs, int num_q_heads, int num_kv_heads, in
     // which splits them evenly across all CTAs.  The threshold is twice the
     // CTAs resident on a GB300 (two per SM); a fixed number keeps the plan,
     // and so the workspace size, independent of the current device.
-    const long units = static_cast<long>(num_seqs) * num_kv_heads;
+    const long units = static_cast<long>(num_layers) * num_seqs * num_kv_heads;
     const long many = 2L * 2 * 152;
     if (units >= many)
         return max_seq_len <= 2048 ? 0 : 2048;
@@ -104,16 +105,18 @@ static int resolve_partition(int num_seqs, int num_q_heads, int num_kv_heads, in
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // Workspace: [256-byte header: status, work counter][arrive counters
-// S*Hkv u32][partial outputs S*Hq*max_parts*D f32][partial (m, l) pairs].
+// L*S*Hkv u32][partial outputs L*S*Hq*max_parts*D f32][partial (m, l) pairs]
+// for L layers (stream-K: partial slots per CTA instead, whatever L).
 struct Plan {
     int partition;  // 0 = no split
     int max_parts;
     size_t arrive_off, part_o_off, part_ml_off, bytes;
 };
 
-static bool make_plan(int S, int Hq, int Hkv, int D, int B, int max_len, int requested, Plan *pl)
+static bool make_plan(int NL, int S, int Hq, int Hkv, int D, int B, int max_len, int requested,
+                      Plan *pl)
 {
-    const int P = resolve_partition(S, Hq, Hkv, D, B, max_len, requested);
+    const int P = resolve_partition(NL, S, Hq, Hkv, D, B, max_len, requested);
     if (P == -1)
         return false;
     pl->partition = P;
@@ -124,14 +127,16 @@ static bool make_plan(int S, int Hq, int Hkv, int D, int B, int max_len, int req
         // Two partial slots per CTA, G rows each.
         const size_t rows = static_cast<size_t>(2) * kStreamKMaxCtas * (Hq / Hkv);
         pl->arrive_off = kWorkspaceHeader;
-        pl->part_o_off = pl->arrive_off + align256(static_cast<size_t>(S) * Hkv * sizeof(unsigned));
+        pl->part_o_off =
+            pl->arrive_off + align256(static_cast<size_t>(NL) * S * Hkv * sizeof(unsigned));
         pl->part_ml_off = pl->part_o_off + align256(rows * D * sizeof(float));
         pl->bytes = pl->part_ml_off + align256(rows * 2 * sizeof(float));
     } else if (P > 0) {
         pl->max_parts = max_len > P ? (max_len + P - 1) / P : 1;
-        const size_t rows = static_cast<size_t>(S) * Hq * pl->max_parts;
+        const size_t rows = static_cast<size_t>(NL) * S * Hq * pl->max_parts;
         pl->arrive_off = kWorkspaceHeader;
-        pl->part_o_off = pl->arrive_off + align256(static_cast<size_t>(S) * Hkv * sizeof(unsigned));
+        pl->part_o_off =
+            pl->arrive_off + align256(static_cast<size_t>(NL) * S * Hkv * sizeof(unsigned));
         pl->part_ml_off = pl->part_o_off + align256(rows * D * sizeof(float));
         pl->bytes = pl->part_ml_off + align256(rows * 2 * sizeof(float));
     }
@@ -150,41 +155,59 @@ size_t pkv_paged_attn_workspace_size(int num_seqs, int num_q_heads, int num_kv_h
                                      int head_dim, int block_size, int max_seq_len,
                                      int partition_tokens)
 {
-    Plan pl;
-    if (!make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
-                   partition_tokens, &pl))
-        return 0;
-    return pl.bytes;
+    return pkv_paged_attn_layers_workspace_size(1, num_seqs, num_q_heads, num_kv_heads,
+                                                head_dim, block_size, max_seq_len,
+                                                partition_tokens);
 }
 
 int pkv_paged_attn_partition_tokens(int num_seqs, int num_q_heads, int num_kv_heads,
                                     int head_dim, int block_size, int max_seq_len,
                                     int partition_tokens)
 {
-    return resolve_partition(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+    return resolve_partition(1, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                              max_seq_len, partition_tokens);
+}
+
+size_t pkv_paged_attn_layers_workspace_size(int num_layers, int num_seqs, int num_q_heads,
+                                            int num_kv_heads, int head_dim, int block_size,
+                                            int max_seq_len, int partition_tokens)
+{
+    Plan pl;
+    if (!make_plan(num_layers, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                   max_seq_len, partition_tokens, &pl))
+        return 0;
+    return pl.bytes;
+}
+
+int pkv_paged_attn_layers_partition_tokens(int num_layers, int num_seqs, int num_q_heads,
+                                           int num_kv_heads, int head_dim, int block_size,
+                                           int max_seq_len, int partition_tokens)
+{
+    return resolve_partition(num_layers, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                             block_size, max_seq_len, partition_tokens);
 }
 
 }  // extern "C"
 
 namespace pkv {
 
-// Decode, optionally with the fused cache write of one new token per
-// sequence (new_k non-null).
-static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_cache,
-                              const void *v_cache, pkv_dtype kv_dtype, float k_scale,
+// Decode of one layer (`layers` null: the tensors in `one`, checked here) or
+// of num_layers layers whose tensors sit in a device table (checked by the
+// kernels), optionally with the fused cache write of one new token per
+// sequence (`append`: the layers' new_k rows, where non-null).
+static pkv_status decode_impl(const LayerPtrs &one, const LayerPtrs *layers, int num_layers,
+                              bool append, pkv_dtype q_dtype, pkv_dtype kv_dtype, float k_scale,
                               float v_scale, const int32_t *block_tables,
                               const int32_t *seq_lens, int num_seqs, int num_q_heads,
                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                              int max_blocks_per_seq, int max_seq_len, float scale, void *out,
+                              int max_blocks_per_seq, int max_seq_len, float scale,
                               pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
-                              int partition_tokens, int flags, void *stream, const void *new_k,
-                              const void *new_v, pkv_dtype new_dtype,
+                              int partition_tokens, int flags, void *stream, pkv_dtype new_dtype,
                               const float *k_head_scales = nullptr,
                               const float *v_head_scales = nullptr)
 {
-    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
-        max_blocks_per_seq <= 0 || max_seq_len < 0)
+    if (num_layers <= 0 || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_blocks <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0)
         return PKV_ERR_INVALID_ARG;
     if (num_q_heads % num_kv_heads != 0)
         return PKV_ERR_INVALID_ARG;
@@ -210,18 +233,28 @@ static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_ca
         (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_MASK)
         return PKV_ERR_INVALID_ARG;
     Plan pl;
-    if (!make_plan(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_seq_len,
-                   partition_tokens, &pl))
+    if (!make_plan(num_layers, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                   max_seq_len, partition_tokens, &pl))
         return PKV_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) || workspace_bytes < pl.bytes)
         return PKV_ERR_WORKSPACE;
     if (num_seqs == 0)
         return PKV_OK;
-    if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out)
+    if (!block_tables || !seq_lens || !aligned(block_tables, 4) || !aligned(seq_lens, 4))
         return PKV_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-        !aligned(block_tables, 4) || !aligned(seq_lens, 4))
-        return PKV_ERR_INVALID_ARG;
+    if (layers) {
+        if (!aligned(layers, alignof(LayerPtrs)))
+            return PKV_ERR_INVALID_ARG;
+    } else {
+        if (!one.q || !one.k_cache || !one.v_cache || !one.out)
+            return PKV_ERR_INVALID_ARG;
+        if (!aligned(one.q, 16) || !aligned(one.k_cache, 16) || !aligned(one.v_cache, 16) ||
+            !aligned(one.out, 16))
+            return PKV_ERR_INVALID_ARG;
+        if (append && (!one.new_k || !one.new_v || !aligned(one.new_k, 16) ||
+                       !aligned(one.new_v, 16)))
+            return PKV_ERR_INVALID_ARG;
+    }
 
     const int impl = flags & PKV_FLAG_IMPL_MASK;
     const bool mma_ok = mma_supports(kv_dtype, q_dtype, head_dim, group);
@@ -232,12 +265,13 @@ static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_ca
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     DecodeParams p;
     std::memset(&p, 0, sizeof p);
-    p.q = q;
-    p.k_cache = k_cache;
-    p.v_cache = v_cache;
+    p.one = one;
+    if (!append)
+        p.one.new_k = p.one.new_v = nullptr;
+    p.layers = layers;
+    p.num_layers = num_layers;
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
-    p.out = out;
     p.status = reinterpret_cast<int *>(ws);
     p.counter = reinterpret_cast<unsigned *>(ws + 4);
     const bool partials = pl.partition != 0;
@@ -268,8 +302,7 @@ static pkv_status decode_impl(const void *q, pkv_dtype q_dtype, const void *k_ca
     p.streamk_max_ctas = kStreamKMaxCtas;
     p.fused_merge = (flags & PKV_FLAG_SEPARATE_MERGE) ? 0 : 1;
     p.drop_first_copy = (flags & PKV_FLAG_TEST_DROP_FIRST_COPY) ? 1 : 0;
-    p.new_k = new_k;
-    p.new_v = new_v;
+    p.append = append ? 1 : 0;
     p.new_dtype = new_dtype;
     p.kv_dtype = kv_dtype;
     p.k_scale = k_scale;
@@ -303,11 +336,12 @@ pkv_status pkv_paged_attn_decode(const void *q, pkv_dtype q_dtype, const void *k
                                  pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
                                  int partition_tokens, int flags, void *stream)
 {
-    return decode_impl(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_tables,
+    const LayerPtrs one = {q, nullptr, nullptr, const_cast<void *>(k_cache),
+                           const_cast<void *>(v_cache), out};
+    return decode_impl(one, nullptr, 1, false, q_dtype, kv_dtype, k_scale, v_scale, block_tables,
                        seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       num_blocks, max_blocks_per_seq, max_seq_len, scale, out, out_dtype,
-                       workspace, workspace_bytes, partition_tokens, flags, stream, nullptr,
-                       nullptr, PKV_F32);
+                       num_blocks, max_blocks_per_seq, max_seq_len, scale, out_dtype, workspace,
+                       workspace_bytes, partition_tokens, flags, stream, PKV_F32);
 }
 
 pkv_status pkv_paged_attn_decode_append(const void *q, pkv_dtype q_dtype, const void *new_k,
@@ -325,13 +359,37 @@ pkv_status pkv_paged_attn_decode_append(const void *q, pkv_dtype q_dtype, const 
         return PKV_ERR_UNSUPPORTED;
     if (is_scaled(kv_dtype) && (k_scale == 0.f || v_scale == 0.f))
         return PKV_ERR_INVALID_ARG;
-    if (num_seqs > 0 && (!new_k || !new_v || !aligned(new_k, 16) || !aligned(new_v, 16)))
-        return PKV_ERR_INVALID_ARG;
-    return decode_impl(q, q_dtype, k_cache, v_cache, kv_dtype, k_scale, v_scale, block_tables,
+    const LayerPtrs one = {q, new_k, new_v, k_cache, v_cache, out};
+    return decode_impl(one, nullptr, 1, true, q_dtype, kv_dtype, k_scale, v_scale, block_tables,
                        seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       num_blocks, max_blocks_per_seq, max_seq_len, scale, out, out_dtype,
-                       workspace, workspace_bytes, partition_tokens, flags, stream, new_k, new_v,
-                       new_dtype);
+                       num_blocks, max_blocks_per_seq, max_seq_len, scale, out_dtype, workspace,
+                       workspace_bytes, partition_tokens, flags, stream, new_dtype);
+}
+
+pkv_status pkv_paged_attn_decode_layers(const pkv_layer *layers, int num_layers,
+                                        pkv_dtype q_dtype, pkv_dtype new_dtype,
+                                        pkv_dtype kv_dtype, float k_scale, float v_scale,
+                                        const int32_t *block_tables, const int32_t *seq_lens,
+                                        int num_seqs, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int num_blocks,
+                                        int max_blocks_per_seq, int max_seq_len, float scale,
+                                        pkv_dtype out_dtype, void *workspace,
+                                        size_t workspace_bytes, int partition_tokens, int flags,
+                                        void *stream)
+{
+    static_assert(sizeof(pkv_layer) == sizeof(LayerPtrs), "pkv_layer layout");
+    if (!layers)
+        return PKV_ERR_INVALID_ARG;
+    if (new_dtype != PKV_F32 && new_dtype != PKV_BF16)
+        return PKV_ERR_UNSUPPORTED;
+    if (is_scaled(kv_dtype) && (k_scale == 0.f || v_scale == 0.f))
+        return PKV_ERR_INVALID_ARG;
+    const LayerPtrs none = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+    return decode_impl(none, reinterpret_cast<const LayerPtrs *>(layers), num_layers, true,
+                       q_dtype, kv_dtype, k_scale, v_scale, block_tables, seq_lens, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_seq_len, scale, out_dtype, workspace,
+                       workspace_bytes, partition_tokens, flags, stream, new_dtype);
 }
 
 pkv_status pkv_paged_attn_decode_head_scaled(
@@ -347,11 +405,13 @@ pkv_status pkv_paged_attn_decode_head_scaled(
     if (num_seqs > 0 && (!k_head_scales || !v_head_scales || !aligned(k_head_scales, 4) ||
                          !aligned(v_head_scales, 4)))
         return PKV_ERR_INVALID_ARG;
-    return decode_impl(q, q_dtype, k_cache, v_cache, kv_dtype, 1.0f, 1.0f, block_tables,
+    const LayerPtrs one = {q, nullptr, nullptr, const_cast<void *>(k_cache),
+                           const_cast<void *>(v_cache), out};
+    return decode_impl(one, nullptr, 1, false, q_dtype, kv_dtype, 1.0f, 1.0f, block_tables,
                        seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       num_blocks, max_blocks_per_seq, max_seq_len, scale, out, out_dtype,
-                       workspace, workspace_bytes, partition_tokens, flags, stream, nullptr,
-                       nullptr, PKV_F32, k_head_scales, v_head_scales);
+                       num_blocks, max_blocks_per_seq, max_seq_len, scale, out_dtype, workspace,
+                       workspace_bytes, partition_tokens, flags, stream, PKV_F32, k_head_scales,
+                       v_head_scales);
 }
 
 static pkv_status reshape_impl(const void *k, const void *v, pkv_dtype in_dtype,

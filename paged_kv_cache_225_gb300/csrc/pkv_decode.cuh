@@ -101,11 +101,11 @@ template <int KV, int D, int Budget> struct Ring {
     static constexpr int kRingBytes = R * kStageBytes;
 };
 
-__device__ __forceinline__ float load_q(const DecodeParams &p, size_t idx)
+__device__ __forceinline__ float load_q(const DecodeParams &p, const void *q, size_t idx)
 {
     if (p.q_dtype == PKV_F32)
-        return static_cast<const float *>(p.q)[idx];
-    const unsigned short b = static_cast<const unsigned short *>(p.q)[idx];
+        return static_cast<const float *>(q)[idx];
+    const unsigned short b = static_cast<const unsigned short *>(q)[idx];
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
@@ -203,8 +203,8 @@ struct SimtPolicy {
         }
     }
 
-    __device__ static void begin(State &st, const DecodeParams &p, int s, int hkv, int lane,
-                                 unsigned char *extra)
+    __device__ static void begin(State &st, const DecodeParams &p, const void *q, int s, int hkv,
+                                 int lane, unsigned char *extra)
     {
 #pragma unroll
         for (int g = 0; g < GT; ++g) {
@@ -219,8 +219,8 @@ struct SimtPolicy {
         for (int idx = threadIdx.x; idx < D * GT; idx += kThreads) {
             const int d = idx / GT, g = idx - d * GT;
             float v = 0.f;
-            if (g < G)
-                v = load_q(p, (static_cast<size_t>(s) * p.num_q_heads + hkv * G + g) * D + d);
+            if (g < G && q != nullptr)  // null: a skipped layer's unit, zero query
+                v = load_q(p, q, (static_cast<size_t>(s) * p.num_q_heads + hkv * G + g) * D + d);
             const int half = d / kHalf;
             sq[half * kQHalfStride + (d - half * kHalf) * GT + g] = v;
         }
@@ -389,16 +389,18 @@ struct MmaStateBase {
     }
 
     // Query fragments (B operand of S^T = K^T Q^T): lane (r, c) holds
-    // q[head 8n+r][16ks + 2c, +1] and [16ks + 8 + 2c, +1]; heads >= G are 0.
+    // q[head 8n+r][16ks + 2c, +1] and [16ks + 8 + 2c, +1]; heads >= G are 0,
+    // and so is every head when q is null (a skipped layer's unit).
     template <bool F16>
-    __device__ static void load_q_frags(State &st, const DecodeParams &p, int s, int hkv, int lane)
+    __device__ static void load_q_frags(State &st, const DecodeParams &p, const void *q, int s,
+                                        int hkv, int lane)
     {
         const int r = lane >> 2, c = lane & 3;
         const int G = p.group;
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
             const int g = 8 * n + r;
-            const bool ok = g < G;
+            const bool ok = g < G && q != nullptr;
             const size_t row = (static_cast<size_t>(s) * p.num_q_heads + hkv * G + (ok ? g : 0)) * D;
 #pragma unroll
             for (int ks = 0; ks < KS; ++ks) {
@@ -409,9 +411,9 @@ struct MmaStateBase {
                     if (ok) {
                         if (!F16) {
                             w = *reinterpret_cast<const uint32_t *>(
-                                static_cast<const unsigned short *>(p.q) + row + d);
+                                static_cast<const unsigned short *>(q) + row + d);
                         } else {
-                            const float a = load_q(p, row + d), b = load_q(p, row + d + 1);
+                            const float a = load_q(p, q, row + d), b = load_q(p, q, row + d + 1);
                             w = pack_f16(a, b);
                         }
                     }
@@ -490,11 +492,11 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
         uint32_t v[MT][4];  // V A fragments, one per 16-row head_dim tile
     };
 
-    __device__ static void begin(State &st, const DecodeParams &p, int s, int hkv, int lane,
-                                 unsigned char *)
+    __device__ static void begin(State &st, const DecodeParams &p, const void *q, int s, int hkv,
+                                 int lane, unsigned char *)
     {
         Base::reset(st);
-        Base::template load_q_frags<false>(st, p, s, hkv, lane);
+        Base::template load_q_frags<false>(st, p, q, s, hkv, lane);
     }
 
     __device__ static void load(Frags &f, const unsigned char *sK, const unsigned char *sV,
@@ -660,11 +662,11 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
         uint32_t v[MT / 2][4];  // raw codes of 32 head_dim rows of V per entry
     };
 
-    __device__ static void begin(State &st, const DecodeParams &p, int s, int hkv, int lane,
-                                 unsigned char *)
+    __device__ static void begin(State &st, const DecodeParams &p, const void *q, int s, int hkv,
+                                 int lane, unsigned char *)
     {
         Base::reset(st);
-        Base::template load_q_frags<true>(st, p, s, hkv, lane);
+        Base::template load_q_frags<true>(st, p, q, s, hkv, lane);
     }
 
     __device__ static void load(Frags &f, const unsigned char *sK, const unsigned char *sV,
@@ -799,11 +801,11 @@ struct MmaInt4Policy : MmaStateBase<D, NT> {
         uint32_t v[MT][2];  // per head_dim tile: bytes 2c, 2c+1 of rows g and g + 8
     };
 
-    __device__ static void begin(State &st, const DecodeParams &p, int s, int hkv, int lane,
-                                 unsigned char *)
+    __device__ static void begin(State &st, const DecodeParams &p, const void *q, int s, int hkv,
+                                 int lane, unsigned char *)
     {
         Base::reset(st);
-        Base::template load_q_frags<true>(st, p, s, hkv, lane);
+        Base::template load_q_frags<true>(st, p, q, s, hkv, lane);
     }
 
     __device__ static void load(Frags &f, const unsigned char *sK, const unsigned char *sV,
@@ -899,8 +901,9 @@ constexpr int kNewRowBytes = 2 * 128 * 4;
 
 // Starts copying the new K and V rows of (s, hkv) into `buf` (shared memory)
 // without waiting; write_new_token_from(buf) consumes them.
-__device__ __forceinline__ void prefetch_new_rows(const DecodeParams &p, int s, int hkv, int D,
-                                                  unsigned char *buf, int lane)
+__device__ __forceinline__ void prefetch_new_rows(const DecodeParams &p, const LayerPtrs &lt,
+                                                  int s, int hkv, int D, unsigned char *buf,
+                                                  int lane)
 {
     const int eb = p.new_dtype == PKV_F32 ? 4 : 2;
     const int row_bytes = D * eb;  // multiple of 16
@@ -909,7 +912,7 @@ __device__ __forceinline__ void prefetch_new_rows(const DecodeParams &p, int s, 
         const bool is_v = c * 16 >= row_bytes;
         const int off = c * 16 - (is_v ? row_bytes : 0);
         const unsigned char *src =
-            static_cast<const unsigned char *>(is_v ? p.new_v : p.new_k) + src0 + off;
+            static_cast<const unsigned char *>(is_v ? lt.new_v : lt.new_k) + src0 + off;
         cp_async_16(buf + (is_v ? row_bytes : 0) + off, src);
     }
     cp_async_commit();
@@ -917,8 +920,10 @@ __device__ __forceinline__ void prefetch_new_rows(const DecodeParams &p, int s, 
 
 // Writes the new token of (s, hkv) from the rows prefetch_new_rows staged in
 // shared memory into slot (L - 1) % 16 of block phys, then fences the writes
-// against the bulk copy of that page that follows.
-__device__ __forceinline__ void write_new_token_from(const DecodeParams &p, int hkv, int L,
+// against the bulk copy of that page that follows.  kc_head / vc_head point
+// at KV head hkv's tile of block 0 of the layer's caches.
+__device__ __forceinline__ void write_new_token_from(const DecodeParams &p, const void *kc_head,
+                                                     const void *vc_head, int hkv, int L,
                                                      int phys, int D, const unsigned char *buf,
                                                      int lane)
 {
@@ -926,9 +931,9 @@ __device__ __forceinline__ void write_new_token_from(const DecodeParams &p, int 
     __syncwarp();
     const int t = (L - 1) % kBlockSize;
     const int row_bytes = D * (p.new_dtype == PKV_F32 ? 4 : 2);
-    const size_t dst0 = (static_cast<size_t>(phys) * p.num_kv_heads + hkv) * D;
-    void *kc = const_cast<void *>(p.k_cache);
-    void *vc = const_cast<void *>(p.v_cache);
+    const size_t dst0 = static_cast<size_t>(phys) * p.num_kv_heads * D;
+    void *kc = const_cast<void *>(kc_head);
+    void *vc = const_cast<void *>(vc_head);
     const float kq = unit_k_quant(p, hkv), vq = unit_v_quant(p, hkv);
     for (int d = lane; d < D; d += 32) {
         const size_t g = (dst0 + d) * kBlockSize + t;
@@ -941,15 +946,14 @@ __device__ __forceinline__ void write_new_token_from(const DecodeParams &p, int 
 
 // The converted K/V rows of the listed new tokens stored into their slots,
 // without a fence (the caller fences before the copies it orders).  Entry e
-// of `w` is (s, hkv, L, phys): rows new_k/new_v[s, hkv] go to slot
-// (L - 1) % 16 of block phys.  Each lane handles head_dim elements
-// lane + 32j; all loads of a pair of entries are issued before their stores.
-__device__ __forceinline__ void write_token_rows(const DecodeParams &p, const int (*w)[4], int e0,
+// of `w` is (s, hkv, L, phys, layer): that layer's rows new_k/new_v[s, hkv]
+// go to slot (L - 1) % 16 of block phys of its caches.  Each lane handles
+// head_dim elements lane + 32j; all loads of a pair of entries are issued
+// before their stores.
+__device__ __forceinline__ void write_token_rows(const DecodeParams &p, const int (*w)[5], int e0,
                                                  int n, int step, int D, int lane)
 {
     constexpr int kJ = 4;  // head_dim <= 128
-    void *kc = const_cast<void *>(p.k_cache);
-    void *vc = const_cast<void *>(p.v_cache);
     for (int e = e0; e < n; e += 2 * step) {
         float kv[2][kJ], vv[2][kJ];
 #pragma unroll
@@ -957,13 +961,14 @@ __device__ __forceinline__ void write_token_rows(const DecodeParams &p, const in
             const int ee = e + x * step;
             if (ee >= n)
                 break;
+            const LayerPtrs &lt = layer_ptrs(p, w[ee][4]);
             const size_t src0 = (static_cast<size_t>(w[ee][0]) * p.num_kv_heads + w[ee][1]) * D;
 #pragma unroll
             for (int j = 0; j < kJ; ++j) {
                 const int d = lane + 32 * j;
                 if (d < D) {
-                    kv[x][j] = load_in(p.new_k, p.new_dtype, src0 + d);
-                    vv[x][j] = load_in(p.new_v, p.new_dtype, src0 + d);
+                    kv[x][j] = load_in(lt.new_k, p.new_dtype, src0 + d);
+                    vv[x][j] = load_in(lt.new_v, p.new_dtype, src0 + d);
                 }
             }
         }
@@ -975,6 +980,9 @@ __device__ __forceinline__ void write_token_rows(const DecodeParams &p, const in
             const int t = (w[ee][2] - 1) % kBlockSize;
             const size_t dst0 = (static_cast<size_t>(w[ee][3]) * p.num_kv_heads + w[ee][1]) * D;
             const float kq = unit_k_quant(p, w[ee][1]), vq = unit_v_quant(p, w[ee][1]);
+            const LayerPtrs &lt = layer_ptrs(p, w[ee][4]);
+            void *kc = lt.k_cache;
+            void *vc = lt.v_cache;
 #pragma unroll
             for (int j = 0; j < kJ; ++j) {
                 const int d = lane + 32 * j;
@@ -1036,14 +1044,18 @@ __device__ bool find_unit(const DecodeParams &p, int u, int &cur_s, int &cur_bas
     }
 }
 
-// Total full partitions over all sequences (warp-collective).
-__device__ __forceinline__ int count_full_parts(const DecodeParams &p, int lane)
+// Total full partitions (kTail: remainder items) over all sequences of one
+// layer (warp-collective).
+template <bool kTail>
+__device__ __forceinline__ int count_parts(const DecodeParams &p, int lane)
 {
     int tot = 0;
     for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
         int n = 0;
-        if (s0 + lane < p.num_seqs)
-            n = full_parts(clamp_len(p, __ldg(p.seq_lens + s0 + lane)), p.partition);
+        if (s0 + lane < p.num_seqs) {
+            const int L = clamp_len(p, __ldg(p.seq_lens + s0 + lane));
+            n = kTail ? tail_parts(L, p.partition) : full_parts(L, p.partition);
+        }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
             n += __shfl_xor_sync(kFullMask, n, off);
@@ -1053,11 +1065,11 @@ __device__ __forceinline__ int count_full_parts(const DecodeParams &p, int lane)
 }
 
 // Combines the four warps' (m, l, O) states of one item (at the start of each
-// warp's ring) and writes the output rows (one partition) or the item's
-// normalised partial (split sequences).
+// warp's ring) and writes the output rows of `out` (one partition) or the
+// item's normalised partial (split sequences; gs = layer * S + s).
 template <int D, int GP>
-__device__ void merge_item(const DecodeParams &p, const unsigned char *smem, int ring_bytes, int s,
-                           int hkv, int part, int nparts)
+__device__ void merge_item(const DecodeParams &p, void *out, const unsigned char *smem,
+                           int ring_bytes, int s, int gs, int hkv, int part, int nparts)
 {
     constexpr int Q4 = D / 4;
     const int G = p.group;
@@ -1087,9 +1099,10 @@ __device__ void merge_item(const DecodeParams &p, const unsigned char *smem, int
         const int h = hkv * G + g;
         if (nparts == 1) {
             const float sc = inv * unit_out_scale(p, hkv);
-            store_out4(p, D, s, h, q4, make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
+            store_out4(p, out, D, s, h, q4,
+                       make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
         } else {
-            const size_t row = (static_cast<size_t>(s) * p.num_q_heads + h) * p.max_parts + part;
+            const size_t row = (static_cast<size_t>(gs) * p.num_q_heads + h) * p.max_parts + part;
             reinterpret_cast<float4 *>(p.part_o + row * D)[q4] =
                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
             if (q4 == 0) {
@@ -1101,13 +1114,18 @@ __device__ void merge_item(const DecodeParams &p, const unsigned char *smem, int
 }
 
 template <class Pol>
-__global__ void __launch_bounds__(kThreads, Pol::kMinBlocks) decode_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
+    decode_kernel(const __grid_constant__ DecodeParams p)
 {
     constexpr int D = Pol::kDim;
     static_assert((Pol::GP * D + 2 * Pol::GP) * 4 <= Pol::kRingBytes,
                   "merge scratch must fit in one warp's ring");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_item[8];
+    // Warp 0's item scheduler (kept in shared memory, not registers, across
+    // the page loop): scan cursors of the two item phases (reset when the
+    // layer changes) and the per-layer item counts of the phases.
+    __shared__ int s_sched[8];
     __shared__ int s_abort;
     __shared__ int s_last;
 
@@ -1133,41 +1151,70 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks) decode_kernel(const
     const size_t block_stride = static_cast<size_t>(Hkv) * tile_stride;
 
     uint32_t pages_done = 0;  // pages this warp has consumed (ring position / phase)
-    // Warp 0 only: scan cursors of the two item phases and the phase-1 size.
-    int full_s = 0, full_base = 0, tail_s = 0, tail_base = 0, n_full = 0;
-    if (p.split && warp == 0)
-        n_full = count_full_parts(p, lane);
+    enum { kFullS, kFullBase, kTailS, kTailBase, kFullLayer, kTailLayer, kNFull, kNTail };
+    if (p.split && warp == 0) {
+        const int n_full = count_parts<false>(p, lane);
+        const int n_tail = count_parts<true>(p, lane);
+        if (lane == 0) {
+            for (int i = 0; i < 6; ++i)
+                s_sched[i] = 0;
+            s_sched[kNFull] = n_full;
+            s_sched[kNTail] = n_tail;
+        }
+        __syncwarp();
+    }
     bool first = true;
 
     for (;;) {
         // ---------------------------------------------- next work item
         if (warp == 0) {
-            int s = 0, part = 0, hkv = 0, L = 0, nparts = 1, item = 0, done = 0;
+            int s = 0, part = 0, hkv = 0, L = 0, nparts = 1, item = 0, done = 0, layer = 0;
             if (p.split) {
                 unsigned v = 0;
                 if (lane == 0)
                     v = atomicAdd(p.counter, 1u);
                 item = static_cast<int>(__shfl_sync(kFullMask, v, 0));
-                const int u = item / Hkv;
-                hkv = item - u * Hkv;
-                int k = 0;
-                bool found;
-                if (u < n_full) {
-                    found = find_unit<false>(p, u, full_s, full_base, lane, s, k, L);
-                    part = k;
-                } else {
-                    found = find_unit<true>(p, u - n_full, tail_s, tail_base, lane, s, k, L);
-                    part = full_parts(L, P);
+                // Every layer's full partitions first, then every layer's
+                // remainders; layer-major inside each phase.
+                const int n_full = s_sched[kNFull], n_tail = s_sched[kNTail];
+                const long full_items = static_cast<long>(n_full) * Hkv;
+                long r = item;
+                const bool tail = r >= full_items * p.num_layers;
+                if (tail)
+                    r -= full_items * p.num_layers;
+                const long per = tail ? static_cast<long>(n_tail) * Hkv : full_items;
+                layer = per > 0 ? static_cast<int>(r / per) : p.num_layers;
+                bool found = false;
+                if (layer < p.num_layers) {
+                    r -= static_cast<long>(layer) * per;
+                    const int u = static_cast<int>(r / Hkv);
+                    hkv = static_cast<int>(r - static_cast<long>(u) * Hkv);
+                    int k = 0;
+                    const int o = tail ? kTailS : kFullS;  // this phase's cursors
+                    int cs = s_sched[o], cb = s_sched[o + 1];
+                    if (layer != s_sched[tail ? kTailLayer : kFullLayer])
+                        cs = cb = 0;
+                    found = tail ? find_unit<true>(p, u, cs, cb, lane, s, k, L)
+                                 : find_unit<false>(p, u, cs, cb, lane, s, k, L);
+                    part = tail ? full_parts(L, P) : k;
+                    __syncwarp();
+                    if (lane == 0) {
+                        s_sched[o] = cs;
+                        s_sched[o + 1] = cb;
+                        s_sched[tail ? kTailLayer : kFullLayer] = layer;
+                    }
                 }
                 done = found ? 0 : 1;
                 nparts = parts_of(L, P);
             } else {
                 item = first ? static_cast<int>(blockIdx.x) : INT_MAX;
-                if (item >= S * Hkv) {
+                if (item >= S * Hkv * p.num_layers) {
                     done = 1;
                 } else {
-                    s = item / Hkv;
-                    hkv = item - s * Hkv;
+                    layer = item / (S * Hkv);
+                    const int r = item - layer * (S * Hkv);
+                    s = r / Hkv;
+                    hkv = r - s * Hkv;
                     L = clamp_len(p, __ldg(p.seq_lens + s));
                 }
             }
@@ -1179,6 +1226,7 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks) decode_kernel(const
                 s_item[4] = nparts;
                 s_item[5] = item;
                 s_item[6] = done;
+                s_item[7] = layer;
             }
         }
         first = false;
@@ -1186,7 +1234,14 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks) decode_kernel(const
         if (s_item[6])
             break;
         const int s = s_item[0], part = s_item[1], hkv = s_item[2], L = s_item[3];
-        const int nparts = s_item[4], item = s_item[5];
+        const int nparts = s_item[4], item = s_item[5], layer = s_item[7];
+        const LayerPtrs &lt = layer_ptrs(p, layer);
+        if (!layer_ok(lt)) {  // uniform: every thread reads the same entry
+            if (threadIdx.x == 0)
+                set_status(p.status, PKV_ERR_INVALID_ARG);
+            __syncthreads();  // s_item is rewritten for the next item
+            continue;
+        }
         const float c = unit_score_scale(p, hkv);
 
         // ---------------------------------------------- this warp's pages
@@ -1197,6 +1252,8 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks) decode_kernel(const
         const int nw = npages > warp ? (npages - warp + kWarps - 1) / kWarps : 0;
         const int32_t *bt = p.block_tables + static_cast<size_t>(s) * p.max_blocks + pg0 + warp;
         const size_t head_off = static_cast<size_t>(hkv) * tile_stride;
+        const unsigned char *kbase = static_cast<const unsigned char *>(lt.k_cache) + head_off;
+        const unsigned char *vbase = static_cast<const unsigned char *>(lt.v_cache) + head_off;
 
         int id_reg = -1, id_chunk = -1;
         uint32_t okmask = 0;
@@ -1213,18 +1270,18 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks) decode_kernel(const
         // Fused cache write: the warp that owns the sequence's last page
         // stages the new rows now and writes them just before that page's
         // copy is issued.
-        const int i_new = (p.new_k && t1 == L && L > 0 && npages > 0 &&
+        const int i_new = (p.append && lt.new_k != nullptr && t1 == L && L > 0 && npages > 0 &&
                            (npages - 1) % kWarps == warp)
                               ? (npages - 1) / kWarps
                               : -1;
         if (i_new >= 0)
-            prefetch_new_rows(p, s, hkv, D, newrow, lane);
+            prefetch_new_rows(p, lt, s, hkv, D, newrow, lane);
         auto issue = [&](int i) {
             const int phys = page_id(i);
             const int stg = (pages_done + i) % Pol::R;
             const bool ok = phys >= 0 && phys < p.num_blocks;
             if (i == i_new && ok)
-                write_new_token_from(p, hkv, L, phys, D, newrow, lane);
+                write_new_token_from(p, kbase, vbase, hkv, L, phys, D, newrow, lane);
             okmask = ok ? (okmask | (1u << stg)) : (okmask & ~(1u << stg));
             if (lane == 0) {
                 uint64_t *bar = &bars[stg];
@@ -1235,13 +1292,10 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks) decode_kernel(const
                     mbar_arrive_expect_tx(bar, 2 * Pol::kTileBytes);
                     const bool drop = p.drop_first_copy && item == 0 && warp == 0 && i == 0;
                     if (!drop) {
-                        const size_t off = static_cast<size_t>(phys) * block_stride + head_off;
+                        const size_t off = static_cast<size_t>(phys) * block_stride;
                         unsigned char *dst = ring + stg * Pol::kStageBytes;
-                        bulk_g2s(dst, static_cast<const unsigned char *>(p.k_cache) + off,
-                                 Pol::kTileBytes, bar);
-                        bulk_g2s(dst + Pol::kTileBytes,
-                                 static_cast<const unsigned char *>(p.v_cache) + off,
-                                 Pol::kTileBytes, bar);
+                        bulk_g2s(dst, kbase + off, Pol::kTileBytes, bar);
+                        bulk_g2s(dst + Pol::kTileBytes, vbase + off, Pol::kTileBytes, bar);
                     }
                 }
             }
@@ -1253,7 +1307,7 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks) decode_kernel(const
             issue(issued);
 
         typename Pol::State st;
-        Pol::begin(st, p, s, hkv, lane, extra);
+        Pol::begin(st, p, lt.q, s, hkv, lane, extra);
         __syncthreads();  // policy shared data (SIMT query) is ready
 
         for (int i = 0; i < nw; ++i) {
@@ -1307,8 +1361,13 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks) decode_kernel(const
             Pol::finish(st, so, sm, sl, lane);
         }
         __syncthreads();
-        merge_item<D, Pol::GP>(p, smem, Pol::kRingBytes, s, hkv, part, nparts);
-        if (nparts > 1 && p.fused_merge) {
+        // The item's coordinates again from shared memory (unchanged until
+        // the next item), rather than registers held across the page loop.
+        const int ms = s_item[0], mpart = s_item[1], mhkv = s_item[2], mnparts = s_item[4];
+        const int gs = s_item[7] * S + ms;  // workspace index of (layer, sequence)
+        void *out = layer_ptrs(p, s_item[7]).out;
+        merge_item<D, Pol::GP>(p, out, smem, Pol::kRingBytes, ms, gs, mhkv, mpart, mnparts);
+        if (mnparts > 1 && p.fused_merge) {
             // Publish this partial; the CTA that completes the sequence's last
             // partial merges all of them.  The barrier orders every thread's
             // partial writes before thread 0's gpu-scope fence and arrival.
@@ -1316,13 +1375,13 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks) decode_kernel(const
             if (threadIdx.x == 0) {
                 __threadfence();
                 const unsigned old =
-                    atomicAdd(p.arrive + static_cast<size_t>(s) * Hkv + hkv, 1u);
-                s_last = (old == static_cast<unsigned>(nparts - 1)) ? 1 : 0;
+                    atomicAdd(p.arrive + static_cast<size_t>(gs) * Hkv + mhkv, 1u);
+                s_last = (old == static_cast<unsigned>(mnparts - 1)) ? 1 : 0;
             }
             __syncthreads();
             if (s_last) {
                 __threadfence();
-                merge_partials<D>(p, s, hkv, nparts);
+                merge_partials<D>(p, out, ms, gs, mhkv, mnparts);
             }
         }
         // The rings were used as generic scratch: order that before the next
@@ -1365,11 +1424,12 @@ pkv_status launch_policy(const DecodeParams &p, cudaStream_t stream)
         return rc;
     long grid;
     if (p.split) {
-        const long items = static_cast<long>(p.num_seqs) * p.num_kv_heads * p.max_parts;
+        const long items =
+            static_cast<long>(p.num_layers) * p.num_seqs * p.num_kv_heads * p.max_parts;
         const long slots = static_cast<long>(occ) * device_sm_count();
         grid = items < slots ? items : slots;
     } else {
-        grid = static_cast<long>(p.num_seqs) * p.num_kv_heads;
+        grid = static_cast<long>(p.num_layers) * p.num_seqs * p.num_kv_heads;
     }
     if (grid <= 0)
         return PKV_OK;

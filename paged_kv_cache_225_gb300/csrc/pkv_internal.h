@@ -11,19 +11,33 @@
 
 namespace pkv {
 
+// The tensors of one decode layer (the layout of the public pkv_layer).
+struct LayerPtrs {
+    const void *q;      // [S, Hq, D]
+    const void *new_k;  // [S, Hkv, D] rows of the fused cache write, or null
+    const void *new_v;
+    void *k_cache;      // [N, Hkv, D, 16]
+    void *v_cache;
+    void *out;          // [S, Hq, D]
+};
+static_assert(sizeof(LayerPtrs) == 6 * sizeof(void *), "pkv_layer layout");
+
 // Everything a decode launch needs; passed by value as the kernel parameter.
+// A launch covers num_layers layers that share the block tables and lengths:
+// their tensors come from the device table `layers`, or from `one` when it is
+// null (single-layer calls).  Work of layer l, sequence s is indexed as the
+// global sequence l * S + s in the workspace (partials, arrival counters).
 struct DecodeParams {
-    const void *q;
-    const void *k_cache;
-    const void *v_cache;
+    LayerPtrs one;
+    const LayerPtrs *layers;
+    int num_layers;
     const int32_t *block_tables;
     const int32_t *seq_lens;
-    void *out;
-    float *part_o;        // [S][Hq][max_parts][D] normalised partial outputs
-    float *part_ml;       // [S][Hq][max_parts][2] (max of log2-scaled scores, sum)
+    float *part_o;        // [L*S][Hq][max_parts][D] normalised partial outputs
+    float *part_ml;       // [L*S][Hq][max_parts][2] (max of log2-scaled scores, sum)
     int *status;          // workspace word 0
     unsigned *counter;    // workspace word 1: next work item (split mode)
-    unsigned *arrive;     // [S][Hkv] partials written so far (in-kernel merge)
+    unsigned *arrive;     // [L*S][Hkv] partials written so far (in-kernel merge)
     int q_dtype, out_dtype;
     int num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, max_blocks;
     int max_len;          // caller's bound on seq_lens (<= max_blocks * 16)
@@ -37,12 +51,12 @@ struct DecodeParams {
     int streamk_max_ctas; // CTAs the stream-K partial slots are sized for
     int fused_merge;      // 1: the CTA finishing a sequence's last partial merges it
     int drop_first_copy;  // test hook: never issue the first copy of item 0
-    // Fused cache write (null new_k: none): the new token of sequence s is its
-    // position seq_lens[s] - 1; its K/V rows [S][Hkv][D] of new_dtype are
-    // converted to the cache dtype and written to the cache and into the
-    // page tile the kernel is about to attend.
-    const void *new_k;
-    const void *new_v;
+    // Fused cache write (layers whose new_k is null have none): the new token
+    // of sequence s is its position seq_lens[s] - 1; its K/V rows [S][Hkv][D]
+    // of new_dtype are converted to the cache dtype and written to the cache
+    // and into the page tile the kernel is about to attend.  `append` is set
+    // when any layer may carry new rows.
+    int append;
     int new_dtype;
     int kv_dtype;
     float k_scale, v_scale;

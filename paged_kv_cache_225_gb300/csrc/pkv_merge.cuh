@@ -45,41 +45,65 @@ __device__ __forceinline__ float unit_v_quant(const DecodeParams &p, int hkv)
     return p.v_head_scale ? p.v_scale * __ldg(p.v_head_scale + hkv) : p.v_scale;
 }
 
+// The tensors of layer `layer`: the caller's device table, or the call's own
+// (kernel-parameter) tensors for a single-layer call.
+__device__ __forceinline__ const LayerPtrs &layer_ptrs(const DecodeParams &p, int layer)
+{
+    return p.layers ? p.layers[layer] : p.one;
+}
+
+// A layer entry whose tensors the kernels can use: q, the caches and out
+// non-null and 16-byte aligned, and the new rows either absent or both
+// present and aligned.  Single-layer calls were checked on the host; a bad
+// entry of a device table is reported (PKV_ERR_INVALID_ARG) and its layer
+// is skipped: nothing is read through it or written to it.
+__device__ __forceinline__ bool layer_ok(const LayerPtrs &lt)
+{
+    const auto a16 = [](const void *x) {
+        return x != nullptr && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
+    };
+    const bool rows = (lt.new_k == nullptr && lt.new_v == nullptr) ||
+                      (a16(lt.new_k) && a16(lt.new_v));
+    return a16(lt.q) && a16(lt.k_cache) && a16(lt.v_cache) && a16(lt.out) && rows;
+}
+
 // Partitions of a sequence of L tokens (an empty sequence still has one item,
 // which writes its zero row).
 __device__ __forceinline__ int parts_of(int L, int P) { return L > P ? (L + P - 1) / P : 1; }
 
-// out[s, h, 4*q4 .. 4*q4+3] = v (f32 or bf16 output).
-__device__ __forceinline__ void store_out4(const DecodeParams &p, int D, int s, int h, int q4,
-                                           float4 v)
+// out[s, h, 4*q4 .. 4*q4+3] = v (f32 or bf16 output) for a layer's `out`.
+__device__ __forceinline__ void store_out4(const DecodeParams &p, void *out, int D, int s, int h,
+                                           int q4, float4 v)
 {
     const size_t off = (static_cast<size_t>(s) * p.num_q_heads + h) * D + 4 * q4;
     if (p.out_dtype == PKV_F32) {
-        *reinterpret_cast<float4 *>(static_cast<float *>(p.out) + off) = v;
+        *reinterpret_cast<float4 *>(static_cast<float *>(out) + off) = v;
     } else {
         uint2 w;
         w.x = pack_bf16(v.x, v.y);
         w.y = pack_bf16(v.z, v.w);
-        *reinterpret_cast<uint2 *>(static_cast<unsigned short *>(p.out) + off) = w;
+        *reinterpret_cast<uint2 *>(static_cast<unsigned short *>(out) + off) = w;
     }
 }
 
 // Merges the nparts partials of (sequence s, KV head hkv) for its G query
-// heads and writes the output rows.  Partition i carries its normalised
+// heads and writes the output rows of `out`; gs is the sequence's global
+// index l * S + s (its partial rows).  Partition i carries its normalised
 // output o_i, the max m_i of its log2-scaled scores and l_i = sum 2^(z - m_i);
 // by the associativity of the online-softmax recurrence the full result is
 //     M = max_i m_i,  w_i = l_i 2^(m_i - M),  out = sum_i w_i o_i / sum_i w_i.
 // Partitions are summed in index order, so the result does not depend on
 // which CTA wrote which partial.  Called by all threads of a CTA.
 template <int D>
-__device__ void merge_partials(const DecodeParams &p, int s, int hkv, int nparts)
+__device__ void merge_partials(const DecodeParams &p, void *out, int s, int gs, int hkv,
+                               int nparts)
 {
     constexpr int Q4 = D / 4;
     const int G = p.group;
     for (int idx = threadIdx.x; idx < G * Q4; idx += blockDim.x) {
         const int g = idx / Q4, q4 = idx - g * Q4;
         const int h = hkv * G + g;
-        const size_t row0 = (static_cast<size_t>(s) * p.num_q_heads + h) * p.max_parts;
+        const size_t row0 = (static_cast<size_t>(gs) * p.num_q_heads + h) * p.max_parts;
         const float *ml = p.part_ml + 2 * row0;
         float mx = -INFINITY;
         for (int i = 0; i < nparts; ++i)
@@ -97,7 +121,8 @@ __device__ void merge_partials(const DecodeParams &p, int s, int hkv, int nparts
             acc.w += w * o.w;
         }
         const float sc = (wsum > 0.f ? 1.f / wsum : 0.f) * unit_out_scale(p, hkv);
-        store_out4(p, D, s, h, q4, make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
+        store_out4(p, out, D, s, h, q4,
+                   make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
     }
 }
 

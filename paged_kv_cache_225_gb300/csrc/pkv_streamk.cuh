@@ -1,9 +1,10 @@
 // Stream-K paged decode: the automatic schedule of the decode kernels.
 //
-// The work is the flattened page space: unit u = (sequence s, KV head hkv)
-// in order u = s*Hkv + hkv, each contributing np_u = max(1, ceil(L_s/16))
-// pages (an empty sequence has one virtual page that copies nothing and
-// yields a zero row).  With T pages in total and C resident CTAs, CTA c owns
+// The work is the flattened page space: unit u = (layer l, sequence s, KV
+// head hkv) in order u = (l*S + s)*Hkv + hkv, each contributing
+// np_u = max(1, ceil(L_s/16)) pages (an empty sequence has one virtual page
+// that copies nothing and yields a zero row); the layers share the lengths,
+// so each layer spans the same number of pages.  With T pages in total and C resident CTAs, CTA c owns
 // the contiguous page range [a_c, a_{c+1}), a_c = floor(c*T/C), so every CTA
 // streams the same number of pages +-1 and the grid has no tail.
 //
@@ -48,16 +49,20 @@ constexpr int kWriteBatch = 16;
 
 // A unit of the flattened page space and its global page offset.
 struct Unit {
-    int s, hkv, L, np;
+    int layer, s, hkv, L, np;
     long long off;
 };
 
+// The next unit; past the last sequence of the last layer, s == num_seqs.
 __device__ __forceinline__ void unit_next(const DecodeParams &p, Unit &u)
 {
     u.off += u.np;
     if (++u.hkv == p.num_kv_heads) {
         u.hkv = 0;
-        ++u.s;
+        if (++u.s == p.num_seqs && u.layer + 1 < p.num_layers) {
+            u.s = 0;
+            ++u.layer;
+        }
         u.L = u.s < p.num_seqs ? clamp_len(p, __ldg(p.seq_lens + u.s)) : 0;
         u.np = unit_pages(u.L);
     }
@@ -75,11 +80,12 @@ __device__ __forceinline__ long long range_start(int c, long long T, int C)
     return static_cast<long long>(c) * T / C;
 }
 
-// Merges the partials of unit u = (s, hkv), whose pages [off, off+np) were
-// cut among CTAs c0..c1, and writes its output rows.
+// Merges the partials of unit u = (s, hkv) of a layer, whose pages
+// [off, off+np) were cut among CTAs c0..c1, and writes its output rows of
+// that layer's `out`.
 template <int D>
-__device__ void merge_streamk_partials(const DecodeParams &p, int s, int hkv, long long off,
-                                       int np, long long T, int C)
+__device__ void merge_streamk_partials(const DecodeParams &p, void *out, int s, int hkv,
+                                       long long off, int np, long long T, int C)
 {
     constexpr int Q4 = D / 4;
     const int G = p.group;
@@ -106,16 +112,17 @@ __device__ void merge_streamk_partials(const DecodeParams &p, int s, int hkv, lo
             acc.w += w * o.w;
         }
         const float sc = (wsum > 0.f ? 1.f / wsum : 0.f) * unit_out_scale(p, hkv);
-        store_out4(p, D, s, hkv * G + g, q4,
+        store_out4(p, out, D, s, hkv * G + g, q4,
                    make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
     }
 }
 
 // Combines the four warps' states of one segment (merge scratch) into the
-// output rows (complete unit) or the CTA's partial slot `slot`.
+// output rows of `out` (complete unit; null out: a skipped layer, nothing is
+// written) or the CTA's partial slot `slot`.
 template <int D, int GP>
-__device__ void merge_segment(const DecodeParams &p, const float *scratch, int s, int hkv,
-                              bool complete, int c, int slot)
+__device__ void merge_segment(const DecodeParams &p, void *out, const float *scratch, int s,
+                              int hkv, bool complete, int c, int slot)
 {
     constexpr int Q4 = D / 4;
     constexpr int W = scratch_floats(GP, D);
@@ -144,8 +151,9 @@ __device__ void merge_segment(const DecodeParams &p, const float *scratch, int s
         const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
         if (complete) {
             const float sc = inv * unit_out_scale(p, hkv);
-            store_out4(p, D, s, hkv * G + g, q4,
-                       make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
+            if (out)
+                store_out4(p, out, D, s, hkv * G + g, q4,
+                           make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
         } else {
             const size_t row = (static_cast<size_t>(c) * 2 + slot) * G + g;
             reinterpret_cast<float4 *>(p.part_o + row * D)[q4] =
@@ -159,7 +167,8 @@ __device__ void merge_segment(const DecodeParams &p, const float *scratch, int s
 }
 
 template <class Pol>
-__global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const DecodeParams p)
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_streamk_kernel(const __grid_constant__ DecodeParams p)
 {
     constexpr int D = Pol::kDim;
     constexpr int R = Pol::R;
@@ -168,11 +177,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
                   "merge scratch rows must stay 16-byte aligned");
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ long long s_red[kWarps];
-    __shared__ int s_start[4];  // start unit: s, hkv, L; found flag
+    __shared__ int s_start[4];  // start unit: s, hkv, L (in its layer); found flag
     __shared__ long long s_start_off;
     __shared__ int s_abort;
     __shared__ int s_last;
-    __shared__ int s_w[kWriteBatch][4];  // fused write list: s, hkv, L, physical page
+    __shared__ int s_w[kWriteBatch][5];  // fused write list: s, hkv, L, physical page, layer
     __shared__ int s_wn, s_wmore;
 
     const int warp = threadIdx.x >> 5;
@@ -184,19 +193,22 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
     float *scratch = reinterpret_cast<float *>(extra + Pol::kExtraBytes);
 
     // ---------------------------------------------- this CTA's page range
-    long long T = 0;
+    long long T1 = 0;  // pages of one layer
     for (int b0 = 0; b0 < p.num_seqs; b0 += kThreads) {
         long long v = 0;
         if (b0 + threadIdx.x < p.num_seqs)
             v = static_cast<long long>(Hkv) *
                 unit_pages(clamp_len(p, __ldg(p.seq_lens + b0 + threadIdx.x)));
-        T += block_sum(v, s_red);
+        T1 += block_sum(v, s_red);
     }
+    const long long T = T1 * p.num_layers;
     const int C = static_cast<int>(T < gridDim.x ? T : static_cast<long long>(gridDim.x));
     const int cta = blockIdx.x;
     if (cta >= C)
         return;  // uniform
     const long long a = range_start(cta, T, C), b = range_start(cta + 1, T, C);
+    const int a_layer = static_cast<int>(a / T1);
+    const long long a1 = a - a_layer * T1;  // page a inside its layer
 
     // Unit holding page a: scan the per-sequence page counts.
     if (threadIdx.x == 0)
@@ -226,13 +238,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
         for (int w = 0; w < warp; ++w)
             before += s_red[w];
         const long long lo = before + incl - v, hi = before + incl;
-        if (sq < p.num_seqs && lo <= a && a < hi) {
+        if (sq < p.num_seqs && lo <= a1 && a1 < hi) {
             const int np = unit_pages(Ls);
-            const long long r = a - lo;
+            const long long r = a1 - lo;
             s_start[0] = sq;
             s_start[1] = static_cast<int>(r / np);
             s_start[2] = Ls;
-            s_start_off = lo + (r / np) * np;
+            s_start_off = a_layer * T1 + lo + (r / np) * np;
             s_start[3] = 1;
         }
         for (int w = 0; w < kWarps; ++w)
@@ -257,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
     __syncthreads();
 
     Unit start;
+    start.layer = a_layer;
     start.s = s_start[0];
     start.hkv = s_start[1];
     start.L = s_start[2];
@@ -270,6 +283,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
     // This warp's pages are global pages a + warp + 4i, ring position i.
     Unit iu = start;
     int id_reg = -1, id_base = -1;
+    // Cache bases of the issue unit's layer (a skipped layer copies nothing).
+    int i_layer = -1;
+    bool i_ok = false;
+    const unsigned char *ikc = nullptr, *ivc = nullptr;
     uint32_t pos_i = 0, pos_c = 0;
     const uint32_t n_mine = (b - a > warp) ? static_cast<uint32_t>((b - a - warp + kWarps - 1) / kWarps) : 0u;
     uint32_t okmask = 0;
@@ -290,8 +307,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
                          : -1;
         }
         const int phys = __shfl_sync(kFullMask, id_reg, (pg - id_base) >> 2);
+        if (iu.layer != i_layer) {
+            i_layer = iu.layer;
+            const LayerPtrs &lt = layer_ptrs(p, i_layer);
+            i_ok = layer_ok(lt);
+            ikc = static_cast<const unsigned char *>(lt.k_cache);
+            ivc = static_cast<const unsigned char *>(lt.v_cache);
+        }
         const int stg = pos_i % R;
-        const bool real = iu.L > 0;  // a virtual page of an empty sequence copies nothing
+        // A virtual page of an empty sequence, or a page of a skipped layer,
+        // copies nothing.
+        const bool real = iu.L > 0 && i_ok;
         const bool ok = real && phys >= 0 && phys < p.num_blocks;
         okmask = ok ? (okmask | (1u << stg)) : (okmask & ~(1u << stg));
         if (lane == 0) {
@@ -307,11 +333,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
                     const size_t off = static_cast<size_t>(phys) * block_stride +
                                        static_cast<size_t>(iu.hkv) * tile_stride;
                     unsigned char *dst = ring + stg * Pol::kStageBytes;
-                    bulk_g2s(dst, static_cast<const unsigned char *>(p.k_cache) + off,
-                             Pol::kTileBytes, bar);
-                    bulk_g2s(dst + Pol::kTileBytes,
-                             static_cast<const unsigned char *>(p.v_cache) + off, Pol::kTileBytes,
-                             bar);
+                    bulk_g2s(dst, ikc + off, Pol::kTileBytes, bar);
+                    bulk_g2s(dst + Pol::kTileBytes, ivc + off, Pol::kTileBytes, bar);
                 }
             }
         }
@@ -329,21 +352,24 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
     // them against the copies the barrier releases.  (Writing them per warp,
     // where the page is copied, serialised several dependent loads of the
     // same warp under full memory load: about 7 us per token.)
-    if (p.new_k) {
+    if (p.append) {
         Unit wu = start;
         for (;;) {
             if (threadIdx.x == 0) {
                 int n = 0;
                 while (wu.off < b && n < kWriteBatch) {
                     const long long g_last = wu.off + wu.np - 1;
-                    if (wu.L > 0 && g_last >= a) {
+                    const LayerPtrs &wl = layer_ptrs(p, wu.layer);
+                    if (wu.L > 0 && g_last >= a && g_last < b && wl.new_k != nullptr &&
+                        layer_ok(wl)) {
                         const int phys = __ldg(p.block_tables +
                                                static_cast<size_t>(wu.s) * p.max_blocks + wu.np - 1);
-                        if (g_last < b && phys >= 0 && phys < p.num_blocks) {
+                        if (phys >= 0 && phys < p.num_blocks) {
                             s_w[n][0] = wu.s;
                             s_w[n][1] = wu.hkv;
                             s_w[n][2] = wu.L;
                             s_w[n][3] = phys;
+                            s_w[n][4] = wu.layer;
                             ++n;
                         }
                     }
@@ -368,7 +394,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
     Unit su = start;
     bool aborted = false;
     typename Pol::State st;
-    Pol::begin(st, p, su.s, su.hkv, lane, extra);
+    // The query of a unit (null for a skipped layer: a zero query).
+    auto unit_q = [&](const Unit &u) -> const void * {
+        const LayerPtrs &lt = layer_ptrs(p, u.layer);
+        if (layer_ok(lt))
+            return lt.q;
+        if (threadIdx.x == 0)
+            set_status(p.status, PKV_ERR_INVALID_ARG);
+        return nullptr;
+    };
+    Pol::begin(st, p, unit_q(su), su.s, su.hkv, lane, extra);
     __syncthreads();  // policy shared data (SIMT query) is ready
     for (int k = 0;; ++k) {
         const float c = unit_score_scale(p, su.hkv);
@@ -424,10 +459,12 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
         // their latency overlaps the merge below.
         if constexpr (!Pol::kSharedBegin)
             if (!last)
-                Pol::begin(st, p, nu.s, nu.hkv, lane, extra);
+                Pol::begin(st, p, unit_q(nu), nu.s, nu.hkv, lane, extra);
         __syncthreads();
         const int slot = (k == 0) ? 0 : 1;
-        merge_segment<D, Pol::GP>(p, scratch, su.s, su.hkv, complete, cta, slot);
+        const LayerPtrs &sl = layer_ptrs(p, su.layer);
+        void *sout = layer_ok(sl) ? sl.out : nullptr;
+        merge_segment<D, Pol::GP>(p, sout, scratch, su.s, su.hkv, complete, cta, slot);
         if (!complete) {
             // Publish this partial; the CTA writing the unit's last partial
             // merges them all.  The barrier orders every thread's partial
@@ -437,14 +474,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
                 __threadfence();
                 const int n_ch =
                     owner_cta(su.off + su.np - 1, T, C) - owner_cta(su.off, T, C) + 1;
-                const unsigned old =
-                    atomicAdd(p.arrive + static_cast<size_t>(su.s) * Hkv + su.hkv, 1u);
+                const size_t gs = static_cast<size_t>(su.layer) * p.num_seqs + su.s;
+                const unsigned old = atomicAdd(p.arrive + gs * Hkv + su.hkv, 1u);
                 s_last = (old == static_cast<unsigned>(n_ch - 1)) ? 1 : 0;
             }
             __syncthreads();
-            if (s_last) {
+            if (s_last && sout) {
                 __threadfence();
-                merge_streamk_partials<D>(p, su.s, su.hkv, su.off, su.np, T, C);
+                merge_streamk_partials<D>(p, sout, su.s, su.hkv, su.off, su.np, T, C);
             }
         }
         __syncthreads();  // scratch is free again
@@ -458,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_streamk_kernel(const Decod
             break;
         su = nu;
         if constexpr (Pol::kSharedBegin) {
-            Pol::begin(st, p, su.s, su.hkv, lane, extra);
+            Pol::begin(st, p, unit_q(su), su.s, su.hkv, lane, extra);
             __syncthreads();  // policy shared data (SIMT query) is ready
         }
     }

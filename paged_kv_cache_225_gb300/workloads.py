@@ -277,6 +277,23 @@ def make_workload(cfg: DecodeConfig | str, seed: Optional[int] = None,
             tables[s, nb[s]] = perm[cursor]
             cursor += 1
 
+    q, k_cache, v_cache, new_k, new_v = _draw_values(cfg, rng, N, tables, L, nb)
+    slots = None
+    if cfg.new_tokens:
+        slots = np.empty(S, dtype=np.int64)
+        for s in range(S):
+            pos = int(L[s])
+            slots[s] = int(tables[s, pos // B]) * B + pos % B
+
+    return Workload(cfg=cfg, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=tables,
+                    seq_lens=L, new_k=new_k, new_v=new_v, slot_mapping=slots,
+                    scale=1.0 / math.sqrt(D))
+
+
+def _draw_values(cfg: DecodeConfig, rng: np.random.Generator, N: int, tables: np.ndarray,
+                 L: np.ndarray, nb: np.ndarray):
+    """q, the K and V pools and the new rows of one layer, in that draw order."""
+    S, Hq, Hkv, D, B = cfg.num_seqs, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim, cfg.block_size
     q = round_to_storage(rng.standard_normal((S, Hq, D), dtype=np.float32), cfg.q_dtype)
     k_pool = _normal_pool(rng, (N, Hkv, D, B))
     v_pool = _normal_pool(rng, (N, Hkv, D, B))
@@ -299,18 +316,35 @@ def make_workload(cfg: DecodeConfig | str, seed: Optional[int] = None,
     v_cache = _pool_to_storage(v_pool, cfg.kv_dtype)
     del v_pool
 
-    new_k = new_v = slots = None
+    new_k = new_v = None
     if cfg.new_tokens:
         new_k = round_to_storage(rng.standard_normal((S, Hkv, D), dtype=np.float32), cfg.q_dtype)
         new_v = round_to_storage(rng.standard_normal((S, Hkv, D), dtype=np.float32), cfg.q_dtype)
-        slots = np.empty(S, dtype=np.int64)
-        for s in range(S):
-            pos = int(L[s])
-            slots[s] = int(tables[s, pos // B]) * B + pos % B
+    return q, k_cache, v_cache, new_k, new_v
 
-    return Workload(cfg=cfg, q=q, k_cache=k_cache, v_cache=v_cache, block_tables=tables,
-                    seq_lens=L, new_k=new_k, new_v=new_v, slot_mapping=slots,
-                    scale=1.0 / math.sqrt(D))
+
+def make_layers(cfg: DecodeConfig | str, num_layers: int, seed: Optional[int] = None,
+                seq_lens: Optional[np.ndarray] = None) -> list:
+    """num_layers workloads of one decoder stack over the same batch: layer 0 is
+    ``make_workload(cfg, seed)``; every other layer shares its block tables,
+    lengths and slots and draws its own q, K/V pools and new rows (same
+    recipe) from ``default_rng((seed, layer))``."""
+    if isinstance(cfg, str):
+        if seed is None:
+            seed = CONFIG_SEED[cfg]
+        cfg = CONFIGS[cfg]
+    if seed is None:
+        seed = 0
+    w0 = make_workload(cfg, seed=seed, seq_lens=seq_lens)
+    B = cfg.block_size
+    nb = (w0.seq_lens.astype(np.int64) + B - 1) // B
+    out = [w0]
+    for layer in range(1, num_layers):
+        rng = np.random.default_rng((seed, layer))
+        q, kc, vc, nk, nv = _draw_values(cfg, rng, w0.num_blocks, w0.block_tables, w0.seq_lens,
+                                         nb)
+        out.append(dataclasses.replace(w0, q=q, k_cache=kc, v_cache=vc, new_k=nk, new_v=nv))
+    return out
 
 
 # ------------------------------------------------------------------ several queries per sequence

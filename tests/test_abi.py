@@ -273,3 +273,67 @@ def test_head_scaled_entries_reject_non_fp8_and_missing_scales():
     r[11] = FP8
     r[12] = None
     assert L.pkv_reshape_and_cache_head_scaled(*r) == INVALID
+
+
+# ------------------------------------------------ several layers in one launch
+
+def test_layers_plan_counts_every_layers_units():
+    P, PL = pkv.partition_tokens, pkv.layers_partition_tokens
+    for args in ((128, 64, 8, 128, 514, 0), (64, 32, 8, 128, 4097, 0), (8, 64, 8, 128, 32769, 0),
+                 (4, 4, 4, 64, 65, -1), (4, 4, 4, 64, 65, 48), (128, 64, 8, 128, 14626, -2)):
+        assert PL(1, *args) == P(*args)
+    # 512 (sequence, KV head) units per layer: stream-K alone, whole units with two layers.
+    assert P(64, 32, 8, 128, 4097, 0) == pkv.SCHEDULE_STREAMK
+    assert PL(2, 64, 32, 8, 128, 4097, 0) == 2048
+    assert PL(8, 4, 4, 4, 64, 65, 0) == pkv.SCHEDULE_STREAMK      # tiny: 128 units
+    assert PL(0, 4, 4, 4, 64, 65, 0) == -1
+
+
+def test_layers_workspace_size():
+    W1, WL = pkv.workspace_size, pkv.layers_workspace_size
+
+    def a(x):
+        return (x + 255) // 256 * 256
+    S, Hq, Hkv, D, L, P = 8, 64, 8, 128, 32769, 512
+    parts = -(-L // P)
+    for NL in (1, 3):
+        rows = NL * S * Hq * parts
+        assert WL(NL, S, Hq, Hkv, D, L, P) == 256 + a(NL * S * Hkv * 4) + a(rows * D * 4) + \
+            a(rows * 8)
+    assert WL(1, S, Hq, Hkv, D, L, P) == W1(S, Hq, Hkv, D, L, P)
+    # Stream-K: partial slots per CTA, arrival counters per (layer, sequence, KV head).
+    G = Hq // Hkv
+    rows = 2 * 1024 * G
+    assert WL(4, S, Hq, Hkv, D, L, -2) == 256 + a(4 * S * Hkv * 4) + a(rows * D * 4) + a(rows * 8)
+    assert WL(3, 4, 4, 4, 64, 65, -1) == 256
+
+
+def _layers(**kw):
+    args = dict(table=0x1000, NL=2, q_dtype=BF16, new_dtype=BF16, kv_dtype=BF16, ks=1.0, vs=1.0,
+                bt=0x4000, sl=0x5000, S=2, Hq=8, Hkv=2, D=128, B=16, N=10, maxb=4, maxl=64,
+                scale=0.1, out_dtype=F32, ws=0x7000, wsb=1 << 26, part=0, flags=0)
+    args.update(kw)
+    return pkv.lib().pkv_paged_attn_decode_layers(
+        args["table"], args["NL"], args["q_dtype"], args["new_dtype"], args["kv_dtype"],
+        args["ks"], args["vs"], args["bt"], args["sl"], args["S"], args["Hq"], args["Hkv"],
+        args["D"], args["B"], args["N"], args["maxb"], args["maxl"], args["scale"],
+        args["out_dtype"], args["ws"], args["wsb"], args["part"], args["flags"], None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(table=0), INVALID),
+    (dict(table=0x1004), INVALID),                # entries hold pointers: 8-byte aligned
+    (dict(NL=0), INVALID),
+    (dict(NL=-1), INVALID),
+    (dict(new_dtype=FP8), UNSUPPORTED),
+    (dict(kv_dtype=FP8, ks=0.0), INVALID),
+    (dict(Hq=6, Hkv=4), INVALID),
+    (dict(D=96), UNSUPPORTED),
+    (dict(ws=0), WORKSPACE),
+    (dict(wsb=100), WORKSPACE),
+    (dict(bt=0x4002), INVALID),
+    (dict(part=40), INVALID),
+    (dict(S=0), OK),
+])
+def test_layers_argument_errors(kw, code):
+    assert _layers(**kw) == code
