@@ -137,6 +137,9 @@ struct SimtPolicy {
     };
     static constexpr bool kStaged = false;  // reads K/V straight from the stage
     static constexpr bool kSharedBegin = true;  // begin() writes the query to shared memory
+    // No separate single-layer kernel form (its many instantiations are built
+    // once, in the layered form that serves both).
+    static constexpr bool kSingleForm = false;
     static constexpr int kMinBlocks = 2;        // CTAs per SM the registers are bounded for
     struct Frags {};
     __device__ static void load(Frags &, const unsigned char *, const unsigned char *, int) {}
@@ -485,6 +488,7 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
     static constexpr int KS = Base::KS, MT = Base::MT;
     static constexpr bool kStaged = Staged;
     static constexpr bool kSharedBegin = false;  // begin() only fills registers
+    static constexpr bool kSingleForm = true;    // single-layer calls get their own form
     static constexpr int kMinBlocks = 2;
 
     struct Frags {
@@ -636,6 +640,7 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
     static constexpr int KS = Base::KS, MT = Base::MT;
     static constexpr bool kStaged = Staged;
     static constexpr bool kSharedBegin = false;  // begin() only fills registers
+    static constexpr bool kSingleForm = true;    // single-layer calls get their own form
     // Two N tiles (more than 8 heads per KV head) need more registers than
     // four CTAs per SM leave: three there.
     static constexpr int kMinBlocks = Staged ? 2 : (NT == 1 ? PKV_FP8_MIN_BLOCKS : 3);
@@ -782,6 +787,7 @@ struct MmaInt4Policy : MmaStateBase<D, NT> {
     static constexpr int KS = Base::KS, MT = Base::MT;
     static constexpr bool kStaged = Staged;
     static constexpr bool kSharedBegin = false;
+    static constexpr bool kSingleForm = true;
     static constexpr int kMinBlocks = Staged ? 2 : (NT == 1 ? PKV_FP8_MIN_BLOCKS : 3);
     static constexpr int kRow = kBlockSize / 2;  // bytes of one head_dim row
 
@@ -950,6 +956,7 @@ __device__ __forceinline__ void write_new_token_from(const DecodeParams &p, cons
 // go to slot (L - 1) % 16 of block phys of its caches.  Each lane handles
 // head_dim elements lane + 32j; all loads of a pair of entries are issued
 // before their stores.
+template <bool kMulti>
 __device__ __forceinline__ void write_token_rows(const DecodeParams &p, const int (*w)[5], int e0,
                                                  int n, int step, int D, int lane)
 {
@@ -961,7 +968,7 @@ __device__ __forceinline__ void write_token_rows(const DecodeParams &p, const in
             const int ee = e + x * step;
             if (ee >= n)
                 break;
-            const LayerPtrs &lt = layer_ptrs(p, w[ee][4]);
+            const LayerPtrs lt = layer_ptrs<kMulti>(p, w[ee][4]);
             const size_t src0 = (static_cast<size_t>(w[ee][0]) * p.num_kv_heads + w[ee][1]) * D;
 #pragma unroll
             for (int j = 0; j < kJ; ++j) {
@@ -980,7 +987,7 @@ __device__ __forceinline__ void write_token_rows(const DecodeParams &p, const in
             const int t = (w[ee][2] - 1) % kBlockSize;
             const size_t dst0 = (static_cast<size_t>(w[ee][3]) * p.num_kv_heads + w[ee][1]) * D;
             const float kq = unit_k_quant(p, w[ee][1]), vq = unit_v_quant(p, w[ee][1]);
-            const LayerPtrs &lt = layer_ptrs(p, w[ee][4]);
+            const LayerPtrs lt = layer_ptrs<kMulti>(p, w[ee][4]);
             void *kc = lt.k_cache;
             void *vc = lt.v_cache;
 #pragma unroll
@@ -1113,7 +1120,9 @@ __device__ void merge_item(const DecodeParams &p, void *out, const unsigned char
     }
 }
 
-template <class Pol>
+// kMulti = false: the form for single-layer calls, with the layer logic
+// compiled out (tensor-core policies); true: any number of layers.
+template <class Pol, bool kMulti>
 __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
     decode_kernel(const __grid_constant__ DecodeParams p)
 {
@@ -1169,7 +1178,29 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
         // ---------------------------------------------- next work item
         if (warp == 0) {
             int s = 0, part = 0, hkv = 0, L = 0, nparts = 1, item = 0, done = 0, layer = 0;
-            if (p.split) {
+            if (p.split && !kMulti) {
+                unsigned v = 0;
+                if (lane == 0)
+                    v = atomicAdd(p.counter, 1u);
+                item = static_cast<int>(__shfl_sync(kFullMask, v, 0));
+                // Full partitions first, then remainders.
+                const int u = item / Hkv;
+                hkv = item - u * Hkv;
+                const int n_full = s_sched[kNFull];
+                const bool tail = u >= n_full;
+                const int o = tail ? kTailS : kFullS;  // this phase's cursors
+                int cs = s_sched[o], cb = s_sched[o + 1], k = 0;
+                const bool found = tail ? find_unit<true>(p, u - n_full, cs, cb, lane, s, k, L)
+                                        : find_unit<false>(p, u, cs, cb, lane, s, k, L);
+                part = tail ? full_parts(L, P) : k;
+                __syncwarp();
+                if (lane == 0) {
+                    s_sched[o] = cs;
+                    s_sched[o + 1] = cb;
+                }
+                done = found ? 0 : 1;
+                nparts = parts_of(L, P);
+            } else if (p.split) {
                 unsigned v = 0;
                 if (lane == 0)
                     v = atomicAdd(p.counter, 1u);
@@ -1208,10 +1239,10 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
                 nparts = parts_of(L, P);
             } else {
                 item = first ? static_cast<int>(blockIdx.x) : INT_MAX;
-                if (item >= S * Hkv * p.num_layers) {
+                if (item >= S * Hkv * (kMulti ? p.num_layers : 1)) {
                     done = 1;
                 } else {
-                    layer = item / (S * Hkv);
+                    layer = kMulti ? item / (S * Hkv) : 0;
                     const int r = item - layer * (S * Hkv);
                     s = r / Hkv;
                     hkv = r - s * Hkv;
@@ -1235,8 +1266,8 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
             break;
         const int s = s_item[0], part = s_item[1], hkv = s_item[2], L = s_item[3];
         const int nparts = s_item[4], item = s_item[5], layer = s_item[7];
-        const LayerPtrs &lt = layer_ptrs(p, layer);
-        if (!layer_ok(lt)) {  // uniform: every thread reads the same entry
+        const LayerPtrs lt = layer_ptrs<kMulti>(p, layer);
+        if (!layer_usable<kMulti>(p, lt)) {  // uniform: every thread reads the same entry
             if (threadIdx.x == 0)
                 set_status(p.status, PKV_ERR_INVALID_ARG);
             __syncthreads();  // s_item is rewritten for the next item
@@ -1364,8 +1395,9 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
         // The item's coordinates again from shared memory (unchanged until
         // the next item), rather than registers held across the page loop.
         const int ms = s_item[0], mpart = s_item[1], mhkv = s_item[2], mnparts = s_item[4];
-        const int gs = s_item[7] * S + ms;  // workspace index of (layer, sequence)
-        void *out = layer_ptrs(p, s_item[7]).out;
+        const int mlayer = kMulti ? s_item[7] : 0;
+        const int gs = mlayer * S + ms;  // workspace index of (layer, sequence)
+        void *out = layer_ptrs<kMulti>(p, mlayer).out;
         merge_item<D, Pol::GP>(p, out, smem, Pol::kRingBytes, ms, gs, mhkv, mpart, mnparts);
         if (mnparts > 1 && p.fused_merge) {
             // Publish this partial; the CTA that completes the sequence's last
@@ -1400,9 +1432,9 @@ constexpr int decode_smem_bytes()
            kWarps * kNewRowBytes;
 }
 
-// Launches decode_kernel<Pol>: one CTA per item without split, else a
+// Launches decode_kernel<Pol, kMulti>: one CTA per item without split, else a
 // persistent grid sized from the occupancy of this instantiation.
-template <class Pol>
+template <class Pol, bool kMulti>
 pkv_status launch_policy(const DecodeParams &p, cudaStream_t stream)
 {
     constexpr int smem = decode_smem_bytes<Pol>();
@@ -1410,11 +1442,11 @@ pkv_status launch_policy(const DecodeParams &p, cudaStream_t stream)
     static ContextCache cache;
     int occ = 1;
     const pkv_status rc = cache.get(&occ, [](int *v) -> pkv_status {
-        if (cudaFuncSetAttribute(decode_kernel<Pol>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(decode_kernel<Pol, kMulti>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  smem) != cudaSuccess)
             return PKV_ERR_CUDA;
         int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<Pol>, kThreads,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_kernel<Pol, kMulti>, kThreads,
                                                           smem) != cudaSuccess)
             return PKV_ERR_CUDA;
         *v = o > 0 ? o : 1;
@@ -1433,7 +1465,7 @@ pkv_status launch_policy(const DecodeParams &p, cudaStream_t stream)
     }
     if (grid <= 0)
         return PKV_OK;
-    decode_kernel<Pol><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
+    decode_kernel<Pol, kMulti><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -12,8 +12,8 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__
     const int gs = blockIdx.x / p.num_kv_heads;  // layer * S + sequence
     const int hkv = blockIdx.x - gs * p.num_kv_heads;
     const int layer = gs / p.num_seqs, s = gs - layer * p.num_seqs;
-    const LayerPtrs &lt = layer_ptrs(p, layer);
-    if (!layer_ok(lt))
+    const LayerPtrs lt = layer_ptrs(p, layer);
+    if (!layer_usable(p, lt))
         return;  // reported by the decode kernel
     const int L = clamp_len(p, __ldg(p.seq_lens + s));
     const int n = parts_of(L, p.partition);

@@ -45,20 +45,36 @@ __device__ __forceinline__ float unit_v_quant(const DecodeParams &p, int hkv)
     return p.v_head_scale ? p.v_scale * __ldg(p.v_head_scale + hkv) : p.v_scale;
 }
 
-// The tensors of layer `layer`: the caller's device table, or the call's own
-// (kernel-parameter) tensors for a single-layer call.
-__device__ __forceinline__ const LayerPtrs &layer_ptrs(const DecodeParams &p, int layer)
+// The tensors of layer `layer`, by value: a single-layer call's own (kernel
+// parameters, read from the constant bank), else the caller's device table
+// entry (read-only loads).  kMulti = false: the kernel form compiled for
+// single-layer calls only.
+template <bool kMulti = true>
+__device__ __forceinline__ LayerPtrs layer_ptrs(const DecodeParams &p, int layer)
 {
-    return p.layers ? p.layers[layer] : p.one;
+    if (!kMulti || p.layers == nullptr)
+        return p.one;
+    const unsigned long long *e = reinterpret_cast<const unsigned long long *>(p.layers + layer);
+    LayerPtrs lt;
+    lt.q = reinterpret_cast<const void *>(__ldg(e + 0));
+    lt.new_k = reinterpret_cast<const void *>(__ldg(e + 1));
+    lt.new_v = reinterpret_cast<const void *>(__ldg(e + 2));
+    lt.k_cache = reinterpret_cast<void *>(__ldg(e + 3));
+    lt.v_cache = reinterpret_cast<void *>(__ldg(e + 4));
+    lt.out = reinterpret_cast<void *>(__ldg(e + 5));
+    return lt;
 }
 
-// A layer entry whose tensors the kernels can use: q, the caches and out
-// non-null and 16-byte aligned, and the new rows either absent or both
-// present and aligned.  Single-layer calls were checked on the host; a bad
-// entry of a device table is reported (PKV_ERR_INVALID_ARG) and its layer
-// is skipped: nothing is read through it or written to it.
-__device__ __forceinline__ bool layer_ok(const LayerPtrs &lt)
+// Whether a layer's tensors can be used: a single-layer call's were checked
+// on the host; a table entry needs q, the caches and out non-null and
+// 16-byte aligned, and the new rows either absent or both present and
+// aligned.  A bad entry is reported (PKV_ERR_INVALID_ARG) and its layer is
+// skipped: nothing is read through it or written to it.
+template <bool kMulti = true>
+__device__ __forceinline__ bool layer_usable(const DecodeParams &p, const LayerPtrs &lt)
 {
+    if (!kMulti || p.layers == nullptr)
+        return true;
     const auto a16 = [](const void *x) {
         return x != nullptr && (reinterpret_cast<uintptr_t>(x) & 15u) == 0;
     };

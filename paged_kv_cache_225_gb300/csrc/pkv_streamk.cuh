@@ -54,12 +54,13 @@ struct Unit {
 };
 
 // The next unit; past the last sequence of the last layer, s == num_seqs.
+template <bool kMulti>
 __device__ __forceinline__ void unit_next(const DecodeParams &p, Unit &u)
 {
     u.off += u.np;
     if (++u.hkv == p.num_kv_heads) {
         u.hkv = 0;
-        if (++u.s == p.num_seqs && u.layer + 1 < p.num_layers) {
+        if (++u.s == p.num_seqs && kMulti && u.layer + 1 < p.num_layers) {
             u.s = 0;
             ++u.layer;
         }
@@ -166,7 +167,8 @@ __device__ void merge_segment(const DecodeParams &p, void *out, const float *scr
     }
 }
 
-template <class Pol>
+// kMulti = false: the form for single-layer calls (layer logic compiled out).
+template <class Pol, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_streamk_kernel(const __grid_constant__ DecodeParams p)
 {
@@ -201,13 +203,13 @@ __global__ void __launch_bounds__(kThreads, 2)
                 unit_pages(clamp_len(p, __ldg(p.seq_lens + b0 + threadIdx.x)));
         T1 += block_sum(v, s_red);
     }
-    const long long T = T1 * p.num_layers;
+    const long long T = T1 * (kMulti ? p.num_layers : 1);
     const int C = static_cast<int>(T < gridDim.x ? T : static_cast<long long>(gridDim.x));
     const int cta = blockIdx.x;
     if (cta >= C)
         return;  // uniform
     const long long a = range_start(cta, T, C), b = range_start(cta + 1, T, C);
-    const int a_layer = static_cast<int>(a / T1);
+    const int a_layer = kMulti ? static_cast<int>(a / T1) : 0;
     const long long a1 = a - a_layer * T1;  // page a inside its layer
 
     // Unit holding page a: scan the per-sequence page counts.
@@ -294,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto issue_next = [&]() {
         const long long g = a + warp + static_cast<long long>(kWarps) * pos_i;
         while (g >= iu.off + iu.np) {
-            unit_next(p, iu);
+            unit_next<kMulti>(p, iu);
             id_base = -1;
         }
         const int pg = static_cast<int>(g - iu.off);
@@ -309,8 +311,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int phys = __shfl_sync(kFullMask, id_reg, (pg - id_base) >> 2);
         if (iu.layer != i_layer) {
             i_layer = iu.layer;
-            const LayerPtrs &lt = layer_ptrs(p, i_layer);
-            i_ok = layer_ok(lt);
+            const LayerPtrs lt = layer_ptrs<kMulti>(p, i_layer);
+            i_ok = layer_usable<kMulti>(p, lt);
             ikc = static_cast<const unsigned char *>(lt.k_cache);
             ivc = static_cast<const unsigned char *>(lt.v_cache);
         }
@@ -359,9 +361,9 @@ __global__ void __launch_bounds__(kThreads, 2)
                 int n = 0;
                 while (wu.off < b && n < kWriteBatch) {
                     const long long g_last = wu.off + wu.np - 1;
-                    const LayerPtrs &wl = layer_ptrs(p, wu.layer);
+                    const LayerPtrs wl = layer_ptrs<kMulti>(p, wu.layer);
                     if (wu.L > 0 && g_last >= a && g_last < b && wl.new_k != nullptr &&
-                        layer_ok(wl)) {
+                        layer_usable<kMulti>(p, wl)) {
                         const int phys = __ldg(p.block_tables +
                                                static_cast<size_t>(wu.s) * p.max_blocks + wu.np - 1);
                         if (phys >= 0 && phys < p.num_blocks) {
@@ -373,14 +375,14 @@ __global__ void __launch_bounds__(kThreads, 2)
                             ++n;
                         }
                     }
-                    unit_next(p, wu);
+                    unit_next<kMulti>(p, wu);
                 }
                 s_wn = n;
                 s_wmore = (wu.off < b) ? 1 : 0;
             }
             __syncthreads();
             const int n = s_wn;
-            write_token_rows(p, s_w, warp, n, kWarps, D, lane);
+            write_token_rows<kMulti>(p, s_w, warp, n, kWarps, D, lane);
             fence_proxy_async_all();
             const int more = s_wmore;
             __syncthreads();  // the list is reused; every write is fenced
@@ -396,8 +398,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     typename Pol::State st;
     // The query of a unit (null for a skipped layer: a zero query).
     auto unit_q = [&](const Unit &u) -> const void * {
-        const LayerPtrs &lt = layer_ptrs(p, u.layer);
-        if (layer_ok(lt))
+        const LayerPtrs lt = layer_ptrs<kMulti>(p, u.layer);
+        if (layer_usable<kMulti>(p, lt))
             return lt.q;
         if (threadIdx.x == 0)
             set_status(p.status, PKV_ERR_INVALID_ARG);
@@ -454,7 +456,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         Pol::finish(st, mine, mine + Pol::GP * D, mine + Pol::GP * D + Pol::GP, lane);
         Unit nu = su;
         if (!last)
-            unit_next(p, nu);
+            unit_next<kMulti>(p, nu);
         // Register-only policies start the next segment's query loads now, so
         // their latency overlaps the merge below.
         if constexpr (!Pol::kSharedBegin)
@@ -462,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 2)
                 Pol::begin(st, p, unit_q(nu), nu.s, nu.hkv, lane, extra);
         __syncthreads();
         const int slot = (k == 0) ? 0 : 1;
-        const LayerPtrs &sl = layer_ptrs(p, su.layer);
-        void *sout = layer_ok(sl) ? sl.out : nullptr;
+        const LayerPtrs sl = layer_ptrs<kMulti>(p, su.layer);
+        void *sout = layer_usable<kMulti>(p, sl) ? sl.out : nullptr;
         merge_segment<D, Pol::GP>(p, sout, scratch, su.s, su.hkv, complete, cta, slot);
         if (!complete) {
             // Publish this partial; the CTA writing the unit's last partial
@@ -501,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-template <class Pol>
+template <class Pol, bool kMulti>
 pkv_status launch_streamk(const DecodeParams &p, cudaStream_t stream)
 {
     constexpr int smem = kWarps * Pol::kRingBytes + kWarps * Pol::R * 8 + Pol::kExtraBytes +
@@ -510,11 +512,11 @@ pkv_status launch_streamk(const DecodeParams &p, cudaStream_t stream)
     static ContextCache cache;
     int occ = 1;
     const pkv_status rc = cache.get(&occ, [](int *v) -> pkv_status {
-        if (cudaFuncSetAttribute(decode_streamk_kernel<Pol>,
+        if (cudaFuncSetAttribute(decode_streamk_kernel<Pol, kMulti>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
             return PKV_ERR_CUDA;
         int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_streamk_kernel<Pol>, kThreads,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, decode_streamk_kernel<Pol, kMulti>, kThreads,
                                                           smem) != cudaSuccess)
             return PKV_ERR_CUDA;
         *v = o > 0 ? o : 1;
@@ -527,7 +529,7 @@ pkv_status launch_streamk(const DecodeParams &p, cudaStream_t stream)
         grid = p.streamk_max_ctas;
     if (grid <= 0 || p.num_seqs <= 0)
         return PKV_OK;
-    decode_streamk_kernel<Pol><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
+    decode_streamk_kernel<Pol, kMulti><<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -536,8 +538,14 @@ pkv_status launch_streamk(const DecodeParams &p, cudaStream_t stream)
 template <class Pol>
 pkv_status launch_any(const DecodeParams &p, cudaStream_t stream)
 {
-    return p.streamk ? launch_streamk<typename Pol::StreamK>(p, stream)
-                     : launch_policy<Pol>(p, stream);
+    // Single-layer calls of the tensor-core policies run the form with the
+    // layer logic compiled out.
+    if constexpr (Pol::kSingleForm)
+        if (p.layers == nullptr)
+            return p.streamk ? launch_streamk<typename Pol::StreamK, false>(p, stream)
+                             : launch_policy<Pol, false>(p, stream);
+    return p.streamk ? launch_streamk<typename Pol::StreamK, true>(p, stream)
+                     : launch_policy<Pol, true>(p, stream);
 }
 
 }  // namespace pkv
