@@ -67,6 +67,9 @@ CONFIG_TEXT = {
     "chunked_prefill_8b": "chunked prefill on the Llama-3-8B-shaped layer: 4 seqs with a "
                           "256-token prompt chunk (context U[1024,4096]) + 60 decoding seqs "
                           "(U[512,4096]), 32 q/8 kv heads, D=128, bf16 KV",
+    "spec_verify_70b_fp8": "speculative verification on the Llama-3-70B-shaped layer with an "
+                           "fp8-e5m2 KV cache (scale 1): 128 seqs x 5 causal queries, 64 q/8 kv "
+                           "heads, D=128, lognormal lengths (median 2048, sigma 0.8)",
 }
 
 
@@ -656,9 +659,16 @@ def run_reference(args):
 # --------------------------------------------- several queries per sequence
 
 def _query_rows(w):
-    """Slots of every query token and the K/V rows the pool holds there."""
+    """Slots of every query token and the K/V rows the pool holds there, as
+    bf16 bits: the stored values (codes times the dequant scale for fp8 /
+    INT4 caches, exact in bf16), so writing them back stores the same codes."""
     base = w.cfg.base
     B = base.block_size
+    kf = W.storage_to_float32(w.k_cache, base.kv_dtype)
+    vf = W.storage_to_float32(w.v_cache, base.kv_dtype)
+    if base.kv_dtype in W.SCALED:
+        kf = kf * np.float32(base.kv_scale)
+        vf = vf * np.float32(base.kv_scale)
     slots, ks, vs = [], [], []
     for s in range(w.seq_lens.size):
         L = int(w.seq_lens[s])
@@ -666,10 +676,11 @@ def _query_rows(w):
         for pos in range(L - n, L):
             blk = int(w.block_tables[s, pos // B])
             slots.append(blk * B + pos % B)
-            ks.append(w.k_cache[blk, :, :, pos % B])
-            vs.append(w.v_cache[blk, :, :, pos % B])
-    return (np.asarray(slots, dtype=np.int64), np.ascontiguousarray(np.stack(ks)),
-            np.ascontiguousarray(np.stack(vs)))
+            ks.append(kf[blk, :, :, pos % B])
+            vs.append(vf[blk, :, :, pos % B])
+    return (np.asarray(slots, dtype=np.int64),
+            W.round_to_storage(np.ascontiguousarray(np.stack(ks)), W.BF16),
+            W.round_to_storage(np.ascontiguousarray(np.stack(vs)), W.BF16))
 
 
 def run_prefill(args):
@@ -693,16 +704,21 @@ def run_prefill(args):
     ab = prefill_algorithmic(w)
     slots, new_k, new_v = _query_rows(w)
     write_bytes = T * Hkv * D * 2 * (2 + W.ELEM_BYTES[base.kv_dtype])
+    ks = vs = base.kv_scale
 
     def t(a, dt):
         a = np.ascontiguousarray(a)
         if dt == W.BF16:
             return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        if dt == W.FP8_E5M2:
+            return torch.from_numpy(a).view(torch.float8_e5m2)
+        if dt == W.FP8_E4M3:
+            return torch.from_numpy(a).view(torch.float8_e4m3fn)
         return torch.from_numpy(a)
 
     host = {"q": t(w.q, base.q_dtype), "q_start": torch.from_numpy(w.q_start),
             "tables": torch.from_numpy(w.block_tables), "lens": torch.from_numpy(w.seq_lens),
-            "new_k": t(new_k, base.kv_dtype), "new_v": t(new_v, base.kv_dtype),
+            "new_k": t(new_k, W.BF16), "new_v": t(new_v, W.BF16),
             "slots": torch.from_numpy(slots)}
     kc = t(w.k_cache, base.kv_dtype).to(dev)
     vc = t(w.v_cache, base.kv_dtype).to(dev)
@@ -716,10 +732,12 @@ def run_prefill(args):
     def attend(dd):
         pkv.paged_attn_prefill(dd["q"], dd["q_start"], kc, vc, dd["tables"], dd["lens"],
                                w.scale, out, max_q_len=max_q, max_seq_len=max_len,
-                               partition_tokens=args.partition, workspace=ws)
+                               partition_tokens=args.partition, workspace=ws,
+                               k_scale=ks, v_scale=vs)
 
     def step(dd):
-        pkv.reshape_and_cache(dd["new_k"], dd["new_v"], dd["slots"], kc, vc)
+        pkv.reshape_and_cache(dd["new_k"], dd["new_v"], dd["slots"], kc, vc, k_scale=ks,
+                              v_scale=vs)
         attend(dd)
 
     sampler = ClockSampler(local, enabled=not args.no_clocks)
@@ -829,8 +847,11 @@ def run_prefill(args):
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "tensor": {"achieved_tflops": tflops, "bf16_peak_tflops": bf16_peak,
                                 "frac": tflops / bf16_peak,
-                                "note": "tcgen05.mma kind::f16 (M = 128 rows, padded); "
-                                        "P.V issued twice (bf16 high part + residual)"}},
+                                "note": ("tcgen05.mma kind::f16 (M = 128 rows, padded); "
+                                         "P.V issued twice (bf16 high part + residual)"
+                                         if base.kv_dtype == W.BF16 else
+                                         "mma.sync m16n8k16 f16 (cache codes widened in "
+                                         "registers), 16-row warp tiles")}},
         "gpu_launches": K * launches,
         "clocks": clocks,
     }
@@ -856,6 +877,7 @@ def _oracle_prefill_seqs(w, seqs, threads):
     return oracle.paged_prefill(np.ascontiguousarray(np.concatenate(qs)), base.q_dtype,
                                 q_start, w.k_cache, w.v_cache, base.kv_dtype,
                                 np.ascontiguousarray(w.block_tables[idx]), lens, w.scale,
+                                k_scale=base.kv_scale, v_scale=base.kv_scale,
                                 num_threads=threads)
 
 

@@ -304,9 +304,12 @@ pkv_status pkv_paged_attn_decode_head_scaled(
  *   q_start      int32 [num_seqs + 1] (device), non-decreasing, q_start[0] = 0,
  *                q_start[num_seqs] = num_tokens.
  *   k_cache,
- *   v_cache      [num_blocks, num_kv_heads, head_dim, 16] BF16 (device).
+ *   v_cache      [num_blocks, num_kv_heads, head_dim, 16] of kv_dtype (device):
+ *                BF16, FP8_E5M2, FP8_E4M3 or INT4 (layouts as for
+ *                pkv_paged_attn_decode).
  *   k_scale,
- *   v_scale      reserved for quantised caches; ignored for BF16.
+ *   v_scale      dequant scales of fp8 / INT4 caches (value = code * scale),
+ *                finite and non-zero; ignored for BF16.
  *   block_tables, seq_lens   as for pkv_paged_attn_decode.
  *   max_q_len    host bound on every n_s; max_seq_len bound on every L_s.
  *   out          [num_tokens, num_q_heads, head_dim], F32 or BF16 (device).
@@ -316,9 +319,11 @@ pkv_status pkv_paged_attn_decode_head_scaled(
  *   partition_tokens   0 automatic, -1 never split a context, > 0 (multiple
  *                of 16) split every context into partitions of that many
  *                tokens merged with log-sum-exp weights.
- *   flags        PKV_FLAG_IMPL_AUTO (= PKV_FLAG_IMPL_TC, the tcgen05 kernel) or
- *                PKV_FLAG_IMPL_MMA (the mma.sync kernel), optionally
- *                PKV_FLAG_TEST_DROP_FIRST_COPY.
+ *   flags        PKV_FLAG_IMPL_AUTO (bf16 caches: the tcgen05 kernel; fp8 and
+ *                INT4 caches: the mma.sync kernel, whose fragments widen the
+ *                codes to f16 in registers as decode does), PKV_FLAG_IMPL_TC
+ *                (bf16 only; PKV_ERR_UNSUPPORTED otherwise) or
+ *                PKV_FLAG_IMPL_MMA, optionally PKV_FLAG_TEST_DROP_FIRST_COPY.
  * head_dim 64 or 128, up to 16 query heads per KV head.  Errors as for
  * pkv_paged_attn_decode; on the device a sequence with n_s > L_s, n_s >
  * max_q_len, or q_start outside [0, num_tokens] is reported as

@@ -515,18 +515,20 @@ def paged_attn_prefill(q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Te
                        seq_lens: torch.Tensor, scale: float, out: torch.Tensor, *,
                        max_q_len: Optional[int] = None, max_seq_len: Optional[int] = None,
                        partition_tokens: int = 0, workspace: Optional[torch.Tensor] = None,
-                       stream: Optional[torch.cuda.Stream] = None,
-                       flags: int = 0) -> torch.Tensor:
+                       stream: Optional[torch.cuda.Stream] = None, flags: int = 0,
+                       k_scale: float = 1.0, v_scale: float = 1.0) -> torch.Tensor:
     """Causal paged attention of several query tokens per sequence.
 
     q [T, Hq, D] bf16; q_start int32 [S+1] (queries of sequence s are rows
     q_start[s]..q_start[s+1]-1, its last positions); k_cache, v_cache
-    [N, Hkv, D, 16] bf16 already holding the queries' K/V; block_tables int32
-    [S, max_blocks]; seq_lens int32 [S] (queries included); out [T, Hq, D]
-    f32/bf16.  ``max_q_len`` defaults to T, ``max_seq_len`` to max_blocks*16.
-    ``flags``: ``IMPL["auto"]`` / ``IMPL["tc"]`` run the tcgen05 kernel,
-    ``IMPL["mma"]`` the mma.sync one (same results within the bf16
-    tolerance).  Returns ``out``.
+    [N, Hkv, D, 16] bf16 / fp8 (e5m2, e4m3) / INT4 (uint8, [N, Hkv, D, 8])
+    already holding the queries' K/V, with dequant scales k_scale, v_scale;
+    block_tables int32 [S, max_blocks]; seq_lens int32 [S] (queries
+    included); out [T, Hq, D] f32/bf16.  ``max_q_len`` defaults to T,
+    ``max_seq_len`` to max_blocks*16.  ``flags``: ``IMPL["auto"]`` runs the
+    tcgen05 kernel on bf16 caches and the mma.sync one on the others;
+    ``IMPL["tc"]`` (bf16 only) / ``IMPL["mma"]`` choose (same results within
+    the tolerance).  Returns ``out``.
     """
     dev = q.device
     for t, name, nd in ((q, "q", 3), (q_start, "q_start", 1), (k_cache, "k_cache", 4),
@@ -558,7 +560,8 @@ def paged_attn_prefill(q: torch.Tensor, q_start: torch.Tensor, k_cache: torch.Te
         workspace = get_workspace(need, dev)
     rc = L.pkv_paged_attn_prefill(
         q.data_ptr(), _dtype_code(q, "q"), q_start.data_ptr(), k_cache.data_ptr(),
-        v_cache.data_ptr(), _dtype_code(k_cache, "k_cache"), 1.0, 1.0, block_tables.data_ptr(),
+        v_cache.data_ptr(), _dtype_code(k_cache, "k_cache"), float(k_scale), float(v_scale),
+        block_tables.data_ptr(),
         seq_lens.data_ptr(), S, T, Hq, Hkv, D, B, N, max_blocks, int(max_q_len),
         int(max_seq_len), float(scale), out.data_ptr(), _dtype_code(out, "out"),
         workspace.data_ptr(), workspace.numel() * workspace.element_size(),

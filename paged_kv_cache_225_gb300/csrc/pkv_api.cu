@@ -578,8 +578,6 @@ pkv_status pkv_paged_attn_prefill(const void *q, pkv_dtype q_dtype, const int32_
                                   pkv_dtype out_dtype, void *workspace, size_t workspace_bytes,
                                   int partition_tokens, int flags, void *stream)
 {
-    (void)k_scale;
-    (void)v_scale;
     if (num_seqs < 0 || num_tokens < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         num_blocks <= 0 || max_blocks_per_seq <= 0 || max_seq_len < 0 || max_q_len < 0)
         return PKV_ERR_INVALID_ARG;
@@ -587,8 +585,14 @@ pkv_status pkv_paged_attn_prefill(const void *q, pkv_dtype q_dtype, const int32_
         return PKV_ERR_INVALID_ARG;
     if (static_cast<long>(max_seq_len) > static_cast<long>(max_blocks_per_seq) * kBlockSize)
         return PKV_ERR_INVALID_ARG;
-    if (q_dtype != PKV_BF16 || kv_dtype != PKV_BF16)
+    if (q_dtype != PKV_BF16 || (kv_dtype != PKV_BF16 && !is_scaled(kv_dtype)))
         return PKV_ERR_UNSUPPORTED;
+    // fp8 / INT4 caches run on the mma.sync kernel; the tcgen05 one is bf16 only.
+    if (is_scaled(kv_dtype) && (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_TC)
+        return PKV_ERR_UNSUPPORTED;
+    if (is_scaled(kv_dtype) &&
+        (!std::isfinite(k_scale) || !std::isfinite(v_scale) || k_scale == 0.f || v_scale == 0.f))
+        return PKV_ERR_INVALID_ARG;
     if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
         return PKV_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128)
@@ -642,12 +646,22 @@ pkv_status pkv_paged_attn_prefill(const void *q, pkv_dtype q_dtype, const int32_
     p.max_len = max_seq_len;
     p.max_q_len = max_q_len;
     p.group = group;
-    p.score_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.kv_dtype = kv_dtype;
+    const bool scaled = is_scaled(kv_dtype);
+    p.score_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634 *
+                                       (scaled ? k_scale : 1.0f));
+    p.out_scale = scaled ? v_scale : 1.0f;
+    if (kv_dtype == PKV_FP8_E4M3) {  // codes widened to 2^-8 times their value
+        p.score_scale *= kE4m3Shift;
+        p.out_scale *= kE4m3Shift;
+    }
     p.partition = pl.partition > 0 ? pl.partition : max_blocks_per_seq * kBlockSize;
     p.max_parts = pl.max_parts;
     p.drop_first_copy = (flags & PKV_FLAG_TEST_DROP_FIRST_COPY) ? 1 : 0;
-    // Automatic: the tcgen05 kernel (faster on every measured layer).
-    p.impl = (flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_MMA ? PKV_FLAG_IMPL_MMA : PKV_FLAG_IMPL_TC;
+    // Automatic: the tcgen05 kernel for bf16 caches (faster on every measured
+    // layer), the mma.sync kernel for fp8 / INT4 caches.
+    p.impl = ((flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_MMA || scaled) ? PKV_FLAG_IMPL_MMA
+                                                                          : PKV_FLAG_IMPL_TC;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess)  // status word and work counter
         return PKV_ERR_CUDA;

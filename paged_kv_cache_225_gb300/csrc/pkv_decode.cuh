@@ -616,7 +616,7 @@ struct MmaBf16Policy : MmaStateBase<D, NT> {
 
 // Two-tile head groups keep three CTAs per SM and a 12 KB ring (their merge
 // scratch needs more than 8 KB per warp).
-constexpr int compact_ring_budget(int nt)
+__host__ __device__ constexpr int compact_ring_budget(int nt)
 {
     return nt == 1 ? PKV_FP8_RING_BYTES_PER_WARP : 12 * 1024;
 }

@@ -86,7 +86,9 @@ struct PrefillParams {
     int max_len;             // bound on seq_lens
     int max_q_len;           // bound on n_s
     int group;
-    float score_scale;       // scale * log2(e)
+    int kv_dtype;            // BF16, or an fp8 / INT4 cache (mma.sync kernel only)
+    float score_scale;       // scale * log2(e) (* k_scale for fp8 / INT4 caches)
+    float out_scale;         // v_scale for fp8 / INT4 caches, else 1
     int partition;           // tokens per partition (multiple of 16)
     int max_parts;           // 1: no split
     int drop_first_copy;     // test hook: never issue the first copy of item 0

@@ -55,8 +55,8 @@ static_assert(kRowBlock % kRowTile == 0 && kRowBlock <= kWarps * kRowTile, "row 
 #endif
 constexpr int kPrefillRingBytes = PKV_PREFILL_RING_BYTES;
 
-template <int D> struct PrefillGeom {
-    static constexpr int kTileBytes = D * kBlockSize * 2;  // bf16 page tile
+template <int KV, int D> struct PrefillGeom {
+    static constexpr int kTileBytes = tile_bytes(KV, D);   // one K or V page tile
     static constexpr int kStageBytes = 2 * kTileBytes;     // K then V
     static constexpr int NS = kPrefillRingBytes / kStageBytes;
     static constexpr int kRingBytes = NS * kStageBytes;
@@ -200,6 +200,157 @@ __device__ __forceinline__ void prefill_page_smem(typename MmaStateBase<D, 2>::S
             mma_bf16(st.o[mt][n], vf[mt], bl0[n], bl1[n]);
 }
 
+// fp8 (e5m2 / e4m3) page for one warp's 16 rows: the decode fp8 policy's
+// fragments (codes widened to f16 in registers; S^T row r <-> page token 2r,
+// row r + 8 <-> token 2r + 1, and the matching P^T slots), the per-row causal
+// limit of causal_update, and V zeroed past the sequence end.  K fragments
+// are read before the softmax and V fragments after it.
+template <int KV, int D, int NT>
+__device__ __forceinline__ void prefill_page_fp8(typename MmaStateBase<D, 2>::State &st,
+                                                 const unsigned char *sK,
+                                                 const unsigned char *sV, int valid,
+                                                 const int (&lim)[2][2], int lane, float c)
+{
+    using Base = MmaStateBase<D, 2>;
+    using Pol = MmaFp8Policy<D, 1, compact_ring_budget(1), false, KV>;  // widening only
+    constexpr int KS = Base::KS, MT = Base::MT;
+    const int r = lane >> 2, cc = lane & 3;
+    const int mi = lane >> 3, ri = lane & 7;
+    float sacc[NT][4], sodd[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            sacc[n][e] = sodd[n][e] = 0.f;
+    const uint32_t ka = smem_u32(sK) + (8 * mi + ri) * 16;
+#pragma unroll
+    for (int kp = 0; kp < KS / 2; ++kp) {
+        uint32_t w[4];
+        ldsm_x4_t(w, ka + kp * 32 * 16);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t a[4] = {Pol::widen(w[2 * h], false), Pol::widen(w[2 * h], true),
+                                   Pol::widen(w[2 * h + 1], false), Pol::widen(w[2 * h + 1], true)};
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                mma_f16(h ? sodd[n] : sacc[n], a, st.qf[2 * kp + h][n][0],
+                        st.qf[2 * kp + h][n][1]);
+        }
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            sacc[n][e] += sodd[n][e];
+    uint32_t b0[NT], b1[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        float pr[4], alpha[2];
+        if (causal_update(sacc[n], 2 * r, 2 * r + 1, lim[n], c, st.m[n], st.l[n], pr, alpha))
+            Base::rescale(st, n, alpha);
+        b0[n] = movmatrix_t(pack_f16(pr[0], pr[1]));
+        b1[n] = movmatrix_t(pack_f16(pr[2], pr[3]));
+    }
+    // P^T slots (2c, 2c+1) <-> tokens (4c, 4c+2), (2c+8, 2c+9) <-> (4c+1, 4c+3).
+    uint32_t me = 0xffffffffu, mo = 0xffffffffu;
+    if (valid < kBlockSize) {  // past the sequence end: zero V (may hold NaN)
+        me = (4 * cc < valid ? 0x0000ffffu : 0u) | (4 * cc + 2 < valid ? 0xffff0000u : 0u);
+        mo = (4 * cc + 1 < valid ? 0x0000ffffu : 0u) | (4 * cc + 3 < valid ? 0xffff0000u : 0u);
+    }
+    const uint32_t va = smem_u32(sV) + (8 * mi + ri) * 16;
+#pragma unroll
+    for (int mp = 0; mp < MT / 2; ++mp) {
+        uint32_t w[4];
+        ldsm_x4(w, va + mp * 32 * 16);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t a[4] = {Pol::widen(w[2 * h], false) & me,
+                                   Pol::widen(w[2 * h + 1], false) & me,
+                                   Pol::widen(w[2 * h], true) & mo,
+                                   Pol::widen(w[2 * h + 1], true) & mo};
+#pragma unroll
+            for (int n = 0; n < NT; ++n)
+                mma_f16(st.o[2 * mp + h][n], a, b0[n], b1[n]);
+        }
+    }
+}
+
+// INT4 page for one warp's 16 rows: the decode INT4 policy's fragments
+// (nibble pairs gathered with byte / halfword loads and widened to exact f16
+// integers; same token order as fp8) with the per-row causal limit.  Codes
+// past the sequence end are finite and P is 0 there: no V mask.
+template <int D, int NT>
+__device__ __forceinline__ void prefill_page_int4(typename MmaStateBase<D, 2>::State &st,
+                                                  const unsigned char *sK,
+                                                  const unsigned char *sV,
+                                                  const int (&lim)[2][2], int lane, float c)
+{
+    using Base = MmaStateBase<D, 2>;
+    using Pol = MmaInt4Policy<D, 1>;  // widening only
+    constexpr int KS = Base::KS, MT = Base::MT;
+    constexpr int kRow = Pol::kRow;
+    const int r = lane >> 2, cc = lane & 3;
+    float sacc[NT][4], sodd[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            sacc[n][e] = sodd[n][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+        const unsigned char *row = sK + (16 * ks + 2 * cc) * kRow + r;
+        const uint32_t k0 = static_cast<uint32_t>(row[0]) |
+                            (static_cast<uint32_t>(row[kRow]) << 16);
+        const uint32_t k1 = static_cast<uint32_t>(row[8 * kRow]) |
+                            (static_cast<uint32_t>(row[9 * kRow]) << 16);
+        const uint32_t a[4] = {Pol::widen(k0, false), Pol::widen(k0, true), Pol::widen(k1, false),
+                               Pol::widen(k1, true)};
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+            mma_f16((ks & 1) ? sodd[n] : sacc[n], a, st.qf[ks][n][0], st.qf[ks][n][1]);
+    }
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            sacc[n][e] += sodd[n][e];
+    uint32_t b0[NT], b1[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        float pr[4], alpha[2];
+        if (causal_update(sacc[n], 2 * r, 2 * r + 1, lim[n], c, st.m[n], st.l[n], pr, alpha))
+            Base::rescale(st, n, alpha);
+        b0[n] = movmatrix_t(pack_f16(pr[0], pr[1]));
+        b1[n] = movmatrix_t(pack_f16(pr[2], pr[3]));
+    }
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+        const unsigned char *row = sV + (16 * mt + r) * kRow + 2 * cc;
+        const uint32_t v0 = __byte_perm(*reinterpret_cast<const unsigned short *>(row), 0u, 0x4140u);
+        const uint32_t v1 =
+            __byte_perm(*reinterpret_cast<const unsigned short *>(row + 8 * kRow), 0u, 0x4140u);
+        const uint32_t a[4] = {Pol::widen(v0, false), Pol::widen(v1, false), Pol::widen(v0, true),
+                               Pol::widen(v1, true)};
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+            mma_f16(st.o[mt][n], a, b0[n], b1[n]);
+    }
+}
+
+// One page of one warp's row tile in the cache's dtype.
+template <int KV, int D, int NT>
+__device__ __forceinline__ void prefill_page(typename MmaStateBase<D, 2>::State &st,
+                                             const unsigned char *sK, const unsigned char *sV,
+                                             int valid, const int (&lim)[2][2], int lane, float c)
+{
+    if constexpr (KV == PKV_BF16)
+        prefill_page_smem<D, NT>(st, sK, sV, valid, lim, lane, c);
+    else if constexpr (KV == PKV_INT4)
+        prefill_page_int4<D, NT>(st, sK, sV, lim, lane, c);
+    else
+        prefill_page_fp8<KV, D, NT>(st, sK, sV, valid, lim, lane, c);
+}
+
 __device__ __forceinline__ void store_row4(const PrefillParams &p, int D, int token, int h,
                                            int q4, float4 v)
 {
@@ -214,11 +365,11 @@ __device__ __forceinline__ void store_row4(const PrefillParams &p, int D, int to
     }
 }
 
-template <int D>
+template <int KV, int D>
 __global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
     prefill_kernel(const PrefillParams p)
 {
-    using Geo = PrefillGeom<D>;
+    using Geo = PrefillGeom<KV, D>;
     using Base = MmaStateBase<D, 2>;
     constexpr int NS = Geo::NS;
     constexpr int KS = Base::KS;
@@ -319,10 +470,13 @@ __global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int d = 16 * ks + 8 * hh + 2 * cc;
-                        st.qf[ks][n][hh] =
-                            ok ? *reinterpret_cast<const uint32_t *>(
-                                     static_cast<const unsigned short *>(p.q) + qrow + d)
-                               : 0u;
+                        uint32_t w = ok ? *reinterpret_cast<const uint32_t *>(
+                                              static_cast<const unsigned short *>(p.q) + qrow + d)
+                                        : 0u;
+                        // fp8 / INT4 pages are widened to f16: the query too.
+                        if constexpr (KV != PKV_BF16)
+                            w = pack_f16(bf16_lo(w), bf16_hi(w));
+                        st.qf[ks][n][hh] = w;
                     }
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
@@ -334,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
 
         // ------------------------------------------------ page stream
         const int32_t *table = p.block_tables + static_cast<size_t>(s) * p.max_blocks + pg0;
-        const size_t tile_stride = static_cast<size_t>(D) * kBlockSize * 2;
+        const size_t tile_stride = static_cast<size_t>(Geo::kTileBytes);
         const size_t block_stride = tile_stride * p.num_kv_heads;
         int issued = 0;  // pages issued (warp 0)
         bool aborted = false;
@@ -423,9 +577,9 @@ __global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
                         lim[n][e] = v < valid ? v : valid;
                     }
                 if (two_tiles)
-                    prefill_page_smem<D, 2>(st, sk, sk + Geo::kTileBytes, valid, lim, lane, c);
+                    prefill_page<KV, D, 2>(st, sk, sk + Geo::kTileBytes, valid, lim, lane, c);
                 else
-                    prefill_page_smem<D, 1>(st, sk, sk + Geo::kTileBytes, valid, lim, lane, c);
+                    prefill_page<KV, D, 1>(st, sk, sk + Geo::kTileBytes, valid, lim, lane, c);
             }
             // The stage is free once every lane's reads are done.
             fence_proxy_async();
@@ -487,7 +641,9 @@ __global__ void __launch_bounds__(kThreads, PKV_PREFILL_MIN_CTAS)
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
             const float4 o4 = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
             if (nparts_r == 1) {
-                store_row4(p, D, q0 + i, h, q4, o4);
+                const float sc = p.out_scale;
+                store_row4(p, D, q0 + i, h, q4,
+                           make_float4(o4.x * sc, o4.y * sc, o4.z * sc, o4.w * sc));
             } else {
                 const size_t prow =
                     (static_cast<size_t>(q0 + i) * p.num_q_heads + h) * p.max_parts + part;
@@ -551,24 +707,24 @@ __global__ void __launch_bounds__(kThreads) prefill_merge_kernel(const PrefillPa
             acc.z += w * o.z;
             acc.w += w * o.w;
         }
-        const float sc = wsum > 0.f ? 1.f / wsum : 0.f;
+        const float sc = (wsum > 0.f ? 1.f / wsum : 0.f) * p.out_scale;
         store_row4(p, D, t, h, q4, make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
     }
 }
 
-template <int D>
+template <int KV, int D>
 pkv_status launch_prefill_d(const PrefillParams &p, cudaStream_t stream)
 {
-    using Geo = PrefillGeom<D>;
+    using Geo = PrefillGeom<KV, D>;
     // Resident CTAs per SM, once the shared-memory attribute is set (per context).
     static ContextCache cache;
     int occ = 1;
     const pkv_status rc = cache.get(&occ, [](int *v) -> pkv_status {
-        if (cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_kernel<KV, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Geo::kSmem) != cudaSuccess)
             return PKV_ERR_CUDA;
         int o = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, prefill_kernel<D>, kThreads,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, prefill_kernel<KV, D>, kThreads,
                                                           Geo::kSmem) != cudaSuccess)
             return PKV_ERR_CUDA;
         *v = o > 0 ? o : 1;
@@ -582,7 +738,7 @@ pkv_status launch_prefill_d(const PrefillParams &p, cudaStream_t stream)
     const long grid = items < slots ? items : slots;
     if (grid <= 0)
         return PKV_OK;
-    prefill_kernel<D><<<static_cast<unsigned>(grid), kThreads, Geo::kSmem, stream>>>(p);
+    prefill_kernel<KV, D><<<static_cast<unsigned>(grid), kThreads, Geo::kSmem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess)
         return PKV_ERR_CUDA;
     return launch_prefill_merge(p, stream);
@@ -602,15 +758,38 @@ pkv_status launch_prefill_merge(const PrefillParams &p, cudaStream_t stream)
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+template <int KV>
+static pkv_status launch_prefill_kv(const PrefillParams &p, cudaStream_t stream)
+{
+    return p.head_dim == 128 ? launch_prefill_d<KV, 128>(p, stream)
+                             : launch_prefill_d<KV, 64>(p, stream);
+}
+
 pkv_status launch_prefill(const PrefillParams &p, int kv_dtype, cudaStream_t stream)
 {
-    if (kv_dtype != PKV_BF16 || p.group < 1 || p.group > 16)
+    if (p.group < 1 || p.group > 16)
         return PKV_ERR_UNSUPPORTED;
     if (p.head_dim != 128 && p.head_dim != 64)
         return PKV_ERR_UNSUPPORTED;
-    if (p.impl == PKV_FLAG_IMPL_TC)
-        return launch_prefill_tc(p, stream);
-    return p.head_dim == 128 ? launch_prefill_d<128>(p, stream) : launch_prefill_d<64>(p, stream);
+    switch (kv_dtype) {
+    case PKV_BF16:
+        if (p.impl == PKV_FLAG_IMPL_TC)
+            return launch_prefill_tc(p, stream);
+        return launch_prefill_kv<PKV_BF16>(p, stream);
+    // fp8 and INT4 caches: the mma.sync kernel (its fragments widen the codes
+    // in registers, as the decode kernels do).
+    case PKV_FP8_E5M2:
+        return p.impl == PKV_FLAG_IMPL_TC ? PKV_ERR_UNSUPPORTED
+                                          : launch_prefill_kv<PKV_FP8_E5M2>(p, stream);
+    case PKV_FP8_E4M3:
+        return p.impl == PKV_FLAG_IMPL_TC ? PKV_ERR_UNSUPPORTED
+                                          : launch_prefill_kv<PKV_FP8_E4M3>(p, stream);
+    case PKV_INT4:
+        return p.impl == PKV_FLAG_IMPL_TC ? PKV_ERR_UNSUPPORTED
+                                          : launch_prefill_kv<PKV_INT4>(p, stream);
+    default:
+        return PKV_ERR_UNSUPPORTED;
+    }
 }
 
 }  // namespace pkv

@@ -402,6 +402,15 @@ PREFILL_CONFIGS = {
                           kv_dtype=BF16, len_dist="uniform", len_lo=512, len_hi=4096,
                           new_tokens=False),
         q_len=1, chunk_seqs=4, chunk_len=256, chunk_ctx_lo=1024, chunk_ctx_hi=4096),
+    # The speculative-verification layer over an fp8-e5m2 cache (scale 1),
+    # the KV dtype of the pages' vLLM serving setup.
+    "spec_verify_70b_fp8": PrefillConfig(
+        name="spec_verify_70b_fp8",
+        base=DecodeConfig(name="spec_verify_70b_fp8", num_seqs=128, num_q_heads=64,
+                          num_kv_heads=8, head_dim=128, block_size=16, q_dtype=BF16,
+                          kv_dtype=FP8_E5M2, len_dist="lognormal", len_median=2048.0,
+                          len_sigma=0.8, len_lo=16, len_hi=32768, new_tokens=False),
+        q_len=5),
 }
 PREFILL_SEED = {name: 100 + i for i, name in enumerate(PREFILL_CONFIGS)}
 

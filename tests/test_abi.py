@@ -191,10 +191,12 @@ def test_prefill_workspace_size():
 def _prefill(**kw):
     args = dict(q=0x1000, q_dtype=BF16, qs=0x1800, k=0x2000, v=0x3000, kv_dtype=BF16, bt=0x4000,
                 sl=0x5000, S=2, T=6, Hq=8, Hkv=2, D=128, B=16, N=10, maxb=4, maxq=4, maxl=64,
-                scale=0.1, out=0x6000, out_dtype=F32, ws=0x7000, wsb=1 << 26, part=0, flags=0)
+                scale=0.1, out=0x6000, out_dtype=F32, ws=0x7000, wsb=1 << 26, part=0, flags=0,
+                ks=1.0, vs=1.0)
     args.update(kw)
     return pkv.lib().pkv_paged_attn_prefill(
-        args["q"], args["q_dtype"], args["qs"], args["k"], args["v"], args["kv_dtype"], 1.0, 1.0,
+        args["q"], args["q_dtype"], args["qs"], args["k"], args["v"], args["kv_dtype"],
+        args["ks"], args["vs"],
         args["bt"], args["sl"], args["S"], args["T"], args["Hq"], args["Hkv"], args["D"],
         args["B"], args["N"], args["maxb"], args["maxq"], args["maxl"], args["scale"],
         args["out"], args["out_dtype"], args["ws"], args["wsb"], args["part"], args["flags"], None)
@@ -205,8 +207,16 @@ def _prefill(**kw):
     (dict(D=96), UNSUPPORTED),
     (dict(B=32), UNSUPPORTED),
     (dict(Hq=34, Hkv=2), UNSUPPORTED),
-    (dict(q_dtype=F32), UNSUPPORTED),             # tensor-core path: bf16 q and KV
-    (dict(kv_dtype=FP8), UNSUPPORTED),
+    (dict(q_dtype=F32), UNSUPPORTED),             # tensor-core paths: bf16 q
+    (dict(kv_dtype=F32), UNSUPPORTED),
+    (dict(kv_dtype=FP8, ws=0), WORKSPACE),        # fp8 / INT4 caches accepted (mma.sync)
+    (dict(kv_dtype=pkv.FP8_E4M3, ws=0), WORKSPACE),
+    (dict(kv_dtype=pkv.INT4, ws=0), WORKSPACE),
+    (dict(kv_dtype=FP8, flags=0x2, ws=0), WORKSPACE),
+    (dict(kv_dtype=FP8, flags=0x3), UNSUPPORTED),  # the tcgen05 kernel is bf16 only
+    (dict(kv_dtype=pkv.INT4, ks=0.0), INVALID),
+    (dict(kv_dtype=FP8, vs=float("nan")), INVALID),
+    (dict(kv_dtype=BF16, ks=0.0, ws=0), WORKSPACE),  # scales ignored for bf16
     (dict(out_dtype=FP8), UNSUPPORTED),
     (dict(maxl=65), INVALID),
     (dict(T=-1), INVALID),
