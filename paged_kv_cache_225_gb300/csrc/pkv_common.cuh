@@ -203,6 +203,16 @@ __device__ __forceinline__ float e5m2_to_float(uint32_t code)
     return __half2float(__ushort_as_half(static_cast<unsigned short>((code & 0xffu) << 8)));
 }
 
+// prmt.b32 in its default mode: each selector nibble picks one of the eight
+// bytes of (a, b); a nibble with bit 3 set writes the sign bit of the picked
+// byte replicated over the result byte instead.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
+{
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
 // Two e5m2 codes (bytes `b_lo`, `b_hi` of w, selected by a byte_perm selector)
 // widened to an f16x2 word: each code lands in the high byte of its half.
 __device__ __forceinline__ uint32_t e5m2x2_to_f16x2(uint32_t w, uint32_t sel)

@@ -646,20 +646,27 @@ struct MmaFp8Policy : MmaStateBase<D, NT> {
     static constexpr int kMinBlocks = Staged ? 2 : (NT == 1 ? PKV_FP8_MIN_BLOCKS : 3);
     static constexpr uint32_t kSelEven = 0x2404u;  // bytes 0, 2 -> high bytes of two f16
     static constexpr uint32_t kSelOdd = 0x3414u;   // bytes 1, 3 -> high bytes of two f16
+    // e4m3: byte 0 / 2 (or 1 / 3) into the low byte of each half, the sign of
+    // that byte replicated over the half's high byte.
+    static constexpr uint32_t kSignSelEven = 0xA280u;
+    static constexpr uint32_t kSignSelOdd = 0xB391u;
 
     // Codes (bytes 0, 2) or (bytes 1, 3) of w as an f16x2 word.  e5m2 is the
     // high byte of the binary16 with the same value.  e4m3: the code's sign
     // to bit 15 and its 7 exponent/mantissa bits to bits 13..7 make a binary16
     // of exactly 2^-8 times the code's value, normal and subnormal codes alike
     // (both formats have 3 ... 10 mantissa bits and biases 7 / 15); the host
-    // folds the 2^8 into the score and output scales (kE4m3Shift).
+    // folds the 2^8 into the score and output scales (kE4m3Shift).  With the
+    // sign replicated over the high byte, one shift by 7 puts the sign's
+    // lowest copy at bit 15 and the 7 bits at 13..7; the mask drops the rest
+    // (the code's own sign at bit 14, the other copies): three ALU operations
+    // per pair of codes.
     __device__ static uint32_t widen(uint32_t w, bool odd)
     {
-        const uint32_t h = e5m2x2_to_f16x2(w, odd ? kSelOdd : kSelEven);  // codes in high bytes
         if constexpr (KV == PKV_FP8_E5M2)
-            return h;
+            return e5m2x2_to_f16x2(w, odd ? kSelOdd : kSelEven);  // codes in high bytes
         else
-            return (h & 0x80008000u) | ((h >> 1) & 0x3f803f80u);
+            return (prmt(w, 0u, odd ? kSignSelOdd : kSignSelEven) << 7) & 0xbf80bf80u;
     }
 
     struct Frags {
@@ -792,12 +799,23 @@ struct MmaInt4Policy : MmaStateBase<D, NT> {
     static constexpr int kRow = kBlockSize / 2;  // bytes of one head_dim row
 
     // Low (odd = false) or high nibbles of the two bytes of y (bits 0-7 and
-    // 16-23) as an f16x2 word of signed integers.
+    // 16-23) as an f16x2 word of signed integers.  A low nibble n under the
+    // 0x6400 exponent reads 1024 + (n ^ 8); a high nibble is masked in place,
+    // reads 1024 + 16 (n ^ 8), and is scaled by 1/16 in the same (exact) FMA:
+    // one ALU operation per pair either way, no shift.
     __device__ static uint32_t widen(uint32_t y, bool odd)
     {
-        const uint32_t h = ((odd ? y >> 4 : y) & 0x000f000fu) ^ 0x64086408u;
-        const __half2 v = __hsub2(*reinterpret_cast<const __half2 *>(&h),
-                                  __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
+        if (!odd) {
+            const uint32_t h = (y & 0x000f000fu) ^ 0x64086408u;
+            const __half2 v =
+                __hsub2(*reinterpret_cast<const __half2 *>(&h),
+                        __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408)));
+            return *reinterpret_cast<const uint32_t *>(&v);
+        }
+        const uint32_t h = (y & 0x00f000f0u) ^ 0x64806480u;
+        const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2c00), __ushort_as_half(0x2c00));
+        const __half2 minus72 = __halves2half2(__ushort_as_half(0xd480), __ushort_as_half(0xd480));
+        const __half2 v = __hfma2(*reinterpret_cast<const __half2 *>(&h), sixteenth, minus72);
         return *reinterpret_cast<const uint32_t *>(&v);
     }
 
@@ -820,10 +838,12 @@ struct MmaInt4Policy : MmaStateBase<D, NT> {
         const int g = lane >> 2, c = lane & 3;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
+            // Bytes of two rows side by side: a multiply-add (FMA pipe), not a
+            // byte permute (ALU pipe).
             const unsigned char *r = sK + (16 * ks + 2 * c) * kRow + g;
-            f.k[ks][0] = static_cast<uint32_t>(r[0]) | (static_cast<uint32_t>(r[kRow]) << 16);
+            f.k[ks][0] = static_cast<uint32_t>(r[kRow]) * 65536u + static_cast<uint32_t>(r[0]);
             f.k[ks][1] =
-                static_cast<uint32_t>(r[8 * kRow]) | (static_cast<uint32_t>(r[9 * kRow]) << 16);
+                static_cast<uint32_t>(r[9 * kRow]) * 65536u + static_cast<uint32_t>(r[8 * kRow]);
         }
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) {

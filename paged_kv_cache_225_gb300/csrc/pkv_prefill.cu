@@ -299,10 +299,10 @@ __device__ __forceinline__ void prefill_page_int4(typename MmaStateBase<D, 2>::S
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
         const unsigned char *row = sK + (16 * ks + 2 * cc) * kRow + r;
-        const uint32_t k0 = static_cast<uint32_t>(row[0]) |
-                            (static_cast<uint32_t>(row[kRow]) << 16);
-        const uint32_t k1 = static_cast<uint32_t>(row[8 * kRow]) |
-                            (static_cast<uint32_t>(row[9 * kRow]) << 16);
+        const uint32_t k0 = static_cast<uint32_t>(row[kRow]) * 65536u +
+                            static_cast<uint32_t>(row[0]);
+        const uint32_t k1 = static_cast<uint32_t>(row[9 * kRow]) * 65536u +
+                            static_cast<uint32_t>(row[8 * kRow]);
         const uint32_t a[4] = {Pol::widen(k0, false), Pol::widen(k0, true), Pol::widen(k1, false),
                                Pol::widen(k1, true)};
 #pragma unroll
