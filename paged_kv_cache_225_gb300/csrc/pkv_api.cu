@@ -520,11 +520,31 @@ static int resolve_prefill_partition(int S, int T, int Hq, int Hkv, int B, int m
     return max_len <= P ? 0 : static_cast<int>(P);
 }
 
+// Workspace of the several-queries call: [256-byte header: status word,
+// work counter, the routed decode's work counter][partials of the
+// several-queries kernels][the routed decode's arrival counters and
+// partials, as its own plan lays them out after its header].
 struct PrefillPlan {
     int partition;  // 0 = no split
     int max_parts;
     size_t part_o_off, part_ml_off, bytes;
+    bool route;     // one-query sequences run on the decode kernels
+    Plan dec;       // their decode plan
+    size_t dec_off; // where the decode plan's bytes after its header start
 };
+
+// Mixed batches -- some sequences with one query, others with several, as
+// chunked prefill schedules prompt chunks with decoding sequences -- and
+// all-one-query batches send their one-query sequences to the decode
+// kernels: on the several-queries kernels a one-query sequence is an item
+// of G rows padded to the tensor-core tile (128 rows on tcgen05), while the
+// decode kernels put the page's tokens on the MMA and stream it at the decode
+// rate.  A batch whose every sequence has max_q_len queries (speculative
+// verification) stays on the several-queries kernels.
+static bool route_single(int S, int T, int max_q_len)
+{
+    return S > 0 && T > 0 && (max_q_len == 1 || static_cast<long>(T) < static_cast<long>(S) * max_q_len);
+}
 
 static bool make_prefill_plan(int S, int T, int Hq, int Hkv, int D, int B, int max_q_len,
                               int max_len, int requested, PrefillPlan *pl)
@@ -541,6 +561,14 @@ static bool make_prefill_plan(int S, int T, int Hq, int Hkv, int D, int B, int m
         pl->part_o_off = kWorkspaceHeader;
         pl->part_ml_off = pl->part_o_off + align256(rows * D * sizeof(float));
         pl->bytes = pl->part_ml_off + align256(rows * 2 * sizeof(float));
+    }
+    pl->route = route_single(S, T, max_q_len);
+    pl->dec_off = 0;
+    if (pl->route) {  // the caller's partition request applies to both kernels
+        if (!make_plan(1, S, Hq, Hkv, D, B, max_len, requested, &pl->dec))
+            return false;
+        pl->dec_off = align256(pl->bytes);
+        pl->bytes = pl->dec_off + (pl->dec.bytes - kWorkspaceHeader);
     }
     return true;
 }
@@ -665,10 +693,60 @@ pkv_status pkv_paged_attn_prefill(const void *q, pkv_dtype q_dtype, const int32_
     // layer), the mma.sync kernel for fp8 / INT4 caches.
     p.impl = ((flags & PKV_FLAG_IMPL_MASK) == PKV_FLAG_IMPL_MMA || scaled) ? PKV_FLAG_IMPL_MMA
                                                                           : PKV_FLAG_IMPL_TC;
+    p.skip_single = pl.route ? 1 : 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess)  // status word and work counter
+    // Status word and the two work counters.
+    if (cudaMemsetAsync(ws, 0, 16, st) != cudaSuccess)
         return PKV_ERR_CUDA;
-    return launch_prefill(p, kv_dtype, st);
+    pkv_status rc = PKV_OK;
+    if (max_q_len > 1 || !pl.route)
+        rc = launch_prefill(p, kv_dtype, st);
+    if (rc != PKV_OK || !pl.route)
+        return rc;
+
+    // The one-query sequences: decode, reading and writing row q_start[s].
+    const Plan &dp = pl.dec;
+    unsigned char *dws = ws + pl.dec_off - kWorkspaceHeader;  // the decode plan's offsets
+    DecodeParams d;
+    std::memset(&d, 0, sizeof d);
+    d.one = {q, nullptr, nullptr, const_cast<void *>(k_cache), const_cast<void *>(v_cache), out};
+    d.num_layers = 1;
+    d.block_tables = block_tables;
+    d.seq_lens = seq_lens;
+    d.status = reinterpret_cast<int *>(ws);
+    d.counter = reinterpret_cast<unsigned *>(ws + 8);
+    const bool partials = dp.partition != 0;
+    d.arrive = partials ? reinterpret_cast<unsigned *>(dws + dp.arrive_off) : nullptr;
+    d.part_o = partials ? reinterpret_cast<float *>(dws + dp.part_o_off) : nullptr;
+    d.part_ml = partials ? reinterpret_cast<float *>(dws + dp.part_ml_off) : nullptr;
+    d.q_dtype = q_dtype;
+    d.out_dtype = out_dtype;
+    d.num_seqs = num_seqs;
+    d.num_q_heads = num_q_heads;
+    d.num_kv_heads = num_kv_heads;
+    d.head_dim = head_dim;
+    d.num_blocks = num_blocks;
+    d.max_blocks = max_blocks_per_seq;
+    d.max_len = max_seq_len;
+    d.group = group;
+    d.score_scale = p.score_scale;  // same folding (k_scale, the e4m3 shift) as the mma policies
+    d.out_scale = p.out_scale;
+    d.partition = dp.partition > 0 ? dp.partition : max_blocks_per_seq * kBlockSize;
+    d.max_parts = dp.max_parts;
+    d.split = dp.partition > 0 ? 1 : 0;
+    d.streamk = dp.partition == kStreamK ? 1 : 0;
+    d.streamk_max_ctas = kStreamKMaxCtas;
+    d.fused_merge = 1;
+    d.new_dtype = PKV_F32;
+    d.kv_dtype = kv_dtype;
+    d.k_scale = k_scale;
+    d.v_scale = v_scale;
+    d.q_rows = q_start;
+    d.num_rows = num_tokens;
+    if (partials && cudaMemsetAsync(dws + dp.arrive_off, 0, dp.part_o_off - dp.arrive_off, st) !=
+                        cudaSuccess)
+        return PKV_ERR_CUDA;
+    return launch_decode_mma(d, kv_dtype, st);
 }
 
 pkv_status pkv_copy_blocks(void *k_cache, void *v_cache, pkv_dtype kv_dtype, int num_kv_heads,

@@ -1044,7 +1044,7 @@ __device__ bool find_unit(const DecodeParams &p, int u, int &cur_s, int &cur_bas
         const int sl = cur_s + lane;
         int n = 0, Ls = 0;
         if (sl < S) {
-            Ls = clamp_len(p, __ldg(p.seq_lens + sl));
+            Ls = seq_len_of(p, sl);
             n = kTail ? tail_parts(Ls, P) : full_parts(Ls, P);
         }
         int incl = n;
@@ -1080,7 +1080,7 @@ __device__ __forceinline__ int count_parts(const DecodeParams &p, int lane)
     for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
         int n = 0;
         if (s0 + lane < p.num_seqs) {
-            const int L = clamp_len(p, __ldg(p.seq_lens + s0 + lane));
+            const int L = seq_len_of(p, s0 + lane);
             n = kTail ? tail_parts(L, p.partition) : full_parts(L, p.partition);
         }
 #pragma unroll
@@ -1266,7 +1266,7 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
                     const int r = item - layer * (S * Hkv);
                     s = r / Hkv;
                     hkv = r - s * Hkv;
-                    L = clamp_len(p, __ldg(p.seq_lens + s));
+                    L = seq_len_of(p, s);
                 }
             }
             if (lane == 0) {
@@ -1358,7 +1358,11 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
             issue(issued);
 
         typename Pol::State st;
-        Pol::begin(st, p, lt.q, s, hkv, lane, extra);
+        {
+            const int qrow = unit_row(p, s);  // s, or the routed query's row
+            Pol::begin(st, p, qrow >= 0 ? lt.q : nullptr, qrow >= 0 ? qrow : 0, hkv, lane,
+                       extra);
+        }
         __syncthreads();  // policy shared data (SIMT query) is ready
 
         for (int i = 0; i < nw; ++i) {

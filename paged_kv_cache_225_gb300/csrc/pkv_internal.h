@@ -64,6 +64,13 @@ struct DecodeParams {
     // a code of head h stands for code * k_scale * k_head_scale[h].
     const float *k_head_scale;
     const float *v_head_scale;
+    // A several-queries call's one-query sequences served by the decode
+    // kernels (null: plain decode): q_rows is its q_start [S + 1] over
+    // num_rows rows of q and out; sequence s is attended only when it has
+    // exactly one query, read from and written to row q_rows[s]; the others
+    // count as empty and write nothing.
+    const int32_t *q_rows;
+    int num_rows;
 };
 
 // Paged attention of several query tokens per sequence (chunked prefill,
@@ -93,6 +100,7 @@ struct PrefillParams {
     int max_parts;           // 1: no split
     int drop_first_copy;     // test hook: never issue the first copy of item 0
     int impl;                // PKV_FLAG_IMPL_MMA (mma.sync) or PKV_FLAG_IMPL_TC (tcgen05)
+    int skip_single;         // 1: one-query sequences are served by the decode kernels
 };
 
 constexpr int kBlockSize = 16;

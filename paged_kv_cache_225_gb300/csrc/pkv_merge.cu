@@ -15,7 +15,7 @@ __global__ void __launch_bounds__(kThreads) merge_kernel(const __grid_constant__
     const LayerPtrs lt = layer_ptrs(p, layer);
     if (!layer_usable(p, lt))
         return;  // reported by the decode kernel
-    const int L = clamp_len(p, __ldg(p.seq_lens + s));
+    const int L = seq_len_of(p, s);
     const int n = parts_of(L, p.partition);
     if (n <= 1)
         return;  // the decode kernel wrote this row directly

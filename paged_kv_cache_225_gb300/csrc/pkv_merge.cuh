@@ -25,6 +25,26 @@ __device__ __forceinline__ int clamp_len(const DecodeParams &p, int L)
     return L;
 }
 
+// Row of q and out that holds sequence s's query: s in plain decode; for a
+// several-queries call's one-query sequences, q_rows[s] (-1: sequence s does
+// not have exactly one query, or its rows are out of range -- it is skipped).
+__device__ __forceinline__ int unit_row(const DecodeParams &p, int s)
+{
+    if (p.q_rows == nullptr)
+        return s;
+    const int a = __ldg(p.q_rows + s), b = __ldg(p.q_rows + s + 1);
+    return (b - a == 1 && a >= 0 && b <= p.num_rows) ? a : -1;
+}
+
+// The attended length of sequence s: its clamped seq_len, or 0 for a
+// sequence the call skips (it then writes no output row).
+__device__ __forceinline__ int seq_len_of(const DecodeParams &p, int s)
+{
+    if (p.q_rows != nullptr && unit_row(p, s) < 0)
+        return 0;
+    return clamp_len(p, __ldg(p.seq_lens + s));
+}
+
 // Score scale (log2 domain) and output scale of the units of KV head hkv:
 // the per-head factors of an fp8 cache multiply the per-tensor ones.
 __device__ __forceinline__ float unit_score_scale(const DecodeParams &p, int hkv)
@@ -87,11 +107,15 @@ __device__ __forceinline__ bool layer_usable(const DecodeParams &p, const LayerP
 // which writes its zero row).
 __device__ __forceinline__ int parts_of(int L, int P) { return L > P ? (L + P - 1) / P : 1; }
 
-// out[s, h, 4*q4 .. 4*q4+3] = v (f32 or bf16 output) for a layer's `out`.
+// out[row of s, h, 4*q4 .. 4*q4+3] = v (f32 or bf16 output) for a layer's
+// `out`; nothing for a sequence the call skips.
 __device__ __forceinline__ void store_out4(const DecodeParams &p, void *out, int D, int s, int h,
                                            int q4, float4 v)
 {
-    const size_t off = (static_cast<size_t>(s) * p.num_q_heads + h) * D + 4 * q4;
+    const int row = unit_row(p, s);
+    if (row < 0)
+        return;
+    const size_t off = (static_cast<size_t>(row) * p.num_q_heads + h) * D + 4 * q4;
     if (p.out_dtype == PKV_F32) {
         *reinterpret_cast<float4 *>(static_cast<float *>(out) + off) = v;
     } else {

@@ -680,6 +680,8 @@ __global__ void __launch_bounds__(kThreads) prefill_merge_kernel(const PrefillPa
     const int a = __ldg(p.q_start + s), b = __ldg(p.q_start + s + 1);
     if (a < 0 || b > p.num_tokens || b < a || b - a > L || b - a > p.max_q_len || t < a || t >= b)
         return;  // reported by the attention kernel
+    if (p.skip_single && b - a == 1)
+        return;  // a one-query sequence: served by the decode kernels
     const int pos = L - (b - a) + (t - a);
     const int nparts = parts_of(pos + 1, p.partition);
     if (nparts <= 1)

@@ -43,6 +43,8 @@ __device__ __forceinline__ int seq_parts(const PrefillParams &p, int L)
 template <int RB>
 __device__ __forceinline__ int seq_item_count(const PrefillParams &p, const SeqInfo &si)
 {
+    if (p.skip_single && si.nq == 1)
+        return 0;  // served by the decode kernels
     const int blocks = (si.nq * p.group + RB - 1) / RB;
     return p.num_kv_heads * seq_parts(p, si.L) * blocks;
 }

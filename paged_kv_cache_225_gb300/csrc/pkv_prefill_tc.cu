@@ -601,6 +601,13 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
             int ent = lane < npages ? __ldg(table + lane) : -1;
             int ent_next = 32 + lane < npages ? __ldg(table + 32 + lane) : -1;
             const int nchunks = (npages + kChunk - 1) / kChunk;
+            // A warp whose 32 rows all lie past the item's rows (items of
+            // fewer than 128 rows: 40 in speculative verification) skips the
+            // score, softmax and P work and the output; it still waits for
+            // each chunk's scores (its threads zero V past the sequence end
+            // after the copy landed) and makes every arrival.  Its rows of P
+            // and O hold stale values that feed only rows never written.
+            const bool live = __any_sync(kFullMask, cur.row_ok);
             for (int j = 0; j < nchunks; ++j, ++gc) {
                 const int jp = j * kChunk;  // first page of the chunk
                 if (jp > 0 && (jp & 31) == 0) {
@@ -622,85 +629,89 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
                 tc_fence_after();
                 const uint32_t scol = tmem + lane_base + Geo::kSCol + Geo::kSCols * (gc % SB);
                 const int tb = (cur.pg0 + jp) * kBlockSize;  // position of the chunk's token 0
-                // Scaled scores, -inf where the row does not see the token.
-                float xs[kTok];
+                if (live) {
+                    // Scaled scores, -inf where the row does not see the token.
+                    float xs[kTok];
 #pragma unroll
-                for (int x = 0; x < kChunk; ++x) {
-                    float part[16];
-                    tmem_ld16(scol + 16 * x, part);
-                    int v = cur.pos - (tb + 16 * x) + 1;
-                    v = v < 0 ? 0 : (v > kBlockSize ? kBlockSize : v);
-                    const int lim = (cur.row_ok && good[x]) ? v : 0;
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        xs[16 * x + e] = e < lim ? part[e] * c : -INFINITY;
-                }
-                float mx;
-                {
-                    float r[kTok / 2];
-#pragma unroll
-                    for (int e = 0; e < kTok / 2; ++e)
-                        r[e] = fmaxf(xs[e], xs[e + kTok / 2]);
-#pragma unroll
-                    for (int w = kTok / 4; w >= 1; w >>= 1)
-#pragma unroll
-                        for (int e = 0; e < w; ++e)
-                            r[e] = fmaxf(r[e], r[e + w]);
-                    mx = r[0];
-                }
-                const bool need = mx > m + kLazy;  // false when nothing is visible
-                float alpha = 1.f;
-                if (need) {
-                    alpha = m == -INFINITY ? 0.f : MmaSoftmax::ex2(m - mx);
-                    l *= alpha;
-                    m = mx;
-                }
-                if (o_valid && __any_sync(kFullMask, need)) {
-                    // O holds earlier chunks: rescale it once their P V is done.
-                    if (!warp_wait(&pv_done[(gc - 1) % SB], ((gc - 1) / SB) & 1, abort)) {
-                        failed = true;
-                        break;
-                    }
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 16) {
-                        float ov[16];
-                        tmem_ld16(tmem + lane_base + c0, ov);
+                    for (int x = 0; x < kChunk; ++x) {
+                        float part[16];
+                        tmem_ld16(scol + 16 * x, part);
+                        int v = cur.pos - (tb + 16 * x) + 1;
+                        v = v < 0 ? 0 : (v > kBlockSize ? kBlockSize : v);
+                        const int lim = (cur.row_ok && good[x]) ? v : 0;
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            ov[e] *= alpha;
-                        tmem_st16(tmem + lane_base + c0, ov);
+                            xs[16 * x + e] = e < lim ? part[e] * c : -INFINITY;
+                    }
+                    float mx;
+                    {
+                        float r[kTok / 2];
+#pragma unroll
+                        for (int e = 0; e < kTok / 2; ++e)
+                            r[e] = fmaxf(xs[e], xs[e + kTok / 2]);
+#pragma unroll
+                        for (int w = kTok / 4; w >= 1; w >>= 1)
+#pragma unroll
+                            for (int e = 0; e < w; ++e)
+                                r[e] = fmaxf(r[e], r[e + w]);
+                        mx = r[0];
+                    }
+                    const bool need = mx > m + kLazy;  // false when nothing is visible
+                    float alpha = 1.f;
+                    if (need) {
+                        alpha = m == -INFINITY ? 0.f : MmaSoftmax::ex2(m - mx);
+                        l *= alpha;
+                        m = mx;
+                    }
+                    if (o_valid && __any_sync(kFullMask, need)) {
+                        // O holds earlier chunks: rescale it once their P V is done.
+                        if (!warp_wait(&pv_done[(gc - 1) % SB], ((gc - 1) / SB) & 1, abort)) {
+                            failed = true;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 16) {
+                            float ov[16];
+                            tmem_ld16(tmem + lane_base + c0, ov);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                ov[e] *= alpha;
+                            tmem_st16(tmem + lane_base + c0, ov);
+                        }
+                        tmem_wait_st();
+                    }
+                    // P over the consumed scores: high parts in the first half of
+                    // the buffer, residuals in the second (bf16 pairs).  A row
+                    // that has seen nothing keeps m = -inf and P = 0.
+                    const bool seen = m != -INFINITY;
+                    uint32_t hi[kTok / 2], lo[kTok / 2];
+                    float psum = 0.f;
+#pragma unroll
+                    for (int e = 0; e < kTok; e += 2) {
+                        const float a = seen ? MmaSoftmax::ex2(xs[e] - m) : 0.f;
+                        const float b = seen ? MmaSoftmax::ex2(xs[e + 1] - m) : 0.f;
+                        psum += a + b;
+                        hi[e / 2] = pack_bf16(a, b);
+                        lo[e / 2] = pack_bf16(a - bf16_lo(hi[e / 2]), b - bf16_hi(hi[e / 2]));
+                    }
+                    l += psum;
+#pragma unroll
+                    for (int c0 = 0; c0 < kTok / 2; c0 += 16) {
+                        uint32_t w[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = hi[c0 + e];
+                        tmem_st16u(scol + c0, w);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            w[e] = lo[c0 + e];
+                        tmem_st16u(scol + kTok / 2 + c0, w);
                     }
                     tmem_wait_st();
-                }
-                // P over the consumed scores: high parts in the first half of
-                // the buffer, residuals in the second (bf16 pairs).  A row
-                // that has seen nothing keeps m = -inf and P = 0.
-                const bool seen = m != -INFINITY;
-                uint32_t hi[kTok / 2], lo[kTok / 2];
-                float psum = 0.f;
-#pragma unroll
-                for (int e = 0; e < kTok; e += 2) {
-                    const float a = seen ? MmaSoftmax::ex2(xs[e] - m) : 0.f;
-                    const float b = seen ? MmaSoftmax::ex2(xs[e + 1] - m) : 0.f;
-                    psum += a + b;
-                    hi[e / 2] = pack_bf16(a, b);
-                    lo[e / 2] = pack_bf16(a - bf16_lo(hi[e / 2]), b - bf16_hi(hi[e / 2]));
-                }
-                l += psum;
-#pragma unroll
-                for (int c0 = 0; c0 < kTok / 2; c0 += 16) {
-                    uint32_t w[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        w[e] = hi[c0 + e];
-                    tmem_st16u(scol + c0, w);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        w[e] = lo[c0 + e];
-                    tmem_st16u(scol + kTok / 2 + c0, w);
-                }
-                tmem_wait_st();
+                }  // live
+                if (failed)
+                    break;
                 // Past the sequence end the V tile may hold anything (NaN):
                 // zero those tokens, since P = 0 does not cancel NaN.
                 bool zeroed = false;
@@ -741,7 +752,7 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
                 load_q(nxt);
 
             // ------------------------------------------------ output rows
-            if (o_valid) {
+            if (o_valid && live) {
                 if (!warp_wait(&pv_done[(gc - 1) % SB], ((gc - 1) / SB) & 1, abort)) {
                     failed = true;
                     break;
@@ -753,7 +764,7 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const size_t orow = static_cast<size_t>(cur.q0 + cur.qi) * p.num_q_heads + cur.h;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 16) {
+            for (int c0 = 0; c0 < (live ? D : 0); c0 += 16) {
                 float ov[16];
                 if (o_valid) {
                     tmem_ld16(tmem + lane_base + c0, ov);

@@ -64,7 +64,7 @@ __device__ __forceinline__ void unit_next(const DecodeParams &p, Unit &u)
             u.s = 0;
             ++u.layer;
         }
-        u.L = u.s < p.num_seqs ? clamp_len(p, __ldg(p.seq_lens + u.s)) : 0;
+        u.L = u.s < p.num_seqs ? seq_len_of(p, u.s) : 0;
         u.np = unit_pages(u.L);
     }
 }
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         long long v = 0;
         if (b0 + threadIdx.x < p.num_seqs)
             v = static_cast<long long>(Hkv) *
-                unit_pages(clamp_len(p, __ldg(p.seq_lens + b0 + threadIdx.x)));
+                unit_pages(seq_len_of(p, b0 + threadIdx.x));
         T1 += block_sum(v, s_red);
     }
     const long long T = T1 * (kMulti ? p.num_layers : 1);
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         int Ls = 0;
         long long v = 0;
         if (sq < p.num_seqs) {
-            Ls = clamp_len(p, __ldg(p.seq_lens + sq));
+            Ls = seq_len_of(p, sq);
             v = static_cast<long long>(Hkv) * unit_pages(Ls);
         }
         // Block-wide inclusive scan of v (warp scans + warp offsets).
@@ -396,16 +396,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     Unit su = start;
     bool aborted = false;
     typename Pol::State st;
-    // The query of a unit (null for a skipped layer: a zero query).
+    // The query of a unit (null for a skipped layer or sequence: a zero
+    // query) and its row of q.
     auto unit_q = [&](const Unit &u) -> const void * {
         const LayerPtrs lt = layer_ptrs<kMulti>(p, u.layer);
-        if (layer_usable<kMulti>(p, lt))
-            return lt.q;
-        if (threadIdx.x == 0)
-            set_status(p.status, PKV_ERR_INVALID_ARG);
-        return nullptr;
+        if (!layer_usable<kMulti>(p, lt)) {
+            if (threadIdx.x == 0)
+                set_status(p.status, PKV_ERR_INVALID_ARG);
+            return nullptr;
+        }
+        return unit_row(p, u.s) >= 0 ? lt.q : nullptr;
     };
-    Pol::begin(st, p, unit_q(su), su.s, su.hkv, lane, extra);
+    auto q_row = [&](const Unit &u) -> int {
+        const int r = unit_row(p, u.s);
+        return r >= 0 ? r : 0;
+    };
+    Pol::begin(st, p, unit_q(su), q_row(su), su.hkv, lane, extra);
     __syncthreads();  // policy shared data (SIMT query) is ready
     for (int k = 0;; ++k) {
         const float c = unit_score_scale(p, su.hkv);
@@ -461,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 2)
         // their latency overlaps the merge below.
         if constexpr (!Pol::kSharedBegin)
             if (!last)
-                Pol::begin(st, p, unit_q(nu), nu.s, nu.hkv, lane, extra);
+                Pol::begin(st, p, unit_q(nu), q_row(nu), nu.hkv, lane, extra);
         __syncthreads();
         const int slot = (k == 0) ? 0 : 1;
         const LayerPtrs sl = layer_ptrs<kMulti>(p, su.layer);
@@ -497,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 2)
             break;
         su = nu;
         if constexpr (Pol::kSharedBegin) {
-            Pol::begin(st, p, unit_q(su), su.s, su.hkv, lane, extra);
+            Pol::begin(st, p, unit_q(su), q_row(su), su.hkv, lane, extra);
             __syncthreads();  // policy shared data (SIMT query) is ready
         }
     }

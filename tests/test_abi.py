@@ -188,6 +188,28 @@ def test_prefill_workspace_size():
         W(4, 20, 6, 4, 64, 8, 200, 0)                     # heads do not divide
 
 
+def test_prefill_workspace_of_a_mixed_batch_holds_the_routed_decode():
+    """A batch that mixes one-query sequences with longer ones (fewer query
+    rows than num_seqs * max_q_len) sends the one-query sequences to the
+    decode kernels: the workspace adds that decode plan's counters and
+    partials after the several-queries partials."""
+    W, WD = pkv.prefill_workspace_size, pkv.workspace_size
+
+    def a(x):
+        return (x + 255) // 256 * 256
+    S, Hq, Hkv, D, L, P = 64, 32, 8, 128, 4096, 512
+    T = 4 * 256 + 60                                   # chunked prefill: 4 chunks + 60 decodes
+    parts = -(-L // P)
+    rows = T * Hq * parts
+    own = 256 + a(rows * D * 4) + a(rows * 8)
+    assert W(S, T, Hq, Hkv, D, 256, L, P) == a(own) + WD(S, Hq, Hkv, D, L, P) - 256
+    # Uniform batches (every sequence has max_q_len queries) route nothing.
+    assert W(S, S * 5, Hq, Hkv, D, 5, L, P) == 256 + a(S * 5 * Hq * parts * D * 4) + \
+        a(S * 5 * Hq * parts * 8)
+    # All one-query: the decode plan only (after the 256-byte header).
+    assert W(S, S, Hq, Hkv, D, 1, L, -1) == 256
+
+
 def _prefill(**kw):
     args = dict(q=0x1000, q_dtype=BF16, qs=0x1800, k=0x2000, v=0x3000, kv_dtype=BF16, bt=0x4000,
                 sl=0x5000, S=2, T=6, Hq=8, Hkv=2, D=128, B=16, N=10, maxb=4, maxq=4, maxl=64,
