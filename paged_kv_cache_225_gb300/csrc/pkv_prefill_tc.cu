@@ -29,11 +29,13 @@
 //  * The running max is updated lazily (only when a score exceeds it by
 //    2^8); O is then rescaled in TMEM by the rows' threads once the previous
 //    P V has completed.
-//  * Each page tile [head_dim][16 tokens] is copied as two halves of 8
-//    tokens, so that it lands as [half][head_dim][8]: the interleaved
-//    (no-swizzle) layout of 8-row x 16-byte core matrices.  The two K tiles
-//    of a stage are adjacent, so one MMA with N = 32 reads both (MN-major);
-//    V tiles are read K-major.
+//  * Each page tile [head_dim][16 tokens] (32-byte rows) is copied whole by
+//    one tensor-map load in the 32-byte swizzle mode: row d lands at 32 d
+//    with its two 16-byte halves exchanged when bit 7 of the address is set,
+//    which is the 32-byte-swizzled operand layout of the MMA (atoms of 8
+//    rows x 32 bytes).  Every 32-byte sector of the cache is requested once
+//    and whole.  The two K tiles of a stage are adjacent, so one MMA with
+//    N = 32 reads both (MN-major); V tiles are read K-major.
 //  * Every wait is bounded; a timeout records PKV_ERR_TIMEOUT, stops every
 //    role, lets copies and MMAs in flight finish and frees TMEM.
 #include <cuda.h>  // CUtensorMap and its enums; the encoder is looked up at run time
@@ -60,7 +62,7 @@ static_assert(kChunk == 2 || kChunk == 4, "two or four pages per step");
 
 template <int D> struct TcGeom {
     static constexpr int kTile = D * kBlockSize * 2;  // one K or V page tile (bf16)
-    static constexpr int kHalf = kTile / 2;           // 8 tokens of every head_dim row
+    static constexpr int kRow = kBlockSize * 2;       // one head_dim row: 32 bytes
     static constexpr int kVOff = kChunk * kTile;      // V tiles follow the K tiles
     static constexpr int kStage = 2 * kChunk * kTile;
     static constexpr int kSCols = kChunk * kBlockSize;  // score columns per buffer
@@ -89,15 +91,19 @@ __device__ __forceinline__ void tc_fence_after()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor, interleaved (no swizzle) layout: start
-// address, byte distance between core matrices along K (leading) and along
-// M / N (stride), descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo)
+// Shared-memory matrix descriptor of a 32-byte-swizzled operand (atoms of
+// 8 rows x 32 bytes, the 16-byte halves of a row exchanged where address bit
+// 7 is set): start address, the leading byte offset (MN-major: distance
+// between atoms along M / N; unused K-major), the stride byte offset
+// (distance between 8-row groups), descriptor version 1, layout code 6
+// (32-byte swizzle).
+__device__ __forceinline__ uint64_t smem_desc_sw32(uint32_t addr, uint32_t lbo, uint32_t sbo)
 {
     uint64_t d = static_cast<uint64_t>((addr >> 4) & 0x3fffu);
     d |= static_cast<uint64_t>((lbo >> 4) & 0x3fffu) << 16;
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3fffu) << 32;
     d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(6) << 61;
     return d;
 }
 
@@ -232,7 +238,7 @@ __device__ __forceinline__ void store_out4(const PrefillParams &p, int D, size_t
 }
 
 struct TcMaps {
-    CUtensorMap k0, k1, v0, v1;  // K / V caches, token halves 0 and 1
+    CUtensorMap k, v;  // K / V caches, one box = one page tile
 };
 
 struct TcItem {
@@ -307,7 +313,11 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
     const int G = p.group;
     const uint32_t smem0 = smem_u32(smem);
 
-    if (warp == kProducerWarp) {
+    if (smem0 & 255u) {
+        // The swizzled tiles need 256-byte aligned stages: report, run nothing.
+        if (threadIdx.x == 0)
+            set_status(p.status, PKV_ERR_UNSUPPORTED);
+    } else if (warp == kProducerWarp) {
         // ------------------------------------------------------- producer
         int cur_s = 0, cur_base = 0;
         uint32_t gc = 0;  // chunks issued by this CTA
@@ -391,10 +401,8 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
                                 unsigned char *dk = st + x * Geo::kTile;
                                 unsigned char *dv = st + Geo::kVOff + x * Geo::kTile;
                                 const int c2 = phys[x] * p.num_kv_heads + it.hkv;
-                                tma_load_3d(dk, &maps.k0, 0, 0, c2, &full[stg]);
-                                tma_load_3d(dk + Geo::kHalf, &maps.k1, 0, 0, c2, &full[stg]);
-                                tma_load_3d(dv, &maps.v0, 0, 0, c2, &full[stg]);
-                                tma_load_3d(dv + Geo::kHalf, &maps.v1, 0, 0, c2, &full[stg]);
+                                tma_load_3d(dk, &maps.k, 0, 0, c2, &full[stg]);
+                                tma_load_3d(dv, &maps.v, 0, 0, c2, &full[stg]);
                             }
                         }
                     }
@@ -433,8 +441,10 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
                 for (int x = 0; x < kChunk; ++x) {
                     if (!s_ok[stg][x])
                         continue;
-                    const uint64_t vdesc = smem_desc(
-                        smem0 + stg * Geo::kStage + Geo::kVOff + x * Geo::kTile, Geo::kHalf, 128);
+                    // K-major: one 32-byte row (16 tokens) per dim, 8-dim groups 256 B apart.
+                    const uint64_t vdesc = smem_desc_sw32(
+                        smem0 + stg * Geo::kStage + Geo::kVOff + x * Geo::kTile, 16,
+                        8 * Geo::kRow);
                     tc_mma_ta(tmem, pcol + 8 * x, vdesc, kIdPV, o_started);
                     tc_mma_ta(tmem, pcol + Geo::kSCols / 2 + 8 * x, vdesc, kIdPV, true);
                     o_started = true;
@@ -477,12 +487,17 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
                     tc_fence_after();
                     // Scores of both pages in one MMA per k step (absent or
                     // bad pages leave stale columns that the softmax masks).
+                    // MN-major: 16 tokens per row, the second page's tile
+                    // one tile further (the leading offset), 8-dim groups
+                    // 256 B apart; k step ks starts at dim 16 ks.
                     const uint32_t scol = tmem + Geo::kSCol + Geo::kSCols * (gc % SB);
                     const uint32_t kaddr = smem0 + stg * Geo::kStage;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
                         tc_mma_ta(scol, tmem + Geo::kQCol + 8 * ks,
-                                  smem_desc(kaddr + ks * 256, 128, Geo::kHalf), kIdS, ks > 0);
+                                  smem_desc_sw32(kaddr + ks * 16 * Geo::kRow, Geo::kTile,
+                                                 8 * Geo::kRow),
+                                  kIdS, ks > 0);
                     tc_commit(&s_full[gc % SB]);
                     if (j >= SB - 1 && !issue_pv(gc - (SB - 1))) {
                         failed = true;
@@ -720,10 +735,14 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
                     const int valid = cur.it.L - (tb + 16 * x);
                     if (good[x] && valid > 0 && valid < kBlockSize) {
                         if (t < D) {
+                            // Row t of the swizzled tile: half h of the row
+                            // sits at half h ^ (bit 2 of t).
                             unsigned short *vt = reinterpret_cast<unsigned short *>(
-                                smem + (gc % NS) * Geo::kStage + Geo::kVOff + x * Geo::kTile);
+                                smem + (gc % NS) * Geo::kStage + Geo::kVOff + x * Geo::kTile +
+                                t * Geo::kRow);
+                            const int sw = static_cast<int>(smem_u32(vt) >> 7) & 1;
                             for (int e = valid; e < kBlockSize; ++e)
-                                vt[(e >> 3) * (Geo::kHalf / 2) + t * 8 + (e & 7)] = 0;
+                                vt[(((e >> 3) ^ sw) << 3) + (e & 7)] = 0;
                         }
                         zeroed = true;
                     }
@@ -839,18 +858,18 @@ EncodeTiledFn encoder()
     return fn;
 }
 
-// Token half `half` of every [head_dim][16] tile of a bf16 cache, viewed as
-// [num_blocks * num_kv_heads][head_dim][8]: one box is a page's half tile.
-bool encode_half(EncodeTiledFn enc, CUtensorMap *map, const void *cache, int half, int D,
-                 long tiles)
+// Every [head_dim][16] tile of a bf16 cache, viewed as
+// [num_blocks * num_kv_heads][head_dim][16]: one box is a page tile, stored
+// in the 32-byte swizzle mode (the box's 32-byte rows fill the swizzle span).
+bool encode_tile(EncodeTiledFn enc, CUtensorMap *map, const void *cache, int D, long tiles)
 {
-    const cuuint64_t dims[3] = {8, static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(tiles)};
+    const cuuint64_t dims[3] = {kBlockSize, static_cast<cuuint64_t>(D),
+                                static_cast<cuuint64_t>(tiles)};
     const cuuint64_t strides[2] = {kBlockSize * 2, static_cast<cuuint64_t>(D) * kBlockSize * 2};
-    const cuuint32_t box[3] = {8, static_cast<cuuint32_t>(D), 1};
+    const cuuint32_t box[3] = {kBlockSize, static_cast<cuuint32_t>(D), 1};
     const cuuint32_t es[3] = {1, 1, 1};
-    void *base = const_cast<unsigned char *>(static_cast<const unsigned char *>(cache) + 16 * half);
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(cache), dims, strides,
+               box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -903,10 +922,8 @@ pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
     if (tiles >= (1L << 31))
         return PKV_ERR_UNSUPPORTED;
     TcMaps maps;
-    if (!encode_half(enc, &maps.k0, p.k_cache, 0, D, tiles) ||
-        !encode_half(enc, &maps.k1, p.k_cache, 1, D, tiles) ||
-        !encode_half(enc, &maps.v0, p.v_cache, 0, D, tiles) ||
-        !encode_half(enc, &maps.v1, p.v_cache, 1, D, tiles))
+    if (!encode_tile(enc, &maps.k, p.k_cache, D, tiles) ||
+        !encode_tile(enc, &maps.v, p.v_cache, D, tiles))
         return PKV_ERR_CUDA;
     const long blocks = (static_cast<long>(p.max_q_len) * p.group + kTcRows - 1) / kTcRows;
     const long items = static_cast<long>(p.num_seqs) * p.num_kv_heads * p.max_parts * blocks;
