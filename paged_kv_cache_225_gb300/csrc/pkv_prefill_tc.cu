@@ -9,21 +9,22 @@
 // a sequence of L cached tokens attends the rows t <= L - n + i.
 //
 // How it is laid out on the GPU (not taken from the pages):
-//  * An item is (sequence, KV head, context partition, block of up to 128
-//    rows), a row being one (query token, grouped query head) pair.  Every
-//    K/V page crosses HBM once per item.
+//  * An item is (sequence, KV head, context partition, block of up to M
+//    rows), a row being one (query token, grouped query head) pair; M = 128,
+//    or 64 when no sequence has more rows.  Every K/V page crosses HBM once
+//    per item.
 //  * Six warps with fixed roles.  Warp 4 (producer) pulls items from an
 //    atomic counter, hands them to the others through a two-slot queue, and
 //    copies K and V with tensor-map (TMA) loads into a ring of stages of two
 //    pages each.  Warp 5 (one thread) issues the MMAs.  Warps 0-3 own one row
-//    per thread (TMEM lane = row): Q, softmax, P, rescaling, output.
-//  * Tensor memory holds O (128 x head_dim f32), two score buffers of 32
+//    per thread (the row's TMEM lane): Q, softmax, P, rescaling, output.
+//  * Tensor memory holds O (M x head_dim f32), two score buffers of 32
 //    columns and the item's Q (bf16 pairs, the A operand of S).
-//    Per chunk of two pages: S = Q K^T (M = 128, N = 32 tokens, head_dim / 16
+//    Per chunk of two pages: S = Q K^T (M rows, N = 32 tokens, head_dim / 16
 //    MMAs of K = 16); each row's thread reads its 32 scores, applies the
 //    causal limit and the online softmax, and writes P back over its
 //    consumed scores as a bf16 high part and a bf16 residual; then
-//    O += P_hi V + P_lo V (M = 128, N = head_dim, K = 16 per page) with P
+//    O += P_hi V + P_lo V (M rows, N = head_dim, K = 16 per page) with P
 //    read from tensor memory.  The scores of chunk i + 1 are issued before
 //    P V of chunk i.
 //  * The running max is updated lazily (only when a score exceeds it by
@@ -46,8 +47,16 @@ namespace pkv {
 
 namespace {
 
-constexpr int kTcRows = 128;  // rows per item = the MMA's M
+// Rows per item = the MMA's M: 128, or 64 when no sequence has more than 64
+// rows (speculative verification: 5 queries x 8 grouped heads = 40).  An
+// M = 64 accumulator holds row 16 w + i in lane 32 w + i (i < 16) of TMEM
+// lane quarter w; the A operand read from TMEM (Q, P) uses the same lanes.
+template <int M> __host__ __device__ constexpr int tc_rows_ok()
+{
+    return M == 64 || M == 128;
+}
 constexpr int kTcThreads = 192;
+constexpr int kQueue = 4;  // item queue slots (the producer publishes up to three items ahead)
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 
@@ -182,6 +191,50 @@ __device__ __forceinline__ void tmem_wait_st()
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Sixteen-lane accesses of an M = 64 accumulator (a warp's 16 rows in lanes
+// 0-15 of its quarter).  Thread i of the warp holds rows i / 4 and i / 4 + 8.
+// 16x256b, four repetitions of 8 columns: registers 4 j .. 4 j + 3 are
+// columns 8 j + 2 (i % 4) and 8 j + 2 (i % 4) + 1 of the first row, then the
+// same columns of the second.  16x128b, four repetitions of 4 columns:
+// registers 2 j and 2 j + 1 are column 4 j + i % 4 of the two rows.
+__device__ __forceinline__ void tmem_ld_r16(uint32_t taddr, float (&v)[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st_r16(uint32_t taddr, const float (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_c8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x128b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
+}
+
 // 3-D tensor-map load of one box into shared memory, completing on bar.
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, uint64_t *bar)
@@ -223,6 +276,17 @@ __device__ __forceinline__ void tc_fail(const PrefillParams &p, volatile int *ab
     *abort = 1;
 }
 
+__device__ __forceinline__ void store_out2(const PrefillParams &p, int D, size_t orow, int col,
+                                           float2 v)
+{
+    const size_t off = orow * D + col;
+    if (p.out_dtype == PKV_F32)
+        *reinterpret_cast<float2 *>(static_cast<float *>(p.out) + off) = v;
+    else
+        *reinterpret_cast<uint32_t *>(static_cast<unsigned short *>(p.out) + off) =
+            pack_bf16(v.x, v.y);
+}
+
 __device__ __forceinline__ void store_out4(const PrefillParams &p, int D, size_t orow, int q4,
                                            float4 v)
 {
@@ -258,19 +322,20 @@ __device__ __forceinline__ TcItem read_item(const int *slot)
     return it;
 }
 
-template <int D>
+template <int D, int kTcRows>
 __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ TcMaps maps)
 {
     using Geo = TcGeom<D>;
+    static_assert(tc_rows_ok<kTcRows>(), "M is 64 or 128");
     constexpr int NS = Geo::NS;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[NS], empty[NS];
     constexpr int SB = Geo::kSBufs;
     __shared__ __align__(8) uint64_t s_full[SB], p_full[SB], pv_done[SB];
-    __shared__ __align__(8) uint64_t item_full[2], item_empty[2];
+    __shared__ __align__(8) uint64_t item_full[kQueue], item_empty[kQueue];
     __shared__ __align__(8) uint64_t q_full, o_free, drain;
-    __shared__ int s_item[2][8];
+    __shared__ int s_item[kQueue][8];
     __shared__ int s_ok[NS][kChunk];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort;
@@ -288,7 +353,7 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
             mbar_init(&p_full[i], 4);
             mbar_init(&pv_done[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kQueue; ++i) {
             mbar_init(&item_full[i], 1);
             mbar_init(&item_empty[i], 5);  // the MMA thread and the four softmax warps
         }
@@ -319,6 +384,11 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
             set_status(p.status, PKV_ERR_UNSUPPORTED);
     } else if (warp == kProducerWarp) {
         // ------------------------------------------------------- producer
+        // Items are claimed from the counter one at a time, when the
+        // previous item's copies are all issued (claiming earlier unbalances
+        // the CTAs' last items).  The query rows of a claimed item are
+        // prefetched into L2 for the softmax warps, which load them a ring's
+        // worth of chunks later.
         int cur_s = 0, cur_base = 0;
         uint32_t gc = 0;  // chunks issued by this CTA
         bool stop = false;
@@ -330,10 +400,10 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
             PrefillItem it;
             const bool ok = find_prefill_item<kTcRows>(p, static_cast<int>(u), cur_s, cur_base,
                                                        lane, it);
-            const int slot = k & 1;
+            const int slot = k % kQueue;
             int free_ok = 1;
-            if (k >= 2 && lane == 0)
-                free_ok = tc_wait(&item_empty[slot], ((k - 2) >> 1) & 1, abort);
+            if (k >= kQueue && lane == 0)
+                free_ok = tc_wait(&item_empty[slot], ((k - kQueue) / kQueue) & 1, abort);
             free_ok = __shfl_sync(kFullMask, free_ok, 0);
             if (!free_ok) {
                 if (lane == 0)
@@ -355,6 +425,15 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
                 break;
             const int row0 = it.rb * kTcRows;
             const int nrows = min(kTcRows, it.nq * G - row0);
+            for (int r = lane; r < nrows; r += 32) {
+                const int R = row0 + r;
+                const unsigned char *qrow =
+                    static_cast<const unsigned char *>(p.q) +
+                    (static_cast<size_t>(it.q0 + R / G) * p.num_q_heads + it.hkv * G + R % G) * D * 2;
+#pragma unroll
+                for (int b = 0; b < D * 2; b += 128)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(qrow + b));
+            }
             int pg0, npages;
             item_pages(p, it.L, it.nq, row0, nrows, it.part, pg0, npages);
             const int32_t *table = p.block_tables + static_cast<size_t>(it.s) * p.max_blocks + pg0;
@@ -454,8 +533,8 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
                 return true;
             };
             for (int k = 0; !failed; ++k) {
-                const int slot = k & 1;
-                if (!tc_wait(&item_full[slot], (k >> 1) & 1, abort)) {
+                const int slot = k % kQueue;
+                if (!tc_wait(&item_full[slot], (k / kQueue) & 1, abort)) {
                     failed = true;
                     break;
                 }
@@ -517,7 +596,7 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
             tc_commit(&drain);
             mbar_wait_bounded(&drain, 0, kWaitLimitNs);
         }
-    } else {
+    } else if constexpr (kTcRows == 128) {
         // ---------------------------------------- Q, softmax and output
         const int t = threadIdx.x;  // row of the item = TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
@@ -536,8 +615,8 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
         // ended) or an abort (false, !ended).
         auto next_item = [&](RowItem &ri, bool &ended) -> bool {
             for (;;) {
-                const int slot = k & 1;
-                if (!warp_wait(&item_full[slot], (k >> 1) & 1, abort)) {
+                const int slot = k % kQueue;
+                if (!warp_wait(&item_full[slot], (k / kQueue) & 1, abort)) {
                     ended = false;
                     return false;
                 }
@@ -823,6 +902,327 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
         }
         if (failed)
             tc_fail(p, abort);
+    } else {
+        // ------------------------- Q, softmax and output, 64-row items
+        // Warp w owns rows 16 w .. 16 w + 15 (TMEM lanes 0-15 of its
+        // quarter).  Each thread holds two of them, rows g and g + 8 of the
+        // warp's sixteen, and a quarter of each chunk's columns (8 of 32);
+        // the four threads of a row combine their maxima by shuffles and
+        // their sums at the end.
+        const int t = threadIdx.x;  // V rows zeroed by this thread (t < head_dim)
+        const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+        const int g = lane >> 2, qd = lane & 3;
+        const float c = p.score_scale;
+        constexpr float kLazy = MmaSoftmax::kLazy;
+        constexpr int kTok = Geo::kSCols;  // tokens per chunk
+        static_assert(kTok == 32, "four 16x256b repetitions cover a chunk's scores");
+        uint32_t gc = 0;
+        int k = 0;  // queue entries read
+
+        struct RowPair {
+            TcItem it;
+            int pg0, npages, q0;
+            bool ok[2];
+            int qi[2], h[2], pos[2];  // rows 16 w + g and 16 w + g + 8
+            bool q_ok;                // lane < 16: Q row 16 w + lane
+            int q_qi, q_h;
+        };
+        auto next_item = [&](RowPair &ri, bool &ended) -> bool {
+            for (;;) {
+                const int slot = k % kQueue;
+                if (!warp_wait(&item_full[slot], (k / kQueue) & 1, abort)) {
+                    ended = false;
+                    return false;
+                }
+                const TcItem it = read_item(s_item[slot]);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&item_empty[slot]);
+                ++k;
+                if (!it.valid) {
+                    ended = true;
+                    return false;
+                }
+                const int row0 = it.rb * kTcRows;
+                const int nrows = min(kTcRows, it.nq * G - row0);
+                int pg0, npages;
+                item_pages(p, it.L, it.nq, row0, nrows, it.part, pg0, npages);
+                if (npages == 0)
+                    continue;
+                ri.it = it;
+                ri.pg0 = pg0;
+                ri.npages = npages;
+                ri.q0 = __ldg(p.q_start + it.s);  // validated by the item scan
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const int r = 16 * warp + g + 8 * x;
+                    ri.ok[x] = r < nrows;
+                    const int R = row0 + (ri.ok[x] ? r : 0);
+                    ri.qi[x] = R / G;
+                    ri.h[x] = it.hkv * G + R % G;
+                    ri.pos[x] = it.L - it.nq + ri.qi[x];
+                }
+                const int rq = 16 * warp + lane;
+                ri.q_ok = lane < 16 && rq < nrows;
+                const int RQ = row0 + (ri.q_ok ? rq : 0);
+                ri.q_qi = RQ / G;
+                ri.q_h = it.hkv * G + RQ % G;
+                return true;
+            }
+        };
+        // Q row (zero past the item) into tensor memory, lanes 0-15 of the
+        // quarter; callers have seen every score of the previous item.
+        auto load_q = [&](const RowPair &ri) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                static_cast<const unsigned short *>(p.q) +
+                (static_cast<size_t>(ri.q0 + ri.q_qi) * p.num_q_heads + ri.q_h) * D);
+            uint4 v[D / 8];
+#pragma unroll
+            for (int e = 0; e < D / 8; ++e)
+                v[e] = ri.q_ok ? __ldg(src + e) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int c0 = 0; c0 < D / 2; c0 += 16) {
+                uint32_t r[16];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    r[4 * e] = v[c0 / 4 + e].x;
+                    r[4 * e + 1] = v[c0 / 4 + e].y;
+                    r[4 * e + 2] = v[c0 / 4 + e].z;
+                    r[4 * e + 3] = v[c0 / 4 + e].w;
+                }
+                tmem_st16u(tmem + lane_base + Geo::kQCol + c0, r);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&q_full);
+        };
+
+        RowPair cur;
+        bool ended = false;
+        bool have = next_item(cur, ended);
+        bool failed = !have && !ended;
+        if (have)
+            load_q(cur);
+        while (have) {
+            float m[2] = {-INFINITY, -INFINITY};
+            float l[2] = {0.f, 0.f};  // this thread's columns only
+            bool o_valid = false;
+            const int npages = cur.npages;
+            const int32_t *table =
+                p.block_tables + static_cast<size_t>(cur.it.s) * p.max_blocks + cur.pg0;
+            int ent = lane < npages ? __ldg(table + lane) : -1;
+            int ent_next = 32 + lane < npages ? __ldg(table + 32 + lane) : -1;
+            const int nchunks = (npages + kChunk - 1) / kChunk;
+            const bool live = __any_sync(kFullMask, cur.ok[0] || cur.ok[1]);
+            for (int j = 0; j < nchunks; ++j, ++gc) {
+                const int jp = j * kChunk;
+                if (jp > 0 && (jp & 31) == 0) {
+                    ent = ent_next;
+                    ent_next = jp + 32 + lane < npages ? __ldg(table + jp + 32 + lane) : -1;
+                }
+                bool good[kChunk];
+                bool any_good = false;
+#pragma unroll
+                for (int x = 0; x < kChunk; ++x) {
+                    const int phys = __shfl_sync(kFullMask, ent, (jp + x) & 31);
+                    good[x] = jp + x < npages && phys >= 0 && phys < p.num_blocks;
+                    any_good = any_good || good[x];
+                }
+                if (!warp_wait(&s_full[gc % SB], (gc / SB) & 1, abort)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t scol = tmem + lane_base + Geo::kSCol + Geo::kSCols * (gc % SB);
+                const int tb = (cur.pg0 + jp) * kBlockSize;
+                if (live) {
+                    // xs[4 r + 2 x + e]: row x, column 8 r + 2 qd + e; scaled,
+                    // -inf where the row does not see the token.
+                    float xs[16];
+                    tmem_ld_r16(scol, xs);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int x = 0; x < 2; ++x)
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int col = 8 * r + 2 * qd + e;
+                                const bool vis = cur.ok[x] && good[r >> 1] && tb + col <= cur.pos[x];
+                                xs[4 * r + 2 * x + e] = vis ? xs[4 * r + 2 * x + e] * c : -INFINITY;
+                            }
+                    float mx[2];
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        float a = fmaxf(fmaxf(xs[2 * x], xs[2 * x + 1]),
+                                        fmaxf(xs[4 + 2 * x], xs[5 + 2 * x]));
+                        float b = fmaxf(fmaxf(xs[8 + 2 * x], xs[9 + 2 * x]),
+                                        fmaxf(xs[12 + 2 * x], xs[13 + 2 * x]));
+                        a = fmaxf(a, b);
+                        a = fmaxf(a, __shfl_xor_sync(kFullMask, a, 1));
+                        mx[x] = fmaxf(a, __shfl_xor_sync(kFullMask, a, 2));
+                    }
+                    bool need_any = false;
+                    float alpha[2] = {1.f, 1.f};
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        if (mx[x] > m[x] + kLazy) {  // false when nothing is visible
+                            alpha[x] = m[x] == -INFINITY ? 0.f : MmaSoftmax::ex2(m[x] - mx[x]);
+                            l[x] *= alpha[x];
+                            m[x] = mx[x];
+                            need_any = true;
+                        }
+                    }
+                    if (o_valid && __any_sync(kFullMask, need_any)) {
+                        // O holds earlier chunks: rescale it once their P V is done.
+                        if (!warp_wait(&pv_done[(gc - 1) % SB], ((gc - 1) / SB) & 1, abort)) {
+                            failed = true;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            float ov[16];
+                            tmem_ld_r16(tmem + lane_base + c0, ov);
+#pragma unroll
+                            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                                for (int x = 0; x < 2; ++x) {
+                                    ov[4 * r + 2 * x] *= alpha[x];
+                                    ov[4 * r + 2 * x + 1] *= alpha[x];
+                                }
+                            tmem_st_r16(tmem + lane_base + c0, ov);
+                        }
+                        tmem_wait_st();
+                    }
+                    // P over the consumed scores: high parts in the first
+                    // half of the buffer, residuals in the second; column
+                    // 4 r + qd of a row holds its tokens 8 r + 2 qd, + 1.
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int r = 0; r < 4; ++r)
+#pragma unroll
+                        for (int x = 0; x < 2; ++x) {
+                            const bool seen = m[x] != -INFINITY;
+                            const float a = seen ? MmaSoftmax::ex2(xs[4 * r + 2 * x] - m[x]) : 0.f;
+                            const float b =
+                                seen ? MmaSoftmax::ex2(xs[4 * r + 2 * x + 1] - m[x]) : 0.f;
+                            l[x] += a + b;
+                            const uint32_t w = pack_bf16(a, b);
+                            hi[2 * r + x] = w;
+                            lo[2 * r + x] = pack_bf16(a - bf16_lo(w), b - bf16_hi(w));
+                        }
+                    tmem_st_c8(scol, hi);
+                    tmem_st_c8(scol + kTok / 2, lo);
+                    tmem_wait_st();
+                }  // live
+                if (failed)
+                    break;
+                // Past the sequence end the V tile may hold anything (NaN):
+                // zero those tokens, since P = 0 does not cancel NaN.
+                bool zeroed = false;
+#pragma unroll
+                for (int x = 0; x < kChunk; ++x) {
+                    const int valid = cur.it.L - (tb + 16 * x);
+                    if (good[x] && valid > 0 && valid < kBlockSize) {
+                        if (t < D) {
+                            unsigned short *vt = reinterpret_cast<unsigned short *>(
+                                smem + (gc % NS) * Geo::kStage + Geo::kVOff + x * Geo::kTile +
+                                t * Geo::kRow);
+                            const int sw = static_cast<int>(smem_u32(vt) >> 7) & 1;
+                            for (int e = valid; e < kBlockSize; ++e)
+                                vt[(((e >> 3) ^ sw) << 3) + (e & 7)] = 0;
+                        }
+                        zeroed = true;
+                    }
+                }
+                if (zeroed)
+                    fence_proxy_async();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(&p_full[gc % SB]);
+                o_valid = o_valid || any_good;
+            }
+            if (failed)
+                break;
+
+            RowPair nxt;
+            bool nended = false;
+            const bool have_next = next_item(nxt, nended);
+            if (!have_next && !nended) {
+                failed = true;
+                break;
+            }
+            if (have_next)
+                load_q(nxt);
+
+            // ------------------------------------------------ output rows
+            if (o_valid && live) {
+                if (!warp_wait(&pv_done[(gc - 1) % SB], ((gc - 1) / SB) & 1, abort)) {
+                    failed = true;
+                    break;
+                }
+                tc_fence_after();
+            }
+            float inv[2];
+            bool write[2];
+            int nparts_r[2];
+            size_t orow[2];
+#pragma unroll
+            for (int x = 0; x < 2; ++x) {
+                l[x] += __shfl_xor_sync(kFullMask, l[x], 1);
+                l[x] += __shfl_xor_sync(kFullMask, l[x], 2);
+                nparts_r[x] = p.max_parts > 1 ? parts_of(cur.pos[x] + 1, p.partition) : 1;
+                write[x] = cur.ok[x] && cur.it.part < nparts_r[x];
+                inv[x] = l[x] > 0.f ? 1.f / l[x] : 0.f;
+                orow[x] = static_cast<size_t>(cur.q0 + cur.qi[x]) * p.num_q_heads + cur.h[x];
+            }
+#pragma unroll 1
+            for (int c0 = 0; c0 < (live ? D : 0); c0 += 32) {
+                float ov[16];
+                if (o_valid) {
+                    tmem_ld_r16(tmem + lane_base + c0, ov);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        ov[e] = 0.f;
+                }
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    if (!write[x])
+                        continue;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int col = c0 + 8 * r + 2 * qd;
+                        const float2 v = make_float2(ov[4 * r + 2 * x] * inv[x],
+                                                     ov[4 * r + 2 * x + 1] * inv[x]);
+                        if (nparts_r[x] == 1) {
+                            store_out2(p, D, orow[x], col, v);
+                        } else {
+                            const size_t prow = orow[x] * p.max_parts + cur.it.part;
+                            *reinterpret_cast<float2 *>(p.part_o + prow * D + col) = v;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int x = 0; x < 2; ++x)
+                if (write[x] && nparts_r[x] > 1 && qd == 0) {
+                    const size_t prow = orow[x] * p.max_parts + cur.it.part;
+                    p.part_ml[2 * prow] = m[x];
+                    p.part_ml[2 * prow + 1] = l[x];
+                }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&o_free);
+            cur = nxt;
+            have = have_next;
+        }
+        if (failed)
+            tc_fail(p, abort);
     }
 
     tc_fence_before();
@@ -874,7 +1274,7 @@ bool encode_tile(EncodeTiledFn enc, CUtensorMap *map, const void *cache, int D, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int kTcRows>
 pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
 {
     using Geo = TcGeom<D>;
@@ -883,9 +1283,9 @@ pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
     int occ = 1;
     const pkv_status crc = cache.get(&occ, [](int *out_occ) -> pkv_status {
         // Two CTAs per SM need the largest shared-memory carveout.
-        if (cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_tc_kernel<D, kTcRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Geo::kSmem) != cudaSuccess ||
-            cudaFuncSetAttribute(prefill_tc_kernel<D>,
+            cudaFuncSetAttribute(prefill_tc_kernel<D, kTcRows>,
                                  cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return PKV_ERR_CUDA;
@@ -895,7 +1295,7 @@ pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
         // layer): shared memory, registers and the 512 TMEM columns.
         cudaFuncAttributes fa;
         int dev = 0, smem_sm = 0, reserved = 0;
-        if (cudaFuncGetAttributes(&fa, prefill_tc_kernel<D>) != cudaSuccess ||
+        if (cudaFuncGetAttributes(&fa, prefill_tc_kernel<D, kTcRows>) != cudaSuccess ||
             cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
                 cudaSuccess ||
@@ -931,7 +1331,7 @@ pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
     const long grid = items < slots ? items : slots;
     if (grid <= 0)
         return PKV_OK;
-    prefill_tc_kernel<D><<<static_cast<unsigned>(grid), kTcThreads, Geo::kSmem, stream>>>(p, maps);
+    prefill_tc_kernel<D, kTcRows><<<static_cast<unsigned>(grid), kTcThreads, Geo::kSmem, stream>>>(p, maps);
     if (cudaGetLastError() != cudaSuccess)
         return PKV_ERR_CUDA;
     return launch_prefill_merge(p, stream);
@@ -941,7 +1341,11 @@ pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
 
 pkv_status launch_prefill_tc(const PrefillParams &p, cudaStream_t stream)
 {
-    return p.head_dim == 128 ? launch_tc_d<128>(p, stream) : launch_tc_d<64>(p, stream);
+    // 64-row items when every sequence's rows fit one (no padding to 128).
+    if (static_cast<long>(p.max_q_len) * p.group <= 64)
+        return p.head_dim == 128 ? launch_tc_d<128, 64>(p, stream)
+                                 : launch_tc_d<64, 64>(p, stream);
+    return p.head_dim == 128 ? launch_tc_d<128, 128>(p, stream) : launch_tc_d<64, 128>(p, stream);
 }
 
 }  // namespace pkv

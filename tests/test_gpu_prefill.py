@@ -127,6 +127,28 @@ def test_edge_shapes(case, part):
     assert max_abs(out, ref) <= TOL[W.BF16]
 
 
+@pytest.mark.parametrize("lens,qlens,Hq,Hkv,D", [
+    ([300, 64, 17, 129], [8, 5, 1, 3], 64, 8, 128),       # G=8: 64 rows, the 64-row tile full
+    ([200, 31, 16, 90], [16, 2, 9, 13], 32, 8, 64),       # G=4: 64 rows, page-edge lengths
+    ([700, 21], [21, 7], 12, 4, 128),                     # G=3: 63 rows
+])
+@pytest.mark.parametrize("part", [0, 16, 96])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_items_of_at_most_64_rows(lens, qlens, Hq, Hkv, D, part, out_dtype):
+    # Every sequence's rows fit 64: the tcgen05 kernel takes its M = 64 form.
+    w = _edge(lens, qlens, seed=sum(lens) + D, Hq=Hq, Hkv=Hkv, D=D)
+    d = _device(w)
+    out, status = _gpu(w, d, partition_tokens=part, out_dtype=out_dtype)
+    assert status == 0
+    ref = _oracle(w)
+    if out_dtype == torch.bfloat16:
+        ref = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
+        tol = TOL[W.BF16] + 2.0 ** -7 * np.abs(ref).max()
+    else:
+        tol = TOL[W.BF16]
+    assert max_abs(out, ref) <= tol
+
+
 @pytest.mark.parametrize("Hq,Hkv,D", [(8, 8, 64), (16, 8, 128), (40, 8, 128), (96, 8, 128),
                                        (24, 2, 64)])
 def test_head_groups(Hq, Hkv, D):
