@@ -9,34 +9,73 @@
 
 namespace pkv {
 
-// One CTA per new token; threads stride over (head, dim).
+// A CTA takes 32 consecutive new tokens and 64 of their (head, dim)
+// elements.  The rows are read coalesced (elements on the lanes) into a
+// shared-memory tile of the raw input words; then, tokens on the lanes, one
+// warp store writes element e of the 32 tokens: tokens in consecutive slots
+// of a page land in consecutive cells of that page's [head_dim][16] row, so
+// the store covers one or two 32-byte sectors where a token at a time wrote
+// a partial sector per element.  Tile rows are padded to 65 words, so the
+// token-strided reads hit distinct banks.
+constexpr int kCacheTokens = 32;
+constexpr int kCacheElems = 64;
+constexpr int kTileWords = kCacheElems + 1;  // one tile row, in 32-bit words
+
 __global__ void __launch_bounds__(256)
     reshape_and_cache_kernel(const void *k, const void *v, int in_dtype,
-                             const int64_t *slot_mapping, int num_kv_heads, int head_dim,
-                             int num_blocks, void *k_cache, void *v_cache, int kv_dtype,
-                             float k_scale, float v_scale, const float *k_head_scale,
-                             const float *v_head_scale, int32_t *status)
+                             const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                             int head_dim, int num_blocks, void *k_cache, void *v_cache,
+                             int kv_dtype, float k_scale, float v_scale,
+                             const float *k_head_scale, const float *v_head_scale,
+                             int32_t *status)
 {
-    const int i = blockIdx.x;
+    __shared__ uint32_t tk[kCacheTokens * kTileWords], tv[kCacheTokens * kTileWords];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int n = num_kv_heads * head_dim;
+    const int t0 = blockIdx.x * kCacheTokens;
+    const int e0 = blockIdx.y * kCacheElems;
+    const int ne = min(kCacheElems, n - e0);
+    // Raw words: element c of tile row r at word r * kTileWords + c (f32) or
+    // half-word 2 r * kTileWords + c (bf16).
+    const bool f32 = in_dtype == PKV_F32;
+    const int rs = f32 ? kTileWords : 2 * kTileWords;  // row stride in elements
+    for (int r = warp; r < kCacheTokens && t0 + r < num_tokens; r += 8) {
+        const size_t row = static_cast<size_t>(t0 + r) * n + e0;
+        for (int c = lane; c < ne; c += 32) {
+            if (f32) {
+                reinterpret_cast<float *>(tk)[r * rs + c] = static_cast<const float *>(k)[row + c];
+                reinterpret_cast<float *>(tv)[r * rs + c] = static_cast<const float *>(v)[row + c];
+            } else {
+                reinterpret_cast<unsigned short *>(tk)[r * rs + c] =
+                    static_cast<const unsigned short *>(k)[row + c];
+                reinterpret_cast<unsigned short *>(tv)[r * rs + c] =
+                    static_cast<const unsigned short *>(v)[row + c];
+            }
+        }
+    }
+    __syncthreads();
+    const int i = t0 + lane;
+    if (i >= num_tokens)
+        return;
     const int64_t slot = __ldg(slot_mapping + i);
     if (slot < 0)
-        return;
+        return;  // no slot: skipped
     const int64_t blk = slot / kBlockSize;
     const int off = static_cast<int>(slot - blk * kBlockSize);
     if (blk >= num_blocks) {
-        if (threadIdx.x == 0)
+        if (blockIdx.y == 0 && warp == 0)
             set_status(status, PKV_ERR_OUT_OF_RANGE);
         return;
     }
-    const int n = num_kv_heads * head_dim;
-    for (int e = threadIdx.x; e < n; e += blockDim.x) {
-        const size_t src = static_cast<size_t>(i) * n + e;
+    for (int c = warp; c < ne; c += 8) {
+        const int e = e0 + c;
         const size_t dst = (static_cast<size_t>(blk) * n + e) * kBlockSize + off;
         const int h = e / head_dim;
         const float ks = k_head_scale ? k_scale * __ldg(k_head_scale + h) : k_scale;
         const float vs = v_head_scale ? v_scale * __ldg(v_head_scale + h) : v_scale;
-        store_kv(k_cache, kv_dtype, dst, k, in_dtype, src, ks);
-        store_kv(v_cache, kv_dtype, dst, v, in_dtype, src, vs);
+        const size_t j = static_cast<size_t>(lane) * rs + c;
+        store_kv(k_cache, kv_dtype, dst, tk, in_dtype, j, ks);
+        store_kv(v_cache, kv_dtype, dst, tv, in_dtype, j, vs);
     }
 }
 
@@ -50,11 +89,16 @@ pkv_status launch_reshape_and_cache(const void *k, const void *v, int in_dtype,
 {
     if (num_tokens <= 0)
         return PKV_OK;
-    const int n = num_kv_heads * head_dim;
-    const int threads = n >= 256 ? 256 : ((n + 31) / 32) * 32;
-    reshape_and_cache_kernel<<<num_tokens, threads, 0, stream>>>(
-        k, v, in_dtype, slot_mapping, num_kv_heads, head_dim, num_blocks, k_cache, v_cache,
-        kv_dtype, k_scale, v_scale, k_head_scale, v_head_scale, status);
+    const long n = static_cast<long>(num_kv_heads) * head_dim;
+    const long gx = (static_cast<long>(num_tokens) + kCacheTokens - 1) / kCacheTokens;
+    const long gy = (n + kCacheElems - 1) / kCacheElems;
+    if (gy > 65535)
+        return PKV_ERR_UNSUPPORTED;
+    reshape_and_cache_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256,
+                               0, stream>>>(k, v, in_dtype, slot_mapping, num_tokens,
+                                            num_kv_heads, head_dim, num_blocks, k_cache, v_cache,
+                                            kv_dtype, k_scale, v_scale, k_head_scale,
+                                            v_head_scale, status);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -666,13 +666,21 @@ __global__ void __launch_bounds__(kThreads) prefill_merge_kernel(const PrefillPa
 {
     const int t = blockIdx.x / p.num_kv_heads;
     const int hkv = blockIdx.x - t * p.num_kv_heads;
-    int lo = 0, hi = p.num_seqs;  // q_start[lo] <= t < q_start[hi]
+    // The sequence of token t: q_start[lo] <= t < q_start[hi].  Each warp
+    // probes 32 points per round, narrowing the range 32-fold (two rounds of
+    // independent loads up to 1024 sequences, where halving takes ten
+    // dependent ones).  A non-monotone q_start gives some s that the checks
+    // below reject.
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = p.num_seqs;
     while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldg(p.q_start + mid) <= t)
-            lo = mid;
-        else
-            hi = mid;
+        const int step = (hi - lo + 31) / 32;
+        const int at = lo + lane * step;
+        const bool le = lane == 0 || (at < hi && __ldg(p.q_start + at) <= t);
+        const unsigned bal = __ballot_sync(kFullMask, le);
+        const int last = 31 - __clz(bal);
+        lo += last * step;
+        hi = min(hi, lo + step);
     }
     const int s = lo;
     int L = __ldg(p.seq_lens + s);
