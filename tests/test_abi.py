@@ -168,6 +168,8 @@ def test_prefill_partition_plan():
     # 2048-token partitions for long ones.
     assert P(128, 640, 64, 8, 128, 5, 2000, 0) == 0
     assert P(128, 640, 64, 8, 128, 5, 14563, 0) == 2048
+    # One wave of items (304..607 estimated): no split, no merge.
+    assert P(64, 4 * 256 + 60, 32, 8, 128, 256, 4352, 0) == 0    # chunked prefill: 544
     # Few items: split so that about four items per resident CTA exist.
     assert P(2, 8, 64, 8, 128, 5, 32768, 0) == 1024       # 16 items -> 38 parts
     assert P(2, 8, 64, 8, 128, 5, 300, 0) == 256
