@@ -1024,20 +1024,31 @@ __device__ __forceinline__ void write_token_rows(const DecodeParams &p, const in
 }
 
 
-// Counts of the two item phases of a sequence of L tokens under partition
-// P: full partitions first, then the one shorter remainder (or the single
-// item of an empty sequence).  Issuing every full partition before any
-// remainder leaves short items for the end of the grid.
+// Item phases of the partitioned schedule: every full partition first, then
+// the remainders -- at most one per sequence, shorter than a partition --
+// in three size classes, largest first (remainder >= 2P/3, >= P/3, the rest,
+// which includes the single item of an empty sequence).  Handing out the
+// largest items first and the shortest last leaves the grid's final wave
+// with short items.
+constexpr int kPhases = 4;
 __device__ __forceinline__ int full_parts(int L, int P) { return L / P; }
-__device__ __forceinline__ int tail_parts(int L, int P) { return (L % P != 0 || L == 0) ? 1 : 0; }
+__device__ __forceinline__ int phase_parts(int L, int P, int ph)
+{
+    if (ph == 0)
+        return L / P;
+    const int r = L % P;
+    if (r == 0 && L != 0)
+        return 0;  // no remainder
+    const int cls = 3 * r >= 2 * P ? 1 : (3 * r >= P ? 2 : 3);
+    return cls == ph ? 1 : 0;
+}
 
-// Warp-collective scan over sequences: finds the sequence holding unit u of a
-// stream in which sequence s contributes count(L_s) units.  `cur_s` /
-// `cur_base` remember where the previous search ended (u only grows).
-// Returns false when u lies past the last sequence.
-template <bool kTail>
-__device__ bool find_unit(const DecodeParams &p, int u, int &cur_s, int &cur_base, int lane,
-                          int &s_out, int &k_out, int &L_out)
+// Warp-collective scan over sequences: finds the sequence holding unit u of
+// phase ph, in which sequence s contributes phase_parts(L_s) units.
+// `cur_s` / `cur_base` remember where the previous search of that phase
+// ended (u only grows).  Returns false when u lies past the last sequence.
+__device__ inline bool find_unit(const DecodeParams &p, int u, int ph, int &cur_s,
+                                 int &cur_base, int lane, int &s_out, int &k_out, int &L_out)
 {
     const int S = p.num_seqs, P = p.partition;
     for (;;) {
@@ -1045,7 +1056,7 @@ __device__ bool find_unit(const DecodeParams &p, int u, int &cur_s, int &cur_bas
         int n = 0, Ls = 0;
         if (sl < S) {
             Ls = seq_len_of(p, sl);
-            n = kTail ? tail_parts(Ls, P) : full_parts(Ls, P);
+            n = phase_parts(Ls, P, ph);
         }
         int incl = n;
 #pragma unroll
@@ -1071,24 +1082,26 @@ __device__ bool find_unit(const DecodeParams &p, int u, int &cur_s, int &cur_bas
     }
 }
 
-// Total full partitions (kTail: remainder items) over all sequences of one
-// layer (warp-collective).
-template <bool kTail>
-__device__ __forceinline__ int count_parts(const DecodeParams &p, int lane)
+// Items of each phase over all sequences of one layer (warp-collective).
+__device__ __forceinline__ void count_phases(const DecodeParams &p, int lane, int (&n)[kPhases])
 {
-    int tot = 0;
-    for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
-        int n = 0;
-        if (s0 + lane < p.num_seqs) {
-            const int L = seq_len_of(p, s0 + lane);
-            n = kTail ? tail_parts(L, p.partition) : full_parts(L, p.partition);
-        }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
-            n += __shfl_xor_sync(kFullMask, n, off);
-        tot += n;
+    for (int ph = 0; ph < kPhases; ++ph)
+        n[ph] = 0;
+    for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
+        int L = 0;
+        const bool in = s0 + lane < p.num_seqs;
+        if (in)
+            L = seq_len_of(p, s0 + lane);
+#pragma unroll
+        for (int ph = 0; ph < kPhases; ++ph) {
+            int c = in ? phase_parts(L, p.partition, ph) : 0;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                c += __shfl_xor_sync(kFullMask, c, off);
+            n[ph] += c;
+        }
     }
-    return tot;
 }
 
 // Combines the four warps' (m, l, O) states of one item (at the start of each
@@ -1152,9 +1165,9 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_item[8];
     // Warp 0's item scheduler (kept in shared memory, not registers, across
-    // the page loop): scan cursors of the two item phases (reset when the
-    // layer changes) and the per-layer item counts of the phases.
-    __shared__ int s_sched[8];
+    // the page loop): scan cursors of the item phases (reset when the layer
+    // changes) and the per-layer item counts of the phases.
+    __shared__ int s_sched[4 * kPhases];
     __shared__ int s_abort;
     __shared__ int s_last;
 
@@ -1180,16 +1193,19 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
     const size_t block_stride = static_cast<size_t>(Hkv) * tile_stride;
 
     uint32_t pages_done = 0;  // pages this warp has consumed (ring position / phase)
-    enum { kFullS, kFullBase, kTailS, kTailBase, kFullLayer, kTailLayer, kNFull, kNTail };
+    // s_sched: per phase ph, scan cursor (sequence, base) at 2 ph and
+    // 2 ph + 1, the layer the cursor belongs to at kLayer + ph, and the
+    // phase's item count per layer at kCount + ph.
+    enum { kLayer = 2 * kPhases, kCount = 3 * kPhases };
     if (p.split && warp == 0) {
-        const int n_full = count_parts<false>(p, lane);
-        const int n_tail = count_parts<true>(p, lane);
-        if (lane == 0) {
-            for (int i = 0; i < 6; ++i)
-                s_sched[i] = 0;
-            s_sched[kNFull] = n_full;
-            s_sched[kNTail] = n_tail;
-        }
+        int n[kPhases];
+        count_phases(p, lane, n);
+        if (lane == 0)
+            for (int ph = 0; ph < kPhases; ++ph) {
+                s_sched[2 * ph] = s_sched[2 * ph + 1] = 0;
+                s_sched[kLayer + ph] = 0;
+                s_sched[kCount + ph] = n[ph];
+            }
         __syncwarp();
     }
     bool first = true;
@@ -1203,20 +1219,22 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
                 if (lane == 0)
                     v = atomicAdd(p.counter, 1u);
                 item = static_cast<int>(__shfl_sync(kFullMask, v, 0));
-                // Full partitions first, then remainders.
-                const int u = item / Hkv;
+                // The phases in order: full partitions, then the remainders
+                // by size class.
+                int u = item / Hkv;
                 hkv = item - u * Hkv;
-                const int n_full = s_sched[kNFull];
-                const bool tail = u >= n_full;
-                const int o = tail ? kTailS : kFullS;  // this phase's cursors
-                int cs = s_sched[o], cb = s_sched[o + 1], k = 0;
-                const bool found = tail ? find_unit<true>(p, u - n_full, cs, cb, lane, s, k, L)
-                                        : find_unit<false>(p, u, cs, cb, lane, s, k, L);
-                part = tail ? full_parts(L, P) : k;
+                int ph = 0;
+                while (ph < kPhases - 1 && u >= s_sched[kCount + ph]) {
+                    u -= s_sched[kCount + ph];
+                    ++ph;
+                }
+                int cs = s_sched[2 * ph], cb = s_sched[2 * ph + 1], k = 0;
+                const bool found = find_unit(p, u, ph, cs, cb, lane, s, k, L);
+                part = ph ? full_parts(L, P) : k;
                 __syncwarp();
                 if (lane == 0) {
-                    s_sched[o] = cs;
-                    s_sched[o + 1] = cb;
+                    s_sched[2 * ph] = cs;
+                    s_sched[2 * ph + 1] = cb;
                 }
                 done = found ? 0 : 1;
                 nparts = parts_of(L, P);
@@ -1225,15 +1243,16 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
                 if (lane == 0)
                     v = atomicAdd(p.counter, 1u);
                 item = static_cast<int>(__shfl_sync(kFullMask, v, 0));
-                // Every layer's full partitions first, then every layer's
-                // remainders; layer-major inside each phase.
-                const int n_full = s_sched[kNFull], n_tail = s_sched[kNTail];
-                const long full_items = static_cast<long>(n_full) * Hkv;
+                // The phases in order, every layer's items of a phase before
+                // the next phase; layer-major inside each phase.
                 long r = item;
-                const bool tail = r >= full_items * p.num_layers;
-                if (tail)
-                    r -= full_items * p.num_layers;
-                const long per = tail ? static_cast<long>(n_tail) * Hkv : full_items;
+                int ph = 0;
+                while (ph < kPhases - 1 &&
+                       r >= static_cast<long>(s_sched[kCount + ph]) * Hkv * p.num_layers) {
+                    r -= static_cast<long>(s_sched[kCount + ph]) * Hkv * p.num_layers;
+                    ++ph;
+                }
+                const long per = static_cast<long>(s_sched[kCount + ph]) * Hkv;
                 layer = per > 0 ? static_cast<int>(r / per) : p.num_layers;
                 bool found = false;
                 if (layer < p.num_layers) {
@@ -1241,18 +1260,16 @@ __global__ void __launch_bounds__(kThreads, Pol::kMinBlocks)
                     const int u = static_cast<int>(r / Hkv);
                     hkv = static_cast<int>(r - static_cast<long>(u) * Hkv);
                     int k = 0;
-                    const int o = tail ? kTailS : kFullS;  // this phase's cursors
-                    int cs = s_sched[o], cb = s_sched[o + 1];
-                    if (layer != s_sched[tail ? kTailLayer : kFullLayer])
+                    int cs = s_sched[2 * ph], cb = s_sched[2 * ph + 1];
+                    if (layer != s_sched[kLayer + ph])
                         cs = cb = 0;
-                    found = tail ? find_unit<true>(p, u, cs, cb, lane, s, k, L)
-                                 : find_unit<false>(p, u, cs, cb, lane, s, k, L);
-                    part = tail ? full_parts(L, P) : k;
+                    found = find_unit(p, u, ph, cs, cb, lane, s, k, L);
+                    part = ph ? full_parts(L, P) : k;
                     __syncwarp();
                     if (lane == 0) {
-                        s_sched[o] = cs;
-                        s_sched[o + 1] = cb;
-                        s_sched[tail ? kTailLayer : kFullLayer] = layer;
+                        s_sched[2 * ph] = cs;
+                        s_sched[2 * ph + 1] = cb;
+                        s_sched[kLayer + ph] = layer;
                     }
                 }
                 done = found ? 0 : 1;
