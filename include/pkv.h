@@ -106,7 +106,8 @@ typedef enum {
  * the first 256 bytes hold the status word and a work counter).
  *   partition_tokens:
  *     0  = automatic: with at least 608 (sequence, KV head) units, one pass
- *          per unit when max_seq_len <= 2048, else 1536-token partitions;
+ *          per unit when max_seq_len <= 2048, else 4096-token partitions
+ *          (full partitions first, then the remainders, largest first);
  *          with fewer units, the stream-K schedule (PKV_SCHEDULE_STREAMK):
  *          the flattened (sequence, KV head, page) space is cut into one
  *          equal contiguous range per CTA, and sequences cut by range

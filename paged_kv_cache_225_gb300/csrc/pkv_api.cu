@@ -89,19 +89,22 @@ static int resolve_partition(int num_layers, int num_seqs, int num_q_heads, int 
     if (requested != 0)
         return -1;
     // Automatic choice.  Many (sequence, KV head) units keep every CTA busy
-    // with whole units: one pass each when contexts are short, else 1536-token
-    // items scheduled dynamically (few partials, no per-unit boundaries inside
-    // an item; measured on GB300 on the 70B-shaped layers: 1536 and 1792
-    // beat 2048 by about 1.3% -- a shorter last wave of items -- while 1024
-    // and 512 lose to the extra partials and item boundaries).  Few units --
-    // long contexts on a small batch -- use stream-K, which splits them
-    // evenly across all CTAs.  The threshold is twice the CTAs resident on a
-    // GB300 (two per SM); a fixed number keeps the plan, and so the
-    // workspace size, independent of the current device.
+    // with whole units: one pass each when contexts are short, else 4096-token
+    // items scheduled dynamically, full partitions first and the remainders
+    // by size class, largest first, so that the grid ends on short items.
+    // Measured on GB300 on the 70B-shaped layers (bf16 / e4m3 / INT4, us):
+    // 1536 tokens 237.8 / 134.3 / 150.2, 2048 235.8 / 130.1 / 147.6, 3072
+    // 230.7 / 122.7 / 144.9, 4096 227.0 / 122.8 / 141.3, 6144 232.5 / 155.2
+    // / 165.6: longer items mean fewer partials and item boundaries until the
+    // items get too few for the resident CTAs.  Few units -- long contexts
+    // on a small batch -- use stream-K, which splits them evenly across all
+    // CTAs.  The threshold is twice the CTAs resident on a GB300 (two per
+    // SM); a fixed number keeps the plan, and so the workspace size,
+    // independent of the current device.
     const long units = static_cast<long>(num_layers) * num_seqs * num_kv_heads;
     const long many = 2L * 2 * 152;
     if (units >= many)
-        return max_seq_len <= 2048 ? 0 : 1536;
+        return max_seq_len <= 2048 ? 0 : 4096;
     return kStreamK;
 }
 
@@ -577,7 +580,7 @@ static bool make_prefill_plan(int S, int T, int Hq, int Hkv, int D, int B, int m
         // prefill (512 units), stream-K 130 us, items 115 us.
         int dreq = requested;
         if (requested == 0 && static_cast<long>(S) * Hkv >= 3L * 152)
-            dreq = max_len <= 2048 ? -1 : 1536;
+            dreq = max_len <= 2048 ? -1 : 4096;
         if (!make_plan(1, S, Hq, Hkv, D, B, max_len, dreq, &pl->dec))
             return false;
         pl->dec_off = align256(pl->bytes);

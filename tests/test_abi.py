@@ -53,9 +53,9 @@ def test_partition_plan():
     assert P(4, 4, 4, 64, 65, 48) == 48
     assert P(4, 4, 4, 64, 65, 40) == -1           # not a multiple of the block size
     # Automatic: many (sequence, KV head) units -> one pass (short contexts) or
-    # 1536-token items; few units -> stream-K.
+    # 4096-token items; few units -> stream-K.
     assert P(128, 64, 8, 128, 514, 0) == 0              # fp8 chat mix: 1024 units
-    assert P(128, 64, 8, 128, 14626, 0) == 1536         # 70B-shaped layer: 1024 units
+    assert P(128, 64, 8, 128, 14626, 0) == 4096         # 70B-shaped layer: 1024 units
     assert P(64, 32, 8, 128, 4097, 0) == pkv.SCHEDULE_STREAMK    # 8B-shaped: 512 units
     assert P(8, 64, 8, 128, 32769, 0) == pkv.SCHEDULE_STREAMK    # long context: 64 units
     assert P(1, 8, 8, 128, 512, 0) == pkv.SCHEDULE_STREAMK
@@ -318,7 +318,7 @@ def test_layers_plan_counts_every_layers_units():
         assert PL(1, *args) == P(*args)
     # 512 (sequence, KV head) units per layer: stream-K alone, whole units with two layers.
     assert P(64, 32, 8, 128, 4097, 0) == pkv.SCHEDULE_STREAMK
-    assert PL(2, 64, 32, 8, 128, 4097, 0) == 1536
+    assert PL(2, 64, 32, 8, 128, 4097, 0) == 4096
     assert PL(8, 4, 4, 4, 64, 65, 0) == pkv.SCHEDULE_STREAMK      # tiny: 128 units
     assert PL(0, 4, 4, 4, 64, 65, 0) == -1
 
