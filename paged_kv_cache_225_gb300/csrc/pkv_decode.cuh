@@ -1026,11 +1026,17 @@ __device__ __forceinline__ void write_token_rows(const DecodeParams &p, const in
 
 // Item phases of the partitioned schedule: every full partition first, then
 // the remainders -- at most one per sequence, shorter than a partition --
-// in three size classes, largest first (remainder >= 2P/3, >= P/3, the rest,
-// which includes the single item of an empty sequence).  Handing out the
+// in size classes, largest first (three: remainder >= 2P/3, >= P/3, the
+// rest, which includes the single item of an empty sequence).  Handing out the
 // largest items first and the shortest last leaves the grid's final wave
 // with short items.
-constexpr int kPhases = 4;
+// Remainder size classes (same box, 70B bf16 / e4m3 / INT4 layers at
+// 4096-token partitions, us): three 230.2 / 124.6 / 143.2, five 229.8 /
+// 125.8 / 142.5, eight 236.4 / 129.3 / 144.1.
+#ifndef PKV_REMAINDER_CLASSES
+#define PKV_REMAINDER_CLASSES 3
+#endif
+constexpr int kPhases = 1 + PKV_REMAINDER_CLASSES;
 __device__ __forceinline__ int full_parts(int L, int P) { return L / P; }
 __device__ __forceinline__ int phase_parts(int L, int P, int ph)
 {
@@ -1039,7 +1045,8 @@ __device__ __forceinline__ int phase_parts(int L, int P, int ph)
     const int r = L % P;
     if (r == 0 && L != 0)
         return 0;  // no remainder
-    const int cls = 3 * r >= 2 * P ? 1 : (3 * r >= P ? 2 : 3);
+    constexpr int nc = kPhases - 1;
+    const int cls = 1 + (nc - 1) - static_cast<int>((static_cast<long long>(r) * nc) / P);
     return cls == ph ? 1 : 0;
 }
 
