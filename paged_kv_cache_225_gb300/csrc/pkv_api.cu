@@ -494,7 +494,7 @@ namespace pkv {
 // Split plan of the several-queries kernel.  Items are (sequence, KV head,
 // partition, 64-row block); the host knows only T, S and the length bounds,
 // so it estimates the unsplit item count from them.  Enough items keep every
-// CTA busy without a split (contexts over 2048 tokens still use 2048-token
+// CTA busy without a split (contexts over 2048 tokens still use 4096-token
 // partitions so long items do not dominate the tail); fewer are split so
 // that about four items per resident CTA exist.
 static int resolve_prefill_partition(int S, int T, int Hq, int Hkv, int B, int max_q_len,
@@ -513,8 +513,11 @@ static int resolve_prefill_partition(int S, int T, int Hq, int Hkv, int B, int m
     const long blocks = (static_cast<long>(T) * G + 63) / 64;
     const long est = static_cast<long>(Hkv) * (blocks > S ? blocks : S);
     const long many = 2L * 2 * 152;
+    // Two waves or more: 4096-token partitions (the tcgen05 kernel hands out
+    // the last partitions largest first; verification layer, same box: 2048
+    // tokens 324.8 us, 3072 317.5, 4096 315.2).
     if (est >= many)
-        return max_len <= 2048 ? 0 : 2048;
+        return max_len <= 2048 ? 0 : 4096;
     // One wave of items or more (two CTAs per SM): no split -- no partials
     // and no merge (measured on GB300, chunked prefill of the 8B layer,
     // 544 estimated items: no split 258 us, 2048-token partitions 275 us).

@@ -101,6 +101,111 @@ __device__ bool find_prefill_item(const PrefillParams &p, int u, int &cur_s, int
 }
 
 
+// Phases of the items for the tcgen05 kernel: every partition of a sequence
+// but its last first, then the last partitions in three size classes,
+// largest first (size relative to the partition length, or to max_len when
+// contexts are not split), so that the grid ends on short items.
+constexpr int kPrefillPhases = 4;
+__device__ __forceinline__ int prefill_phase_parts(const PrefillParams &p, int L, int ph)
+{
+    const int parts = seq_parts(p, L);
+    if (ph == 0)
+        return parts - 1;
+    const bool split = p.max_parts > 1;
+    const int span = split ? p.partition : (p.max_len > 0 ? p.max_len : 1);
+    const int rem = split ? L - (parts - 1) * p.partition : L;  // in [0, span]
+    constexpr int nc = kPrefillPhases - 1;
+    int cls = 1 + (nc - 1) - static_cast<int>((static_cast<long long>(rem) * nc) / span);
+    cls = cls < 1 ? 1 : (cls > nc ? nc : cls);
+    return cls == ph ? 1 : 0;
+}
+
+// Items of sequence si in phase ph: KV heads x its partitions of the phase x
+// row blocks of RB rows.
+template <int RB>
+__device__ __forceinline__ int seq_phase_items(const PrefillParams &p, const SeqInfo &si, int ph)
+{
+    if (p.skip_single && si.nq == 1)
+        return 0;  // served by the decode kernels
+    const int blocks = (si.nq * p.group + RB - 1) / RB;
+    return p.num_kv_heads * prefill_phase_parts(p, si.L, ph) * blocks;
+}
+
+// Items of each phase over all sequences (warp-collective).
+template <int RB>
+__device__ __forceinline__ void count_prefill_phases(const PrefillParams &p, int lane,
+                                                     int (&n)[kPrefillPhases])
+{
+#pragma unroll
+    for (int ph = 0; ph < kPrefillPhases; ++ph)
+        n[ph] = 0;
+    for (int s0 = 0; s0 < p.num_seqs; s0 += 32) {
+        SeqInfo si = {0, 0, 0};
+        if (s0 + lane < p.num_seqs)
+            si = seq_info(p, s0 + lane);
+#pragma unroll
+        for (int ph = 0; ph < kPrefillPhases; ++ph) {
+            int c = seq_phase_items<RB>(p, si, ph);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+                c += __shfl_xor_sync(kFullMask, c, off);
+            n[ph] += c;
+        }
+    }
+}
+
+// Warp-collective: maps item u of phase ph to its (sequence, KV head,
+// partition, row block), with that phase's scan position (cur_s, cur_base);
+// u only grows within a phase.  Returns false past the phase's last item.
+template <int RB>
+__device__ bool find_prefill_item_phase(const PrefillParams &p, int u, int ph, int &cur_s,
+                                        int &cur_base, int lane, PrefillItem &it)
+{
+    const int S = p.num_seqs;
+    for (;;) {
+        const int sl = cur_s + lane;
+        int n = 0;
+        SeqInfo si = {0, 0, 0};
+        if (sl < S) {
+            si = seq_info(p, sl);
+            n = seq_phase_items<RB>(p, si, ph);
+        }
+        int incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(kFullMask, incl, off);
+            if (lane >= off)
+                incl += t;
+        }
+        const int tot = __shfl_sync(kFullMask, incl, 31);
+        if (u < cur_base + tot) {
+            const unsigned bal = __ballot_sync(kFullMask, cur_base + incl > u);
+            const int ln = __ffs(bal) - 1;
+            const int excl = __shfl_sync(kFullMask, incl - n, ln);
+            it.s = cur_s + ln;
+            it.L = __shfl_sync(kFullMask, si.L, ln);
+            it.q0 = __shfl_sync(kFullMask, si.q0, ln);
+            it.nq = __shfl_sync(kFullMask, si.nq, ln);
+            const int k = u - cur_base - excl;
+            const int blocks = (it.nq * p.group + RB - 1) / RB;
+            const int parts = seq_parts(p, it.L);
+            it.rb = k % blocks;
+            if (ph == 0) {
+                it.part = (k / blocks) % (parts - 1);
+                it.hkv = k / (blocks * (parts - 1));
+            } else {
+                it.part = parts - 1;
+                it.hkv = k / blocks;
+            }
+            return true;
+        }
+        if (cur_s + 32 >= S)
+            return false;
+        cur_base += tot;
+        cur_s += 32;
+    }
+}
+
 // Pages of an item: the context partition [t0, t1) cut at the last position
 // any of its rows sees.  pg0 is the first page's index in the block table.
 __device__ __forceinline__ void item_pages(const PrefillParams &p, int L, int nq, int row0,

@@ -165,9 +165,9 @@ def test_prefill_partition_plan():
     assert P(4, 20, 8, 2, 64, 8, 200, 48) == 48
     assert P(4, 20, 8, 2, 64, 8, 200, 40) == -1          # not a multiple of the block size
     # Enough (KV head, 64-row block) items: no split for short contexts,
-    # 2048-token partitions for long ones.
+    # 4096-token partitions for long ones.
     assert P(128, 640, 64, 8, 128, 5, 2000, 0) == 0
-    assert P(128, 640, 64, 8, 128, 5, 14563, 0) == 2048
+    assert P(128, 640, 64, 8, 128, 5, 14563, 0) == 4096
     # One wave of items (304..607 estimated): no split, no merge.
     assert P(64, 4 * 256 + 60, 32, 8, 128, 256, 4352, 0) == 0    # chunked prefill: 544
     # Few items: split so that about four items per resident CTA exist.
