@@ -322,7 +322,7 @@ __device__ __forceinline__ TcItem read_item(const int *slot)
     return it;
 }
 
-template <int D, int kTcRows>
+template <int D, int kTcRows, bool kPhased>
 __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
     prefill_tc_kernel(const PrefillParams p, const __grid_constant__ TcMaps maps)
 {
@@ -389,12 +389,12 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
         // the CTAs' last items).  The query rows of a claimed item are
         // prefetched into L2 for the softmax warps, which load them a ring's
         // worth of chunks later.
-        // Split contexts: item phases (largest items first) and each phase's
-        // scan position.  Unsplit calls keep sequence order (measured on the
-        // unsplit chunked prefill: 267 -> 283 us with the phases).
-        const bool phased = p.max_parts > 1;
+        // Split contexts (kPhased): item phases (largest items first) and
+        // each phase's scan position.  Unsplit calls keep sequence order
+        // (measured on the unsplit chunked prefill: 267 -> 283 us with the
+        // phases).
         int nph[kPrefillPhases];
-        if (phased) {
+        if constexpr (kPhased) {
             count_prefill_phases<kTcRows>(p, lane, nph);
         } else {
 #pragma unroll
@@ -415,18 +415,18 @@ __global__ void __launch_bounds__(kTcThreads, kChunk == 2 ? 2 : 1)
             PrefillItem it;
             bool ok = false;
             int r = static_cast<int>(u);
-            if (!phased) {
+            if constexpr (!kPhased) {
                 ok = find_prefill_item<kTcRows>(p, r, cur[0], cur[1], lane, it);
-                r = INT_MAX;
-            }
+            } else {
 #pragma unroll
-            for (int ph = 0; ph < kPrefillPhases && phased; ++ph) {
-                if (!ok && (r < nph[ph] || ph == kPrefillPhases - 1)) {
-                    ok = find_prefill_item_phase<kTcRows>(p, r, ph, cur[2 * ph],
-                                                          cur[2 * ph + 1], lane, it);
-                    r = INT_MAX;  // found or past the end: no later phase
-                } else if (!ok) {
-                    r -= nph[ph];
+                for (int ph = 0; ph < kPrefillPhases; ++ph) {
+                    if (!ok && (r < nph[ph] || ph == kPrefillPhases - 1)) {
+                        ok = find_prefill_item_phase<kTcRows>(p, r, ph, cur[2 * ph],
+                                                              cur[2 * ph + 1], lane, it);
+                        r = INT_MAX;  // found or past the end: no later phase
+                    } else if (!ok) {
+                        r -= nph[ph];
+                    }
                 }
             }
             const int slot = k % kQueue;
@@ -1303,7 +1303,7 @@ bool encode_tile(EncodeTiledFn enc, CUtensorMap *map, const void *cache, int D, 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, int kTcRows>
+template <int D, int kTcRows, bool kPhased>
 pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
 {
     using Geo = TcGeom<D>;
@@ -1312,9 +1312,9 @@ pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
     int occ = 1;
     const pkv_status crc = cache.get(&occ, [](int *out_occ) -> pkv_status {
         // Two CTAs per SM need the largest shared-memory carveout.
-        if (cudaFuncSetAttribute(prefill_tc_kernel<D, kTcRows>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(prefill_tc_kernel<D, kTcRows, kPhased>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Geo::kSmem) != cudaSuccess ||
-            cudaFuncSetAttribute(prefill_tc_kernel<D, kTcRows>,
+            cudaFuncSetAttribute(prefill_tc_kernel<D, kTcRows, kPhased>,
                                  cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared) != cudaSuccess)
             return PKV_ERR_CUDA;
@@ -1324,7 +1324,7 @@ pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
         // layer): shared memory, registers and the 512 TMEM columns.
         cudaFuncAttributes fa;
         int dev = 0, smem_sm = 0, reserved = 0;
-        if (cudaFuncGetAttributes(&fa, prefill_tc_kernel<D, kTcRows>) != cudaSuccess ||
+        if (cudaFuncGetAttributes(&fa, prefill_tc_kernel<D, kTcRows, kPhased>) != cudaSuccess ||
             cudaGetDevice(&dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) !=
                 cudaSuccess ||
@@ -1360,7 +1360,7 @@ pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
     const long grid = items < slots ? items : slots;
     if (grid <= 0)
         return PKV_OK;
-    prefill_tc_kernel<D, kTcRows><<<static_cast<unsigned>(grid), kTcThreads, Geo::kSmem, stream>>>(p, maps);
+    prefill_tc_kernel<D, kTcRows, kPhased><<<static_cast<unsigned>(grid), kTcThreads, Geo::kSmem, stream>>>(p, maps);
     if (cudaGetLastError() != cudaSuccess)
         return PKV_ERR_CUDA;
     return launch_prefill_merge(p, stream);
@@ -1370,11 +1370,19 @@ pkv_status launch_tc_d(const PrefillParams &p, cudaStream_t stream)
 
 pkv_status launch_prefill_tc(const PrefillParams &p, cudaStream_t stream)
 {
-    // 64-row items when every sequence's rows fit one (no padding to 128).
-    if (static_cast<long>(p.max_q_len) * p.group <= 64)
-        return p.head_dim == 128 ? launch_tc_d<128, 64>(p, stream)
-                                 : launch_tc_d<64, 64>(p, stream);
-    return p.head_dim == 128 ? launch_tc_d<128, 128>(p, stream) : launch_tc_d<64, 128>(p, stream);
+    // 64-row items when every sequence's rows fit one (no padding to 128);
+    // the size-ordered item phases when contexts are split.
+    const bool m64 = static_cast<long>(p.max_q_len) * p.group <= 64;
+    const bool split = p.max_parts > 1;
+    if (p.head_dim == 128)
+        return m64 ? (split ? launch_tc_d<128, 64, true>(p, stream)
+                            : launch_tc_d<128, 64, false>(p, stream))
+                   : (split ? launch_tc_d<128, 128, true>(p, stream)
+                            : launch_tc_d<128, 128, false>(p, stream));
+    return m64 ? (split ? launch_tc_d<64, 64, true>(p, stream)
+                        : launch_tc_d<64, 64, false>(p, stream))
+               : (split ? launch_tc_d<64, 128, true>(p, stream)
+                        : launch_tc_d<64, 128, false>(p, stream));
 }
 
 }  // namespace pkv
