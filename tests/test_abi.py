@@ -210,6 +210,13 @@ def test_prefill_workspace_of_a_mixed_batch_holds_the_routed_decode():
         a(S * 5 * Hq * parts * 8)
     # All one-query: the decode plan only (after the 256-byte header).
     assert W(S, S, Hq, Hkv, D, 1, L, -1) == 256
+    # Automatic plan of the chunked-prefill mix (64 x 8 = 512 units, one wave
+    # of decode CTAs or more): the prompt chunks unsplit (about 544 items),
+    # the one-query sequences on 4096-token decode items, not stream-K.
+    L2 = 4096 + 256
+    assert pkv.prefill_partition_tokens(S, T, Hq, Hkv, D, 256, L2, 0) == 0
+    assert W(S, T, Hq, Hkv, D, 256, L2, 0) == WD(S, Hq, Hkv, D, L2, 4096)
+    assert WD(S, Hq, Hkv, D, L2, 4096) != WD(S, Hq, Hkv, D, L2, pkv.SCHEDULE_STREAMK)
 
 
 def _prefill(**kw):
